@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the KVarN K4V2 g128 hot path on GB300.
+
+Workload (default): one decode step of paged attention over a K4V2 g128 packed cache --
+batch 64, seq_len = 128 * U{8..128} (mean ~8.7K tokens), 32 query heads over 8 KV heads,
+head_dim 128, randomly permuted block table; the cache is built from the synthetic outlier
+generator by kvarn_quantize_tiles.  One step = kvarn_append_token (one new fp16 K/V token per
+sequence, sealing full tiles) + kvarn_decode_attention over the sealed pages and the partial
+tile.  The metric counts attended KV tokens (all heads of a token) per second.
+
+Also measured in the same run: kvarn_quantize_tiles throughput on one layer of 8 KV heads x
+16384 tokens x head_dim 128 (L2 flushed between launches).
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica (weak scaling, no collective on
+the data path); value = tokens of all ranks / slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "K4V2 g128 decode-attn KV tokens/s & HBM GB/s; quantize tokens/s (1 GB300)"
+WORKLOAD = ("paged decode attention + append: batch 64, seq_len 128*U{8..128}, 32 q heads / 8 kv "
+            "heads, head_dim 128, K4V2 g128 packed cache, permuted block table")
+BATCH, HQ, HKV, D0, MIN_PAGES, MAX_PAGES, SEED = 64, 32, 8, 128, 8, 128, 3
+Q_TOKENS, Q_HEADS = 16384, 8   # quantise-throughput layer
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,power.draw")
+
+    def __init__(self, device_id: str):
+        self.device_id = device_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.device_id, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[2:6]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _device_id(torch):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(0).uuid).replace("GPU-", "")
+    except Exception:
+        return os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+
+
+# ------------------------------------------------------------------------------------------------
+# KVarN (CUDA) arm
+# ------------------------------------------------------------------------------------------------
+
+def _setup_decode(torch, kv, synth, steps_total):
+    dev = torch.device("cuda")
+    shape = synth.decode_batch(BATCH, HQ, HKV, D0, seed=SEED, min_pages=MIN_PAGES, max_pages=MAX_PAGES)
+    lens0 = shape["seq_lens"].to(torch.int64)
+    base_table = shape["block_table"]
+    n_seal_pages = int((lens0 // 128).sum())
+    grow = steps_total // 128 + 2                    # pages each sequence may seal while timed
+    width = base_table.shape[1] + grow
+    n_pool = n_seal_pages + BATCH * grow
+    table = torch.zeros((BATCH, width), dtype=torch.int32)
+    extra = torch.arange(n_seal_pages, n_pool, dtype=torch.int32).view(BATCH, grow)
+    for b in range(BATCH):
+        n = int(lens0[b]) // 128
+        table[b, :n] = base_table[b, :n]
+        table[b, n:n + grow] = extra[b]
+    desc = kv.desc_from_preset(D0, HKV)
+    pool = kv.alloc_pool(desc, n_pool, device=dev)
+    total = int(lens0.sum())
+    k_all, v_all = synth.outlier_kv(total, HKV, D0, seed=SEED, device=dev)
+    page_ids = torch.cat([base_table[b, :int(lens0[b]) // 128] for b in range(BATCH)]).to(dev)
+    kv.quantize_tiles(desc, k_all, v_all, page_ids, pool)
+    torch.cuda.synchronize()
+    del k_all, v_all
+    torch.cuda.empty_cache()
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 1)
+    n_sets = 4
+    qs = [torch.randn((BATCH, HQ, D0), generator=g, device=dev).half() for _ in range(n_sets)]
+    kn = [torch.randn((BATCH, HKV, D0), generator=g, device=dev).half() for _ in range(n_sets)]
+    vn = [torch.randn((BATCH, HKV, D0), generator=g, device=dev).half() for _ in range(n_sets)]
+    return {
+        "desc": desc, "pool": pool, "table": table.to(dev), "lens0": lens0, "qs": qs, "kn": kn, "vn": vn,
+        "pk": torch.zeros((BATCH, HKV, 128, D0), dtype=torch.float16, device=dev),
+        "pv": torch.zeros((BATCH, HKV, 128, D0), dtype=torch.float16, device=dev),
+        "lens": [lens0.to(torch.int32).to(dev), torch.zeros(BATCH, dtype=torch.int32, device=dev)],
+        "out": torch.empty((BATCH, HQ, D0), dtype=torch.float16, device=dev),
+        "ws": kv.alloc_workspace(desc, BATCH, HQ, width, device=dev),
+        "status": torch.zeros(1, dtype=torch.int32, device=dev),
+        "rec_bytes": desc.page_record_bytes,
+    }
+
+
+def _decode_bytes(lens, rec_bytes):
+    """Algorithmic bytes of one decode launch: packed pages + partial fp16 tokens + q + out."""
+    sealed = sum(int(L) // 128 for L in lens)
+    part = sum(int(L) % 128 for L in lens)
+    return (sealed * HKV * rec_bytes + part * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2)
+
+
+def _run_kvarn(args, torch, world, rank):
+    from calibration_free_kv_gb300 import build as kbuild
+    kbuild.build()
+    from calibration_free_kv_gb300 import kvarn as kv
+    from calibration_free_kv_gb300 import synth
+
+    dev = torch.device("cuda")
+    S = _setup_decode(torch, kv, synth, args.warmup + 2 * args.steps + 4)
+    stream = torch.cuda.current_stream()
+    state = {"cur": 0, "step": 0}
+
+    def step(q=None, kn=None, vn=None, ev=None):
+        i = state["step"] % len(S["qs"])
+        q = S["qs"][i] if q is None else q
+        kn = S["kn"][i] if kn is None else kn
+        vn = S["vn"][i] if vn is None else vn
+        c = state["cur"]
+        kv.append_token(S["desc"], kn, vn, S["pk"], S["pv"], S["lens"][c], S["table"], S["pool"],
+                        seq_lens_out=S["lens"][1 - c], status=S["status"], stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        kv.decode_attention(S["desc"], q, S["pool"], S["table"], S["lens"][1 - c], S["out"], S["ws"],
+                            partial_k=S["pk"], partial_v=S["pv"], softmax_scale=1 / math.sqrt(D0),
+                            status=S["status"], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        state["cur"] = 1 - c
+        state["step"] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    lens_before = S["lens"][state["cur"]].to(torch.int64).cpu()
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(_device_id(torch))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(ev=dec_ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    status = int(S["status"].item())
+    if status != 0:
+        raise RuntimeError("device status %d during the timed steps" % status)
+
+    # attended tokens per step: lengths after each step's append
+    tokens = sum(int(lens_before.sum()) + BATCH * (i + 1) for i in range(args.steps))
+    dec_bytes = [_decode_bytes((lens_before + i + 1).tolist(), S["rec_bytes"]) for i in range(args.steps)]
+    peak, peak_kind = _peaks()
+    avg_dec = statistics.mean(dec_ms)
+    achieved = statistics.mean(dec_bytes) / (avg_dec * 1e-3) / 1e9
+
+    # ---- end to end through the public API: pinned host q/k/v in, fp16 out back each step
+    h_q = [t.cpu().pin_memory() for t in S["qs"]]
+    h_k = [t.cpu().pin_memory() for t in S["kn"]]
+    h_v = [t.cpu().pin_memory() for t in S["vn"]]
+    h_out = torch.empty((BATCH, HQ, D0), dtype=torch.float16).pin_memory()
+    d_q = torch.empty_like(S["qs"][0])
+    d_k = torch.empty_like(S["kn"][0])
+    d_v = torch.empty_like(S["vn"][0])
+    e_steps = args.steps
+    lens_e = S["lens"][state["cur"]].to(torch.int64).cpu()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e_steps):
+        j = i % len(h_q)
+        d_q.copy_(h_q[j], non_blocking=True)
+        d_k.copy_(h_k[j], non_blocking=True)
+        d_v.copy_(h_v[j], non_blocking=True)
+        step(q=d_q, kn=d_k, vn=d_v)
+        h_out.copy_(S["out"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_tokens = sum(int(lens_e.sum()) + BATCH * (i + 1) for i in range(e_steps))
+
+    # ---- quantise throughput: one layer, 8 KV heads x 16384 tokens x head_dim 128
+    qdesc = kv.desc_from_preset(D0, Q_HEADS)
+    kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, D0, seed=2, device=dev)
+    qpool = kv.alloc_pool(qdesc, Q_TOKENS // 128, device=dev)
+    qids = torch.arange(Q_TOKENS // 128, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    q_ms = []
+    for rep in range(3 + 20):
+        flush.fill_(float(rep))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kv.quantize_tiles(qdesc, kq, vq, qids, qpool, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            q_ms.append(a.elapsed_time(b))
+    q_med = statistics.median(q_ms)
+    q_bytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
+    q_gbs = q_bytes / (q_med * 1e-3) / 1e9
+
+    # ---- aggregate over ranks (replicas)
+    if world > 1:
+        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    value = world * tokens / (elapsed_ms * 1e-3)
+    e2e_value = world * e2e_tokens / (e2e_ms * 1e-3)
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC,
+        "value": value,
+        "unit": "KV tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "dtype_detail": "fp16 MMA operands (exact integer codes, hi+lo split scales) with f32 "
+                        "accumulation; f32 quantisation; u4/u2 packed cache",
+        "data": "synthetic (outlier generator: N(0,1), 4 channels x20-50 per head, lognormal token "
+                "scales; seeds 3 and 2)",
+        "config": {
+            "workload": WORKLOAD.replace("batch 64", "batch %d" % BATCH),
+            "batch": BATCH, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D0,
+            "seq_len": "128*U{8..128}", "mean_seq_len": float(lens_before.double().mean()),
+            "preset": "kvarn_k4v2_g128",
+            "l2": "inputs larger than L2: each decode reads %.0f MB of packed cache" % (dec_bytes[0] / 1e6),
+        },
+        "decode_hbm_gbs": achieved,
+        "decode_us": avg_dec * 1e3,
+        "roofline": {
+            "kernel": "kvarn_decode_attention (decode_kernel + combine_kernel)",
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "traffic": None, "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
+        },
+        "quantize": {
+            "workload": "one layer, 8 KV heads x 16384 tokens x head_dim 128 (K and V), L2 flushed",
+            "tokens_per_s": Q_TOKENS / (q_med * 1e-3),
+            "us": q_med * 1e3, "hbm_gbs": q_gbs, "frac": q_gbs / peak,
+            "algorithmic_bytes": q_bytes,
+        },
+        "e2e": {"value": e2e_value, "unit": "KV tokens/s",
+                "h2d_bytes_per_step": (BATCH * HQ * D0 + 2 * BATCH * HKV * D0) * 2,
+                "d2h_bytes_per_step": BATCH * HQ * D0 * 2},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (baseline) arm
+# ------------------------------------------------------------------------------------------------
+
+def _oracle_sample(seconds: float, seed: int = SEED):
+    """Time the float64 oracle's decode attention on whole (sequence, kv head) caches of the
+    workload until `seconds` of CPU work: returns (KV tokens/s, description)."""
+    import numpy as np
+    import torch
+    from calibration_free_kv_gb300 import synth
+    from oracle import kvarn_oracle as ko
+
+    shape = synth.decode_batch(BATCH, HQ, HKV, D0, seed=seed, min_pages=MIN_PAGES, max_pages=MAX_PAGES)
+    lens = shape["seq_lens"].tolist()
+    q = shape["q"].double().numpy()
+    done_tokens, done_units, t_total = 0, 0, 0.0
+    b = 0
+    group = HQ // HKV
+    while t_total < seconds or done_units == 0:
+        L = lens[b % BATCH]
+        k, v = synth.outlier_kv(L, 1, D0, seed=seed * 7 + b)
+        n = L // 128
+        kt = k[:, 0].double().numpy().reshape(n, 128, D0)
+        vt = v[:, 0].double().numpy().reshape(n, 128, D0)
+        kq = ko.quantize_tile(kt, "K")
+        vq = ko.quantize_tile(vt, "V")
+        fields = ("codes", "scale", "zero", "factor")
+        recs = [ko.pack_record({f: kq[f][i] for f in fields}, {f: vq[f][i] for f in fields})
+                for i in range(n)]
+        t0 = time.perf_counter()
+        ko.decode_sequence(q[b % BATCH, :group], recs, None, None, 1 / math.sqrt(D0), D0)
+        t_total += time.perf_counter() - t0
+        done_tokens += L
+        done_units += 1
+        b += 1
+    # one (sequence, kv head) unit covers L tokens for 1 of the HKV heads
+    value = done_tokens / HKV / t_total
+    desc = ("%d whole (sequence, kv head) decode units (%d token-heads, 4 query heads each) of the "
+            "workload through the float64 oracle (dequantise + textbook attention); %.1f s"
+            % (done_units, done_tokens, t_total))
+    return value, desc, t_total
+
+
+def _run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    per_step = max(1.0, 20.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_sample(per_step * 0.25)
+    vals, total_t, descs = [], 0.0, []
+    for i in range(args.steps):
+        v, d, t = _oracle_sample(per_step, seed=SEED + i)
+        vals.append(v)
+        total_t += t
+        descs.append(d)
+    value = statistics.mean(vals)
+    cores = os.cpu_count()
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (outlier generator)",
+        "config": {"workload": WORKLOAD, "batch": BATCH, "num_q_heads": HQ, "num_kv_heads": HKV,
+                   "head_dim": D0, "seq_len": "128*U{8..128}", "preset": "kvarn_k4v2_g128"},
+        "cpu_baseline": {"value": value, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": descs[0] if descs else ""},
+        "e2e": {"value": value, "unit": "KV tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("kvarn", "reference"), default="kvarn")
+    ap.add_argument("--batch", type=int, default=64,
+                    help="decode batch (64 = the benchmark workload; smaller only for profiling)")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="CPU work of the oracle baseline sample (kvarn arm)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    global BATCH
+    BATCH = args.batch
+    world, rank, local = _dist_env()
+
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return
+        res = _run_reference(args, world, rank)
+        if res is not None:
+            print(json.dumps(res))
+        return
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    res = _run_kvarn(args, torch, world, rank)
+    if rank == 0 and res is not None:
+        value, desc, t = _oracle_sample(args.cpu_seconds)
+        res["cpu_baseline"] = {"value": value, "unit": "KV tokens/s", "cores": os.cpu_count(),
+                               "kind": "oracle", "sample": desc}
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,106 @@
+// Shared device helpers and the page-record geometry of the KVarN kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "kvarn.h"
+
+namespace kvarn {
+
+constexpr int kTile = 128;                 // tokens per tile == tokens per page
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Byte offsets of the sections of one (page, kv head) record for padded head_dim d.
+struct RecordLayout {
+  int kcodes, vcodes, kscale, kzero, kfactor, vscale, vzero, vfactor, bytes;
+};
+
+__host__ __device__ constexpr RecordLayout record_layout(int d) {
+  return RecordLayout{0,
+                      kTile * d / 2,
+                      kTile * d / 2 + kTile * d / 4,
+                      kTile * d / 2 + kTile * d / 4 + 2 * d,
+                      kTile * d / 2 + kTile * d / 4 + 4 * d,
+                      kTile * d / 2 + kTile * d / 4 + 4 * d + 2 * kTile,
+                      kTile * d / 2 + kTile * d / 4 + 4 * d + 4 * kTile,
+                      kTile * d / 2 + kTile * d / 4 + 4 * d + 6 * kTile,
+                      kTile * d / 2 + kTile * d / 4 + 6 * d + 6 * kTile};
+}
+
+__device__ __forceinline__ void flag_error(int32_t* status, int bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// (x & mask) | bits in one LOP3.
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t bits) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(bits));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier + 1-D bulk copy (TMA engine, no tensor map) ---------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy completing on `bar`.  dst/src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~2 s of wall time (or 2^26 polls) and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 26); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+  }
+  return false;
+}
+
+}  // namespace kvarn

@@ -1,0 +1,120 @@
+// KVarN page record -> fp16 K/V in the original basis (sm_103a).
+//
+// K~[t][j] = r[t] (code s'[j] + z'[j]),  V~[t][j] = c[j] (code s'[t] + z'[t])  (rotated basis),
+// then each token row is multiplied by H_d / sqrt(d) (the rotation is its own inverse) and the
+// padded channels are dropped [hotdry §非对称量化与尺度折叠: scales multiplied back at read;
+// vatt §四個步驟: orthonormal rotation, invertible].  Not on the decode path: used for
+// checking and for consumers that want plain fp16 K/V back.
+#include "common.cuh"
+#include "params.cuh"
+
+namespace kvarn {
+
+
+template <int D>
+struct DequantShape {
+  static constexpr int kLd = D + 4;
+  static constexpr int kSmemBytes = kTile * kLd * 4;
+};
+
+// grid.x = pages * Hkv * 2, block = 128 threads (one token row each while decoding codes).
+template <int D>
+__global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
+  constexpr RecordLayout RL = record_layout(D);
+  constexpr int LD = DequantShape<D>::kLd;
+  extern __shared__ __align__(16) float smem_x[];
+  const int unit = blockIdx.x >> 1;
+  const bool is_v = (blockIdx.x & 1) != 0;
+  const int h = unit % p.num_kv_heads;
+  const int pi = unit / p.num_kv_heads;
+  int64_t page = p.page_ids[pi];
+  if (page < 0 || page >= p.num_pool_pages) {
+    if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
+    page = 0;
+  }
+  const uint8_t* rec = p.pool + (page * p.num_kv_heads + h) * (int64_t)RL.bytes;
+  const int t = threadIdx.x;
+  const int g_t = t & 7, rho_or_h = (t & 15) >> 3;
+
+  if (!is_v) {
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(rec + RL.kcodes);
+    const __half* ks = reinterpret_cast<const __half*>(rec + RL.kscale);
+    const __half* kz = reinterpret_cast<const __half*>(rec + RL.kzero);
+    const float r = __half2float(reinterpret_cast<const __half*>(rec + RL.kfactor)[t]);
+    const int mi = t >> 4, rho = rho_or_h;
+    for (int kk = 0; kk < D / 16; ++kk) {
+      for (int tq = 0; tq < 4; ++tq) {
+        const int lane = 4 * g_t + tq;
+        const uint32_t w = kw[((mi * (D / 64) + kk / 4) * 32 + lane) * 4 + (kk & 3)];
+        for (int hh = 0; hh < 2; ++hh)
+          for (int pp = 0; pp < 2; ++pp) {
+            const int j = 16 * kk + 8 * hh + 2 * tq + pp;
+            const uint32_t code = (w >> (4 * (hh + 2 * rho + 4 * pp))) & 15u;
+            smem_x[t * LD + j] =
+                r * fmaf((float)code, __half2float(ks[j]), __half2float(kz[j]));
+          }
+      }
+    }
+  } else {
+    const uint32_t* vw = reinterpret_cast<const uint32_t*>(rec + RL.vcodes);
+    const float s = __half2float(reinterpret_cast<const __half*>(rec + RL.vscale)[t]);
+    const float z = __half2float(reinterpret_cast<const __half*>(rec + RL.vzero)[t]);
+    const __half* vc = reinterpret_cast<const __half*>(rec + RL.vfactor);
+    const int ks = t >> 4, ks2 = ks >> 1, f = ks & 1, hh = rho_or_h;
+    const int tq = (t & 7) >> 1, pp = t & 1;
+    for (int mc = 0; mc < D / 16; ++mc)
+      for (int g = 0; g < 8; ++g) {
+        const int lane = 4 * g + tq;
+        const uint32_t w = vw[((ks2 * (D / 64) + mc / 4) * 32 + lane) * 4 + (mc & 3)];
+        for (int rho = 0; rho < 2; ++rho) {
+          const int j = 16 * mc + g + 8 * rho;
+          const uint32_t code = (w >> (2 * (2 * f + hh + 4 * rho + 8 * pp))) & 3u;
+          smem_x[t * LD + j] = __half2float(vc[j]) * fmaf((float)code, s, z);
+        }
+      }
+  }
+  __syncthreads();
+  // inverse rotation along channels: log2(D) butterfly stages over the whole tile
+  for (int hstep = 1; hstep < D; hstep <<= 1) {
+    for (int idx = threadIdx.x; idx < kTile * D / 2; idx += blockDim.x) {
+      const int row = idx / (D / 2), k = idx - row * (D / 2);
+      const int i0 = (k / hstep) * 2 * hstep + (k % hstep);
+      const float a = smem_x[row * LD + i0], b = smem_x[row * LD + i0 + hstep];
+      smem_x[row * LD + i0] = a + b;
+      smem_x[row * LD + i0 + hstep] = a - b;
+    }
+    __syncthreads();
+  }
+  const float isd = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+  __half* dst = (is_v ? p.v_out : p.k_out) + ((int64_t)pi * p.num_kv_heads + h) * kTile * p.d0;
+  for (int idx = threadIdx.x; idx < kTile * p.d0; idx += blockDim.x) {
+    const int row = idx / p.d0, j = idx - row * p.d0;
+    dst[idx] = __float2half_rn(smem_x[row * LD + j] * isd);
+  }
+}
+
+template <int D>
+static int launch_dequant_t(const DequantParams& p, int num_pages, cudaStream_t stream) {
+  constexpr int kSmem = DequantShape<D>::kSmemBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(dequantize_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem) != cudaSuccess)
+      return KVARN_ERR_CUDA;
+    attr_set = true;
+  }
+  dequantize_kernel<D><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
+int launch_dequant_any(int d, const DequantParams& p, int num_pages, cudaStream_t stream) {
+  if (num_pages <= 0) return KVARN_OK;
+  switch (d) {
+    case 64: return launch_dequant_t<64>(p, num_pages, stream);
+    case 128: return launch_dequant_t<128>(p, num_pages, stream);
+    case 256: return launch_dequant_t<256>(p, num_pages, stream);
+    default: return KVARN_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace kvarn

@@ -1,0 +1,229 @@
+// C ABI of the KVarN kernels: argument validation, launch configuration, status codes.
+// Nothing here allocates, synchronises or keeps state between calls.
+#include <cstring>
+
+#include "common.cuh"
+
+#include "params.cuh"
+
+using namespace kvarn;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_desc(const kvarn_desc* d) {
+  if (d == nullptr) return KVARN_ERR_INVALID_ARG;
+  if (d->tile_tokens != kTile || d->k_bits != 4 || d->v_bits != 2) return KVARN_ERR_UNSUPPORTED;
+  if (d->head_dim < 8 || d->head_dim > 256 || d->head_dim % 8 != 0) return KVARN_ERR_UNSUPPORTED;
+  const int dp = d->head_dim_padded;
+  if (!(dp == 64 || dp == 128 || dp == 256) || d->head_dim > dp) return KVARN_ERR_UNSUPPORTED;
+  if (d->num_kv_heads < 1) return KVARN_ERR_INVALID_ARG;
+  if (d->sinkhorn_iters < 0 || d->sinkhorn_iters > 8) return KVARN_ERR_UNSUPPORTED;
+  if (!(d->sinkhorn_eps > 0.0f)) return KVARN_ERR_INVALID_ARG;
+  if (d->page_record_bytes != record_layout(dp).bytes) return KVARN_ERR_INVALID_ARG;
+  return KVARN_OK;
+}
+
+int padded_dim(int d0) {
+  int d = 64;
+  while (d < d0) d *= 2;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, kvarn_desc* out) {
+  if (preset == nullptr || out == nullptr) return KVARN_ERR_INVALID_ARG;
+  if (std::strcmp(preset, "kvarn_k4v2_g128") != 0) return KVARN_ERR_UNSUPPORTED;
+  if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0) return KVARN_ERR_UNSUPPORTED;
+  if (num_kv_heads < 1) return KVARN_ERR_INVALID_ARG;
+  kvarn_desc d;
+  d.head_dim = head_dim;
+  d.head_dim_padded = padded_dim(head_dim);
+  d.num_kv_heads = num_kv_heads;
+  d.tile_tokens = kTile;
+  d.k_bits = 4;
+  d.v_bits = 2;
+  d.sinkhorn_iters = 4;
+  d.sinkhorn_eps = 1e-6f;
+  d.page_record_bytes = record_layout(d.head_dim_padded).bytes;
+  *out = d;
+  return KVARN_OK;
+}
+
+int64_t kvarn_page_record_bytes(const kvarn_desc* desc) {
+  if (check_desc(desc) != KVARN_OK) return -1;
+  return desc->page_record_bytes;
+}
+
+int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, int64_t tok_stride,
+                         int64_t head_stride, int num_tiles, const int32_t* page_ids,
+                         void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
+                         void* stream) {
+  int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (num_tiles < 0) return KVARN_ERR_INVALID_ARG;
+  if (num_tiles == 0) return KVARN_OK;
+  if (k == nullptr || v == nullptr || page_ids == nullptr || page_pool == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(page_pool)) return KVARN_ERR_INVALID_ARG;
+  if (tok_stride <= 0 || head_stride < 0 || tok_stride % 8 != 0 || head_stride % 8 != 0)
+    return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1) return KVARN_ERR_INVALID_ARG;
+  if ((int64_t)num_tiles * desc->num_kv_heads * 2 > 0x7fffffffLL) return KVARN_ERR_INVALID_ARG;
+  QuantizeParams p{};
+  p.k = static_cast<const __half*>(k);
+  p.v = static_cast<const __half*>(v);
+  p.tok_stride = tok_stride;
+  p.head_stride = head_stride;
+  p.page_ids = page_ids;
+  p.pool = static_cast<uint8_t*>(page_pool);
+  p.num_pool_pages = num_pool_pages;
+  p.rec_bytes = desc->page_record_bytes;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.d0 = desc->head_dim;
+  p.iters = desc->sinkhorn_iters;
+  p.eps = desc->sinkhorn_eps;
+  p.status = dev_status;
+  p.append = 0;
+  return launch_quantize_any(desc->head_dim_padded, p, num_tiles * desc->num_kv_heads,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, const void* v_new,
+                       void* partial_k, void* partial_v, const int32_t* seq_lens,
+                       int32_t* seq_lens_out, const int32_t* block_table, int max_pages,
+                       void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
+                       void* stream) {
+  int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || max_pages < 1) return KVARN_ERR_INVALID_ARG;
+  if (batch == 0) return KVARN_OK;
+  if (k_new == nullptr || v_new == nullptr || partial_k == nullptr || partial_v == nullptr ||
+      seq_lens == nullptr || block_table == nullptr || page_pool == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(partial_k) || !aligned16(partial_v) ||
+      !aligned16(page_pool))
+    return KVARN_ERR_INVALID_ARG;
+  if (seq_lens_out != nullptr && static_cast<const void*>(seq_lens_out) == seq_lens)
+    return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1) return KVARN_ERR_INVALID_ARG;
+  QuantizeParams p{};
+  p.k_new = static_cast<const __half*>(k_new);
+  p.v_new = static_cast<const __half*>(v_new);
+  p.partial_k = static_cast<__half*>(partial_k);
+  p.partial_v = static_cast<__half*>(partial_v);
+  p.seq_lens = seq_lens;
+  p.seq_lens_out = seq_lens_out;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.pool = static_cast<uint8_t*>(page_pool);
+  p.num_pool_pages = num_pool_pages;
+  p.rec_bytes = desc->page_record_bytes;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.d0 = desc->head_dim;
+  p.iters = desc->sinkhorn_iters;
+  p.eps = desc->sinkhorn_eps;
+  p.status = dev_status;
+  p.append = 1;
+  return launch_quantize_any(desc->head_dim_padded, p, batch * desc->num_kv_heads,
+                             static_cast<cudaStream_t>(stream));
+}
+
+static int decode_pages_per_split(int max_pages) {
+  (void)max_pages;
+  return 16;
+}
+
+size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
+                                    int max_pages) {
+  if (check_desc(desc) != KVARN_OK || batch < 0 || num_q_heads < 1 || max_pages < 1) return 0;
+  const int pps = decode_pages_per_split(max_pages);
+  const int64_t max_splits = (max_pages + pps - 1) / pps + 1;
+  return (size_t)batch * num_q_heads * max_splits * (desc->head_dim_padded + 4) * sizeof(float);
+}
+
+int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                           const void* page_pool, int64_t num_pool_pages,
+                           const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                           const void* partial_k, const void* partial_v, float softmax_scale,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || num_q_heads < 1 || max_pages < 1) return KVARN_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return KVARN_ERR_UNSUPPORTED;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (!(group == 1 || group == 2 || group == 4 || group == 8)) return KVARN_ERR_UNSUPPORTED;
+  const int nt = group <= 4 ? 1 : 2;
+  if (nt == 2 && desc->head_dim_padded == 256) return KVARN_ERR_UNSUPPORTED;
+  if (batch == 0) return KVARN_OK;
+  if (q == nullptr || page_pool == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      out == nullptr || workspace == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(page_pool) || !aligned16(workspace)) return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1 || !(softmax_scale > 0.0f)) return KVARN_ERR_INVALID_ARG;
+  const size_t need = kvarn_decode_workspace_bytes(desc, batch, num_q_heads, max_pages);
+  if (workspace_bytes < need) return KVARN_ERR_WORKSPACE_TOO_SMALL;
+  const int pps = decode_pages_per_split(max_pages);
+  DecodeParams p{};
+  p.q = static_cast<const __half*>(q);
+  p.pool = static_cast<const uint8_t*>(page_pool);
+  p.num_pool_pages = num_pool_pages;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.seq_lens = seq_lens;
+  p.partial_k = static_cast<const __half*>(partial_k);
+  p.partial_v = static_cast<const __half*>(partial_v);
+  p.qscale = softmax_scale * kLog2e;
+  p.out = static_cast<__half*>(out);
+  p.part = static_cast<float*>(workspace);
+  p.batch = batch;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.group = group;
+  p.d0 = desc->head_dim;
+  p.pages_per_split = pps;
+  p.max_splits = (max_pages + pps - 1) / pps + 1;
+  p.status = dev_status;
+  return launch_decode_any(desc->head_dim_padded, nt, p, static_cast<cudaStream_t>(stream));
+}
+
+int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_t num_pool_pages,
+                           const int32_t* page_ids, int num_pages, void* k_out, void* v_out,
+                           int32_t* dev_status, void* stream) {
+  int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (num_pages < 0) return KVARN_ERR_INVALID_ARG;
+  if (num_pages == 0) return KVARN_OK;
+  if (page_pool == nullptr || page_ids == nullptr || k_out == nullptr || v_out == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1) return KVARN_ERR_INVALID_ARG;
+  DequantParams p{};
+  p.pool = static_cast<const uint8_t*>(page_pool);
+  p.num_pool_pages = num_pool_pages;
+  p.page_ids = page_ids;
+  p.k_out = static_cast<__half*>(k_out);
+  p.v_out = static_cast<__half*>(v_out);
+  p.num_kv_heads = desc->num_kv_heads;
+  p.d0 = desc->head_dim;
+  p.status = dev_status;
+  return launch_dequant_any(desc->head_dim_padded, p, num_pages, static_cast<cudaStream_t>(stream));
+}
+
+const char* kvarn_status_string(int status) {
+  switch (status) {
+    case KVARN_OK: return "ok";
+    case KVARN_ERR_INVALID_ARG: return "invalid argument (null pointer, size, stride or alignment)";
+    case KVARN_ERR_UNSUPPORTED: return "unsupported configuration (preset, head_dim, bits or GQA group)";
+    case KVARN_ERR_WORKSPACE_TOO_SMALL: return "decode workspace smaller than kvarn_decode_workspace_bytes";
+    case KVARN_ERR_CUDA: return "CUDA launch or attribute call failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

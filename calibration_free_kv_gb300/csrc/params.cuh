@@ -1,0 +1,69 @@
+// Launch parameters of the KVarN kernels, shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kvarn {
+
+struct QuantizeParams {
+  // tile mode
+  const __half* k;
+  const __half* v;
+  int64_t tok_stride;
+  int64_t head_stride;
+  const int32_t* page_ids;
+  // append mode
+  const __half* k_new;
+  const __half* v_new;
+  __half* partial_k;
+  __half* partial_v;
+  const int32_t* seq_lens;
+  int32_t* seq_lens_out;
+  const int32_t* block_table;
+  int max_pages;
+  // common
+  uint8_t* pool;
+  int64_t num_pool_pages;
+  int64_t rec_bytes;
+  int num_kv_heads;
+  int d0;
+  int iters;
+  float eps;
+  int32_t* status;
+  int append;  // 0: quantise whole tiles, 1: append one token and seal full tiles
+};
+
+struct DecodeParams {
+  const __half* q;
+  const uint8_t* pool;
+  int64_t num_pool_pages;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  const __half* partial_k;
+  const __half* partial_v;
+  float qscale;  // softmax_scale * log2(e)
+  __half* out;
+  float* part;   // [batch][Hq][max_splits][D + 4]: m, l, -, -, o~[D]
+  int batch, num_kv_heads, num_q_heads, group, d0;
+  int pages_per_split, max_splits;
+  int32_t* status;
+};
+
+struct DequantParams {
+  const uint8_t* pool;
+  int64_t num_pool_pages;
+  const int32_t* page_ids;
+  __half* k_out;
+  __half* v_out;
+  int num_kv_heads;
+  int d0;
+  int32_t* status;
+};
+
+int launch_quantize_any(int d, const QuantizeParams& p, int units, cudaStream_t stream);
+int launch_decode_any(int d, int nt, const DecodeParams& p, cudaStream_t stream);
+int launch_dequant_any(int d, const DequantParams& p, int num_pages, cudaStream_t stream);
+
+}  // namespace kvarn

@@ -1,0 +1,498 @@
+// KVarN tile quantisation: rotate, variance-normalise, round, fold, pack (sm_103a).
+//
+// One CTA quantises one (tile, kv head, K-or-V) unit of 128 tokens x d channels.
+//  1. rotate: every token row is zero-padded to d and multiplied by H_d / sqrt(d)
+//     [hotdry §Hadamard 旋转: FWHT, fused with the normalisation in one kernel]
+//  2. normalise: channel-std step then token-std step, `iters` times; the log-space factor
+//     updates of the pages telescope, so the kernel keeps the factors themselves
+//     (f_new = 1 / std of the un-normalised axis; unchanged when the std is below eps)
+//     [hotdry §迭代方差归一化; vatt §四個步驟, Sinkhorn paragraph]
+//  3. asymmetric RTN: K 4-bit per channel over tokens, V 2-bit per token over channels;
+//     normalisation factors folded into the fp16 scale/zero [hotdry §非对称量化与尺度折叠]
+//  4. codes packed as m16n8k16 A-operand fragments (layout in kvarn.h).
+//
+// Thread layout.  The unit is viewed as L x C: K has L = tokens, C = channels; V is held
+// transposed, L = channels, C = tokens.  Warp w owns L rows [32(w % NLQ), +32) and C columns
+// [64(w / NLQ), +64); lane (g = lane/4, tq = lane%4) owns L rows {g + 8l : l < 4} and C columns
+// {8u + 2tq + p : u < 8, p < 2} of that block (64 values).  In both K and V the quantisation
+// group runs along L, and each lane's values are exactly the code fragments it packs.
+#include "common.cuh"
+#include "params.cuh"
+
+namespace kvarn {
+
+template <int D>
+struct QuantShape {
+  static constexpr int kThreads = 2 * D;       // D/16 warps, 64 values per thread
+  static constexpr int kLd = D + 8;            // fp32 row stride of the staged tile
+  static constexpr int kSmemBytes = kTile * kLd * 4;
+};
+
+template <int N>
+__device__ __forceinline__ void fwht_regs(float (&v)[N]) {
+#pragma unroll
+  for (int h = 1; h < N; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], b = v[i + h];
+        v[i] = a + b;
+        v[i + h] = a - b;
+      }
+    }
+  }
+}
+
+// One reduce-scatter step across lanes `mask` apart, merging (sum, centred sum of squares)
+// pairs of equal count n with Chan's formula.  Keeps K/2 of the K pairs.
+template <int K>
+__device__ __forceinline__ void rs_chan(float (&s)[K], float (&m2)[K], int mask, bool up, float n) {
+#pragma unroll
+  for (int i = 0; i < K / 2; ++i) {
+    const float s_send = up ? s[i] : s[i + K / 2];
+    const float m_send = up ? m2[i] : m2[i + K / 2];
+    const float s_keep = up ? s[i + K / 2] : s[i];
+    const float m_keep = up ? m2[i + K / 2] : m2[i];
+    const float s_oth = __shfl_xor_sync(0xffffffffu, s_send, mask);
+    const float m_oth = __shfl_xor_sync(0xffffffffu, m_send, mask);
+    const float delta = (s_oth - s_keep) * (1.0f / n);
+    s[i] = s_keep + s_oth;
+    m2[i] = fmaf(delta * delta, 0.5f * n, m_keep + m_oth);
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void rs_minmax(float (&mn)[K], float (&mx)[K], int mask, bool up) {
+#pragma unroll
+  for (int i = 0; i < K / 2; ++i) {
+    const float a_send = up ? mn[i] : mn[i + K / 2];
+    const float b_send = up ? mx[i] : mx[i + K / 2];
+    const float a_keep = up ? mn[i + K / 2] : mn[i];
+    const float b_keep = up ? mx[i + K / 2] : mx[i];
+    mn[i] = fminf(a_keep, __shfl_xor_sync(0xffffffffu, a_send, mask));
+    mx[i] = fmaxf(b_keep, __shfl_xor_sync(0xffffffffu, b_send, mask));
+  }
+}
+
+__device__ __forceinline__ void chan_merge(float& s, float& m2, float s2, float m22, float n) {
+  const float delta = (s2 - s) * (1.0f / n);
+  s = s + s2;
+  m2 = fmaf(delta * delta, 0.5f * n, m2 + m22);
+}
+
+// New factor after one std step.  The log-space update ln f -= ln sigma (sigma = f_old * sd,
+// the std of the current normalised values) telescopes to f = 1 / sd; a std below eps has
+// nothing to normalise and the factor is kept.
+__device__ __forceinline__ float std_step_factor(float f_old, float m2, float inv_count,
+                                                 float eps) {
+  const float sd = sqrtf(fmaxf(m2 * inv_count, 0.0f));
+  const float sigma = f_old * sd;
+  return sigma >= eps ? __frcp_rn(sd) : f_old;
+}
+
+template <int D, bool TRANS>
+__device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, int64_t tok_stride,
+                                              int d0, uint8_t* __restrict__ rec, int iters,
+                                              float eps, float* smem) {
+  constexpr int NTH = QuantShape<D>::kThreads;
+  constexpr int LD = QuantShape<D>::kLd;
+  constexpr int LSIZE = TRANS ? D : kTile;
+  constexpr int CSIZE = TRANS ? kTile : D;
+  constexpr int NLQ = LSIZE / 32;
+  constexpr int NCH = CSIZE / 64;
+  constexpr int QMAX = TRANS ? 3 : 15;
+  constexpr RecordLayout RL = record_layout(D);
+  constexpr float kInvSqrtD = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const int lq = warp % NLQ, ch = warp / NLQ;
+
+  // ---- 1. stage the tile as fp32 and rotate every token row ---------------------------------
+  float* X = smem;
+  {
+    constexpr int CH8 = D / 8;
+    for (int idx = tid; idx < kTile * CH8; idx += NTH) {
+      const int t = idx / CH8, c8 = idx - t * CH8;
+      float v[8];
+      if (c8 * 8 < d0) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + t * tok_stride + c8 * 8));
+        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h2[e]);
+          v[2 * e] = f.x;
+          v[2 * e + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+      }
+      fwht_regs(v);
+      float4* dst = reinterpret_cast<float4*>(X + t * LD + c8 * 8);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    __syncthreads();
+    constexpr int NV = D / 8;
+    for (int idx = tid; idx < kTile * 8; idx += NTH) {
+      const int t = idx >> 3, c0 = idx & 7;
+      float v[NV];
+#pragma unroll
+      for (int k = 0; k < NV; ++k) v[k] = X[t * LD + c0 + 8 * k];
+      fwht_regs(v);
+#pragma unroll
+      for (int k = 0; k < NV; ++k) X[t * LD + c0 + 8 * k] = v[k];
+    }
+    __syncthreads();
+  }
+
+  float x[4][16];
+#pragma unroll
+  for (int l = 0; l < 4; ++l) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (!TRANS) {
+        const int tok = 32 * lq + g + 8 * l, c = 64 * ch + 8 * u + 2 * tq;
+        const float2 f = *reinterpret_cast<const float2*>(X + tok * LD + c);
+        x[l][2 * u] = f.x * kInvSqrtD;
+        x[l][2 * u + 1] = f.y * kInvSqrtD;
+      } else {
+        const int chn = 32 * lq + g + 8 * l, tok = 64 * ch + 8 * u + 2 * tq;
+        x[l][2 * u] = X[tok * LD + chn] * kInvSqrtD;
+        x[l][2 * u + 1] = X[(tok + 1) * LD + chn] * kInvSqrtD;
+      }
+    }
+  }
+  __syncthreads();  // the staged tile is dead; its shared memory becomes reduction scratch
+
+  float2* redL = reinterpret_cast<float2*>(smem);          // [NLQ][CSIZE]
+  float2* redC = redL + NLQ * CSIZE;                         // [NCH][LSIZE]
+  float* fLs = reinterpret_cast<float*>(redC + NCH * LSIZE);  // [LSIZE]
+  float* fCs = fLs + LSIZE;                                   // [CSIZE]
+  float* qmS = fCs + CSIZE;                                   // [CSIZE]
+  float* qiS = qmS + CSIZE;                                   // [CSIZE]
+
+  // Registers hold each lane's 4 L factors and 16 C factors; fLs / fCs in shared memory are
+  // the canonical copies, updated by one designated thread per row / column.
+  float fL[4], fC[16];
+#pragma unroll
+  for (int l = 0; l < 4; ++l) fL[l] = 1.0f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) fC[c] = 1.0f;
+  for (int i = tid; i < LSIZE; i += NTH) fLs[i] = 1.0f;
+  for (int i = tid; i < CSIZE; i += NTH) fCs[i] = 1.0f;
+  __syncthreads();
+
+  // Lane's final column pair after the reduce-scatter over g, and its final row after the
+  // reduce-scatter over tq.
+  const int c_col = 64 * ch + 8 * g + 2 * tq;                // columns c_col, c_col + 1
+  const int l_fin = 2 * (tq & 1) + (tq >> 1);
+  const int l_row = 32 * lq + g + 8 * l_fin;
+
+  // std over L of each C column -> new C factors.
+  auto update_c = [&]() {
+    float s[16], m2[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float y0 = x[0][c] * fL[0], y1 = x[1][c] * fL[1];
+      const float y2 = x[2][c] * fL[2], y3 = x[3][c] * fL[3];
+      const float sum = (y0 + y1) + (y2 + y3);
+      const float mu = sum * 0.25f;
+      const float d0_ = y0 - mu, d1 = y1 - mu, d2 = y2 - mu, d3 = y3 - mu;
+      s[c] = sum;
+      m2[c] = fmaf(d0_, d0_, d1 * d1) + fmaf(d2, d2, d3 * d3);
+    }
+    float s8[8], m8[8], s4[4], m4[4], s2[2], m22[2];
+    rs_chan<16>(s, m2, 16, (lane & 16) != 0, 4.0f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { s8[i] = s[i]; m8[i] = m2[i]; }
+    rs_chan<8>(s8, m8, 8, (lane & 8) != 0, 8.0f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { s4[i] = s8[i]; m4[i] = m8[i]; }
+    rs_chan<4>(s4, m4, 4, (lane & 4) != 0, 16.0f);
+    s2[0] = s4[0]; s2[1] = s4[1]; m22[0] = m4[0]; m22[1] = m4[1];
+    *reinterpret_cast<float4*>(&redL[lq * CSIZE + c_col]) = make_float4(s2[0], m22[0], s2[1], m22[1]);
+    __syncthreads();
+    if (lq == 0) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float ps[NLQ], pm[NLQ];
+#pragma unroll
+        for (int q = 0; q < NLQ; ++q) {
+          const float2 v = redL[q * CSIZE + c_col + e];
+          ps[q] = v.x;
+          pm[q] = v.y;
+        }
+        float n = 32.0f;
+#pragma unroll
+        for (int w = 1; w < NLQ; w <<= 1) {
+#pragma unroll
+          for (int q = 0; q + w < NLQ; q += 2 * w) chan_merge(ps[q], pm[q], ps[q + w], pm[q + w], n);
+          n *= 2.0f;
+        }
+        fCs[c_col + e] = std_step_factor(fCs[c_col + e], pm[0], 1.0f / LSIZE, eps);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float2 f = *reinterpret_cast<const float2*>(&fCs[64 * ch + 8 * u + 2 * tq]);
+      fC[2 * u] = f.x;
+      fC[2 * u + 1] = f.y;
+    }
+  };
+
+  // std over C of each L row -> new L factors.
+  auto update_l = [&]() {
+    float s[4], m2[4];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      float y[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) y[c] = x[l][c] * fC[c];
+      float t8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t8[i] = y[2 * i] + y[2 * i + 1];
+      const float sum = ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
+      const float mu = sum * (1.0f / 16.0f);
+      float a = 0.0f, b = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2) {
+        const float d0_ = y[c] - mu, d1 = y[c + 1] - mu;
+        a = fmaf(d0_, d0_, a);
+        b = fmaf(d1, d1, b);
+      }
+      s[l] = sum;
+      m2[l] = a + b;
+    }
+    float s2[2], m22[2];
+    rs_chan<4>(s, m2, 1, (lane & 1) != 0, 16.0f);
+    s2[0] = s[0]; s2[1] = s[1]; m22[0] = m2[0]; m22[1] = m2[1];
+    rs_chan<2>(s2, m22, 2, (lane & 2) != 0, 32.0f);
+    redC[ch * LSIZE + l_row] = make_float2(s2[0], m22[0]);
+    __syncthreads();
+    if (ch == 0) {
+      float ps[NCH], pm[NCH];
+#pragma unroll
+      for (int q = 0; q < NCH; ++q) {
+        const float2 v = redC[q * LSIZE + l_row];
+        ps[q] = v.x;
+        pm[q] = v.y;
+      }
+      float n = 64.0f;
+#pragma unroll
+      for (int w = 1; w < NCH; w <<= 1) {
+#pragma unroll
+        for (int q = 0; q + w < NCH; q += 2 * w) chan_merge(ps[q], pm[q], ps[q + w], pm[q + w], n);
+        n *= 2.0f;
+      }
+      fLs[l_row] = std_step_factor(fLs[l_row], pm[0], 1.0f / CSIZE, eps);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int l = 0; l < 4; ++l) fL[l] = fLs[32 * lq + g + 8 * l];
+  };
+
+  // ---- 2. variance normalisation: channel-std step, then token-std step -------------------
+  for (int it = 0; it < iters; ++it) {
+    if (!TRANS) {  // K: channels are C, tokens are L
+      update_c();
+      update_l();
+    } else {       // V: channels are L, tokens are C
+      update_l();
+      update_c();
+    }
+  }
+
+  // ---- 3. per-column (along L) min / max of N = x fL fC, scale, zero-point ----------------
+  {
+    float mn[16], mx[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      float a = __fmul_rn(__fmul_rn(x[0][c], fL[0]), fC[c]);
+      float b = a;
+#pragma unroll
+      for (int l = 1; l < 4; ++l) {
+        const float nv = __fmul_rn(__fmul_rn(x[l][c], fL[l]), fC[c]);
+        a = fminf(a, nv);
+        b = fmaxf(b, nv);
+      }
+      mn[c] = a;
+      mx[c] = b;
+    }
+    float mn8[8], mx8[8], mn4[4], mx4[4];
+    rs_minmax<16>(mn, mx, 16, (lane & 16) != 0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { mn8[i] = mn[i]; mx8[i] = mx[i]; }
+    rs_minmax<8>(mn8, mx8, 8, (lane & 8) != 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { mn4[i] = mn8[i]; mx4[i] = mx8[i]; }
+    rs_minmax<4>(mn4, mx4, 4, (lane & 4) != 0);
+    *reinterpret_cast<float4*>(&redL[lq * CSIZE + c_col]) = make_float4(mn4[0], mx4[0], mn4[1], mx4[1]);
+    __syncthreads();
+    __half* scale_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vscale : RL.kscale));
+    __half* zero_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vzero : RL.kzero));
+    if (lq == 0) {
+      float sc[2], ze[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float m = redL[c_col + e].x, M = redL[c_col + e].y;
+#pragma unroll
+        for (int q = 1; q < NLQ; ++q) {
+          m = fminf(m, redL[q * CSIZE + c_col + e].x);
+          M = fmaxf(M, redL[q * CSIZE + c_col + e].y);
+        }
+        const float s = fmaxf(__fdiv_rn(__fsub_rn(M, m), (float)QMAX), 1e-8f);
+        qmS[c_col + e] = m;
+        qiS[c_col + e] = __frcp_rn(s);
+        // folded: s' = s * (1/fC), z' = m * (1/fC)
+        sc[e] = __fdiv_rn(s, fCs[c_col + e]);
+        ze[e] = __fdiv_rn(m, fCs[c_col + e]);
+      }
+      *reinterpret_cast<__half2*>(&scale_out[c_col]) = __floats2half2_rn(sc[0], sc[1]);
+      *reinterpret_cast<__half2*>(&zero_out[c_col]) = __floats2half2_rn(ze[0], ze[1]);
+    }
+    __syncthreads();
+  }
+
+  // token / channel factor of the L axis: r = 1/fL (K) or c = 1/fL (V)
+  {
+    __half* fac_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vfactor : RL.kfactor));
+    if (ch == 0) fac_out[l_row] = __float2half_rn(__frcp_rn(fLs[l_row]));
+  }
+
+  // ---- 4. codes, packed as mma fragments -----------------------------------------------------
+  uint32_t code[4][16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int col = 64 * ch + 8 * (c >> 1) + 2 * tq + (c & 1);
+    const float m = qmS[col], inv = qiS[col];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const float nv = __fmul_rn(__fmul_rn(x[l][c], fL[l]), fC[c]);
+      const float v = __fmul_rn(__fsub_rn(nv, m), inv);
+      const uint32_t q = __float_as_uint(__fadd_rn(v, 12582912.0f)) - 0x4B400000u;
+      code[l][c] = min(q, (uint32_t)QMAX);
+    }
+  }
+  if (!TRANS) {
+    uint8_t* kc = rec + RL.kcodes;
+#pragma unroll
+    for (int lh = 0; lh < 2; ++lh) {
+      uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+          for (int rho = 0; rho < 2; ++rho) {
+            const int nib = (u & 1) + 2 * rho + 4 * p;
+            w[u >> 1] |= code[2 * lh + rho][2 * u + p] << (4 * nib);
+          }
+      const int mi = 2 * lq + lh;
+      *reinterpret_cast<uint4*>(kc + ((mi * (D / 64) + ch) * 32 + lane) * 16) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+    for (int uh = 0; uh < 2; ++uh) {
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh)
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int u = 4 * uh + uu;
+#pragma unroll
+          for (int p = 0; p < 2; ++p)
+#pragma unroll
+            for (int rho = 0; rho < 2; ++rho) {
+              const int slot = 2 * ((u >> 1) & 1) + (u & 1) + 4 * rho + 8 * p;
+              w[lh] |= code[2 * lh + rho][2 * u + p] << (2 * slot);
+            }
+        }
+      const int ks2 = 2 * ch + uh;
+      *reinterpret_cast<uint2*>(vc + (((ks2 * (D / 64) + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
+          make_uint2(w[0], w[1]);
+    }
+  }
+}
+
+// ---- kernels --------------------------------------------------------------------------------
+
+
+// grid.x = units * 2 (K and V of one (tile or sequence, kv head)), block = 2*D threads.
+template <int D>
+__global__ void __launch_bounds__(QuantShape<D>::kThreads)
+    quantize_kernel(QuantizeParams p) {
+  extern __shared__ __align__(16) float smem_q[];
+  const int unit = blockIdx.x >> 1;
+  const bool is_v = (blockIdx.x & 1) != 0;
+  const int h = unit % p.num_kv_heads;
+  const int tile = unit / p.num_kv_heads;
+
+  const __half* src;
+  int64_t tok_stride;
+  int64_t page;
+  if (!p.append) {
+    src = (is_v ? p.v : p.k) + (int64_t)tile * kTile * p.tok_stride + (int64_t)h * p.head_stride;
+    tok_stride = p.tok_stride;
+    page = p.page_ids[tile];
+  } else {
+    // append: tile == sequence index b
+    const int b = tile;
+    const int len = p.seq_lens[b];
+    const int cap = p.max_pages * kTile;
+    if (len < 0 || len >= cap) {
+      if (threadIdx.x == 0 && !is_v && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
+      return;
+    }
+    const int row = len % kTile;
+    __half* part = (is_v ? p.partial_v : p.partial_k) + ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
+    const __half* nw = (is_v ? p.v_new : p.k_new) + ((int64_t)b * p.num_kv_heads + h) * p.d0;
+    for (int c = threadIdx.x * 8; c < p.d0; c += blockDim.x * 8)
+      *reinterpret_cast<uint4*>(part + row * p.d0 + c) = *reinterpret_cast<const uint4*>(nw + c);
+    if (threadIdx.x == 0 && !is_v && h == 0 && p.seq_lens_out != nullptr) p.seq_lens_out[b] = len + 1;
+    if (row != kTile - 1) return;
+    __syncthreads();  // the new row is visible to the whole block
+    src = part;
+    tok_stride = p.d0;
+    page = p.block_table[(int64_t)b * p.max_pages + len / kTile];
+  }
+  if (page < 0 || page >= p.num_pool_pages) {
+    if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
+    return;
+  }
+  uint8_t* rec = p.pool + (page * p.num_kv_heads + h) * p.rec_bytes;
+  if (is_v)
+    quantize_unit<D, true>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
+  else
+    quantize_unit<D, false>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
+}
+
+template <int D>
+static int launch_quantize(const QuantizeParams& p, int units, cudaStream_t stream) {
+  constexpr int kSmem = QuantShape<D>::kSmemBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(quantize_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem) != cudaSuccess)
+      return KVARN_ERR_CUDA;
+    attr_set = true;
+  }
+  quantize_kernel<D><<<units * 2, QuantShape<D>::kThreads, kSmem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
+int launch_quantize_any(int d, const QuantizeParams& p, int units, cudaStream_t stream) {
+  if (units <= 0) return KVARN_OK;
+  switch (d) {
+    case 64: return launch_quantize<64>(p, units, stream);
+    case 128: return launch_quantize<128>(p, units, stream);
+    case 256: return launch_quantize<256>(p, units, stream);
+    default: return KVARN_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace kvarn

@@ -1,0 +1,197 @@
+"""ctypes binding of libkvarn.so: argument marshalling only.
+
+Every function forwards torch tensors (device memory) to the C ABI declared in
+include/kvarn.h and raises KvarnError on a non-zero status.  All arithmetic runs in
+the library's CUDA kernels; there is no CPU or PyTorch fallback.  Importing this module
+loads the library and raises if it has not been built (see ``build.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvarn.so")
+
+KVARN_OK = 0
+KVARN_ERR_INVALID_ARG = -1
+KVARN_ERR_UNSUPPORTED = -2
+KVARN_ERR_WORKSPACE_TOO_SMALL = -3
+KVARN_ERR_CUDA = -4
+DEV_BAD_PAGE_ID = 1
+DEV_SEQ_TOO_LONG = 2
+DEV_WAIT_TIMEOUT = 4
+DEV_NO_PARTIAL = 8
+
+EXPORTED_SYMBOLS = (
+    "kvarn_desc_from_preset",
+    "kvarn_page_record_bytes",
+    "kvarn_quantize_tiles",
+    "kvarn_append_token",
+    "kvarn_decode_workspace_bytes",
+    "kvarn_decode_attention",
+    "kvarn_dequantize_tiles",
+    "kvarn_status_string",
+)
+
+
+class KvarnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (where, status_string(status), status))
+
+
+class KvarnDesc(ctypes.Structure):
+    _fields_ = [
+        ("head_dim", ctypes.c_int32),
+        ("head_dim_padded", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("tile_tokens", ctypes.c_int32),
+        ("k_bits", ctypes.c_int32),
+        ("v_bits", ctypes.c_int32),
+        ("sinkhorn_iters", ctypes.c_int32),
+        ("sinkhorn_eps", ctypes.c_float),
+        ("page_record_bytes", ctypes.c_int64),
+    ]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError("libkvarn.so is not built (run calibration_free_kv_gb300.build.build() "
+                          "or __graft_entry__.build()); there is no fallback path")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    i32, i64 = ctypes.c_int, ctypes.c_int64
+    D = ctypes.POINTER(KvarnDesc)
+    sig = {
+        "kvarn_desc_from_preset": (i32, [ctypes.c_char_p, i32, i32, D]),
+        "kvarn_page_record_bytes": (i64, [D]),
+        "kvarn_quantize_tiles": (i32, [D, P, P, i64, i64, i32, P, P, i64, P, P]),
+        "kvarn_append_token": (i32, [D, i32, P, P, P, P, P, P, P, i32, P, i64, P, P]),
+        "kvarn_decode_workspace_bytes": (ctypes.c_size_t, [D, i32, i32, i32]),
+        "kvarn_decode_attention": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P, ctypes.c_float,
+                                         P, P, ctypes.c_size_t, P, P]),
+        "kvarn_dequantize_tiles": (i32, [D, P, i64, P, i32, P, P, P, P]),
+        "kvarn_status_string": (ctypes.c_char_p, [i32]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def status_string(status: int) -> str:
+    return _lib.kvarn_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != KVARN_OK:
+        raise KvarnError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype, name):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s" % (name, dtype))
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def desc_from_preset(head_dim: int, num_kv_heads: int, preset: str = "kvarn_k4v2_g128",
+                     sinkhorn_iters: int | None = None) -> KvarnDesc:
+    d = KvarnDesc()
+    _check(_lib.kvarn_desc_from_preset(preset.encode(), int(head_dim), int(num_kv_heads),
+                                       ctypes.byref(d)), "kvarn_desc_from_preset")
+    if sinkhorn_iters is not None:
+        d.sinkhorn_iters = int(sinkhorn_iters)
+    return d
+
+
+def page_record_bytes(desc: KvarnDesc) -> int:
+    return int(_lib.kvarn_page_record_bytes(ctypes.byref(desc)))
+
+
+def alloc_pool(desc: KvarnDesc, num_pages: int, device="cuda") -> torch.Tensor:
+    """A page pool tensor [num_pages, Hkv, record_bytes] of uint8 (caller-owned memory)."""
+    return torch.zeros((num_pages, desc.num_kv_heads, desc.page_record_bytes), dtype=torch.uint8,
+                       device=device)
+
+
+def quantize_tiles(desc: KvarnDesc, k: torch.Tensor, v: torch.Tensor, page_ids: torch.Tensor,
+                   pool: torch.Tensor, status: torch.Tensor | None = None, stream=None):
+    """k, v: fp16 [tokens, Hkv, d0] (token and head strides taken from the tensors)."""
+    _dev(k, torch.float16, "k")
+    _dev(v, torch.float16, "v")
+    _dev(page_ids, torch.int32, "page_ids")
+    if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 3 or k.stride(2) != 1:
+        raise ValueError("k and v must be [tokens, Hkv, d0] with matching strides, channels contiguous")
+    num_tiles = k.shape[0] // 128
+    if page_ids.numel() < num_tiles:
+        raise ValueError("page_ids shorter than the number of tiles")
+    _check(_lib.kvarn_quantize_tiles(ctypes.byref(desc), _ptr(k), _ptr(v), k.stride(0), k.stride(1),
+                                     num_tiles, _ptr(page_ids), _ptr(pool), pool.shape[0],
+                                     _ptr(status), _stream(stream)), "kvarn_quantize_tiles")
+
+
+def append_token(desc: KvarnDesc, k_new, v_new, partial_k, partial_v, seq_lens, block_table, pool,
+                 seq_lens_out=None, status=None, stream=None):
+    batch = seq_lens.shape[0]
+    _check(_lib.kvarn_append_token(ctypes.byref(desc), batch, _ptr(k_new), _ptr(v_new),
+                                   _ptr(partial_k), _ptr(partial_v), _ptr(seq_lens),
+                                   _ptr(seq_lens_out), _ptr(block_table), block_table.shape[1],
+                                   _ptr(pool), pool.shape[0], _ptr(status), _stream(stream)),
+           "kvarn_append_token")
+
+
+def decode_workspace_bytes(desc: KvarnDesc, batch: int, num_q_heads: int, max_pages: int) -> int:
+    return int(_lib.kvarn_decode_workspace_bytes(ctypes.byref(desc), batch, num_q_heads, max_pages))
+
+
+def alloc_workspace(desc: KvarnDesc, batch: int, num_q_heads: int, max_pages: int, device="cuda"):
+    n = decode_workspace_bytes(desc, batch, num_q_heads, max_pages)
+    return torch.empty((max(n, 16) + 15) // 16 * 4, dtype=torch.float32, device=device)
+
+
+def decode_attention(desc: KvarnDesc, q, pool, block_table, seq_lens, out, workspace,
+                     partial_k=None, partial_v=None, softmax_scale=None, status=None, stream=None):
+    """q, out: fp16 [batch, Hq, d0]; seq_lens: int32 [batch] total lengths."""
+    batch, hq, d0 = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d0)
+    _check(_lib.kvarn_decode_attention(ctypes.byref(desc), batch, hq, _ptr(q), _ptr(pool),
+                                       pool.shape[0], _ptr(block_table), block_table.shape[1],
+                                       _ptr(seq_lens), _ptr(partial_k), _ptr(partial_v),
+                                       float(softmax_scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _ptr(status), _stream(stream)), "kvarn_decode_attention")
+
+
+def dequantize_tiles(desc: KvarnDesc, pool, page_ids, k_out, v_out, status=None, stream=None):
+    _check(_lib.kvarn_dequantize_tiles(ctypes.byref(desc), _ptr(pool), pool.shape[0],
+                                       _ptr(page_ids), page_ids.numel(), _ptr(k_out), _ptr(v_out),
+                                       _ptr(status), _stream(stream)), "kvarn_dequantize_tiles")

@@ -1,0 +1,159 @@
+/*
+ * kvarn.h -- C ABI of the KVarN K4V2 g128 KV-cache path for GB300 (sm_103a).
+ *
+ * What is computed (sources cited by page title and section):
+ *  - [hotdry]  blog.hotdry.top "KVarN Hadamard 旋转与方差归一化：KV-cache 量化的校准算法实现"
+ *  - [aifeeds] ai-feeds.com "KVarN: 方差归一化的KV-Cache量化缓解推理任务中的误差累积"
+ *  - [vatt]    vatt-ghern.pages.dev "KV cache 為什麼能壓到 4-bit／2-bit 還不掉準確度——從
+ *              variance normalization 講起"
+ *
+ * Every 128-token tile of every KV head is (1) zero-padded along head_dim to the next power of
+ * two d [aifeeds §局限], (2) rotated along head_dim by the orthonormal Sylvester Hadamard
+ * H_d / sqrt(d) [hotdry §Hadamard 旋转], (3) variance-normalised by alternating channel-std and
+ * token-std steps whose factors live in log space, for a fixed iteration count [hotdry
+ * §迭代方差归一化; vatt §四個步驟], (4) quantised by asymmetric round-to-nearest, keys to 4 bits
+ * per channel and values to 2 bits per token, with the normalisation factors folded into the
+ * stored fp16 scales [hotdry §非对称量化与尺度折叠].  Decode attention reads the packed cache
+ * directly [vatt §怎麼用: one paged-attention block == one tile; attention computed in fp16
+ * over the quantised cache].
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library allocates
+ *    nothing, keeps no per-call state, never synchronises and launches on `stream`
+ *    (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *  - fp16 means IEEE binary16; all tensors are little-endian and row-major.
+ *  - Return value: KVARN_OK (0) or a negative KVARN_ERR_* code.  Argument errors are found
+ *    on the host before any launch.  Errors that depend on device data (a page id outside
+ *    the pool, a seq_len above the block-table capacity, a copy that did not arrive) are
+ *    OR-ed as KVARN_DEV_* bits into *dev_status when dev_status is non-NULL (a device
+ *    int32 the caller zeroes and reads); the kernels then clamp to in-bounds data and
+ *    never trap.
+ *  - head_dim d0: 8..256 and a multiple of 8; it is padded to d = 64, 128 or 256.
+ *  - GQA: query head hq reads KV head hq / G, G = num_q_heads / num_kv_heads in {1,2,4,8}.
+ *
+ * Page record: the packed K/V of one (page, kv head), record_bytes(d) bytes, 16-byte aligned
+ * sections.  The page pool is [num_pool_pages][num_kv_heads][record_bytes]; record (p, h)
+ * starts at byte ((p * num_kv_heads) + h) * record_bytes.  With T = 128:
+ *    K codes  T*d/2 B   uint32 words of eight 4-bit codes
+ *    V codes  T*d/4 B   uint32 words of sixteen 2-bit codes
+ *    K scale s'[d], K zero z'[d], K token factor r[T],
+ *    V scale s'[T], V zero z'[T], V channel factor c[d]          (fp16)
+ * Dequantised rotated-domain values: K~[t][j] = r[t] (code*s'[j] + z'[j]),
+ * V~[t][j] = c[j] (code*s'[t] + z'[t]); original basis = rows of (.) H_d / sqrt(d), first d0.
+ * K word (mi, kk, lane) [mi < 8, kk < d/16, lane < 32, g = lane/4, tq = lane%4] is word
+ * ((mi*(d/64) + kk/4)*32 + lane)*4 + kk%4; it holds token 16mi + g + 8rho, channel
+ * 16kk + 8h + 2tq + p at nibble h + 2rho + 4p (rho, h, p in {0,1}).
+ * V word (ks2, mc, lane) [ks2 < 4, mc < d/16] is word ((ks2*(d/64) + mc/4)*32 + lane)*4 + mc%4;
+ * it holds channel 16mc + g + 8rho, token 16(2ks2 + f) + 8h + 2tq + p at 2-bit slot
+ * 2f + h + 4rho + 8p.  (Each word is an m16n8k16 A-operand fragment: K as [token x channel],
+ * V transposed as [channel x token].)  record_bytes = 13824 at d = 128, 26880 at d = 256.
+ */
+#ifndef KVARN_H
+#define KVARN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVARN_OK 0
+#define KVARN_ERR_INVALID_ARG (-1)          /* NULL pointer, bad size/stride/alignment      */
+#define KVARN_ERR_UNSUPPORTED (-2)          /* preset, head_dim, bits, tile or GQA group    */
+#define KVARN_ERR_WORKSPACE_TOO_SMALL (-3)  /* decode workspace below the required size     */
+#define KVARN_ERR_CUDA (-4)                 /* a CUDA launch or attribute call failed       */
+
+#define KVARN_DEV_BAD_PAGE_ID 1      /* a page id outside [0, num_pool_pages): page 0 used   */
+#define KVARN_DEV_SEQ_TOO_LONG 2     /* seq_len < 0, or its pages exceed the block table row  */
+#define KVARN_DEV_WAIT_TIMEOUT 4     /* an asynchronous page copy did not arrive in ~2 s     */
+#define KVARN_DEV_NO_PARTIAL 8       /* a length has a remainder but partial_k/v were NULL   */
+
+/* Method constants of one cache.  Fill it with kvarn_desc_from_preset. */
+typedef struct kvarn_desc {
+  int32_t head_dim;          /* d0, true head_dim                                   */
+  int32_t head_dim_padded;   /* d = 64, 128 or 256                                  */
+  int32_t num_kv_heads;      /* Hkv                                                 */
+  int32_t tile_tokens;       /* 128 (one tile == one page) [vatt §怎麼用 knob table]  */
+  int32_t k_bits;            /* 4                                                   */
+  int32_t v_bits;            /* 2                                                   */
+  int32_t sinkhorn_iters;    /* 4 (0..8 accepted)                                   */
+  float sinkhorn_eps;        /* 1e-6, floor of a std before its log                 */
+  int64_t page_record_bytes; /* bytes of one (page, kv head) record                 */
+} kvarn_desc;
+
+/* Fill *out for preset "kvarn_k4v2_g128" [hotdry §核心配置参数: kv_cache_dtype
+ * kvarn_k4v2_g128, block_size 128].  Host only.  UNSUPPORTED for another preset or a
+ * head_dim outside 8..256 / not a multiple of 8; INVALID_ARG for NULL or Hkv < 1. */
+int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, kvarn_desc* out);
+
+/* Bytes of one page record for this descriptor (host only). */
+int64_t kvarn_page_record_bytes(const kvarn_desc* desc);
+
+/* Quantise whole 128-token tiles into page records [hotdry §Hadamard 旋转 to
+ * §非对称量化与尺度折叠].
+ *  k, v        fp16; element (token t, kv head h, channel c < d0) at [t*tok_stride +
+ *              h*head_stride + c]; tile i covers tokens 128i .. 128i+127.  Base 16-byte
+ *              aligned, tok_stride and head_stride multiples of 8 (elements).
+ *  page_ids    device int32 [num_tiles]: tile i is written to record (page_ids[i], h).
+ *  page_pool   device, num_pool_pages pages (see the layout above); written.
+ * num_tiles == 0 is a no-op. */
+int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, int64_t tok_stride,
+                         int64_t head_stride, int num_tiles, const int32_t* page_ids,
+                         void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
+                         void* stream);
+
+/* Append one decode token per sequence and seal full tiles (tile filling implied by paging:
+ * vatt §怎麼用, one block == one tile).
+ *  k_new, v_new          fp16 [batch][Hkv][d0].
+ *  partial_k, partial_v  fp16 [batch][Hkv][128][d0]: the unsealed tile of each sequence.
+ *  seq_lens              device int32 [batch], length BEFORE this token, < max_pages*128
+ *                        (else the sequence is skipped and flagged).  The token goes to
+ *                        row seq_lens[b] % 128 of the partial tile; when that row is 127 the
+ *                        tile is quantised into record (block_table[b][seq_lens[b]/128], h),
+ *                        bit-identical to kvarn_quantize_tiles on the same 128 tokens.
+ *  seq_lens_out          device int32 [batch] or NULL: receives seq_lens[b] + 1.  Must not
+ *                        alias seq_lens.
+ *  block_table           device int32 [batch][max_pages]. */
+int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, const void* v_new,
+                       void* partial_k, void* partial_v, const int32_t* seq_lens,
+                       int32_t* seq_lens_out, const int32_t* block_table, int max_pages,
+                       void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
+                       void* stream);
+
+/* Workspace bytes kvarn_decode_attention needs for this batch shape (host only). */
+size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
+                                    int max_pages);
+
+/* One decode step of attention over the packed cache [vatt §一次 16K context…: decode reads
+ * the whole cache each step; §四個步驟: the rotation keeps q.k unchanged].
+ *  q            fp16 [batch][Hq][d0] (one query per sequence and head).
+ *  block_table  device int32 [batch][max_pages], seq_lens device int32 [batch]: TOTAL length,
+ *               i.e. seq_lens[b]/128 sealed pages plus seq_lens[b]%128 raw tokens in the
+ *               partial tile; seq_lens[b]/128 <= max_pages (else clamped and flagged).  partial_k/partial_v may be NULL only if no length has a
+ *               remainder.
+ *  softmax_scale  tau in softmax(tau q.k).
+ *  out          fp16 [batch][Hq][d0]; a sequence of length 0 gives zeros.
+ *  workspace    device scratch of at least kvarn_decode_workspace_bytes (16-byte aligned). */
+int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                           const void* page_pool, int64_t num_pool_pages,
+                           const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                           const void* partial_k, const void* partial_v, float softmax_scale,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream);
+
+/* Dequantise page records back to fp16 K/V in the original basis [hotdry
+ * §非对称量化与尺度折叠: scales multiplied back at read].
+ *  page_ids  device int32 [num_pages]; k_out, v_out fp16 [num_pages][Hkv][128][d0]. */
+int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_t num_pool_pages,
+                           const int32_t* page_ids, int num_pages, void* k_out, void* v_out,
+                           int32_t* dev_status, void* stream);
+
+/* Static description of a KVARN_OK / KVARN_ERR_* code. */
+const char* kvarn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H */

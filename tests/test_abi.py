@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads and exports every symbol kvarn.h declares (CPU only).
+
+Only host-side entry points are called here (descriptor, sizes, status strings and the
+argument validation that returns before any CUDA call).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kv():
+    from calibration_free_kv_gb300 import build
+    build.build()
+    from calibration_free_kv_gb300 import kvarn
+    return kvarn
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "kvarn.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvarn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("kvarn_quantize_tiles", "kvarn_append_token", "kvarn_decode_attention",
+                     "kvarn_dequantize_tiles"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(kv):
+    lib = ctypes.CDLL(kv.library_path())
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) <= set(kv.EXPORTED_SYMBOLS) | set()
+
+
+def test_preset_descriptor(kv):
+    d = kv.desc_from_preset(128, 8)
+    assert (d.head_dim, d.head_dim_padded, d.num_kv_heads) == (128, 128, 8)
+    assert (d.tile_tokens, d.k_bits, d.v_bits, d.sinkhorn_iters) == (128, 4, 2, 4)
+    assert d.page_record_bytes == 13824 == kv.page_record_bytes(d)
+    assert kv.desc_from_preset(96, 8).head_dim_padded == 128
+    assert kv.desc_from_preset(256, 4).page_record_bytes == 26880
+
+
+def test_record_bytes_match_oracle(kv):
+    from oracle import kvarn_oracle as ko
+    for d0 in (64, 96, 128, 200, 256):
+        desc = kv.desc_from_preset(d0, 2)
+        assert desc.page_record_bytes == ko.record_bytes(ko.padded_head_dim(d0))
+
+
+def test_preset_rejections(kv):
+    with pytest.raises(kv.KvarnError) as e:
+        kv.desc_from_preset(128, 8, preset="kvarn_k2v2_g64")
+    assert e.value.status == kv.KVARN_ERR_UNSUPPORTED
+    for bad in (0, 7, 100, 264):
+        with pytest.raises(kv.KvarnError):
+            kv.desc_from_preset(bad, 8)
+
+
+def test_workspace_size(kv):
+    d = kv.desc_from_preset(128, 8)
+    n = kv.decode_workspace_bytes(d, 64, 32, 128)
+    splits = (128 + 15) // 16 + 1
+    assert n == 64 * 32 * splits * (128 + 4) * 4
+
+
+def test_validation_returns_before_launch(kv):
+    lib = kv._lib
+    d = kv.desc_from_preset(128, 8)
+    null = ctypes.c_void_p(0)
+    st = lib.kvarn_quantize_tiles(ctypes.byref(d), null, null, 1024, 128, 4, null, null, 8, null, null)
+    assert st == kv.KVARN_ERR_INVALID_ARG
+    assert lib.kvarn_quantize_tiles(ctypes.byref(d), null, null, 1024, 128, 0, null, null, 8, null,
+                                    null) == kv.KVARN_OK
+    # G = 3 is not a supported group size
+    st = lib.kvarn_decode_attention(ctypes.byref(d), 2, 24, null, null, 8, null, 4, null, null, null,
+                                    ctypes.c_float(0.1), null, null, 0, null, null)
+    assert st == kv.KVARN_ERR_UNSUPPORTED
+    st = lib.kvarn_decode_attention(ctypes.byref(d), 2, 32, ctypes.c_void_p(16), ctypes.c_void_p(16), 8,
+                                    ctypes.c_void_p(16), 4, ctypes.c_void_p(16), null, null,
+                                    ctypes.c_float(0.1), ctypes.c_void_p(16), ctypes.c_void_p(16), 8,
+                                    null, null)
+    assert st == kv.KVARN_ERR_WORKSPACE_TOO_SMALL
+    bad = kv.KvarnDesc.from_buffer_copy(d)
+    bad.k_bits = 3
+    assert lib.kvarn_dequantize_tiles(ctypes.byref(bad), null, 1, null, 1, null, null, null,
+                                      null) == kv.KVARN_ERR_UNSUPPORTED
+    assert "workspace" in kv.status_string(kv.KVARN_ERR_WORKSPACE_TOO_SMALL)

@@ -200,6 +200,22 @@ def test_sinkhorn_final_rows_unit_std():
         np.testing.assert_allclose(n.std(axis=1), 1.0, atol=1e-12)
 
 
+def test_sinkhorn_leaves_constant_and_zero_tiles_finite():
+    # rows/columns without variance keep their factors: a zero tile keeps r = c = 1 and a
+    # constant column is not blown up by 1/eps (reading of the epsilon floor)
+    n, r, c = ko.sinkhorn_normalise(np.zeros((128, 128)), 4)
+    assert np.all(r == 1.0) and np.all(c == 1.0) and np.all(n == 0.0)
+    x = np.random.default_rng(8).standard_normal((128, 128))
+    x[:, 5] = 2.5
+    n, r, c = ko.sinkhorn_normalise(x, 4)
+    assert np.all(np.isfinite(n)) and np.abs(np.log(r)).max() < 20 and np.abs(np.log(c)).max() < 20
+    # the zero tile dequantises to zeros through the fp16 metadata
+    q = ko.quantize_tile(np.zeros((128, 64)), "K")
+    assert np.all(np.isfinite(q["factor"].astype(np.float64)))
+    back = ko.dequantize_tile(q["codes"], q["scale"], q["zero"], q["factor"], "K", 64)
+    np.testing.assert_array_equal(back, 0.0)
+
+
 def test_sinkhorn_converges():
     # hotdry §迭代方差归一化 step 3 / vatt §四個步驟: the alternation converges and leaves
     # every row and every column with a similar variance (3-5 iterations usually enough)
