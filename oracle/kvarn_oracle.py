@@ -28,7 +28,10 @@ Decode attention is the textbook softmax attention over the dequantised cache
 
 Readings where the pages are silent (each also listed in the design doc):
   * Sylvester Hadamard in natural order, no random signs; scaled by 1/sqrt(d).
-  * std is the population std (ddof 0, mean subtracted); sigma floor EPS=1e-6.
+  * std is the population std (ddof 0, mean subtracted).  A row or column whose std is
+    below EPS=1e-6 has nothing to normalise and keeps its factor (its log factor gains 0);
+    dividing it by EPS instead would grow its factor by 1/EPS every iteration and overflow
+    the fp16 metadata of constant or all-zero tiles.
   * one iteration = channel-std step then token-std step.
   * zero-point is the float group minimum; scale floor 1e-8; round half to even.
   * stored scales, zero-points and factors are IEEE binary16.
@@ -46,7 +49,7 @@ TILE_TOKENS = 128          # one tile == one paged-attention block  [vatt Â§æ€Žé
 K_BITS = 4                 # preset kvarn_k4v2_g128                  [hotdry Â§æ ¸å¿ƒé…ç½®å‚æ•°]
 V_BITS = 2
 SINKHORN_ITERS = 4         # "usually 3-5 iterations"                [hotdry Â§è¿­ä»£æ–¹å·®å½’ä¸€åŒ–, step 3]
-SINKHORN_EPS = 1e-6        # reading: sigma floor (pages give none)
+SINKHORN_EPS = 1e-6        # reading: stds below this are not normalised (pages give no value)
 SCALE_FLOOR = 1e-8         # reading: quantiser step floor for constant groups
 
 
@@ -111,8 +114,8 @@ def sinkhorn_normalise(x: np.ndarray, iters: int = SINKHORN_ITERS,
 
     x: [..., T, d] rotated tile (tokens x channels).  Keeps log row factors lr[T]
     and log column factors lc[d].  Each iteration:
-      column step: sigma_j = std_i(x_ij e^{-lr_i - lc_j}); lc_j += ln max(sigma_j, eps)
-      row step:    sigma_i = std_j(x_ij e^{-lr_i - lc_j}); lr_i += ln max(sigma_i, eps)
+      column step: sigma_j = std_i(x_ij e^{-lr_i - lc_j}); lc_j += ln sigma_j if sigma_j >= eps
+      row step:    sigma_i = std_j(x_ij e^{-lr_i - lc_j}); lr_i += ln sigma_i if sigma_i >= eps
     Returns N = x / (r_i c_j), r = e^{lr}, c = e^{lc}.
     [hotdry Â§è¿­ä»£æ–¹å·®å½’ä¸€åŒ– steps 1-3 and the log-space paragraph;
      vatt Â§å››å€‹æ­¥é©Ÿ, the Sinkhorn paragraph: column then row, log domain]
@@ -125,10 +128,10 @@ def sinkhorn_normalise(x: np.ndarray, iters: int = SINKHORN_ITERS,
     for _ in range(iters):
         cur = x * np.exp(-lr[..., :, None] - lc[..., None, :])
         sigma_c = cur.std(axis=-2)
-        lc = lc + np.log(np.maximum(sigma_c, eps))
+        lc = lc + np.log(np.where(sigma_c >= eps, sigma_c, 1.0))
         cur = x * np.exp(-lr[..., :, None] - lc[..., None, :])
         sigma_r = cur.std(axis=-1)
-        lr = lr + np.log(np.maximum(sigma_r, eps))
+        lr = lr + np.log(np.where(sigma_r >= eps, sigma_r, 1.0))
     r = np.exp(lr)
     c = np.exp(lc)
     n = x / (r[..., :, None] * c[..., None, :])
