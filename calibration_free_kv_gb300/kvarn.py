@@ -35,7 +35,11 @@ EXPORTED_SYMBOLS = (
     "kvarn_decode_attention",
     "kvarn_dequantize_tiles",
     "kvarn_status_string",
+    "kvarn_decode_attention_noalloc",
 )
+
+# Size of the library's fixed decode scratch (KVARN_DECODE_NOALLOC_SCRATCH_BYTES in kvarn.h).
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class KvarnError(RuntimeError):
@@ -76,6 +80,8 @@ def _load():
                                          P, P, ctypes.c_size_t, P, P]),
         "kvarn_dequantize_tiles": (i32, [D, P, i64, P, i32, P, P, P, P]),
         "kvarn_status_string": (ctypes.c_char_p, [i32]),
+        "kvarn_decode_attention_noalloc": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P,
+                                                 ctypes.c_float, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -189,6 +195,21 @@ def decode_attention(desc: KvarnDesc, q, pool, block_table, seq_lens, out, works
                                        float(softmax_scale), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _ptr(status), _stream(stream)), "kvarn_decode_attention")
+
+
+def decode_attention_noalloc(desc: KvarnDesc, q, pool, block_table, seq_lens, out, partial_k=None,
+                             partial_v=None, softmax_scale=None, status=None, stream=None):
+    """decode_attention without a workspace: the split partials go to the library's fixed
+    device buffer (for callers that cannot allocate).  Calls on one device share that buffer,
+    so calls overlapping on the GPU must be serialised by the caller."""
+    batch, hq, d0 = q.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d0)
+    _check(_lib.kvarn_decode_attention_noalloc(ctypes.byref(desc), batch, hq, _ptr(q), _ptr(pool),
+                                               pool.shape[0], _ptr(block_table), block_table.shape[1],
+                                               _ptr(seq_lens), _ptr(partial_k), _ptr(partial_v),
+                                               float(softmax_scale), _ptr(out), _ptr(status),
+                                               _stream(stream)), "kvarn_decode_attention_noalloc")
 
 
 def dequantize_tiles(desc: KvarnDesc, pool, page_ids, k_out, v_out, status=None, stream=None):

@@ -142,6 +142,31 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
                            void* out, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, void* stream);
 
+/* Size of the fixed device buffer used by kvarn_decode_attention_noalloc (16 MiB). */
+#define KVARN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* kvarn_decode_attention without a workspace argument, for callers that cannot allocate
+ * device memory: plugins in engines that plan and own all device memory in advance, code
+ * that must not call cudaMalloc on the decode path (it may synchronise the device), and
+ * embedders without an allocator.  The pages have no counterpart; this is an interface
+ * variant of the decode call above, with identical arguments, results and errors otherwise.
+ *  - The split partials live in a library-owned buffer of
+ *    KVARN_DECODE_NOALLOC_SCRATCH_BYTES per GPU, held from the library's load until exit.
+ *    A shape whose kvarn_decode_workspace_bytes exceeds it returns
+ *    KVARN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *  - The first call on each device looks up the buffer's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call before any
+ *    stream capture.  The current device must own stream and pointers.
+ *  - All calls on a device share the buffer and it keeps the last call's contents; nothing
+ *    in it needs to start at zero.  Calls that overlap on the GPU (other streams, other
+ *    threads) race on it: order them on one stream or serialise them. */
+int kvarn_decode_attention_noalloc(const kvarn_desc* desc, int batch, int num_q_heads,
+                                   const void* q, const void* page_pool, int64_t num_pool_pages,
+                                   const int32_t* block_table, int max_pages,
+                                   const int32_t* seq_lens, const void* partial_k,
+                                   const void* partial_v, float softmax_scale, void* out,
+                                   int32_t* dev_status, void* stream);
+
 /* Dequantise page records back to fp16 K/V in the original basis [hotdry
  * §非对称量化与尺度折叠: scales multiplied back at read].
  *  page_ids  device int32 [num_pages]; k_out, v_out fp16 [num_pages][Hkv][128][d0]. */
