@@ -6,38 +6,42 @@
 // [vatt §四個步驟: the rotation is orthonormal so attention scores are unchanged;
 //  hotdry §非对称量化与尺度折叠: the folded scales are multiplied back at read time]
 //
-// decode_kernel: grid (split, kv head, sequence).  Each CTA owns up to `pages_per_split`
-// sealed pages of one (sequence, kv head), or the raw fp16 partial tile.  Its warps take
-// pages round-robin; each warp streams whole page records into shared memory with 1-D bulk
-// copies (double-buffered on mbarriers), then per page:
-//   QK:  m16n8k16 MMAs, A = 4-bit codes [token x channel] unpacked exactly to fp16,
-//        B = q~ . s'_K split into fp16 hi + lo (columns: 4 heads x {hi, lo}).
-//   softmax: online, in the log2 domain (tau log2(e) folded into q~).
+// decode_kernel: grid (split, kv head, sequence).  A CTA owns up to `pages_per_split` sealed
+// pages of one (sequence, kv head), or the raw fp16 partial tile.  Its 8 warps form 4 pairs;
+// pairs take pages round-robin and stream whole page records into shared memory with 1-D
+// bulk copies (two stages per pair, mbarrier-completed).  The two warps of a pair split each
+// page into token halves and keep independent online-softmax states:
+//   QK:  m16n8k16 MMAs, A = 4-bit codes [token x channel], B = q~ . s'_K split into fp16
+//        hi + lo (columns: 4 heads x {hi, lo}).
+//   softmax: online, log2 domain (tau log2(e) folded into q~).
 //   PV:  m16n8k16 MMAs, A = 2-bit codes^T [channel x token], B = p . s'_V split hi + lo,
 //        moved from the QK accumulator layout with movmatrix.trans.
-// The CTA merges its warps and writes (m, l, unnormalised o~) for its split; combine_kernel
-// merges the splits, divides by l, undoes the rotation and stores fp16.
+// Codes enter the MMAs as exact fp16 subnormals: masking a code into the low mantissa bits
+// of a zero exponent gives code * 2^-24 (code * 2^-22 .. 2^-18 for higher bit positions), so
+// unpacking costs one AND per two codes; the powers of two are folded into B and into the
+// fp32 results.  The CTA merges its warps and writes (m, l, unnormalised o~) for its split;
+// combine_kernel merges the splits, divides by l, undoes the rotation and stores fp16.
 #include "common.cuh"
 #include "params.cuh"
 
 namespace kvarn {
 
-constexpr int kDecWarps = 4;
-constexpr int kDecStages = 2;
-
+constexpr int kDecWarps = 8;            // 4 pairs
+constexpr int kDecPairs = kDecWarps / 2;
+constexpr int kDecStages = 2;           // page records in flight per pair
+constexpr float kTwo24 = 16777216.0f;
 
 template <int D, int NT>
 struct DecodeShape {
   static constexpr int kNH = 4 * NT;                 // head slots per kv head (G padded)
   static constexpr int kRec = record_layout(D).bytes;
   static constexpr int kQld = D + 8;                 // fp32 row stride of q in shared memory
-  static constexpr int kRecBytes = kDecWarps * kDecStages * kRec;
+  static constexpr int kRecBytes = kDecPairs * kDecStages * kRec;
   static constexpr int kQBytes = kNH * kQld * 4;
-  static constexpr int kSmemBytes = kRecBytes + kQBytes + kDecWarps * kDecStages * 8;
+  static constexpr int kSmemBytes = kRecBytes + kQBytes + kDecPairs * kDecStages * 8;
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -54,41 +58,54 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   return r;
 }
 
-// 0x6400 | (code << b) is the fp16 value 1024 + code * 2^b; c = v * 2^-b - 1024 * 2^-b exactly.
-__device__ __forceinline__ uint32_t code_to_f16(uint32_t biased, float inv_pow2) {
-  const __half2 sc = __float2half2_rn(inv_pow2);
-  const __half2 off = __float2half2_rn(-1024.0f * inv_pow2);
-  return h2u(__hfma2(u2h(biased), sc, off));
+__device__ __forceinline__ void pair_sync(int pair) {
+  asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
 }
 
-// K word -> A fragment (a0: row g, a1: row g+8, a2: row g cols+8, a3: row g+8 cols+8).
+// Barrier of the two warps of a pair that also ANDs a predicate over them.
+__device__ __forceinline__ bool pair_sync_and(int pair, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(pair + 1)
+      : "memory");
+  return r != 0;
+}
+
+// K word -> A fragment as fp16 subnormals: a0/a1 (channels 2tq..) = code * 2^-24,
+// a2/a3 (channels 2tq+8..) = code * 2^-20.
 __device__ __forceinline__ void unpack_k(uint32_t x, uint32_t (&a)[4]) {
   const uint32_t y = x >> 8;
-  a[0] = code_to_f16(and_or(x, 0x000F000Fu, 0x64006400u), 1.0f);
-  a[2] = code_to_f16(and_or(x, 0x00F000F0u, 0x64006400u), 1.0f / 16.0f);
-  a[1] = code_to_f16(and_or(y, 0x000F000Fu, 0x64006400u), 1.0f);
-  a[3] = code_to_f16(and_or(y, 0x00F000F0u, 0x64006400u), 1.0f / 16.0f);
+  a[0] = x & 0x000F000Fu;
+  a[2] = x & 0x00F000F0u;
+  a[1] = y & 0x000F000Fu;
+  a[3] = y & 0x00F000F0u;
 }
 
-// V word -> the two A fragments (token blocks 2ks2 and 2ks2+1) it carries.
+// V word -> the A fragments of token blocks 2ks2 (a0) and 2ks2+1 (a1) as fp16 subnormals:
+// block f, token half h -> code * 2^(-24 + 4f + 2h).
 __device__ __forceinline__ void unpack_v(uint32_t x, uint32_t (&a0)[4], uint32_t (&a1)[4]) {
   const uint32_t y = x >> 8;
-  a0[0] = code_to_f16(and_or(x, 0x00030003u, 0x64006400u), 1.0f);
-  a0[2] = code_to_f16(and_or(x, 0x000C000Cu, 0x64006400u), 0.25f);
-  a0[1] = code_to_f16(and_or(y, 0x00030003u, 0x64006400u), 1.0f);
-  a0[3] = code_to_f16(and_or(y, 0x000C000Cu, 0x64006400u), 0.25f);
-  a1[0] = code_to_f16(and_or(x, 0x00300030u, 0x64006400u), 1.0f / 16.0f);
-  a1[2] = code_to_f16(and_or(x, 0x00C000C0u, 0x64006400u), 1.0f / 64.0f);
-  a1[1] = code_to_f16(and_or(y, 0x00300030u, 0x64006400u), 1.0f / 16.0f);
-  a1[3] = code_to_f16(and_or(y, 0x00C000C0u, 0x64006400u), 1.0f / 64.0f);
+  a0[0] = x & 0x00030003u;
+  a0[2] = x & 0x000C000Cu;
+  a0[1] = y & 0x00030003u;
+  a0[3] = y & 0x000C000Cu;
+  a1[0] = x & 0x00300030u;
+  a1[2] = x & 0x00C000C0u;
+  a1[1] = y & 0x00300030u;
+  a1[3] = y & 0x00C000C0u;
 }
 
-// fp32 x -> (hi, lo) fp16 with hi + lo ~ x to ~22 bits; returns hi (sel == 0) or lo.
-__device__ __forceinline__ __half2 split_pick(float x0, float x1, bool lo) {
+// fp32 pair -> fp16 hi (lo == false) or lo = x - hi (lo == true); hi + lo ~ x to ~22 bits.
+__device__ __forceinline__ uint32_t split_pick(float x0, float x1, bool lo) {
   const __half2 hi = __floats2half2_rn(x0, x1);
   const float2 hf = __half22float2(hi);
   const __half2 lw = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-  return lo ? lw : hi;
+  return h2u(lo ? lw : hi);
 }
 
 // Walsh-Hadamard transform of D values spread over a warp, lane holding D/32 consecutive.
@@ -126,9 +143,10 @@ struct WarpAcc {
   float o[D / 16][NT][2];  // head 4nt + tq, channels 16mc + g + 8r (rotated basis)
 };
 
+// One warp's half (tokens 64hf .. 64hf+63) of one page record.
 template <int D, int NT>
-__device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
-                                             const float* __restrict__ qrot, int lane,
+__device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
+                                             const float* __restrict__ qrot, int lane, int hf,
                                              WarpAcc<D, NT>& st) {
   constexpr RecordLayout RL = record_layout(D);
   constexpr int QLD = DecodeShape<D, NT>::kQld;
@@ -140,7 +158,7 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
   const __half* Vz = reinterpret_cast<const __half*>(R + RL.vzero);
   const __half* Vc = reinterpret_cast<const __half*>(R + RL.vfactor);
 
-  // ---- B operand of QK: q~_j s'_j (hi or lo by column parity), and q~ . z' per head ---------
+  // ---- B operand of QK (q~_j s'_j, hi or lo by column parity) and q~ . z' per head ----------
   uint32_t bq[D / 16][NT][2];
   float qz[NT];
 #pragma unroll
@@ -159,8 +177,9 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
       const float2 qa = *reinterpret_cast<const float2*>(qr + j0);
       const float2 qb = *reinterpret_cast<const float2*>(qr + j0 + 8);
       qz[nt] = fmaf(qa.x, z0.x, fmaf(qa.y, z0.y, fmaf(qb.x, z1.x, fmaf(qb.y, z1.y, qz[nt]))));
-      bq[kk][nt][0] = h2u(split_pick(qa.x * s0.x, qa.y * s0.y, lo_col));
-      bq[kk][nt][1] = h2u(split_pick(qb.x * s1.x, qb.y * s1.y, lo_col));
+      bq[kk][nt][0] = split_pick(qa.x * s0.x, qa.y * s0.y, lo_col);
+      // channels 2tq+8.. meet codes scaled by 2^-20 instead of 2^-24
+      bq[kk][nt][1] = split_pick(qb.x * s1.x * 0.0625f, qb.y * s1.y * 0.0625f, lo_col);
     }
   }
   float qzm[NT];
@@ -172,10 +191,11 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
     qzm[nt] = __shfl_sync(0xffffffffu, v, 8 * tq);  // head 4nt + tq lives in lanes g = 2tq
   }
 
-  // ---- QK ---------------------------------------------------------------------------------
-  float lg[8][NT][2];
+  // ---- QK over the 4 m-tiles of this half ----
+  float lg[4][NT][2];
 #pragma unroll
-  for (int mi = 0; mi < 8; ++mi) {
+  for (int i = 0; i < 4; ++i) {
+    const int mi = 4 * hf + i;
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
@@ -196,18 +216,18 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
     const float r1 = __half2float(Kr[16 * mi + g + 8]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      lg[mi][nt][0] = r0 * ((acc[nt][0] + acc[nt][1]) + qzm[nt]);
-      lg[mi][nt][1] = r1 * ((acc[nt][2] + acc[nt][3]) + qzm[nt]);
+      lg[i][nt][0] = r0 * fmaf(acc[nt][0] + acc[nt][1], kTwo24, qzm[nt]);
+      lg[i][nt][1] = r1 * fmaf(acc[nt][2] + acc[nt][3], kTwo24, qzm[nt]);
     }
   }
 
-  // ---- online softmax ------------------------------------------------------------------------
+  // ---- online softmax (per head, over this warp's tokens) ----
   float alpha[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float mx = lg[0][nt][0];
+    float mx = fmaxf(lg[0][nt][0], lg[0][nt][1]);
 #pragma unroll
-    for (int mi = 0; mi < 8; ++mi) mx = fmaxf(mx, fmaxf(lg[mi][nt][0], lg[mi][nt][1]));
+    for (int i = 1; i < 4; ++i) mx = fmaxf(mx, fmaxf(lg[i][nt][0], lg[i][nt][1]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -216,17 +236,17 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
     st.m[nt] = mnew;
     float ps = 0.0f;
 #pragma unroll
-    for (int mi = 0; mi < 8; ++mi)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float pv = exp2f(lg[mi][nt][r] - mnew);
-        lg[mi][nt][r] = pv;
+        const float pv = exp2f(lg[i][nt][r] - mnew);
+        lg[i][nt][r] = pv;
         ps += pv;
       }
     st.l[nt] = fmaf(st.l[nt], alpha[nt], ps);
   }
 
-  // ---- PV --------------------------------------------------------------------------------------
+  // ---- PV over the 4 k-steps (2 V words) of this half ----
   float pacc[D / 16][NT][4];
 #pragma unroll
   for (int mc = 0; mc < D / 16; ++mc)
@@ -236,18 +256,22 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) zs[nt] = 0.0f;
 #pragma unroll
-  for (int ks2 = 0; ks2 < 4; ++ks2) {
+  for (int j2 = 0; j2 < 2; ++j2) {
+    const int ks2 = 2 * hf + j2;
     uint32_t bw[2][NT][2];
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
       const int ks = 2 * ks2 + f;
+      const int li = 2 * j2 + f;  // this half's m-tile index of the same 16 tokens
       const float sv0 = __half2float(Vs[16 * ks + g]), sv1 = __half2float(Vs[16 * ks + g + 8]);
       const float zv0 = __half2float(Vz[16 * ks + g]), zv1 = __half2float(Vz[16 * ks + g + 8]);
+      // compensate the subnormal scale 2^(4f + 2h) of this block's codes (h = 0: rows g)
+      const float c0 = f ? 1.0f / 16.0f : 1.0f, c1 = f ? 1.0f / 64.0f : 0.25f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float p0 = lg[ks][nt][0], p1 = lg[ks][nt][1];
+        const float p0 = lg[li][nt][0], p1 = lg[li][nt][1];
         zs[nt] = fmaf(p0, zv0, fmaf(p1, zv1, zs[nt]));
-        const float w0 = p0 * sv0, w1 = p1 * sv1;
+        const float w0 = p0 * sv0 * c0, w1 = p1 * sv1 * c1;
         const __half hi0 = __float2half_rn(w0), hi1 = __float2half_rn(w1);
         const __half lo0 = __float2half_rn(w0 - __half2float(hi0));
         const __half lo1 = __float2half_rn(w1 - __half2float(hi1));
@@ -281,17 +305,19 @@ __device__ __forceinline__ void process_page(const uint8_t* __restrict__ R,
   }
 #pragma unroll
   for (int mc = 0; mc < D / 16; ++mc) {
-    const float c0 = __half2float(Vc[16 * mc + g]), c1 = __half2float(Vc[16 * mc + g + 8]);
+    const float cj0 = __half2float(Vc[16 * mc + g]), cj1 = __half2float(Vc[16 * mc + g + 8]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      st.o[mc][nt][0] = fmaf(st.o[mc][nt][0], alpha[nt], c0 * ((pacc[mc][nt][0] + pacc[mc][nt][1]) + zs[nt]));
-      st.o[mc][nt][1] = fmaf(st.o[mc][nt][1], alpha[nt], c1 * ((pacc[mc][nt][2] + pacc[mc][nt][3]) + zs[nt]));
+      st.o[mc][nt][0] = fmaf(st.o[mc][nt][0], alpha[nt],
+                             cj0 * fmaf(pacc[mc][nt][0] + pacc[mc][nt][1], kTwo24, zs[nt]));
+      st.o[mc][nt][1] = fmaf(st.o[mc][nt][1], alpha[nt],
+                             cj1 * fmaf(pacc[mc][nt][2] + pacc[mc][nt][3], kTwo24, zs[nt]));
     }
   }
 }
 
 template <int D, int NT>
-__global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams p) {
   using S = DecodeShape<D, NT>;
   constexpr int NH = S::kNH;
   constexpr int REC = S::kRec;
@@ -303,6 +329,8 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams p) 
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = warp >> 1, hf = warp & 1;
+  const int g = lane >> 2, tq = lane & 3;
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
   int len = p.seq_lens[b];
   if (len < 0 || len > cap) {
@@ -318,53 +346,27 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams p) 
     return;
   }
 
-  // ---- queries of this kv head's group: rotated (sealed pages) or original (partial tile) ----
-  for (int hl = warp; hl < NH; hl += kDecWarps) {
-    float v[D / 32];
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      const int j = lane * (D / 32) + e;
-      v[e] = (hl < p.group && j < p.d0)
-                 ? __half2float(p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + j])
-                 : 0.0f;
-    }
-    float sc = p.qscale;
-    if (!partial_split) {
-      warp_fwht<D>(v, lane);
-      sc *= inv_sqrt_d<D>();
-    }
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) qsm[hl * QLD + lane * (D / 32) + e] = v[e] * sc;
-  }
-  __syncthreads();
-
   float* part_base = p.part + ((int64_t)(b * p.num_q_heads + h * p.group) * p.max_splits + split) * (D + 4);
   const int64_t head_stride = (int64_t)p.max_splits * (D + 4);
 
   if (!partial_split) {
-    WarpAcc<D, NT> st;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      st.m[nt] = -INFINITY;
-      st.l[nt] = 0.0f;
-#pragma unroll
-      for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
-    }
     const int first = split * p.pages_per_split;
     const int last = min(n_sealed, first + p.pages_per_split);
-    const int cnt = (last - first - warp + kDecWarps - 1) / kDecWarps;
-    uint64_t* bar = bars + warp * kDecStages;
-    uint8_t* rb = recs + warp * kDecStages * REC;
+    const int cnt = (last - first - pair + kDecPairs - 1) / kDecPairs;  // pages of this pair
+    uint64_t* bar = bars + pair * kDecStages;
+    uint8_t* rb = recs + pair * kDecStages * REC;
     const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
+    const bool producer = (hf == 0 && lane == 0);
     auto page_src = [&](int k) -> const uint8_t* {
-      int64_t id = bt[first + warp + kDecWarps * k];
+      int64_t id = bt[first + pair + kDecPairs * k];
       if (id < 0 || id >= p.num_pool_pages) {
         flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
         id = 0;
       }
       return p.pool + (id * p.num_kv_heads + h) * REC;
     };
-    if (lane == 0) {
+    // start the page stream before anything else
+    if (producer) {
 #pragma unroll
       for (int s = 0; s < kDecStages; ++s) mbar_init(&bar[s], 1);
       fence_mbar_init();
@@ -373,30 +375,56 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams p) 
         bulk_copy_g2s(rb + k * REC, page_src(k), REC, &bar[k]);
       }
     }
-    __syncwarp();
+    // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d)
+    for (int hl = warp; hl < NH; hl += kDecWarps) {
+      float v[D / 32];
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) {
+        const int j = lane * (D / 32) + e;
+        v[e] = (hl < p.group && j < p.d0)
+                   ? __half2float(p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + j])
+                   : 0.0f;
+      }
+      warp_fwht<D>(v, lane);
+      const float sc = p.qscale * inv_sqrt_d<D>();
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) qsm[hl * QLD + lane * (D / 32) + e] = v[e] * sc;
+    }
+    __syncthreads();  // q in shared memory and the barriers initialised for every warp
+
+    WarpAcc<D, NT> st;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      st.m[nt] = -INFINITY;
+      st.l[nt] = 0.0f;
+#pragma unroll
+      for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
+    }
     for (int k = 0; k < cnt; ++k) {
       const int s = k % kDecStages;
-      if (!mbar_wait(&bar[s], (k / kDecStages) & 1)) {
-        // a copy never arrived: report, drain the copies this warp still has in flight, stop
-        if (lane == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
-        for (int k2 = k + 1; k2 < cnt && k2 < k + kDecStages; ++k2)
-          mbar_wait(&bar[k2 % kDecStages], (k2 / kDecStages) & 1);
+      const bool arrived = mbar_wait(&bar[s], (k / kDecStages) & 1);
+      if (!pair_sync_and(pair, arrived)) {
+        // a copy never arrived: report, drain this pair's copies still in flight, stop
+        if (producer) {
+          flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+          for (int k2 = k; k2 < cnt && k2 < k + kDecStages; ++k2)
+            mbar_wait(&bar[k2 % kDecStages], (k2 / kDecStages) & 1);
+        }
         break;
       }
-      process_page<D, NT>(rb + s * REC, qsm, lane, st);
-      __syncwarp();
-      if (lane == 0 && k + kDecStages < cnt) {
+      process_half<D, NT>(rb + s * REC, qsm, lane, hf, st);
+      pair_sync(pair);  // both halves are done with this record
+      if (producer && k + kDecStages < cnt) {
         fence_proxy_async_smem();
         mbar_expect_tx(&bar[s], REC);
         bulk_copy_g2s(rb + s * REC, page_src(k + kDecStages), REC, &bar[s]);
       }
     }
     // ---- merge the warps of this CTA ----
-    __syncthreads();  // every warp is done with its record buffers
+    __syncthreads();  // every pair is done with its record buffers
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;
-    const int g = lane >> 2, tq = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float l = st.l[nt];
@@ -438,6 +466,17 @@ __global__ void __launch_bounds__(kDecWarps * 32) decode_kernel(DecodeParams p) 
   }
 
   // ---- partial tile: raw fp16 tokens in the original basis ---------------------------------
+  for (int hl = warp; hl < NH; hl += kDecWarps) {
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      const int j = lane * (D / 32) + e;
+      qsm[hl * QLD + j] =
+          (hl < p.group && j < p.d0)
+              ? __half2float(p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + j]) * p.qscale
+              : 0.0f;
+    }
+  }
+  __syncthreads();
   {
     constexpr int E = D / 32;
     float m[NH], l[NH], acc[NH][E];
@@ -531,15 +570,35 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   for (int e = 0; e < E; ++e) v[e] = 0.0f;
   if (n_splits > 0) {
     const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
+    // split statistics, one split per lane, 32 per pass
     float M = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) M = fmaxf(M, base[s * (D + 4)]);
-    float lsum = 0.0f;
-    for (int s = 0; s < n_splits; ++s) {
-      const float* src = base + s * (D + 4);
-      const float sc = exp2f(src[0] - M);
-      lsum = fmaf(sc, src[1], lsum);
+    for (int s0 = 0; s0 < n_splits; s0 += 32) {
+      const int s = s0 + lane;
+      float m = s < n_splits ? base[s * (D + 4)] : -INFINITY;
 #pragma unroll
-      for (int e = 0; e < E; ++e) v[e] = fmaf(sc, src[4 + lane * E + e], v[e]);
+      for (int msk = 16; msk > 0; msk >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, msk));
+      M = fmaxf(M, m);
+    }
+    float lsum = 0.0f;
+    for (int s0 = 0; s0 < n_splits; s0 += 32) {
+      const int s = s0 + lane;
+      const float w = s < n_splits ? exp2f(base[s * (D + 4)] - M) : 0.0f;
+      float lw = s < n_splits ? w * base[s * (D + 4) + 1] : 0.0f;
+#pragma unroll
+      for (int msk = 16; msk > 0; msk >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, msk);
+      lsum += lw;
+      const int cnt = min(32, n_splits - s0);
+#pragma unroll 4
+      for (int i = 0; i < cnt; ++i) {
+        const float wi = __shfl_sync(0xffffffffu, w, i);
+        const float* src = base + (s0 + i) * (D + 4) + 4 + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          const float2 o = *reinterpret_cast<const float2*>(src + e);
+          v[e] = fmaf(wi, o.x, v[e]);
+          v[e + 1] = fmaf(wi, o.y, v[e + 1]);
+        }
+      }
     }
     const float inv = inv_sqrt_d<D>() / lsum;
     warp_fwht<D>(v, lane);
@@ -582,18 +641,6 @@ int launch_decode_any(int d, int nt, const DecodeParams& p, cudaStream_t stream)
     if (d == 128) return launch_decode_t<128, 2>(p, stream);
   }
   return KVARN_ERR_UNSUPPORTED;
-}
-
-int decode_smem_bytes(int d, int nt) {
-  if (nt == 1) {
-    if (d == 64) return DecodeShape<64, 1>::kSmemBytes;
-    if (d == 128) return DecodeShape<128, 1>::kSmemBytes;
-    if (d == 256) return DecodeShape<256, 1>::kSmemBytes;
-  } else if (nt == 2) {
-    if (d == 64) return DecodeShape<64, 2>::kSmemBytes;
-    if (d == 128) return DecodeShape<128, 2>::kSmemBytes;
-  }
-  return -1;
 }
 
 }  // namespace kvarn

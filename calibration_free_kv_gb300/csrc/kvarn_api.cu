@@ -133,9 +133,10 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
                              static_cast<cudaStream_t>(stream));
 }
 
+// Sealed pages per decode CTA (the CTA's 4 warp pairs take them round-robin).
 static int decode_pages_per_split(int max_pages) {
   (void)max_pages;
-  return 16;
+  return 32;
 }
 
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
