@@ -49,6 +49,23 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _decode_traffic_ratio():
+    """DRAM bytes / algorithmic bytes of the decode kernel from the committed ncu summary, or
+    None when decode.cu changed since that capture."""
+    import hashlib
+    import re
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_kernel_batch24_d128.md")) as fh:
+            text = fh.read()
+        with open(os.path.join(ROOT, "calibration_free_kv_gb300", "csrc", "decode.cu"), "rb") as fh:
+            digest = hashlib.sha256(fh.read()).hexdigest()
+        want = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
+        ratio = float(re.search(r"traffic_ratio_dram_over_algorithmic:\s*([0-9.]+)", text).group(1))
+        return ratio if want == digest else None
+    except Exception:
+        return None
+
+
 def _dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -319,7 +336,12 @@ def _run_kvarn(args, torch, world, rank):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
-            "traffic": None, "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
+            "traffic": (None if _decode_traffic_ratio() is None
+                        else _decode_traffic_ratio() * statistics.mean(dec_bytes)),
+            "traffic_source": "ncu dram__bytes_read+write of decode_kernel at batch 24, scaled by "
+                              "algorithmic bytes (profiles/decode_kernel_batch24_d128.md); null "
+                              "when decode.cu changed since that capture",
+            "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
         },
         "quantize": {
             "workload": "one layer, 8 KV heads x 16384 tokens x head_dim 128 (K and V), L2 flushed",
