@@ -7,12 +7,15 @@
 //  hotdry §非对称量化与尺度折叠: the folded scales are multiplied back at read time]
 //
 // decode_kernel: grid (split, kv head, sequence).  A CTA owns up to `pages_per_split` sealed
-// pages of one (sequence, kv head), or the raw fp16 partial tile.  Its 8 warps form 4 pairs;
-// pairs take pages round-robin and stream whole page records into shared memory with 1-D
-// bulk copies (two stages per pair, mbarrier-completed).  The two warps of a pair split each
-// page into token halves and keep independent online-softmax states:
+// pages of one (sequence, kv head), or the raw fp16 partial tile.  Whole page records stream
+// into a ring of shared-memory slots with 1-D bulk copies completed on mbarriers: page k of
+// the split goes to slot k % kSlots, and the pair that finishes page k issues page k + kSlots
+// into the slot it freed.  Its 8 warps form 4 pairs that take pages round-robin; the two
+// warps of a pair split each page into token halves and keep independent online-softmax
+// states:
 //   QK:  m16n8k16 MMAs, A = 4-bit codes [token x channel], B = q~ . s'_K split into fp16
-//        hi + lo (columns: 4 heads x {hi, lo}).
+//        hi + lo (columns: 4 heads x {hi, lo}); each warp of the pair builds half of B and
+//        the halves are exchanged through shared memory.
 //   softmax: online, log2 domain (tau log2(e) folded into q~).
 //   PV:  m16n8k16 MMAs, A = 2-bit codes^T [channel x token], B = p . s'_V split hi + lo,
 //        moved from the QK accumulator layout with movmatrix.trans.
@@ -28,17 +31,22 @@ namespace kvarn {
 
 constexpr int kDecWarps = 8;            // 4 pairs
 constexpr int kDecPairs = kDecWarps / 2;
-constexpr int kDecStages = 2;           // page records in flight per pair
 constexpr float kTwo24 = 16777216.0f;
 
 template <int D, int NT>
 struct DecodeShape {
   static constexpr int kNH = 4 * NT;                 // head slots per kv head (G padded)
+  static constexpr int kSlots = NT == 2 ? 6 : 7;     // page records in flight per CTA
   static constexpr int kRec = record_layout(D).bytes;
   static constexpr int kQld = D + 8;                 // fp32 row stride of q in shared memory
-  static constexpr int kRecBytes = kDecPairs * kDecStages * kRec;
+  static constexpr int kRecBytes = kSlots * kRec;
   static constexpr int kQBytes = kNH * kQld * 4;
-  static constexpr int kSmemBytes = kRecBytes + kQBytes + kDecPairs * kDecStages * 8;
+  // per pair: B-operand halves [2][kXWords][32 lanes] u32 and q~.z' halves [2][kNH] f32
+  static constexpr int kXWords = (D / 32) * NT * 2;
+  static constexpr int kXPairBytes = 2 * kXWords * 32 * 4 + 2 * kNH * 4;
+  static constexpr int kXBytes = kDecPairs * kXPairBytes;
+  // mbarriers, then per slot: copies issued and copies consumed (for draining after a timeout)
+  static constexpr int kSmemBytes = kRecBytes + kQBytes + kXBytes + kSlots * 8 + 2 * kSlots * 4;
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -143,30 +151,27 @@ struct WarpAcc {
   float o[D / 16][NT][2];  // head 4nt + tq, channels 16mc + g + 8r (rotated basis)
 };
 
-// One warp's half (tokens 64hf .. 64hf+63) of one page record.
+// This warp's half (k-steps hf*D/32 ..) of the QK B operand -- q~_j s'_j as fp16 hi (even g)
+// or lo (odd g) -- written to the pair's exchange buffer, and its partial q~ . z' per head.
 template <int D, int NT>
-__device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
+__device__ __forceinline__ void build_b_half(const uint8_t* __restrict__ R,
                                              const float* __restrict__ qrot, int lane, int hf,
-                                             WarpAcc<D, NT>& st) {
+                                             uint32_t* __restrict__ xb, float* __restrict__ xq) {
   constexpr RecordLayout RL = record_layout(D);
   constexpr int QLD = DecodeShape<D, NT>::kQld;
+  constexpr int XW = DecodeShape<D, NT>::kXWords;
+  constexpr int NH = DecodeShape<D, NT>::kNH;
   const int g = lane >> 2, tq = lane & 3;
   const __half* Ks = reinterpret_cast<const __half*>(R + RL.kscale);
   const __half* Kz = reinterpret_cast<const __half*>(R + RL.kzero);
-  const __half* Kr = reinterpret_cast<const __half*>(R + RL.kfactor);
-  const __half* Vs = reinterpret_cast<const __half*>(R + RL.vscale);
-  const __half* Vz = reinterpret_cast<const __half*>(R + RL.vzero);
-  const __half* Vc = reinterpret_cast<const __half*>(R + RL.vfactor);
-
-  // ---- B operand of QK (q~_j s'_j, hi or lo by column parity) and q~ . z' per head ----------
-  uint32_t bq[D / 16][NT][2];
   float qz[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) qz[nt] = 0.0f;
   const bool lo_col = (g & 1) != 0;
+  uint32_t* mine = xb + hf * XW * 32 + lane;
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const int j0 = 16 * kk + 2 * tq;
+  for (int i = 0; i < D / 32; ++i) {
+    const int j0 = 16 * (hf * (D / 32) + i) + 2 * tq;
     const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(Ks + j0));
     const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(Ks + j0 + 8));
     const float2 z0 = __half22float2(*reinterpret_cast<const __half2*>(Kz + j0));
@@ -177,19 +182,53 @@ __device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
       const float2 qa = *reinterpret_cast<const float2*>(qr + j0);
       const float2 qb = *reinterpret_cast<const float2*>(qr + j0 + 8);
       qz[nt] = fmaf(qa.x, z0.x, fmaf(qa.y, z0.y, fmaf(qb.x, z1.x, fmaf(qb.y, z1.y, qz[nt]))));
-      bq[kk][nt][0] = split_pick(qa.x * s0.x, qa.y * s0.y, lo_col);
+      mine[((i * NT + nt) * 2) * 32] = split_pick(qa.x * s0.x, qa.y * s0.y, lo_col);
       // channels 2tq+8.. meet codes scaled by 2^-20 instead of 2^-24
-      bq[kk][nt][1] = split_pick(qb.x * s1.x * 0.0625f, qb.y * s1.y * 0.0625f, lo_col);
+      mine[((i * NT + nt) * 2 + 1) * 32] = split_pick(qb.x * s1.x * 0.0625f, qb.y * s1.y * 0.0625f, lo_col);
     }
   }
-  float qzm[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float v = qz[nt];
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
-    qzm[nt] = __shfl_sync(0xffffffffu, v, 8 * tq);  // head 4nt + tq lives in lanes g = 2tq
+    if (tq == 0 && (g & 1) == 0) xq[hf * NH + 4 * nt + (g >> 1)] = v;  // head 4nt + g/2
   }
+}
+
+// Both halves of the QK B operand and the full q~ . z' of the lane's heads (4nt + tq).
+template <int D, int NT>
+__device__ __forceinline__ void gather_b(const uint32_t* __restrict__ xb,
+                                         const float* __restrict__ xq, int lane,
+                                         uint32_t (&bq)[D / 16][NT][2], float (&qzm)[NT]) {
+  constexpr int XW = DecodeShape<D, NT>::kXWords;
+  constexpr int NH = DecodeShape<D, NT>::kNH;
+  const int tq = lane & 3;
+#pragma unroll
+  for (int half = 0; half < 2; ++half)
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        bq[half * (D / 32) + i][nt][0] = xb[(half * XW + (i * NT + nt) * 2) * 32 + lane];
+        bq[half * (D / 32) + i][nt][1] = xb[(half * XW + (i * NT + nt) * 2 + 1) * 32 + lane];
+      }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) qzm[nt] = xq[4 * nt + tq] + xq[NH + 4 * nt + tq];
+}
+
+// One warp's half (tokens 64hf .. 64hf+63) of one page record.
+template <int D, int NT>
+__device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
+                                             const uint32_t (&bq)[D / 16][NT][2],
+                                             const float (&qzm)[NT], int lane, int hf,
+                                             WarpAcc<D, NT>& st) {
+  constexpr RecordLayout RL = record_layout(D);
+  const int g = lane >> 2;
+  const __half* Kr = reinterpret_cast<const __half*>(R + RL.kfactor);
+  const __half* Vs = reinterpret_cast<const __half*>(R + RL.vscale);
+  const __half* Vz = reinterpret_cast<const __half*>(R + RL.vzero);
+  const __half* Vc = reinterpret_cast<const __half*>(R + RL.vfactor);
 
   // ---- QK over the 4 m-tiles of this half ----
   float lg[4][NT][2];
@@ -322,10 +361,14 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   constexpr int NH = S::kNH;
   constexpr int REC = S::kRec;
   constexpr int QLD = S::kQld;
+  constexpr int NS = S::kSlots;
   extern __shared__ __align__(128) uint8_t smem_d[];
   uint8_t* recs = smem_d;
   float* qsm = reinterpret_cast<float*>(smem_d + S::kRecBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes);
+  uint8_t* xch = smem_d + S::kRecBytes + S::kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kXBytes);
+  int* issued = reinterpret_cast<int*>(bars + NS);
+  int* consumed = issued + NS;
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -351,29 +394,28 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
 
   if (!partial_split) {
     const int first = split * p.pages_per_split;
-    const int last = min(n_sealed, first + p.pages_per_split);
-    const int cnt = (last - first - pair + kDecPairs - 1) / kDecPairs;  // pages of this pair
-    uint64_t* bar = bars + pair * kDecStages;
-    uint8_t* rb = recs + pair * kDecStages * REC;
+    const int n = min(n_sealed, first + p.pages_per_split) - first;  // pages of this CTA
     const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
-    const bool producer = (hf == 0 && lane == 0);
-    auto page_src = [&](int k) -> const uint8_t* {
-      int64_t id = bt[first + pair + kDecPairs * k];
+    auto issue = [&](int k) {  // page k of this CTA into slot k % NS (one thread)
+      int64_t id = bt[first + k];
       if (id < 0 || id >= p.num_pool_pages) {
         flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
         id = 0;
       }
-      return p.pool + (id * p.num_kv_heads + h) * REC;
+      const int slot = k % NS;
+      atomicAdd(&issued[slot], 1);  // slots change issuer; shared atomics keep the counts exact
+      mbar_expect_tx(&bars[slot], REC);
+      bulk_copy_g2s(recs + slot * REC, p.pool + (id * p.num_kv_heads + h) * REC, REC, &bars[slot]);
     };
     // start the page stream before anything else
-    if (producer) {
-#pragma unroll
-      for (int s = 0; s < kDecStages; ++s) mbar_init(&bar[s], 1);
-      fence_mbar_init();
-      for (int k = 0; k < kDecStages && k < cnt; ++k) {
-        mbar_expect_tx(&bar[k], REC);
-        bulk_copy_g2s(rb + k * REC, page_src(k), REC, &bar[k]);
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(&bars[s], 1);
+        issued[s] = 0;
+        consumed[s] = 0;
       }
+      fence_mbar_init();
+      for (int k = 0; k < NS && k < n; ++k) issue(k);
     }
     // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d)
     for (int hl = warp; hl < NH; hl += kDecWarps) {
@@ -400,28 +442,36 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
 #pragma unroll
       for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
     }
-    for (int k = 0; k < cnt; ++k) {
-      const int s = k % kDecStages;
-      const bool arrived = mbar_wait(&bar[s], (k / kDecStages) & 1);
-      if (!pair_sync_and(pair, arrived)) {
-        // a copy never arrived: report, drain this pair's copies still in flight, stop
-        if (producer) {
-          flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
-          for (int k2 = k; k2 < cnt && k2 < k + kDecStages; ++k2)
-            mbar_wait(&bar[k2 % kDecStages], (k2 / kDecStages) & 1);
-        }
+    uint32_t* xb = reinterpret_cast<uint32_t*>(xch + pair * S::kXPairBytes);
+    float* xq = reinterpret_cast<float*>(xb + 2 * S::kXWords * 32);
+    for (int k = pair; k < n; k += kDecPairs) {
+      const int slot = k % NS;
+      const uint8_t* R = recs + slot * REC;
+      const bool arrived = mbar_wait(&bars[slot], (k / NS) & 1);
+      build_b_half<D, NT>(R, qsm, lane, hf, xb, xq);
+      if (!pair_sync_and(pair, arrived)) {   // also publishes both B halves to the pair
+        if (threadIdx.x == warp * 32 && hf == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
         break;
       }
-      process_half<D, NT>(rb + s * REC, qsm, lane, hf, st);
-      pair_sync(pair);  // both halves are done with this record
-      if (producer && k + kDecStages < cnt) {
+      if (hf == 0 && lane == 0) atomicAdd(&consumed[slot], 1);
+      uint32_t bq[D / 16][NT][2];
+      float qzm[NT];
+      gather_b<D, NT>(xb, xq, lane, bq, qzm);
+      process_half<D, NT>(R, bq, qzm, lane, hf, st);
+      pair_sync(pair);  // both halves are done with this record and the exchange buffer
+      if (hf == 0 && lane == 0 && k + NS < n) {
         fence_proxy_async_smem();
-        mbar_expect_tx(&bar[s], REC);
-        bulk_copy_g2s(rb + s * REC, page_src(k + kDecStages), REC, &bar[s]);
+        issue(k + NS);
       }
     }
     // ---- merge the warps of this CTA ----
-    __syncthreads();  // every pair is done with its record buffers
+    __syncthreads();  // every pair is done with the ring
+    if (threadIdx.x == 0) {
+      // after a timeout some issued copies were never consumed: wait (bounded) for them
+      for (int s = 0; s < NS; ++s)
+        if (consumed[s] < issued[s]) mbar_wait(&bars[s], (issued[s] - 1) & 1);
+    }
+    __syncthreads();
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;
