@@ -91,9 +91,8 @@ __device__ __forceinline__ float std_step_factor(float f_old, float m2, float in
 }
 
 template <int D, bool TRANS>
-__device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, int64_t tok_stride,
-                                              int d0, uint8_t* __restrict__ rec, int iters,
-                                              float eps, float* smem) {
+__device__ __forceinline__ void stage_and_rotate(const __half* __restrict__ src, int64_t tok_stride,
+                                                 int d0, float* smem, float (&x)[4][16]) {
   constexpr int NTH = QuantShape<D>::kThreads;
   constexpr int LD = QuantShape<D>::kLd;
   constexpr int LSIZE = TRANS ? D : kTile;
@@ -147,7 +146,6 @@ __device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, in
     __syncthreads();
   }
 
-  float x[4][16];
 #pragma unroll
   for (int l = 0; l < 4; ++l) {
 #pragma unroll
@@ -165,6 +163,27 @@ __device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, in
     }
   }
   __syncthreads();  // the staged tile is dead; its shared memory becomes reduction scratch
+
+}
+
+// Normalise, quantise, fold and pack one rotated unit held as x (layout above) into its half of
+// the page record.  smem: reduction scratch of at least 6*max(d,128) floats.
+template <int D, bool TRANS>
+__device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __restrict__ rec,
+                                                 int iters, float eps, float* smem) {
+  constexpr int NTH = QuantShape<D>::kThreads;
+  constexpr int LD = QuantShape<D>::kLd;
+  constexpr int LSIZE = TRANS ? D : kTile;
+  constexpr int CSIZE = TRANS ? kTile : D;
+  constexpr int NLQ = LSIZE / 32;
+  constexpr int NCH = CSIZE / 64;
+  constexpr int QMAX = TRANS ? 3 : 15;
+  constexpr RecordLayout RL = record_layout(D);
+  constexpr float kInvSqrtD = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const int lq = warp % NLQ, ch = warp / NLQ;
 
   float2* redL = reinterpret_cast<float2*>(smem);          // [NLQ][CSIZE]
   float2* redC = redL + NLQ * CSIZE;                         // [NCH][LSIZE]
@@ -419,6 +438,15 @@ __device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, in
   }
 }
 
+template <int D, bool TRANS>
+__device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, int64_t tok_stride,
+                                              int d0, uint8_t* __restrict__ rec, int iters,
+                                              float eps, float* smem) {
+  float x[4][16];
+  stage_and_rotate<D, TRANS>(src, tok_stride, d0, smem, x);
+  quantize_rotated<D, TRANS>(x, rec, iters, eps, smem);
+}
+
 // ---- kernels --------------------------------------------------------------------------------
 
 
@@ -485,11 +513,316 @@ static int launch_quantize(const QuantizeParams& p, int units, cudaStream_t stre
   return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
+// ---- head_dim 128: the rotation on the tensor cores -------------------------------------------
+//
+// Persistent CTAs of 256 threads walk a list of units.  Each CTA builds H_128 once in shared
+// memory and rotates every unit with tcgen05.mma (fp16 operands, exact +-1 entries, fp32
+// accumulation in tensor memory): K as D[token][channel] = Z . H, V as D[channel][token] =
+// H . Z^T, so in both cases the quantisation axis lies along TMEM lanes.  tcgen05.ld with the
+// 16x256b shape hands every thread exactly its 4 x 16 block of the layout used by
+// quantize_rotated.  The next unit's fp16 tile is fetched with cp.async and rotated into the
+// second TMEM buffer while the current unit is normalised and quantised.
+namespace tc {
+constexpr int kThreads = 256;
+constexpr int kOpBytes = 128 * 128 * 2;              // one 128 x 128 fp16 operand
+constexpr uint32_t kLbo = 128;                       // K-adjacent 8x8 core matrices
+constexpr uint32_t kSbo = 2048;                      // row-band-adjacent core matrices
+constexpr int kHOff = 0;
+constexpr int kZOff = kOpBytes;                      // two tile buffers
+constexpr int kScrOff = 3 * kOpBytes;
+constexpr int kScrBytes = 8192;                      // reduction scratch of quantize_rotated
+constexpr int kListCap = 256;                        // units per CTA
+constexpr int kListOff = kScrOff + kScrBytes;
+constexpr int kBarOff = kListOff + kListCap * 4;
+constexpr int kSmemBytes = kBarOff + 64;
+constexpr int kTmemCols = 256;                       // two 128-column fp32 accumulators
+// kind::f16 instruction descriptor: f32 accumulate, f16 A and B, both K-major, N = 128, M = 128
+constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ uint32_t canon(int r, int k) {  // byte offset of element (r, k)
+  return (uint32_t)((r >> 3) * kSbo + (k >> 3) * kLbo + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: no swizzle, canonical K-major layout.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(kLbo >> 4) << 16) |
+         ((uint64_t)(kSbo >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive accumulator columns of 16 TMEM lanes (16x256b, 8 repetitions).
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Source tile and destination record of a unit; false if the unit has nothing to do.
+__device__ __forceinline__ bool unit_io(const QuantizeParams& p, int u, const __half*& src,
+                                        int64_t& tok_stride, uint8_t*& rec) {
+  const int h = (u >> 1) % p.num_kv_heads;
+  const int t = (u >> 1) / p.num_kv_heads;  // tile, or sequence in append mode
+  const bool is_v = (u & 1) != 0;
+  int64_t page;
+  if (!p.append) {
+    src = (is_v ? p.v : p.k) + (int64_t)t * kTile * p.tok_stride + (int64_t)h * p.head_stride;
+    tok_stride = p.tok_stride;
+    page = p.page_ids[t];
+  } else {
+    const int len = p.seq_lens[t];
+    if (len < 0 || len >= p.max_pages * kTile || len % kTile != kTile - 1) return false;
+    src = (is_v ? p.partial_v : p.partial_k) + ((int64_t)t * p.num_kv_heads + h) * kTile * p.d0;
+    tok_stride = p.d0;
+    page = p.block_table[(int64_t)t * p.max_pages + len / kTile];
+  }
+  if (page < 0 || page >= p.num_pool_pages) return false;
+  rec = p.pool + (page * p.num_kv_heads + h) * p.rec_bytes;
+  return true;
+}
+
+// Stage one fp16 tile (128 tokens x d0, zero-padded to 128) into a canonical K-major buffer.
+__device__ __forceinline__ void load_tile(uint32_t zbuf, const __half* src, int64_t tok_stride,
+                                          int d0) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int q = threadIdx.x + kThreads * j;        // bits: [t & 7][c8][t >> 3]
+    const int t = (q & 7) | ((q >> 7) << 3), c8 = (q >> 3) & 15;
+    const bool in = c8 * 8 < d0;
+    cp_async16(zbuf + canon(t, c8 * 8), in ? (const void*)(src + t * tok_stride + c8 * 8) : (const void*)src,
+               in ? 16u : 0u);
+  }
+}
+
+}  // namespace tc
+
+__global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizeParams p, int units) {
+  extern __shared__ __align__(1024) uint8_t smem_tc[];
+  using namespace tc;
+  const uint32_t sbase = smem_u32(smem_tc);
+  int* list = reinterpret_cast<int*>(smem_tc + kListOff);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_tc + kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_tc + kBarOff + 16);
+  int* count = reinterpret_cast<int*>(smem_tc + kBarOff + 24);
+  float* scratch = reinterpret_cast<float*>(smem_tc + kScrOff);
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  // ---- this CTA's units (append mode: write every token first, keep the tiles that seal) ----
+  if (tid == 0) *count = 0;
+  __syncthreads();
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    if (p.append) {
+      const int h = (u >> 1) % p.num_kv_heads, b = (u >> 1) / p.num_kv_heads;
+      const bool is_v = (u & 1) != 0;
+      const int len = p.seq_lens[b];
+      if (len < 0 || len >= p.max_pages * kTile) {
+        if (tid == 0 && !is_v && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
+        continue;
+      }
+      __half* part = (is_v ? p.partial_v : p.partial_k) + ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
+      const __half* nw = (is_v ? p.v_new : p.k_new) + ((int64_t)b * p.num_kv_heads + h) * p.d0;
+      for (int c = tid * 8; c < p.d0; c += kThreads * 8)
+        *reinterpret_cast<uint4*>(part + (len % kTile) * p.d0 + c) = *reinterpret_cast<const uint4*>(nw + c);
+      if (tid == 0 && !is_v && h == 0 && p.seq_lens_out != nullptr) p.seq_lens_out[b] = len + 1;
+      if (len % kTile != kTile - 1) continue;
+    }
+    const __half* src;
+    int64_t ts;
+    uint8_t* rec;
+    if (!tc::unit_io(p, u, src, ts, rec)) {  // page id outside the pool: skip the unit
+      if (tid == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
+      continue;
+    }
+    if (tid == 0) {
+      const int n = *count;
+      if (n < kListCap) list[n] = u;  // the grid is sized so that n stays below kListCap
+      *count = n + 1;
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+  const int n_my = min(*count, kListCap);
+  if (n_my == 0) return;
+
+  // ---- set-up: H_128 in shared memory, two TMEM accumulators, two mbarriers ----
+  for (int q = tid; q < 128 * 16; q += kThreads) {
+    const int n = q >> 4, c8 = q & 15;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k0 = c8 * 8 + 2 * e;
+      const uint32_t lo = (__popc(n & k0) & 1) ? 0xBC00u : 0x3C00u;
+      const uint32_t hi = (__popc(n & (k0 + 1)) & 1) ? 0xBC00u : 0x3C00u;
+      w[e] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(smem_tc + kHOff + canon(n, c8 * 8)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "n"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    mbar_init(&mbar[0], 1);
+    mbar_init(&mbar[1], 1);
+    fence_mbar_init();
+  }
+  {
+    const __half* src;
+    int64_t ts;
+    uint8_t* rec;
+    tc::unit_io(p, list[0], src, ts, rec);
+    load_tile(sbase + kZOff, src, ts, p.d0);
+    cp_async_commit();
+    if (n_my > 1) {
+      tc::unit_io(p, list[1], src, ts, rec);
+      load_tile(sbase + kZOff + kOpBytes, src, ts, p.d0);
+    }
+    cp_async_commit();
+  }
+  const float isd = 0.08838834764831845f;
+  bool ok = true;
+  // issue the rotation of list[i] (its tile is in Z buffer i % 2) into TMEM buffer i % 2
+  auto issue_mma = [&](int i, uint32_t tmem_base) {
+    if (tid == 0) {
+      const bool is_v = (list[i] & 1) != 0;
+      const uint32_t z = sbase + kZOff + (i & 1) * kOpBytes, hm = sbase + kHOff;
+      const uint32_t a = is_v ? hm : z, b = is_v ? z : hm;
+      const uint32_t d = tmem_base + (i & 1) * 128;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t da = smem_desc(a + kk * 2 * kLbo), db = smem_desc(b + kk * 2 * kLbo);
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(da), "l"(db), "r"(kIdesc), "r"((uint32_t)kk));
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(&mbar[i & 1]))
+                   : "memory");
+    }
+  };
+  cp_async_wait<1>();
+  fence_proxy_async_smem();  // H and tile 0 written by the generic proxy, read by the MMA
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  issue_mma(0, tmem_base);
+
+  int issued = 1;  // MMAs issued so far (for draining after a timeout)
+  for (int i = 0; i < n_my; ++i) {
+    // one decision for the whole CTA, so that no thread leaves while others wait at a barrier
+    ok = __syncthreads_and(mbar_wait(&mbar[i & 1], (i >> 1) & 1) ? 1 : 0) != 0;
+    if (!ok && tid == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+    tc_fence_after();
+    float x[4][16];
+    {
+      const uint32_t col = tmem_base + (i & 1) * 128 + 64 * (warp >> 2);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld_16x256b_x8(col + ((uint32_t)(32 * (warp & 3) + 16 * half) << 16), r);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+            x[2 * half][2 * u + pp] = __uint_as_float(r[4 * u + pp]) * isd;
+            x[2 * half + 1][2 * u + pp] = __uint_as_float(r[4 * u + 2 + pp]) * isd;
+          }
+      }
+    }
+    // Z buffer i % 2 is free (its MMA completed): fetch list[i + 2] into it
+    if (i + 2 < n_my) {
+      const __half* src;
+      int64_t ts;
+      uint8_t* rec;
+      tc::unit_io(p, list[i + 2], src, ts, rec);
+      load_tile(sbase + kZOff + (i & 1) * kOpBytes, src, ts, p.d0);
+    }
+    cp_async_commit();
+    // rotate list[i + 1] (loaded one iteration ago) into the other TMEM buffer
+    if (i + 1 < n_my) {
+      cp_async_wait<1>();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (ok) {
+        issue_mma(i + 1, tmem_base);
+        ++issued;
+      }
+    }
+    if (!ok) break;
+    {
+      const __half* src;
+      int64_t ts;
+      uint8_t* rec;
+      tc::unit_io(p, list[i], src, ts, rec);
+      if ((list[i] & 1) != 0)
+        quantize_rotated<128, true>(x, rec, p.iters, p.eps, scratch);
+      else
+        quantize_rotated<128, false>(x, rec, p.iters, p.eps, scratch);
+    }
+    __syncthreads();  // the scratch of this unit is dead before the next one starts
+  }
+  // ---- tear-down: no MMA may still write TMEM when it is released ----
+  cp_async_wait<0>();
+  if (!ok && tid == 0) {  // the last batch issued into each buffer (earlier ones precede it)
+    for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&mbar[j & 1], (j >> 1) & 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "n"(kTmemCols));
+  }
+}
+
+static int launch_quantize_tc(const QuantizeParams& p, int units2, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(quantize_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::kSmemBytes) != cudaSuccess)
+      return KVARN_ERR_CUDA;
+    attr_set = true;
+  }
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int grid = 2 * sms;
+  grid = max(grid, (units2 + tc::kListCap - 1) / tc::kListCap);
+  grid = min(grid, units2);
+  quantize_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(p, units2);
+  return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
 int launch_quantize_any(int d, const QuantizeParams& p, int units, cudaStream_t stream) {
   if (units <= 0) return KVARN_OK;
   switch (d) {
     case 64: return launch_quantize<64>(p, units, stream);
-    case 128: return launch_quantize<128>(p, units, stream);
+    case 128: return launch_quantize_tc(p, units * 2, stream);
     case 256: return launch_quantize<256>(p, units, stream);
     default: return KVARN_ERR_UNSUPPORTED;
   }
