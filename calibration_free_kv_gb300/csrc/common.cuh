@@ -11,21 +11,22 @@ namespace kvarn {
 constexpr int kTile = 128;                 // tokens per tile == tokens per page
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Byte offsets of the sections of one (page, kv head) record for padded head_dim d.
+// Byte offsets of the sections of one (page, kv head) record for padded head_dim d: the K half
+// (codes, scale, zero, token factor) then the V half (codes, scale, zero, channel factor).
 struct RecordLayout {
-  int kcodes, vcodes, kscale, kzero, kfactor, vscale, vzero, vfactor, bytes;
+  int kcodes, kscale, kzero, kfactor, vcodes, vscale, vzero, vfactor, bytes;
 };
 
 __host__ __device__ constexpr RecordLayout record_layout(int d) {
   return RecordLayout{0,
                       kTile * d / 2,
-                      kTile * d / 2 + kTile * d / 4,
-                      kTile * d / 2 + kTile * d / 4 + 2 * d,
-                      kTile * d / 2 + kTile * d / 4 + 4 * d,
-                      kTile * d / 2 + kTile * d / 4 + 4 * d + 2 * kTile,
-                      kTile * d / 2 + kTile * d / 4 + 4 * d + 4 * kTile,
-                      kTile * d / 2 + kTile * d / 4 + 4 * d + 6 * kTile,
-                      kTile * d / 2 + kTile * d / 4 + 6 * d + 6 * kTile};
+                      kTile * d / 2 + 2 * d,
+                      kTile * d / 2 + 4 * d,
+                      kTile * d / 2 + 4 * d + 2 * kTile,
+                      kTile * d / 2 + 4 * d + 2 * kTile + kTile * d / 4,
+                      kTile * d / 2 + 4 * d + 4 * kTile + kTile * d / 4,
+                      kTile * d / 2 + 4 * d + 6 * kTile + kTile * d / 4,
+                      kTile * d / 2 + 6 * d + 6 * kTile + kTile * d / 4};
 }
 
 __device__ __forceinline__ void flag_error(int32_t* status, int bits) {

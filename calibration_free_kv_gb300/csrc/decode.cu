@@ -7,15 +7,15 @@
 //  hotdry §非对称量化与尺度折叠: the folded scales are multiplied back at read time]
 //
 // decode_kernel: grid (split, kv head, sequence).  A CTA owns up to `pages_per_split` sealed
-// pages of one (sequence, kv head), or the raw fp16 partial tile.  Whole page records stream
-// into a ring of shared-memory slots with 1-D bulk copies completed on mbarriers: page k of
-// the split goes to slot k % kSlots, and the pair that finishes page k issues page k + kSlots
-// into the slot it freed.  Its 8 warps form 4 pairs that take pages round-robin; the two
-// warps of a pair split each page into token halves and keep independent online-softmax
-// states:
+// pages of one (sequence, kv head), or the raw fp16 partial tile.  Its 8 warps take whole
+// pages round-robin.  Every warp owns two shared-memory slots, one for the K half of a page
+// record and one for the V half, each filled by a 1-D bulk copy completed on its own
+// mbarrier: the K half of the next page streams in while the warp works on the current
+// page's V half, and the V half of the next page while it works on the next K half.
 //   QK:  m16n8k16 MMAs, A = 4-bit codes [token x channel], B = q~ . s'_K split into fp16
-//        hi + lo (columns: 4 heads x {hi, lo}); each warp of the pair builds half of B and
-//        the halves are exchanged through shared memory.
+//        hi + lo (columns: 4 heads x {hi, lo}); hi = fp16(qh s'), lo = fp16(ql s' + (qh s' -
+//        hi)) with q~ = qh + ql pre-split once per CTA and the product error taken exactly
+//        by an fp16 fma.
 //   softmax: online, log2 domain (tau log2(e) folded into q~).
 //   PV:  m16n8k16 MMAs, A = 2-bit codes^T [channel x token], B = p . s'_V split hi + lo,
 //        moved from the QK accumulator layout with movmatrix.trans.
@@ -29,24 +29,20 @@
 
 namespace kvarn {
 
-constexpr int kDecWarps = 8;            // 4 pairs
-constexpr int kDecPairs = kDecWarps / 2;
+constexpr int kDecWarps = 8;
 constexpr float kTwo24 = 16777216.0f;
 
 template <int D, int NT>
 struct DecodeShape {
   static constexpr int kNH = 4 * NT;                 // head slots per kv head (G padded)
-  static constexpr int kSlots = NT == 2 ? 6 : 7;     // page records in flight per CTA
   static constexpr int kRec = record_layout(D).bytes;
+  static constexpr int kKHalf = record_layout(D).vcodes;   // K codes + K metadata
+  static constexpr int kVHalf = kRec - kKHalf;             // V codes + V metadata
   static constexpr int kQld = D + 8;                 // fp32 row stride of q in shared memory
-  static constexpr int kRecBytes = kSlots * kRec;
-  static constexpr int kQBytes = kNH * kQld * 4;
-  // per pair: B-operand halves [2][kXWords][32 lanes] u32 and q~.z' halves [2][kNH] f32
-  static constexpr int kXWords = (D / 32) * NT * 2;
-  static constexpr int kXPairBytes = 2 * kXWords * 32 * 4 + 2 * kNH * 4;
-  static constexpr int kXBytes = kDecPairs * kXPairBytes;
-  // mbarriers, then per slot: copies issued and copies consumed (for draining after a timeout)
-  static constexpr int kSmemBytes = kRecBytes + kQBytes + kXBytes + kSlots * 8 + 2 * kSlots * 4;
+  static constexpr int kRecBytes = kDecWarps * kRec; // one K slot + one V slot per warp
+  static constexpr int kQBytes = kNH * kQld * 4;     // q~ (fp32) for q~ . z'
+  static constexpr int kQhBytes = 2 * kNH * (D / 2 + 4) * 4;  // q~ as fp16 hi and lo, padded rows
+  static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + kDecWarps * 2 * 8;
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -64,24 +60,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t r;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
   return r;
-}
-
-__device__ __forceinline__ void pair_sync(int pair) {
-  asm volatile("bar.sync %0, 64;" ::"r"(pair + 1) : "memory");
-}
-
-// Barrier of the two warps of a pair that also ANDs a predicate over them.
-__device__ __forceinline__ bool pair_sync_and(int pair, bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, 64, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "r"(pair + 1)
-      : "memory");
-  return r != 0;
 }
 
 // K word -> A fragment as fp16 subnormals: a0/a1 (channels 2tq..) = code * 2^-24,
@@ -151,97 +129,66 @@ struct WarpAcc {
   float o[D / 16][NT][2];  // head 4nt + tq, channels 16mc + g + 8r (rotated basis)
 };
 
-// This warp's half (k-steps hf*D/32 ..) of the QK B operand -- q~_j s'_j as fp16 hi (even g)
-// or lo (odd g) -- written to the pair's exchange buffer, and its partial q~ . z' per head.
+// One column pair of the QK B operand for the lane's head: fp16 hi = qh s' (lanes with even g)
+// or lo = ql s' + (qh s' - hi) (odd g); the fma takes the rounding error of qh s' exactly.
+__device__ __forceinline__ uint32_t b_split(__half2 qh, __half2 ql, __half2 s, bool lo) {
+  const __half2 hi = __hmul2(qh, s);
+  const __half2 err = __hfma2(qh, s, __hneg2(hi));
+  return h2u(lo ? __hfma2(ql, s, err) : hi);
+}
+
+// QK of one whole page from its K half Rk: logits -> probabilities lg (tokens 16mi + g + 8r
+// of head 4nt + tq), online-softmax state updated, alpha = rescale of the previous state.
 template <int D, int NT>
-__device__ __forceinline__ void build_b_half(const uint8_t* __restrict__ R,
-                                             const float* __restrict__ qrot, int lane, int hf,
-                                             uint32_t* __restrict__ xb, float* __restrict__ xq) {
+__device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const float* __restrict__ qsm,
+                                        const __half2* __restrict__ qh2, const __half2* __restrict__ ql2,
+                                        int lane, WarpAcc<D, NT>& st, float (&lg)[8][NT][2],
+                                        float (&alpha)[NT]) {
   constexpr RecordLayout RL = record_layout(D);
   constexpr int QLD = DecodeShape<D, NT>::kQld;
-  constexpr int XW = DecodeShape<D, NT>::kXWords;
-  constexpr int NH = DecodeShape<D, NT>::kNH;
+  constexpr int QH = D / 2 + 4;  // half2 row stride of qh / ql
   const int g = lane >> 2, tq = lane & 3;
-  const __half* Ks = reinterpret_cast<const __half*>(R + RL.kscale);
-  const __half* Kz = reinterpret_cast<const __half*>(R + RL.kzero);
+  const __half2* Ks2 = reinterpret_cast<const __half2*>(Rk + RL.kscale);
+  const __half2* Kz2 = reinterpret_cast<const __half2*>(Rk + RL.kzero);
+  const __half* Kr = reinterpret_cast<const __half*>(Rk + RL.kfactor);
+
+  uint32_t bq[D / 16][NT][2];
   float qz[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) qz[nt] = 0.0f;
   const bool lo_col = (g & 1) != 0;
-  uint32_t* mine = xb + hf * XW * 32 + lane;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) {
-    const int j0 = 16 * (hf * (D / 32) + i) + 2 * tq;
-    const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(Ks + j0));
-    const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(Ks + j0 + 8));
-    const float2 z0 = __half22float2(*reinterpret_cast<const __half2*>(Kz + j0));
-    const float2 z1 = __half22float2(*reinterpret_cast<const __half2*>(Kz + j0 + 8));
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int j0 = 16 * kk + 2 * tq;
+    const __half2 s0 = Ks2[j0 >> 1], s1 = Ks2[(j0 + 8) >> 1];
+    const float2 z0 = __half22float2(Kz2[j0 >> 1]), z1 = __half22float2(Kz2[(j0 + 8) >> 1]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float* qr = qrot + (4 * nt + (g >> 1)) * QLD;
-      const float2 qa = *reinterpret_cast<const float2*>(qr + j0);
-      const float2 qb = *reinterpret_cast<const float2*>(qr + j0 + 8);
+      const int head = 4 * nt + (g >> 1);
+      const float2 qa = *reinterpret_cast<const float2*>(qsm + head * QLD + j0);
+      const float2 qb = *reinterpret_cast<const float2*>(qsm + head * QLD + j0 + 8);
       qz[nt] = fmaf(qa.x, z0.x, fmaf(qa.y, z0.y, fmaf(qb.x, z1.x, fmaf(qb.y, z1.y, qz[nt]))));
-      mine[((i * NT + nt) * 2) * 32] = split_pick(qa.x * s0.x, qa.y * s0.y, lo_col);
-      // channels 2tq+8.. meet codes scaled by 2^-20 instead of 2^-24
-      mine[((i * NT + nt) * 2 + 1) * 32] = split_pick(qb.x * s1.x * 0.0625f, qb.y * s1.y * 0.0625f, lo_col);
+      bq[kk][nt][0] = b_split(qh2[head * QH + (j0 >> 1)], ql2[head * QH + (j0 >> 1)], s0, lo_col);
+      bq[kk][nt][1] = b_split(qh2[head * QH + ((j0 + 8) >> 1)], ql2[head * QH + ((j0 + 8) >> 1)], s1, lo_col);
     }
   }
+  float qzm[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float v = qz[nt];
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
-    if (tq == 0 && (g & 1) == 0) xq[hf * NH + 4 * nt + (g >> 1)] = v;  // head 4nt + g/2
+    qzm[nt] = __shfl_sync(0xffffffffu, v, 8 * tq);  // head 4nt + tq lives in lanes g = 2tq
   }
-}
-
-// Both halves of the QK B operand and the full q~ . z' of the lane's heads (4nt + tq).
-template <int D, int NT>
-__device__ __forceinline__ void gather_b(const uint32_t* __restrict__ xb,
-                                         const float* __restrict__ xq, int lane,
-                                         uint32_t (&bq)[D / 16][NT][2], float (&qzm)[NT]) {
-  constexpr int XW = DecodeShape<D, NT>::kXWords;
-  constexpr int NH = DecodeShape<D, NT>::kNH;
-  const int tq = lane & 3;
 #pragma unroll
-  for (int half = 0; half < 2; ++half)
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        bq[half * (D / 32) + i][nt][0] = xb[(half * XW + (i * NT + nt) * 2) * 32 + lane];
-        bq[half * (D / 32) + i][nt][1] = xb[(half * XW + (i * NT + nt) * 2 + 1) * 32 + lane];
-      }
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) qzm[nt] = xq[4 * nt + tq] + xq[NH + 4 * nt + tq];
-}
-
-// One warp's half (tokens 64hf .. 64hf+63) of one page record.
-template <int D, int NT>
-__device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
-                                             const uint32_t (&bq)[D / 16][NT][2],
-                                             const float (&qzm)[NT], int lane, int hf,
-                                             WarpAcc<D, NT>& st) {
-  constexpr RecordLayout RL = record_layout(D);
-  const int g = lane >> 2;
-  const __half* Kr = reinterpret_cast<const __half*>(R + RL.kfactor);
-  const __half* Vs = reinterpret_cast<const __half*>(R + RL.vscale);
-  const __half* Vz = reinterpret_cast<const __half*>(R + RL.vzero);
-  const __half* Vc = reinterpret_cast<const __half*>(R + RL.vfactor);
-
-  // ---- QK over the 4 m-tiles of this half ----
-  float lg[4][NT][2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int mi = 4 * hf + i;
+  for (int mi = 0; mi < 8; ++mi) {
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
 #pragma unroll
     for (int kq = 0; kq < D / 64; ++kq) {
       const uint4 w4 =
-          *reinterpret_cast<const uint4*>(R + RL.kcodes + ((mi * (D / 64) + kq) * 32 + lane) * 16);
+          *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi * (D / 64) + kq) * 32 + lane) * 16);
       const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -255,18 +202,15 @@ __device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
     const float r1 = __half2float(Kr[16 * mi + g + 8]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      lg[i][nt][0] = r0 * fmaf(acc[nt][0] + acc[nt][1], kTwo24, qzm[nt]);
-      lg[i][nt][1] = r1 * fmaf(acc[nt][2] + acc[nt][3], kTwo24, qzm[nt]);
+      lg[mi][nt][0] = r0 * fmaf(acc[nt][0] + acc[nt][1], kTwo24, qzm[nt]);
+      lg[mi][nt][1] = r1 * fmaf(acc[nt][2] + acc[nt][3], kTwo24, qzm[nt]);
     }
   }
-
-  // ---- online softmax (per head, over this warp's tokens) ----
-  float alpha[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float mx = fmaxf(lg[0][nt][0], lg[0][nt][1]);
 #pragma unroll
-    for (int i = 1; i < 4; ++i) mx = fmaxf(mx, fmaxf(lg[i][nt][0], lg[i][nt][1]));
+    for (int mi = 1; mi < 8; ++mi) mx = fmaxf(mx, fmaxf(lg[mi][nt][0], lg[mi][nt][1]));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
@@ -275,17 +219,26 @@ __device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
     st.m[nt] = mnew;
     float ps = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int mi = 0; mi < 8; ++mi)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float pv = exp2f(lg[i][nt][r] - mnew);
-        lg[i][nt][r] = pv;
+        const float pv = exp2f(lg[mi][nt][r] - mnew);
+        lg[mi][nt][r] = pv;
         ps += pv;
       }
     st.l[nt] = fmaf(st.l[nt], alpha[nt], ps);
   }
+}
 
-  // ---- PV over the 4 k-steps (2 V words) of this half ----
+// PV of one whole page from its V half Rv with the probabilities of qk_page.
+template <int D, int NT>
+__device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const float (&lg)[8][NT][2],
+                                        const float (&alpha)[NT], int lane, WarpAcc<D, NT>& st) {
+  constexpr RecordLayout RL = record_layout(D);
+  const int g = lane >> 2;
+  const __half* Vs = reinterpret_cast<const __half*>(Rv + (RL.vscale - RL.vcodes));
+  const __half* Vz = reinterpret_cast<const __half*>(Rv + (RL.vzero - RL.vcodes));
+  const __half* Vc = reinterpret_cast<const __half*>(Rv + (RL.vfactor - RL.vcodes));
   float pacc[D / 16][NT][4];
 #pragma unroll
   for (int mc = 0; mc < D / 16; ++mc)
@@ -295,20 +248,18 @@ __device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) zs[nt] = 0.0f;
 #pragma unroll
-  for (int j2 = 0; j2 < 2; ++j2) {
-    const int ks2 = 2 * hf + j2;
+  for (int ks2 = 0; ks2 < 4; ++ks2) {
     uint32_t bw[2][NT][2];
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
       const int ks = 2 * ks2 + f;
-      const int li = 2 * j2 + f;  // this half's m-tile index of the same 16 tokens
       const float sv0 = __half2float(Vs[16 * ks + g]), sv1 = __half2float(Vs[16 * ks + g + 8]);
       const float zv0 = __half2float(Vz[16 * ks + g]), zv1 = __half2float(Vz[16 * ks + g + 8]);
       // compensate the subnormal scale 2^(4f + 2h) of this block's codes (h = 0: rows g)
       const float c0 = f ? 1.0f / 16.0f : 1.0f, c1 = f ? 1.0f / 64.0f : 0.25f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float p0 = lg[li][nt][0], p1 = lg[li][nt][1];
+        const float p0 = lg[ks][nt][0], p1 = lg[ks][nt][1];
         zs[nt] = fmaf(p0, zv0, fmaf(p1, zv1, zs[nt]));
         const float w0 = p0 * sv0 * c0, w1 = p1 * sv1 * c1;
         const __half hi0 = __float2half_rn(w0), hi1 = __float2half_rn(w1);
@@ -320,8 +271,7 @@ __device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
     }
 #pragma unroll
     for (int mq = 0; mq < D / 64; ++mq) {
-      const uint4 w4 =
-          *reinterpret_cast<const uint4*>(R + RL.vcodes + ((ks2 * (D / 64) + mq) * 32 + lane) * 16);
+      const uint4 w4 = *reinterpret_cast<const uint4*>(Rv + ((ks2 * (D / 64) + mq) * 32 + lane) * 16);
       const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -356,23 +306,23 @@ __device__ __forceinline__ void process_half(const uint8_t* __restrict__ R,
 }
 
 template <int D, int NT>
-__global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1) decode_kernel(DecodeParams p) {
   using S = DecodeShape<D, NT>;
   constexpr int NH = S::kNH;
   constexpr int REC = S::kRec;
+  constexpr int KH = S::kKHalf;
+  constexpr int VH = S::kVHalf;
   constexpr int QLD = S::kQld;
-  constexpr int NS = S::kSlots;
+  constexpr int QH = D / 2 + 4;
   extern __shared__ __align__(128) uint8_t smem_d[];
   uint8_t* recs = smem_d;
   float* qsm = reinterpret_cast<float*>(smem_d + S::kRecBytes);
-  uint8_t* xch = smem_d + S::kRecBytes + S::kQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kXBytes);
-  int* issued = reinterpret_cast<int*>(bars + NS);
-  int* consumed = issued + NS;
+  __half2* qh2 = reinterpret_cast<__half2*>(smem_d + S::kRecBytes + S::kQBytes);
+  __half2* ql2 = qh2 + NH * QH;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kQhBytes);
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int pair = warp >> 1, hf = warp & 1;
   const int g = lane >> 2, tq = lane & 3;
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
   int len = p.seq_lens[b];
@@ -395,29 +345,36 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
   if (!partial_split) {
     const int first = split * p.pages_per_split;
     const int n = min(n_sealed, first + p.pages_per_split) - first;  // pages of this CTA
+    const int cnt = n > warp ? (n - warp + kDecWarps - 1) / kDecWarps : 0;  // pages of this warp
+    uint8_t* kslot = recs + warp * REC;
+    uint8_t* vslot = kslot + KH;
+    uint64_t* kbar = bars + 2 * warp;
+    uint64_t* vbar = kbar + 1;
     const int32_t* bt = p.block_table + (int64_t)b * p.max_pages;
-    auto issue = [&](int k) {  // page k of this CTA into slot k % NS (one thread)
-      int64_t id = bt[first + k];
+    auto page_src = [&](int j) -> const uint8_t* {  // record of this warp's j-th page
+      int64_t id = bt[first + warp + kDecWarps * j];
       if (id < 0 || id >= p.num_pool_pages) {
         flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
         id = 0;
       }
-      const int slot = k % NS;
-      atomicAdd(&issued[slot], 1);  // slots change issuer; shared atomics keep the counts exact
-      mbar_expect_tx(&bars[slot], REC);
-      bulk_copy_g2s(recs + slot * REC, p.pool + (id * p.num_kv_heads + h) * REC, REC, &bars[slot]);
+      return p.pool + (id * p.num_kv_heads + h) * REC;
     };
-    // start the page stream before anything else
-    if (threadIdx.x == 0) {
-      for (int s = 0; s < NS; ++s) {
-        mbar_init(&bars[s], 1);
-        issued[s] = 0;
-        consumed[s] = 0;
-      }
+    // start this warp's page stream before anything else
+    if (lane == 0) {
+      mbar_init(kbar, 1);
+      mbar_init(vbar, 1);
       fence_mbar_init();
-      for (int k = 0; k < NS && k < n; ++k) issue(k);
+      if (cnt > 0) {
+        const uint8_t* src = page_src(0);
+        mbar_expect_tx(kbar, KH);
+        bulk_copy_g2s(kslot, src, KH, kbar);
+        mbar_expect_tx(vbar, VH);
+        bulk_copy_g2s(vslot, src + KH, VH, vbar);
+      }
     }
-    // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d)
+    // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d): fp32 for q~.z',
+    // fp16 hi + lo for the B operand (channels 8..15 of every 16 pre-divided by 16, the
+    // subnormal scale of their codes)
     for (int hl = warp; hl < NH; hl += kDecWarps) {
       float v[D / 32];
 #pragma unroll
@@ -429,10 +386,20 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
       }
       warp_fwht<D>(v, lane);
       const float sc = p.qscale * inv_sqrt_d<D>();
+      __half* qh = reinterpret_cast<__half*>(qh2 + hl * QH);
+      __half* ql = reinterpret_cast<__half*>(ql2 + hl * QH);
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) qsm[hl * QLD + lane * (D / 32) + e] = v[e] * sc;
+      for (int e = 0; e < D / 32; ++e) {
+        const int j = lane * (D / 32) + e;
+        const float x = v[e] * sc;
+        qsm[hl * QLD + j] = x;
+        const float xb = (j & 15) >= 8 ? x * 0.0625f : x;
+        const __half hi = __float2half_rn(xb);
+        qh[j] = hi;
+        ql[j] = __float2half_rn(xb - __half2float(hi));
+      }
     }
-    __syncthreads();  // q in shared memory and the barriers initialised for every warp
+    __syncthreads();  // q in shared memory for every warp
 
     WarpAcc<D, NT> st;
 #pragma unroll
@@ -442,36 +409,44 @@ __global__ void __launch_bounds__(kDecWarps * 32, 2) decode_kernel(DecodeParams 
 #pragma unroll
       for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
     }
-    uint32_t* xb = reinterpret_cast<uint32_t*>(xch + pair * S::kXPairBytes);
-    float* xq = reinterpret_cast<float*>(xb + 2 * S::kXWords * 32);
-    for (int k = pair; k < n; k += kDecPairs) {
-      const int slot = k % NS;
-      const uint8_t* R = recs + slot * REC;
-      const bool arrived = mbar_wait(&bars[slot], (k / NS) & 1);
-      build_b_half<D, NT>(R, qsm, lane, hf, xb, xq);
-      if (!pair_sync_and(pair, arrived)) {   // also publishes both B halves to the pair
-        if (threadIdx.x == warp * 32 && hf == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+    for (int j = 0; j < cnt; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(kbar, j & 1))) {
+        // a copy never arrived: report, drain this warp's copies still in flight, stop
+        if (lane == 0) {
+          flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+          mbar_wait(kbar, j & 1);
+          mbar_wait(vbar, j & 1);
+        }
         break;
       }
-      if (hf == 0 && lane == 0) atomicAdd(&consumed[slot], 1);
-      uint32_t bq[D / 16][NT][2];
-      float qzm[NT];
-      gather_b<D, NT>(xb, xq, lane, bq, qzm);
-      process_half<D, NT>(R, bq, qzm, lane, hf, st);
-      pair_sync(pair);  // both halves are done with this record and the exchange buffer
-      if (hf == 0 && lane == 0 && k + NS < n) {
+      float lg[8][NT][2], alpha[NT];
+      qk_page<D, NT>(kslot, qsm, qh2, ql2, lane, st, lg, alpha);
+      __syncwarp();
+      const bool more = j + 1 < cnt;
+      const uint8_t* nxt = more ? page_src(j + 1) : nullptr;
+      if (lane == 0 && more) {  // the K slot is free: fetch the next page's K half
         fence_proxy_async_smem();
-        issue(k + NS);
+        mbar_expect_tx(kbar, KH);
+        bulk_copy_g2s(kslot, nxt, KH, kbar);
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(vbar, j & 1))) {
+        if (lane == 0) {
+          flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+          mbar_wait(vbar, j & 1);
+          if (more) mbar_wait(kbar, (j + 1) & 1);
+        }
+        break;
+      }
+      pv_page<D, NT>(vslot, lg, alpha, lane, st);
+      __syncwarp();
+      if (lane == 0 && more) {  // the V slot is free: fetch the next page's V half
+        fence_proxy_async_smem();
+        mbar_expect_tx(vbar, VH);
+        bulk_copy_g2s(vslot, nxt + KH, VH, vbar);
       }
     }
     // ---- merge the warps of this CTA ----
-    __syncthreads();  // every pair is done with the ring
-    if (threadIdx.x == 0) {
-      // after a timeout some issued copies were never consumed: wait (bounded) for them
-      for (int s = 0; s < NS; ++s)
-        if (consumed[s] < issued[s]) mbar_wait(&bars[s], (issued[s] - 1) & 1);
-    }
-    __syncthreads();
+    __syncthreads();  // every warp is done with its slots
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;

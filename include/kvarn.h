@@ -35,9 +35,10 @@
  * sections.  The page pool is [num_pool_pages][num_kv_heads][record_bytes]; record (p, h)
  * starts at byte ((p * num_kv_heads) + h) * record_bytes.  With T = 128:
  *    K codes  T*d/2 B   uint32 words of eight 4-bit codes
+ *    K scale s'[d], K zero z'[d], K token factor r[T]            (fp16)
  *    V codes  T*d/4 B   uint32 words of sixteen 2-bit codes
- *    K scale s'[d], K zero z'[d], K token factor r[T],
  *    V scale s'[T], V zero z'[T], V channel factor c[d]          (fp16)
+ * (the K half, T*d/2 + 4d + 2T bytes, precedes the V half, so each can be fetched alone).
  * Dequantised rotated-domain values: K~[t][j] = r[t] (code*s'[j] + z'[j]),
  * V~[t][j] = c[j] (code*s'[t] + z'[t]); original basis = rows of (.) H_d / sqrt(d), first d0.
  * K word (mi, kk, lane) [mi < 8, kk < d/16, lane < 32, g = lane/4, tq = lane%4] is word

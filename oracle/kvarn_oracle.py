@@ -238,9 +238,9 @@ def dequantize_tile(codes, scale, zero, factor, kind: str, d0: int) -> np.ndarra
 # live with the 128-token block: vatt §怎麼用, "scales hang on each block's
 # metadata").  Sections, all 16-byte aligned, T = 128, d = padded head_dim:
 #   K codes  T*d/2 bytes, uint32 words of eight 4-bit codes
+#   K scale[d], K zero[d], K token factor[T]  (fp16, little endian)
 #   V codes  T*d/4 bytes, uint32 words of sixteen 2-bit codes
-#   K scale[d], K zero[d], K token factor[T], V scale[T], V zero[T],
-#   V channel factor[d]                       (fp16, little endian)
+#   V scale[T], V zero[T], V channel factor[d] (fp16, little endian)
 #
 # K word (mi, kk, lane), mi in [0,8), kk in [0,d/16), lane in [0,32), g = lane//4,
 # tq = lane%4: word index ((mi*(d//64) + kk//4)*32 + lane)*4 + kk%4.  It holds
@@ -261,13 +261,14 @@ def record_bytes(d: int, tokens: int = TILE_TOKENS) -> int:
 
 
 def _section_offsets(d: int):
+    """Byte offsets (K codes, V codes, K scale, K zero, K factor, V scale, V zero, V factor)."""
     t = TILE_TOKENS
     o_kc = 0
-    o_vc = t * d // 2
-    o_ks = o_vc + t * d // 4
+    o_ks = t * d // 2
     o_kz = o_ks + 2 * d
     o_kr = o_kz + 2 * d
-    o_vs = o_kr + 2 * t
+    o_vc = o_kr + 2 * t
+    o_vs = o_vc + t * d // 4
     o_vz = o_vs + 2 * t
     o_vcf = o_vz + 2 * t
     return o_kc, o_vc, o_ks, o_kz, o_kr, o_vs, o_vz, o_vcf
@@ -318,9 +319,11 @@ def pack_record(k: dict, v: dict) -> bytes:
     vw = np.zeros(TILE_TOKENS * d // 16, dtype=np.uint32)
     word, shift = _v_positions(d)
     np.bitwise_or.at(vw, word.ravel(), (qv << shift.astype(np.uint32)).ravel())
-    meta = [k["scale"], k["zero"], k["factor"], v["scale"], v["zero"], v["factor"]]
-    parts = [kw.astype("<u4").tobytes(), vw.astype("<u4").tobytes()]
-    parts += [np.asarray(a, dtype=np.float16).astype("<f2").tobytes() for a in meta]
+    def f16(a):
+        return np.asarray(a, dtype=np.float16).astype("<f2").tobytes()
+
+    parts = [kw.astype("<u4").tobytes(), f16(k["scale"]), f16(k["zero"]), f16(k["factor"]),
+             vw.astype("<u4").tobytes(), f16(v["scale"]), f16(v["zero"]), f16(v["factor"])]
     out = b"".join(parts)
     assert len(out) == record_bytes(d)
     return out
@@ -333,8 +336,8 @@ def unpack_record(rec, d: int):
         raise ValueError("record size does not match head_dim")
     o_kc, o_vc, o_ks, o_kz, o_kr, o_vs, o_vz, o_vcf = _section_offsets(d)
     t = TILE_TOKENS
-    kw = buf[o_kc:o_vc].view("<u4").astype(np.uint32)
-    vw = buf[o_vc:o_ks].view("<u4").astype(np.uint32)
+    kw = buf[o_kc:o_ks].view("<u4").astype(np.uint32)
+    vw = buf[o_vc:o_vs].view("<u4").astype(np.uint32)
     word, shift = _k_positions(d)
     qk = ((kw[word] >> shift.astype(np.uint32)) & 0xF).astype(np.uint8)
     word, shift = _v_positions(d)

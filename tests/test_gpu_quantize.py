@@ -103,10 +103,11 @@ def test_quantize_full_size_sampled(kv):
     kv.quantize_tiles(desc, k, v, torch.arange(128, dtype=torch.int32, device="cuda"), pool2)
     torch.cuda.synchronize()
     assert torch.equal(pool, pool2)
-    # every K code fits 4 bits by construction; scales are finite and positive
-    rl = ko._section_offsets(128)
-    meta = pool[:, :, rl[2]:].contiguous().view(torch.float16)
-    assert torch.isfinite(meta.float()).all()
+    # the fp16 metadata of every record is finite
+    o_kc, o_vc, o_ks, _, _, o_vs, _, _ = ko._section_offsets(128)
+    for lo, hi in ((o_ks, o_vc), (o_vs, pool.shape[-1])):
+        meta = pool[:, :, lo:hi].contiguous().view(torch.float16)
+        assert torch.isfinite(meta.float()).all()
 
 
 @pytest.mark.parametrize("d0", [128, 96, 256])

@@ -359,8 +359,12 @@ def test_code_words_are_mma_fragments(d):
                          {"codes": qv, "scale": np.zeros(128, np.float16), "zero": np.zeros(128, np.float16),
                           "factor": zero})
     buf = np.frombuffer(rec, np.uint8)
-    kw = buf[:128 * d // 2].view("<u4")
-    vw = buf[128 * d // 2:128 * d // 2 + 128 * d // 4].view("<u4")
+    o_kc, o_vc, o_ks, _, _, o_vs, _, _ = ko._section_offsets(d)
+    kw = buf[o_kc:o_ks].view("<u4")
+    vw = buf[o_vc:o_vs].view("<u4")
+    # the K half (codes + metadata) precedes the V half; sections are 16-byte aligned
+    assert o_ks == 128 * d // 2 and o_vc == 128 * d // 2 + 4 * d + 2 * 128
+    assert all(o % 16 == 0 for o in ko._section_offsets(d))
     k_slots = (0, 2, 1, 3)
     v_slots = ((0, 4, 1, 5), (2, 6, 3, 7))
     for lane in range(32):
