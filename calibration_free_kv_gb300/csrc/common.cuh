@@ -50,6 +50,18 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------------
+// A kernel launched with programmatic stream serialization may start before the previous
+// kernel of the stream has finished; grid_dependency_wait() blocks until that kernel has
+// completed and its memory is visible (a no-op when there is no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream (if launched as a dependent) start its CTAs.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier + 1-D bulk copy (TMA engine, no tensor map) ---------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -324,6 +324,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, tq = lane & 3;
+  grid_dependency_wait();  // lengths, partial tiles and pages come from the previous kernel
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
   int len = p.seq_lens[b];
   if (len < 0 || len > cap) {
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
     }
     // ---- merge the warps of this CTA ----
     __syncthreads();  // every warp is done with its slots
+    grid_launch_dependents();
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;
@@ -583,6 +585,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  grid_dependency_wait();  // the split partials of decode_kernel
   if (gw >= p.batch * p.num_q_heads) return;
   const int b = gw / p.num_q_heads;
   const int cap = p.max_pages * kTile + (kTile - 1);
@@ -648,12 +651,25 @@ static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
       return KVARN_ERR_CUDA;
     attr_set = true;
   }
-  dim3 grid(p.max_splits, p.num_kv_heads, p.batch);
-  decode_kernel<D, NT><<<grid, kDecWarps * 32, S::kSmemBytes, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KVARN_ERR_CUDA;
+  // both kernels may start while their predecessor in the stream drains; each waits for it
+  // (griddepcontrol.wait) before touching its results
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.max_splits, p.num_kv_heads, p.batch);
+  cfg.blockDim = dim3(kDecWarps * 32);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT>, p) != cudaSuccess) return KVARN_ERR_CUDA;
   const int warps = p.batch * p.num_q_heads;
-  combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&cfg, combine_kernel<D>, p) != cudaSuccess) return KVARN_ERR_CUDA;
+  return KVARN_OK;
 }
 
 int launch_decode_any(int d, int nt, const DecodeParams& p, cudaStream_t stream) {

@@ -628,6 +628,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
   const int tid = threadIdx.x, warp = tid >> 5;
 
   // ---- this CTA's units (append mode: write every token first, keep the tiles that seal) ----
+  grid_launch_dependents();  // a dependent kernel still waits for this grid to complete
   if (tid == 0) *count = 0;
   __syncthreads();
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
