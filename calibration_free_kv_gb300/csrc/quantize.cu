@@ -213,14 +213,19 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
   auto update_c = [&]() {
     float s[16], m2[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float y0 = x[0][c] * fL[0], y1 = x[1][c] * fL[1];
-      const float y2 = x[2][c] * fL[2], y3 = x[3][c] * fL[3];
-      const float sum = (y0 + y1) + (y2 + y3);
-      const float mu = sum * 0.25f;
-      const float d0_ = y0 - mu, d1 = y1 - mu, d2 = y2 - mu, d3 = y3 - mu;
-      s[c] = sum;
-      m2[c] = fmaf(d0_, d0_, d1 * d1) + fmaf(d2, d2, d3 * d3);
+    for (int u = 0; u < 8; ++u) {  // columns 2u, 2u+1 as packed pairs
+      const float2 y0 = mul2(make_float2(x[0][2 * u], x[0][2 * u + 1]), make_float2(fL[0], fL[0]));
+      const float2 y1 = mul2(make_float2(x[1][2 * u], x[1][2 * u + 1]), make_float2(fL[1], fL[1]));
+      const float2 y2 = mul2(make_float2(x[2][2 * u], x[2][2 * u + 1]), make_float2(fL[2], fL[2]));
+      const float2 y3 = mul2(make_float2(x[3][2 * u], x[3][2 * u + 1]), make_float2(fL[3], fL[3]));
+      const float2 sum = add2(add2(y0, y1), add2(y2, y3));
+      const float2 mu = mul2(sum, make_float2(0.25f, 0.25f));
+      const float2 d0_ = sub2(y0, mu), d1 = sub2(y1, mu), d2 = sub2(y2, mu), d3 = sub2(y3, mu);
+      const float2 q = add2(fma2(d0_, d0_, mul2(d1, d1)), fma2(d2, d2, mul2(d3, d3)));
+      s[2 * u] = sum.x;
+      s[2 * u + 1] = sum.y;
+      m2[2 * u] = q.x;
+      m2[2 * u + 1] = q.y;
     }
     float s8[8], m8[8], s4[4], m4[4], s2[2], m22[2];
     rs_chan<16>(s, m2, 16, (lane & 16) != 0, 4.0f);
@@ -267,23 +272,22 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
     float s[4], m2[4];
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-      float y[16];
+      float2 y[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) y[c] = x[l][c] * fC[c];
-      float t8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) t8[i] = y[2 * i] + y[2 * i + 1];
-      const float sum = ((t8[0] + t8[1]) + (t8[2] + t8[3])) + ((t8[4] + t8[5]) + (t8[6] + t8[7]));
+      for (int u = 0; u < 8; ++u)
+        y[u] = mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fC[2 * u], fC[2 * u + 1]));
+      const float2 t = add2(add2(add2(y[0], y[1]), add2(y[2], y[3])), add2(add2(y[4], y[5]), add2(y[6], y[7])));
+      const float sum = t.x + t.y;
       const float mu = sum * (1.0f / 16.0f);
-      float a = 0.0f, b = 0.0f;
+      const float2 mu2 = make_float2(mu, mu);
+      float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int c = 0; c < 16; c += 2) {
-        const float d0_ = y[c] - mu, d1 = y[c + 1] - mu;
-        a = fmaf(d0_, d0_, a);
-        b = fmaf(d1, d1, b);
+      for (int u = 0; u < 8; ++u) {
+        const float2 d = sub2(y[u], mu2);
+        acc = fma2(d, d, acc);
       }
       s[l] = sum;
-      m2[l] = a + b;
+      m2[l] = acc.x + acc.y;
     }
     float s2[2], m22[2];
     rs_chan<4>(s, m2, 1, (lane & 1) != 0, 16.0f);
@@ -328,17 +332,20 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
   {
     float mn[16], mx[16];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      float a = __fmul_rn(__fmul_rn(x[0][c], fL[0]), fC[c]);
-      float b = a;
+    for (int u = 0; u < 8; ++u) {
+      const float2 fc = make_float2(fC[2 * u], fC[2 * u + 1]);
+      float2 a = mul2(mul2(make_float2(x[0][2 * u], x[0][2 * u + 1]), make_float2(fL[0], fL[0])), fc);
+      float2 b = a;
 #pragma unroll
       for (int l = 1; l < 4; ++l) {
-        const float nv = __fmul_rn(__fmul_rn(x[l][c], fL[l]), fC[c]);
-        a = fminf(a, nv);
-        b = fmaxf(b, nv);
+        const float2 nv = mul2(mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fL[l], fL[l])), fc);
+        a = make_float2(fminf(a.x, nv.x), fminf(a.y, nv.y));
+        b = make_float2(fmaxf(b.x, nv.x), fmaxf(b.y, nv.y));
       }
-      mn[c] = a;
-      mx[c] = b;
+      mn[2 * u] = a.x;
+      mn[2 * u + 1] = a.y;
+      mx[2 * u] = b.x;
+      mx[2 * u + 1] = b.y;
     }
     float mn8[8], mx8[8], mn4[4], mx4[4];
     rs_minmax<16>(mn, mx, 16, (lane & 16) != 0);
@@ -384,15 +391,18 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
   // ---- 4. codes, packed as mma fragments -----------------------------------------------------
   uint32_t code[4][16];
 #pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const int col = 64 * ch + 8 * (c >> 1) + 2 * tq + (c & 1);
-    const float m = qmS[col], inv = qiS[col];
+  for (int u = 0; u < 8; ++u) {
+    const int col = 64 * ch + 8 * u + 2 * tq;
+    const float2 m = *reinterpret_cast<const float2*>(&qmS[col]);
+    const float2 inv = *reinterpret_cast<const float2*>(&qiS[col]);
+    const float2 fc = make_float2(fC[2 * u], fC[2 * u + 1]);
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-      const float nv = __fmul_rn(__fmul_rn(x[l][c], fL[l]), fC[c]);
-      const float v = __fmul_rn(__fsub_rn(nv, m), inv);
-      const uint32_t q = __float_as_uint(__fadd_rn(v, 12582912.0f)) - 0x4B400000u;
-      code[l][c] = min(q, (uint32_t)QMAX);
+      const float2 nv = mul2(mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fL[l], fL[l])), fc);
+      // round half to even: adding 1.5 * 2^23 leaves the rounded integer in the low mantissa bits
+      const float2 v = add2(mul2(sub2(nv, m), inv), make_float2(12582912.0f, 12582912.0f));
+      code[l][2 * u] = min(__float_as_uint(v.x) - 0x4B400000u, (uint32_t)QMAX);
+      code[l][2 * u + 1] = min(__float_as_uint(v.y) - 0x4B400000u, (uint32_t)QMAX);
     }
   }
   if (!TRANS) {
@@ -746,12 +756,16 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
         tmem_ld_16x256b_x8(col + ((uint32_t)(32 * (warp & 3) + 16 * half) << 16), r);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-#pragma unroll
-          for (int pp = 0; pp < 2; ++pp) {
-            x[2 * half][2 * u + pp] = __uint_as_float(r[4 * u + pp]) * isd;
-            x[2 * half + 1][2 * u + pp] = __uint_as_float(r[4 * u + 2 + pp]) * isd;
-          }
+        for (int u = 0; u < 8; ++u) {
+          const float2 a = mul2(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
+                                make_float2(isd, isd));
+          const float2 c = mul2(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
+                                make_float2(isd, isd));
+          x[2 * half][2 * u] = a.x;
+          x[2 * half][2 * u + 1] = a.y;
+          x[2 * half + 1][2 * u] = c.x;
+          x[2 * half + 1][2 * u + 1] = c.y;
+        }
       }
     }
     // Z buffer i % 2 is free (its MMA completed): fetch list[i + 2] into it
