@@ -80,6 +80,49 @@ __device__ __forceinline__ void chan_merge(float& s, float& m2, float s2, float 
   m2 = fmaf(delta * delta, 0.5f * n, m2 + m22);
 }
 
+// chan_merge for two columns at once.
+__device__ __forceinline__ void chan_merge2(float2& s, float2& m2, float2 s2, float2 m22, float n) {
+  const float2 delta = mul2(sub2(s2, s), make_float2(1.0f / n, 1.0f / n));
+  s = add2(s, s2);
+  m2 = fma2(mul2(delta, delta), make_float2(0.5f * n, 0.5f * n), add2(m2, m22));
+}
+
+// rs_chan over pairs of columns: keeps K/2 of the first K pairs.
+template <int K, int N>
+__device__ __forceinline__ void rs_chan2(float2 (&s)[N], float2 (&m2)[N], int mask, bool up, float n) {
+  static_assert(K <= N, "pairs in the array");
+#pragma unroll
+  for (int i = 0; i < K / 2; ++i) {
+    const float2 s_send = up ? s[i] : s[i + K / 2];
+    const float2 m_send = up ? m2[i] : m2[i + K / 2];
+    float2 s_keep = up ? s[i + K / 2] : s[i];
+    float2 m_keep = up ? m2[i + K / 2] : m2[i];
+    const float2 s_oth = make_float2(__shfl_xor_sync(0xffffffffu, s_send.x, mask),
+                                     __shfl_xor_sync(0xffffffffu, s_send.y, mask));
+    const float2 m_oth = make_float2(__shfl_xor_sync(0xffffffffu, m_send.x, mask),
+                                     __shfl_xor_sync(0xffffffffu, m_send.y, mask));
+    chan_merge2(s_keep, m_keep, s_oth, m_oth, n);
+    s[i] = s_keep;
+    m2[i] = m_keep;
+  }
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Barrier among the `count` threads (a multiple of 32) that use barrier `id` (1..15).
+__device__ __forceinline__ void group_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // New factor after one std step.  The log-space update ln f -= ln sigma (sigma = f_old * sd,
 // the std of the current normalised values) telescopes to f = 1 / sd; a std below eps has
 // nothing to normalise and the factor is kept.
@@ -98,10 +141,8 @@ __device__ __forceinline__ void stage_and_rotate(const __half* __restrict__ src,
   constexpr int LSIZE = TRANS ? D : kTile;
   constexpr int CSIZE = TRANS ? kTile : D;
   constexpr int NLQ = LSIZE / 32;
-  constexpr int NCH = CSIZE / 64;
-  constexpr int QMAX = TRANS ? 3 : 15;
-  constexpr RecordLayout RL = record_layout(D);
   constexpr float kInvSqrtD = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+  static_assert(CSIZE % 64 == 0, "C blocks of 64");
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
@@ -166,140 +207,156 @@ __device__ __forceinline__ void stage_and_rotate(const __half* __restrict__ src,
 
 }
 
+// Scratch floats quantize_rotated needs: two [NLQ][CSIZE] and two [NCH][LSIZE] buffers of
+// (sum, centred sum of squares) pairs, plus every warp's copy of its 64 column and 32 row factors.
+template <int D>
+struct RotScratch {
+  static constexpr int kL = D > kTile ? D : kTile;  // LSIZE or CSIZE, whichever is larger
+  static constexpr int kWarps = QuantShape<D>::kThreads / 32;
+  static constexpr int kFloats = 2 * (2 * (kL / 32) * kL) + 2 * (2 * (kL / 64) * kL) + kWarps * 96;
+  static_assert(kFloats * 4 <= QuantShape<D>::kSmemBytes, "scratch fits the staged tile");
+};
+
 // Normalise, quantise, fold and pack one rotated unit held as x (layout above) into its half of
-// the page record.  smem: reduction scratch of at least 6*max(d,128) floats.
+// the page record.  smem: at least RotScratch<D>::kFloats floats of scratch.
+//
+// Reductions along C stay within the two (D = 64: one; D = 256: four) warps that share an L
+// block, reductions along L within the warps that share a C block, so each std step needs one
+// barrier among those warps only.  Every warp of such a group merges the group's partials
+// itself and keeps its own copy of the factors it needs, which removes the second barrier a
+// single merging warp would need to hand its result out.  The partial buffers alternate between
+// two copies from one step to the next: a warp can only refill a copy after every warp of its
+// group has passed the barrier of the step in between, i.e. finished reading it.
 template <int D, bool TRANS>
 __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __restrict__ rec,
                                                  int iters, float eps, float* smem) {
-  constexpr int NTH = QuantShape<D>::kThreads;
-  constexpr int LD = QuantShape<D>::kLd;
   constexpr int LSIZE = TRANS ? D : kTile;
   constexpr int CSIZE = TRANS ? kTile : D;
   constexpr int NLQ = LSIZE / 32;
   constexpr int NCH = CSIZE / 64;
   constexpr int QMAX = TRANS ? 3 : 15;
   constexpr RecordLayout RL = record_layout(D);
-  constexpr float kInvSqrtD = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
   const int lq = warp % NLQ, ch = warp / NLQ;
 
-  float2* redL = reinterpret_cast<float2*>(smem);          // [NLQ][CSIZE]
-  float2* redC = redL + NLQ * CSIZE;                         // [NCH][LSIZE]
-  float* fLs = reinterpret_cast<float*>(redC + NCH * LSIZE);  // [LSIZE]
-  float* fCs = fLs + LSIZE;                                   // [CSIZE]
-  float* qmS = fCs + CSIZE;                                   // [CSIZE]
-  float* qiS = qmS + CSIZE;                                   // [CSIZE]
+  constexpr int kMaxL = RotScratch<D>::kL;
+  float2* redA = reinterpret_cast<float2*>(smem);         // [2][NLQ][CSIZE]  reductions along L
+  float2* redB = redA + 2 * (kMaxL / 32) * kMaxL;          // [2][NCH][LSIZE]  reductions along C
+  float* fCw = reinterpret_cast<float*>(redB + 2 * (kMaxL / 64) * kMaxL) + warp * 96;  // [64]
+  float* fLw = fCw + 64;                                   // [32]
 
-  // Registers hold each lane's 4 L factors and 16 C factors; fLs / fCs in shared memory are
-  // the canonical copies, updated by one designated thread per row / column.
+  // After the reduce-scatters a lane holds the statistics of C columns 64ch + ci, ci + 1 and
+  // of L row 32lq + ri: these are the entries of fCw / fLw it owns.
+  const int ci = 8 * g + 2 * tq;
+  const int l_fin = 2 * (tq & 1) + (tq >> 1);
+  const int ri = g + 8 * l_fin;
+  const int c_col = 64 * ch + ci;
+  const int l_row = 32 * lq + ri;
+
   float fL[4], fC[16];
 #pragma unroll
   for (int l = 0; l < 4; ++l) fL[l] = 1.0f;
 #pragma unroll
   for (int c = 0; c < 16; ++c) fC[c] = 1.0f;
-  for (int i = tid; i < LSIZE; i += NTH) fLs[i] = 1.0f;
-  for (int i = tid; i < CSIZE; i += NTH) fCs[i] = 1.0f;
-  __syncthreads();
+  *reinterpret_cast<float2*>(&fCw[ci]) = make_float2(1.0f, 1.0f);
+  fLw[ri] = 1.0f;
 
-  // Lane's final column pair after the reduce-scatter over g, and its final row after the
-  // reduce-scatter over tq.
-  const int c_col = 64 * ch + 8 * g + 2 * tq;                // columns c_col, c_col + 1
-  const int l_fin = 2 * (tq & 1) + (tq >> 1);
-  const int l_row = 32 * lq + g + 8 * l_fin;
+  auto X = [&](int l, int u) { return make_float2(x[l][2 * u], x[l][2 * u + 1]); };
+  auto FC = [&](int u) { return make_float2(fC[2 * u], fC[2 * u + 1]); };
+  auto FL = [&](int l) { return make_float2(fL[l], fL[l]); };
 
-  // std over L of each C column -> new C factors.
-  auto update_c = [&]() {
-    float s[16], m2[16];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {  // columns 2u, 2u+1 as packed pairs
-      const float2 y0 = mul2(make_float2(x[0][2 * u], x[0][2 * u + 1]), make_float2(fL[0], fL[0]));
-      const float2 y1 = mul2(make_float2(x[1][2 * u], x[1][2 * u + 1]), make_float2(fL[1], fL[1]));
-      const float2 y2 = mul2(make_float2(x[2][2 * u], x[2][2 * u + 1]), make_float2(fL[2], fL[2]));
-      const float2 y3 = mul2(make_float2(x[3][2 * u], x[3][2 * u + 1]), make_float2(fL[3], fL[3]));
-      const float2 sum = add2(add2(y0, y1), add2(y2, y3));
-      const float2 mu = mul2(sum, make_float2(0.25f, 0.25f));
-      const float2 d0_ = sub2(y0, mu), d1 = sub2(y1, mu), d2 = sub2(y2, mu), d3 = sub2(y3, mu);
-      const float2 q = add2(fma2(d0_, d0_, mul2(d1, d1)), fma2(d2, d2, mul2(d3, d3)));
-      s[2 * u] = sum.x;
-      s[2 * u + 1] = sum.y;
-      m2[2 * u] = q.x;
-      m2[2 * u + 1] = q.y;
-    }
-    float s8[8], m8[8], s4[4], m4[4], s2[2], m22[2];
-    rs_chan<16>(s, m2, 16, (lane & 16) != 0, 4.0f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { s8[i] = s[i]; m8[i] = m2[i]; }
-    rs_chan<8>(s8, m8, 8, (lane & 8) != 0, 8.0f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) { s4[i] = s8[i]; m4[i] = m8[i]; }
-    rs_chan<4>(s4, m4, 4, (lane & 4) != 0, 16.0f);
-    s2[0] = s4[0]; s2[1] = s4[1]; m22[0] = m4[0]; m22[1] = m4[1];
-    *reinterpret_cast<float4*>(&redL[lq * CSIZE + c_col]) = make_float4(s2[0], m22[0], s2[1], m22[1]);
-    __syncthreads();
-    if (lq == 0) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float ps[NLQ], pm[NLQ];
-#pragma unroll
-        for (int q = 0; q < NLQ; ++q) {
-          const float2 v = redL[q * CSIZE + c_col + e];
-          ps[q] = v.x;
-          pm[q] = v.y;
-        }
-        float n = 32.0f;
-#pragma unroll
-        for (int w = 1; w < NLQ; w <<= 1) {
-#pragma unroll
-          for (int q = 0; q + w < NLQ; q += 2 * w) chan_merge(ps[q], pm[q], ps[q + w], pm[q + w], n);
-          n *= 2.0f;
-        }
-        fCs[c_col + e] = std_step_factor(fCs[c_col + e], pm[0], 1.0f / LSIZE, eps);
-      }
-    }
-    __syncthreads();
+  // std over L of each C column -> new C factors (the k-th such step uses buffer k % 2)
+  auto update_c = [&](int k) {
+    // Column pairs (2u, 2u + 1): sum and centred sum of squares of 4 rows.  The products are
+    // rounded before a pairwise sum, so identical values give an exact mean and a zero sum of
+    // squares (a constant column has std 0, not rounding noise that could exceed eps).
+    float2 S[8], M[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const float2 f = *reinterpret_cast<const float2*>(&fCs[64 * ch + 8 * u + 2 * tq]);
-      fC[2 * u] = f.x;
-      fC[2 * u + 1] = f.y;
+      const float2 y0 = mul2(X(0, u), FL(0)), y1 = mul2(X(1, u), FL(1));
+      const float2 y2 = mul2(X(2, u), FL(2)), y3 = mul2(X(3, u), FL(3));
+      const float2 s = add2(add2(y0, y1), add2(y2, y3));
+      const float2 mu = mul2(s, make_float2(0.25f, 0.25f));
+      const float2 d0_ = sub2(y0, mu), d1 = sub2(y1, mu), d2 = sub2(y2, mu), d3 = sub2(y3, mu);
+      S[u] = s;
+      M[u] = add2(fma2(d0_, d0_, mul2(d1, d1)), fma2(d2, d2, mul2(d3, d3)));
+    }
+    rs_chan2<8>(S, M, 16, (lane & 16) != 0, 4.0f);
+    rs_chan2<4>(S, M, 8, (lane & 8) != 0, 8.0f);
+    rs_chan2<2>(S, M, 4, (lane & 4) != 0, 16.0f);  // S[0], M[0]: columns c_col, c_col + 1
+    float2 s = S[0], m = M[0];
+    if (NLQ > 1) {
+      float4* buf = reinterpret_cast<float4*>(redA + (k & 1) * NLQ * CSIZE);
+      buf[(lq * CSIZE + c_col) >> 1] = make_float4(s.x, s.y, m.x, m.y);
+      group_sync(1 + ch, NLQ * 32);
+      float2 ps[NLQ], pm[NLQ];
+#pragma unroll
+      for (int q = 0; q < NLQ; ++q) {
+        const float4 v = buf[(q * CSIZE + c_col) >> 1];
+        ps[q] = make_float2(v.x, v.y);
+        pm[q] = make_float2(v.z, v.w);
+      }
+      float n = 32.0f;
+#pragma unroll
+      for (int w = 1; w < NLQ; w <<= 1) {
+#pragma unroll
+        for (int q = 0; q + w < NLQ; q += 2 * w) chan_merge2(ps[q], pm[q], ps[q + w], pm[q + w], n);
+        n *= 2.0f;
+      }
+      m = pm[0];
+    }
+    float2 f = *reinterpret_cast<const float2*>(&fCw[ci]);
+    f.x = std_step_factor(f.x, m.x, 1.0f / LSIZE, eps);
+    f.y = std_step_factor(f.y, m.y, 1.0f / LSIZE, eps);
+    *reinterpret_cast<float2*>(&fCw[ci]) = f;
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float2 v = *reinterpret_cast<const float2*>(&fCw[8 * u + 2 * tq]);
+      fC[2 * u] = v.x;
+      fC[2 * u + 1] = v.y;
     }
   };
 
-  // std over C of each L row -> new L factors.
-  auto update_l = [&]() {
-    float s[4], m2[4];
+  // std over C of each L row -> new L factors (the k-th such step uses buffer k % 2)
+  auto update_l = [&](int k) {
+    float2 S2[2], M2[2];  // rows (0, 1) and (2, 3): sum and centred sum of squares of 16 columns
 #pragma unroll
-    for (int l = 0; l < 4; ++l) {
+    for (int l = 0; l < 4; ++l) {  // rounded products, pairwise sum (exact for a constant row)
       float2 y[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        y[u] = mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fC[2 * u], fC[2 * u + 1]));
+      for (int u = 0; u < 8; ++u) y[u] = mul2(X(l, u), FC(u));
       const float2 t = add2(add2(add2(y[0], y[1]), add2(y[2], y[3])), add2(add2(y[4], y[5]), add2(y[6], y[7])));
-      const float sum = t.x + t.y;
-      const float mu = sum * (1.0f / 16.0f);
-      const float2 mu2 = make_float2(mu, mu);
-      float2 acc = make_float2(0.0f, 0.0f);
+      const float s = t.x + t.y;
+      const float mu = s * (1.0f / 16.0f);
+      float2 q = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const float2 d = sub2(y[u], mu2);
-        acc = fma2(d, d, acc);
+        const float2 d = sub2(y[u], make_float2(mu, mu));
+        q = fma2(d, d, q);
       }
-      s[l] = sum;
-      m2[l] = acc.x + acc.y;
+      if (l & 1) {
+        S2[l >> 1].y = s;
+        M2[l >> 1].y = q.x + q.y;
+      } else {
+        S2[l >> 1].x = s;
+        M2[l >> 1].x = q.x + q.y;
+      }
     }
-    float s2[2], m22[2];
-    rs_chan<4>(s, m2, 1, (lane & 1) != 0, 16.0f);
-    s2[0] = s[0]; s2[1] = s[1]; m22[0] = m2[0]; m22[1] = m2[1];
-    rs_chan<2>(s2, m22, 2, (lane & 2) != 0, 32.0f);
-    redC[ch * LSIZE + l_row] = make_float2(s2[0], m22[0]);
-    __syncthreads();
-    if (ch == 0) {
+    rs_chan2<2>(S2, M2, 1, (lane & 1) != 0, 16.0f);  // rows (0, 1) or (2, 3)
+    float s1[2] = {S2[0].x, S2[0].y}, m1[2] = {M2[0].x, M2[0].y};
+    rs_chan<2>(s1, m1, 2, (lane & 2) != 0, 32.0f);  // row l_fin
+    float s = s1[0], m = m1[0];
+    if (NCH > 1) {
+      float2* buf = redB + (k & 1) * NCH * LSIZE;
+      buf[ch * LSIZE + l_row] = make_float2(s, m);
+      group_sync(1 + NCH + lq, NCH * 32);
       float ps[NCH], pm[NCH];
 #pragma unroll
       for (int q = 0; q < NCH; ++q) {
-        const float2 v = redC[q * LSIZE + l_row];
+        const float2 v = buf[q * LSIZE + l_row];
         ps[q] = v.x;
         pm[q] = v.y;
       }
@@ -310,42 +367,39 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
         for (int q = 0; q + w < NCH; q += 2 * w) chan_merge(ps[q], pm[q], ps[q + w], pm[q + w], n);
         n *= 2.0f;
       }
-      fLs[l_row] = std_step_factor(fLs[l_row], pm[0], 1.0f / CSIZE, eps);
+      m = pm[0];
     }
-    __syncthreads();
+    fLw[ri] = std_step_factor(fLw[ri], m, 1.0f / CSIZE, eps);
+    __syncwarp();
 #pragma unroll
-    for (int l = 0; l < 4; ++l) fL[l] = fLs[32 * lq + g + 8 * l];
+    for (int l = 0; l < 4; ++l) fL[l] = fLw[g + 8 * l];
   };
 
   // ---- 2. variance normalisation: channel-std step, then token-std step -------------------
   for (int it = 0; it < iters; ++it) {
     if (!TRANS) {  // K: channels are C, tokens are L
-      update_c();
-      update_l();
+      update_c(it);
+      update_l(it);
     } else {       // V: channels are L, tokens are C
-      update_l();
-      update_c();
+      update_l(it);
+      update_c(it);
     }
   }
 
-  // ---- 3. per-column (along L) min / max of N = x fL fC, scale, zero-point ----------------
+  // ---- 3. per-column (along L) min / max, scale, zero-point ---------------------------------
+  // N = (x fL) fC with fC > 0 fixed per column, and rounding is monotonic, so the extremes of N
+  // are the extremes of z = x fL times fC, rounded once.
+  float4* qbuf = reinterpret_cast<float4*>(redA + ((iters + 1) & 1) * NLQ * CSIZE + lq * CSIZE + 64 * ch);
   {
     float mn[16], mx[16];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const float2 fc = make_float2(fC[2 * u], fC[2 * u + 1]);
-      float2 a = mul2(mul2(make_float2(x[0][2 * u], x[0][2 * u + 1]), make_float2(fL[0], fL[0])), fc);
-      float2 b = a;
-#pragma unroll
-      for (int l = 1; l < 4; ++l) {
-        const float2 nv = mul2(mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fL[l], fL[l])), fc);
-        a = make_float2(fminf(a.x, nv.x), fminf(a.y, nv.y));
-        b = make_float2(fmaxf(b.x, nv.x), fmaxf(b.y, nv.y));
-      }
-      mn[2 * u] = a.x;
-      mn[2 * u + 1] = a.y;
-      mx[2 * u] = b.x;
-      mx[2 * u + 1] = b.y;
+      const float2 z0 = mul2(X(0, u), FL(0)), z1 = mul2(X(1, u), FL(1));
+      const float2 z2 = mul2(X(2, u), FL(2)), z3 = mul2(X(3, u), FL(3));
+      mn[2 * u] = fminf(fmin3(z0.x, z1.x, z2.x), z3.x);
+      mn[2 * u + 1] = fminf(fmin3(z0.y, z1.y, z2.y), z3.y);
+      mx[2 * u] = fmaxf(fmax3(z0.x, z1.x, z2.x), z3.x);
+      mx[2 * u + 1] = fmaxf(fmax3(z0.y, z1.y, z2.y), z3.y);
     }
     float mn8[8], mx8[8], mn4[4], mx4[4];
     rs_minmax<16>(mn, mx, 16, (lane & 16) != 0);
@@ -355,92 +409,97 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
 #pragma unroll
     for (int i = 0; i < 4; ++i) { mn4[i] = mn8[i]; mx4[i] = mx8[i]; }
     rs_minmax<4>(mn4, mx4, 4, (lane & 4) != 0);
-    *reinterpret_cast<float4*>(&redL[lq * CSIZE + c_col]) = make_float4(mn4[0], mx4[0], mn4[1], mx4[1]);
-    __syncthreads();
-    __half* scale_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vscale : RL.kscale));
-    __half* zero_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vzero : RL.kzero));
-    if (lq == 0) {
-      float sc[2], ze[2];
+    float2 zmin = make_float2(mn4[0], mn4[1]), zmax = make_float2(mx4[0], mx4[1]);
+    if (NLQ > 1) {
+      float4* buf = reinterpret_cast<float4*>(redA + (iters & 1) * NLQ * CSIZE);
+      buf[(lq * CSIZE + c_col) >> 1] = make_float4(zmin.x, zmin.y, zmax.x, zmax.y);
+      group_sync(1 + ch, NLQ * 32);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float m = redL[c_col + e].x, M = redL[c_col + e].y;
-#pragma unroll
-        for (int q = 1; q < NLQ; ++q) {
-          m = fminf(m, redL[q * CSIZE + c_col + e].x);
-          M = fmaxf(M, redL[q * CSIZE + c_col + e].y);
-        }
-        const float s = fmaxf(__fdiv_rn(__fsub_rn(M, m), (float)QMAX), 1e-8f);
-        qmS[c_col + e] = m;
-        qiS[c_col + e] = __frcp_rn(s);
-        // folded: s' = s * (1/fC), z' = m * (1/fC)
-        sc[e] = __fdiv_rn(s, fCs[c_col + e]);
-        ze[e] = __fdiv_rn(m, fCs[c_col + e]);
+      for (int q = 0; q < NLQ; ++q) {
+        if (q == lq) continue;
+        const float4 v = buf[(q * CSIZE + c_col) >> 1];
+        zmin = make_float2(fminf(zmin.x, v.x), fminf(zmin.y, v.y));
+        zmax = make_float2(fmaxf(zmax.x, v.z), fmaxf(zmax.y, v.w));
       }
-      *reinterpret_cast<__half2*>(&scale_out[c_col]) = __floats2half2_rn(sc[0], sc[1]);
-      *reinterpret_cast<__half2*>(&zero_out[c_col]) = __floats2half2_rn(ze[0], ze[1]);
     }
-    __syncthreads();
+    const float2 fc = *reinterpret_cast<const float2*>(&fCw[ci]);
+    const float2 m = mul2(zmin, fc), M = mul2(zmax, fc);
+    const float s0 = fmaxf(__fdiv_rn(__fsub_rn(M.x, m.x), (float)QMAX), 1e-8f);
+    const float s1 = fmaxf(__fdiv_rn(__fsub_rn(M.y, m.y), (float)QMAX), 1e-8f);
+    qbuf[ci >> 1] = make_float4(m.x, m.y, __frcp_rn(s0), __frcp_rn(s1));
+    if (lq == 0) {  // folded: s' = s / fC, z' = m / fC
+      __half* scale_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vscale : RL.kscale));
+      __half* zero_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vzero : RL.kzero));
+      *reinterpret_cast<__half2*>(&scale_out[c_col]) =
+          __floats2half2_rn(__fdiv_rn(s0, fc.x), __fdiv_rn(s1, fc.y));
+      *reinterpret_cast<__half2*>(&zero_out[c_col]) =
+          __floats2half2_rn(__fdiv_rn(m.x, fc.x), __fdiv_rn(m.y, fc.y));
+    }
   }
 
   // token / channel factor of the L axis: r = 1/fL (K) or c = 1/fL (V)
-  {
+  if (ch == 0) {
     __half* fac_out = reinterpret_cast<__half*>(rec + (TRANS ? RL.vfactor : RL.kfactor));
-    if (ch == 0) fac_out[l_row] = __float2half_rn(__frcp_rn(fLs[l_row]));
+    fac_out[l_row] = __float2half_rn(__frcp_rn(fLw[ri]));
   }
+  __syncwarp();
 
   // ---- 4. codes, packed as mma fragments -----------------------------------------------------
+  // (N - m) / s lies in [0, QMAX] for finite input, so adding 1.5 * 2^23 (round half to even)
+  // leaves the code alone in the low byte of the float's bits.
   uint32_t code[4][16];
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int col = 64 * ch + 8 * u + 2 * tq;
-    const float2 m = *reinterpret_cast<const float2*>(&qmS[col]);
-    const float2 inv = *reinterpret_cast<const float2*>(&qiS[col]);
-    const float2 fc = make_float2(fC[2 * u], fC[2 * u + 1]);
+    const float4 q = qbuf[4 * u + tq];
+    const float2 m = make_float2(q.x, q.y), inv = make_float2(q.z, q.w);
 #pragma unroll
     for (int l = 0; l < 4; ++l) {
-      const float2 nv = mul2(mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fL[l], fL[l])), fc);
-      // round half to even: adding 1.5 * 2^23 leaves the rounded integer in the low mantissa bits
+      const float2 nv = mul2(mul2(X(l, u), FL(l)), FC(u));
       const float2 v = add2(mul2(sub2(nv, m), inv), make_float2(12582912.0f, 12582912.0f));
-      code[l][2 * u] = min(__float_as_uint(v.x) - 0x4B400000u, (uint32_t)QMAX);
-      code[l][2 * u + 1] = min(__float_as_uint(v.y) - 0x4B400000u, (uint32_t)QMAX);
+      code[l][2 * u] = __float_as_uint(v.x);
+      code[l][2 * u + 1] = __float_as_uint(v.y);
     }
   }
+  // low bytes of four code registers -> one word, byte i from register i
+  auto gather4 = [](uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x4000), 0x7610);
+  };
   if (!TRANS) {
+    // nibble h + 2 rho + 4 p of word j holds row 2 lh + rho, column 16 j + 8 h + 2 tq + p, so
+    // byte rho + 2 p holds h = 0 in its low and h = 1 in its high nibble
     uint8_t* kc = rec + RL.kcodes;
 #pragma unroll
     for (int lh = 0; lh < 2; ++lh) {
-      uint32_t w[4] = {0u, 0u, 0u, 0u};
+      uint32_t w[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-#pragma unroll
-        for (int p = 0; p < 2; ++p)
-#pragma unroll
-          for (int rho = 0; rho < 2; ++rho) {
-            const int nib = (u & 1) + 2 * rho + 4 * p;
-            w[u >> 1] |= code[2 * lh + rho][2 * u + p] << (4 * nib);
-          }
+      for (int j = 0; j < 4; ++j) {
+        const int c0 = 4 * j, c1 = 4 * j + 2, r0 = 2 * lh, r1 = 2 * lh + 1;
+        const uint32_t lo = gather4(code[r0][c0], code[r1][c0], code[r0][c0 + 1], code[r1][c0 + 1]);
+        const uint32_t hi = gather4(code[r0][c1], code[r1][c1], code[r0][c1 + 1], code[r1][c1 + 1]);
+        w[j] = (lo & 0x0F0F0F0Fu) | ((hi << 4) & 0xF0F0F0F0u);
+      }
       const int mi = 2 * lq + lh;
       *reinterpret_cast<uint4*>(kc + ((mi * (D / 64) + ch) * 32 + lane) * 16) =
           make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
+    // 2-bit slot uu + 4 rho + 8 p of word lh holds row 2 lh + rho, column 2 (4 uh + uu) + p
     uint8_t* vc = rec + RL.vcodes;
 #pragma unroll
     for (int uh = 0; uh < 2; ++uh) {
-      uint32_t w[2] = {0u, 0u};
+      uint32_t w[2];
 #pragma unroll
-      for (int lh = 0; lh < 2; ++lh)
+      for (int lh = 0; lh < 2; ++lh) {
+        uint32_t acc = 0u;
 #pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-          const int u = 4 * uh + uu;
-#pragma unroll
-          for (int p = 0; p < 2; ++p)
-#pragma unroll
-            for (int rho = 0; rho < 2; ++rho) {
-              const int slot = 2 * ((u >> 1) & 1) + (u & 1) + 4 * rho + 8 * p;
-              w[lh] |= code[2 * lh + rho][2 * u + p] << (2 * slot);
-            }
+        for (int uu = 3; uu >= 0; --uu) {
+          const int c = 2 * (4 * uh + uu), r0 = 2 * lh, r1 = 2 * lh + 1;
+          // byte rho + 2 p: row 2 lh + rho, column c + p
+          const uint32_t b = gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
+          acc = (acc << 2) | (b & 0x03030303u);
         }
+        w[lh] = acc;
+      }
       const int ks2 = 2 * ch + uh;
       *reinterpret_cast<uint2*>(vc + (((ks2 * (D / 64) + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
           make_uint2(w[0], w[1]);
@@ -540,7 +599,7 @@ constexpr uint32_t kSbo = 2048;                      // row-band-adjacent core m
 constexpr int kHOff = 0;
 constexpr int kZOff = kOpBytes;                      // two tile buffers
 constexpr int kScrOff = 3 * kOpBytes;
-constexpr int kScrBytes = 8192;                      // reduction scratch of quantize_rotated
+constexpr int kScrBytes = RotScratch<128>::kFloats * 4;  // scratch of quantize_rotated
 constexpr int kListCap = 256;                        // units per CTA
 constexpr int kListOff = kScrOff + kScrBytes;
 constexpr int kBarOff = kListOff + kListCap * 4;
