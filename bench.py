@@ -33,6 +33,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "K4V2 g128 decode-attn KV tokens/s & HBM GB/s; quantize tokens/s (1 GB300)"
+QUANT_OPS_PER_ELEMENT = 37  # fp32 ops per quantised element (derivation at the quantize timing)
+SM_MAX_MHZ = 2070.0
 WORKLOAD = ("paged decode attention + append: batch 64, seq_len 128*U{8..128}, 32 q heads / 8 kv "
             "heads, head_dim 128, K4V2 g128 packed cache, permuted block table")
 BATCH, HQ, HKV, D0, MIN_PAGES, MAX_PAGES, SEED = 64, 32, 8, 128, 8, 128, 3
@@ -296,6 +298,14 @@ def _run_kvarn(args, torch, world, rank):
     q_med = statistics.median(q_ms)
     q_bytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
     q_gbs = q_bytes / (q_med * 1e-3) / 1e9
+    # Quantisation is bound by fp32 arithmetic, not by HBM.  Per element it needs 37 fp32 ops:
+    # 4 in each of the 8 std steps (product with the other axis' factor, its share of the sum,
+    # minus the mean, square-accumulate) and 5 to quantise (two factor products, minus the zero
+    # point, times 1/scale, plus the rounding constant).  Peak: one fp32 op per lane per clock,
+    # 128 lanes per SM.
+    q_elems = 2 * Q_TOKENS * Q_HEADS * D0
+    q_ops = QUANT_OPS_PER_ELEMENT * q_elems / (q_med * 1e-3) / 1e9
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     # ---- aggregate over ranks (replicas)
     if world > 1:
@@ -348,6 +358,13 @@ def _run_kvarn(args, torch, world, rank):
             "tokens_per_s": Q_TOKENS / (q_med * 1e-3),
             "us": q_med * 1e3, "hbm_gbs": q_gbs, "frac": q_gbs / peak,
             "algorithmic_bytes": q_bytes,
+            "roofline": {
+                "kernel": "quantize_tc_kernel", "bound": "alu", "achieved": q_ops,
+                "peak": sms * 128 * (clk.get("sm_mhz") or SM_MAX_MHZ) * 1e-3, "unit": "Gop/s",
+                "frac": q_ops / (sms * 128 * (clk.get("sm_mhz") or SM_MAX_MHZ) * 1e-3),
+                "peak_source": "%d SMs x 128 fp32 lanes x median SM clock under load" % sms,
+                "ops_per_element": QUANT_OPS_PER_ELEMENT,
+            },
         },
         "e2e": {"value": e2e_value, "unit": "KV tokens/s",
                 "h2d_bytes_per_step": (BATCH * HQ * D0 + 2 * BATCH * HKV * D0) * 2,
