@@ -193,6 +193,76 @@ def _decode_bytes(lens, rec_bytes):
     return (sealed * HKV * rec_bytes + part * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2)
 
 
+def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, seed, reps=5):
+    """Decode over `layers` independent packed caches (one pool per layer, one shared permuted
+    block table, every sequence at seq_len), launched back to back on one stream: median ms
+    per pass over all layers, and the algorithmic bytes of one pass."""
+    dev = torch.device("cuda")
+    pages = seq_len // 128
+    desc = kv.desc_from_preset(d0, hkv)
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(batch * pages, generator=g).view(batch, pages).to(torch.int32).to(dev)
+    page_ids = table.reshape(-1).contiguous()
+    lens = torch.full((batch,), seq_len, dtype=torch.int32, device=dev)
+    pools, qs = [], []
+    for layer in range(layers):
+        k, v = synth.outlier_kv(batch * seq_len, hkv, d0, seed=seed * 1000 + layer, device=dev)
+        pool = kv.alloc_pool(desc, batch * pages, device=dev)
+        kv.quantize_tiles(desc, k, v, page_ids, pool)
+        del k, v
+        pools.append(pool)
+        qs.append(torch.randn((batch, hq, d0), generator=g).half().to(dev))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    outs = [torch.empty((batch, hq, d0), dtype=torch.float16, device=dev) for _ in range(layers)]
+    ws = kv.alloc_workspace(desc, batch, hq, pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(d0)
+
+    def one_pass():
+        for layer in range(layers):
+            kv.decode_attention(desc, qs[layer], pools[layer], table, lens, outs[layer], ws,
+                                softmax_scale=scale, status=status, stream=stream)
+
+    for _ in range(3):
+        one_pass()
+    ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        one_pass()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the layered decode" % int(status.item()))
+    nbytes = layers * (batch * pages * hkv * desc.page_record_bytes + 2 * batch * hq * d0 * 2)
+    del pools, outs, ws
+    torch.cuda.empty_cache()
+    return statistics.median(ms), nbytes
+
+
+def _decode_configs(torch, kv, synth, peak):
+    """The 32B-class 64-layer decode step and the long-context shapes, each against bytes/peak."""
+    res = {}
+    for key, cfg in (
+            ("decode_32b_step", dict(batch=32, seq_len=16384, hq=64, hkv=8, d0=128, layers=64, seed=4)),
+            ("decode_long_d256", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=256, layers=1, seed=5)),
+            ("decode_long_d96", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=96, layers=1, seed=5))):
+        ms, nbytes = _time_decode_layers(torch, kv, synth, **cfg)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[key] = {
+            "workload": "%d layer(s) x batch %d at %d tokens, %d q heads / %d kv heads, head_dim %d"
+                        % (cfg["layers"], cfg["batch"], cfg["seq_len"], cfg["hq"], cfg["hkv"], cfg["d0"]),
+            "ms_per_step": ms, "algorithmic_bytes": nbytes, "hbm_gbs": gbs, "frac": gbs / peak,
+            "ideal_ms_at_peak": nbytes / (peak * 1e9) * 1e3,
+            "kv_tokens_per_s": cfg["batch"] * cfg["seq_len"] / (ms * 1e-3),
+        }
+    return res
+
+
 def _run_kvarn(args, torch, world, rank):
     from calibration_free_kv_gb300 import build as kbuild
     kbuild.build()
@@ -307,6 +377,9 @@ def _run_kvarn(args, torch, world, rank):
     q_ops = QUANT_OPS_PER_ELEMENT * q_elems / (q_med * 1e-3) / 1e9
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
+    # ---- the 32B-class step (64 layers, GQA 8) and the long-context shapes (not timed steps)
+    extra = _decode_configs(torch, kv, synth, peak) if not args.no_extra else {}
+
     # ---- aggregate over ranks (replicas)
     if world > 1:
         t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
@@ -366,6 +439,7 @@ def _run_kvarn(args, torch, world, rank):
                 "ops_per_element": QUANT_OPS_PER_ELEMENT,
             },
         },
+        **extra,
         "e2e": {"value": e2e_value, "unit": "KV tokens/s",
                 "h2d_bytes_per_step": (BATCH * HQ * D0 + 2 * BATCH * HKV * D0) * 2,
                 "d2h_bytes_per_step": BATCH * HQ * D0 * 2},
@@ -455,6 +529,8 @@ def main():
                     help="decode batch (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="CPU work of the oracle baseline sample (kvarn arm)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the 64-layer and long-context decode shapes (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -163,12 +163,14 @@ def test_append_rejects_full_block_table(kv):
     assert int(st.status.item()) & kv.DEV_SEQ_TOO_LONG
 
 
-def test_long_context_streaming_sampled(kv):
-    # batch 4 at 130560 + {0, 1, 64, 127} tokens, head_dim 256, 8 KV heads, 32 query heads;
-    # 512 appends (seals every sequence at least 3 times); sampled heads checked at the end
-    st = Stream(kv, batch=4, hkv=8, d0=256, l0=[130560, 130561, 130624, 130687], max_pages=1030,
+@pytest.mark.parametrize("d0", [256, 96])
+def test_long_context_streaming_sampled(kv, d0):
+    # batch 4 at 130560 + {0, 1, 64, 127} tokens, head_dim 256 (and 96, zero-padded to 128),
+    # 8 KV heads, 32 query heads; 512 appends (every seal of every sequence is checked);
+    # sampled heads decoded at the end
+    st = Stream(kv, batch=4, hkv=8, d0=d0, l0=[130560, 130561, 130624, 130687], max_pages=1030,
                 seed=5)
-    q = torch.randn((4, 32, 256), generator=torch.Generator().manual_seed(10)).half()
+    q = torch.randn((4, 32, d0), generator=torch.Generator().manual_seed(10)).half()
     for _ in range(512):
         st.step()
     torch.cuda.synchronize()

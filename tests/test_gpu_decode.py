@@ -253,3 +253,38 @@ def test_decode_full_size_sampled(kv):
         ref = ko.decode_sequence(q[b, h * group:(h + 1) * group].double().numpy(), rl, None, None, scale, d0)
         err = H.assert_decode_close(got[b, h * group:(h + 1) * group], ref, "full size b=%d h=%d" % (b, h))
         print("full size b=%d (L=%d) h=%d: max scaled err %.2e" % (b, L, h, err))
+
+
+def test_decode_32b_layer_sampled(kv):
+    # one layer of the 32B-class decode step: batch 32 at 16384 tokens, 64 query heads over
+    # 8 KV heads (GQA 8), head_dim 128, permuted block table, GPU-quantised cache; three
+    # sampled (sequence, kv head) caches are replaced by oracle records and compared
+    hkv, group, d0, batch, L = 8, 8, 128, 32, 16384
+    pages = L // 128
+    g = torch.Generator().manual_seed(4)
+    table = torch.randperm(batch * pages, generator=g).view(batch, pages).to(torch.int32)
+    desc = kv.desc_from_preset(d0, hkv)
+    pool = kv.alloc_pool(desc, batch * pages)
+    k_all, v_all = synth.outlier_kv(batch * L, hkv, d0, seed=4, device="cuda")
+    kv.quantize_tiles(desc, k_all, v_all, table.reshape(-1).cuda(), pool)
+    torch.cuda.synchronize()
+    picks = [(0, 0), (31, 7), (13, 4)]
+    recs = {}
+    for b, h in picks:
+        kk = k_all[b * L:(b + 1) * L, h].cpu().double().numpy().reshape(pages, 128, d0)
+        vv = v_all[b * L:(b + 1) * L, h].cpu().double().numpy().reshape(pages, 128, d0)
+        r, _, _ = H.oracle_quantize(kk, vv)
+        for i in range(pages):
+            recs[(b, i, h)] = r[i]
+    del k_all, v_all
+    H.upload_records(pool, [(int(table[b, i]), h, r) for (b, i, h), r in recs.items()])
+    q = torch.randn((batch, hkv * group, d0), generator=g).half()
+    scale = 1.0 / math.sqrt(128.0)
+    got, st = _gpu_decode(kv, desc, pool, table.numpy(), [L] * batch, q, None, None, scale)
+    assert st == 0
+    assert np.all(np.isfinite(got))
+    for b, h in picks:
+        rl = [recs[(b, i, h)] for i in range(pages)]
+        ref = ko.decode_sequence(q[b, h * group:(h + 1) * group].double().numpy(), rl, None, None, scale, d0)
+        err = H.assert_decode_close(got[b, h * group:(h + 1) * group], ref, "32B layer b=%d h=%d" % (b, h))
+        print("32B layer b=%d h=%d: max scaled err %.2e" % (b, h, err))
