@@ -82,6 +82,18 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
   return unpack_f2(d);
 }
 
+// three-input min / max (sm_100+)
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // ---- programmatic dependent launch ----------------------------------------------------------
 // A kernel launched with programmatic stream serialization may start before the previous
 // kernel of the stream has finished; grid_dependency_wait() blocks until that kernel has

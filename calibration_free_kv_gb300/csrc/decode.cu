@@ -46,6 +46,7 @@ struct DecodeShape {
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -141,41 +142,41 @@ __device__ __forceinline__ uint32_t b_split(__half2 qh, __half2 ql, __half2 s, b
 // of head 4nt + tq), online-softmax state updated, alpha = rescale of the previous state.
 template <int D, int NT>
 __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const float* __restrict__ qsm,
-                                        const __half2* __restrict__ qh2, const __half2* __restrict__ ql2,
-                                        int lane, WarpAcc<D, NT>& st, float (&lg)[8][NT][2],
-                                        float (&alpha)[NT]) {
+                                        const uint2* __restrict__ qhl, int lane, WarpAcc<D, NT>& st,
+                                        float (&lg)[8][NT][2], float (&alpha)[NT]) {
   constexpr RecordLayout RL = record_layout(D);
   constexpr int QLD = DecodeShape<D, NT>::kQld;
-  constexpr int QH = D / 2 + 4;  // half2 row stride of qh / ql
+  constexpr int QH = D / 2 + 4;  // row stride of qhl (one entry per channel pair)
   const int g = lane >> 2, tq = lane & 3;
   const __half2* Ks2 = reinterpret_cast<const __half2*>(Rk + RL.kscale);
   const __half2* Kz2 = reinterpret_cast<const __half2*>(Rk + RL.kzero);
   const __half* Kr = reinterpret_cast<const __half*>(Rk + RL.kfactor);
 
   uint32_t bq[D / 16][NT][2];
-  float qz[NT];
+  float2 qz2[NT];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) qz[nt] = 0.0f;
+  for (int nt = 0; nt < NT; ++nt) qz2[nt] = make_float2(0.0f, 0.0f);
   const bool lo_col = (g & 1) != 0;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const int j0 = 16 * kk + 2 * tq;
-    const __half2 s0 = Ks2[j0 >> 1], s1 = Ks2[(j0 + 8) >> 1];
-    const float2 z0 = __half22float2(Kz2[j0 >> 1]), z1 = __half22float2(Kz2[(j0 + 8) >> 1]);
+    const int jp = 8 * kk + tq;  // channel pair (16kk + 2tq, +1); jp + 4: (16kk + 2tq + 8, +9)
+    const __half2 s0 = Ks2[jp], s1 = Ks2[jp + 4];
+    const float2 z0 = __half22float2(Kz2[jp]), z1 = __half22float2(Kz2[jp + 4]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int head = 4 * nt + (g >> 1);
-      const float2 qa = *reinterpret_cast<const float2*>(qsm + head * QLD + j0);
-      const float2 qb = *reinterpret_cast<const float2*>(qsm + head * QLD + j0 + 8);
-      qz[nt] = fmaf(qa.x, z0.x, fmaf(qa.y, z0.y, fmaf(qb.x, z1.x, fmaf(qb.y, z1.y, qz[nt]))));
-      bq[kk][nt][0] = b_split(qh2[head * QH + (j0 >> 1)], ql2[head * QH + (j0 >> 1)], s0, lo_col);
-      bq[kk][nt][1] = b_split(qh2[head * QH + ((j0 + 8) >> 1)], ql2[head * QH + ((j0 + 8) >> 1)], s1, lo_col);
+      const float4 q4 = *reinterpret_cast<const float4*>(qsm + head * QLD + 16 * kk + 4 * tq);
+      qz2[nt] = fma2(make_float2(q4.x, q4.y), z0, qz2[nt]);
+      qz2[nt] = fma2(make_float2(q4.z, q4.w), z1, qz2[nt]);
+      const uint2 u0 = qhl[head * QH + jp], u1 = qhl[head * QH + jp + 4];
+      bq[kk][nt][0] = b_split(u2h2(u0.x), u2h2(u0.y), s0, lo_col);
+      bq[kk][nt][1] = b_split(u2h2(u1.x), u2h2(u1.y), s1, lo_col);
     }
   }
   float qzm[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float v = qz[nt];
+    float v = qz2[nt].x + qz2[nt].y;
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     qzm[nt] = __shfl_sync(0xffffffffu, v, 8 * tq);  // head 4nt + tq lives in lanes g = 2tq
@@ -198,35 +199,36 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
         for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a, bq[4 * kq + e][nt][0], bq[4 * kq + e][nt][1]);
       }
     }
-    const float r0 = __half2float(Kr[16 * mi + g]);
-    const float r1 = __half2float(Kr[16 * mi + g + 8]);
+    const float2 r = make_float2(__half2float(Kr[16 * mi + g]), __half2float(Kr[16 * mi + g + 8]));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      lg[mi][nt][0] = r0 * fmaf(acc[nt][0] + acc[nt][1], kTwo24, qzm[nt]);
-      lg[mi][nt][1] = r1 * fmaf(acc[nt][2] + acc[nt][3], kTwo24, qzm[nt]);
+      const float2 t = add2(make_float2(acc[nt][0], acc[nt][2]), make_float2(acc[nt][1], acc[nt][3]));
+      const float2 u = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(qzm[nt], qzm[nt])), r);
+      lg[mi][nt][0] = u.x;
+      lg[mi][nt][1] = u.y;
     }
   }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     float mx = fmaxf(lg[0][nt][0], lg[0][nt][1]);
 #pragma unroll
-    for (int mi = 1; mi < 8; ++mi) mx = fmaxf(mx, fmaxf(lg[mi][nt][0], lg[mi][nt][1]));
+    for (int mi = 1; mi < 8; ++mi) mx = fmax3(mx, lg[mi][nt][0], lg[mi][nt][1]);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const float mnew = fmaxf(st.m[nt], mx);
     alpha[nt] = exp2f(st.m[nt] - mnew);
     st.m[nt] = mnew;
-    float ps = 0.0f;
+    float2 ps = make_float2(0.0f, 0.0f);
 #pragma unroll
-    for (int mi = 0; mi < 8; ++mi)
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float pv = exp2f(lg[mi][nt][r] - mnew);
-        lg[mi][nt][r] = pv;
-        ps += pv;
-      }
-    st.l[nt] = fmaf(st.l[nt], alpha[nt], ps);
+    for (int mi = 0; mi < 8; ++mi) {
+      const float2 d = sub2(make_float2(lg[mi][nt][0], lg[mi][nt][1]), make_float2(mnew, mnew));
+      const float2 pv = make_float2(exp2f(d.x), exp2f(d.y));
+      lg[mi][nt][0] = pv.x;
+      lg[mi][nt][1] = pv.y;
+      ps = add2(ps, pv);
+    }
+    st.l[nt] = fmaf(st.l[nt], alpha[nt], ps.x + ps.y);
   }
 }
 
@@ -244,29 +246,30 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
   for (int mc = 0; mc < D / 16; ++mc)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) pacc[mc][nt][0] = pacc[mc][nt][1] = pacc[mc][nt][2] = pacc[mc][nt][3] = 0.0f;
-  float zs[NT];
+  float2 zs2[NT];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) zs[nt] = 0.0f;
+  for (int nt = 0; nt < NT; ++nt) zs2[nt] = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int ks2 = 0; ks2 < 4; ++ks2) {
     uint32_t bw[2][NT][2];
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
       const int ks = 2 * ks2 + f;
-      const float sv0 = __half2float(Vs[16 * ks + g]), sv1 = __half2float(Vs[16 * ks + g + 8]);
-      const float zv0 = __half2float(Vz[16 * ks + g]), zv1 = __half2float(Vz[16 * ks + g + 8]);
-      // compensate the subnormal scale 2^(4f + 2h) of this block's codes (h = 0: rows g)
+      // token scales with the subnormal scale 2^(4f + 2h) of this block's codes compensated
+      // (h = 0: rows g); the powers of two keep the products exact
       const float c0 = f ? 1.0f / 16.0f : 1.0f, c1 = f ? 1.0f / 64.0f : 0.25f;
+      const float2 svc = make_float2(__half2float(Vs[16 * ks + g]) * c0, __half2float(Vs[16 * ks + g + 8]) * c1);
+      const float2 zv = make_float2(__half2float(Vz[16 * ks + g]), __half2float(Vz[16 * ks + g + 8]));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        const float p0 = lg[ks][nt][0], p1 = lg[ks][nt][1];
-        zs[nt] = fmaf(p0, zv0, fmaf(p1, zv1, zs[nt]));
-        const float w0 = p0 * sv0 * c0, w1 = p1 * sv1 * c1;
-        const __half hi0 = __float2half_rn(w0), hi1 = __float2half_rn(w1);
-        const __half lo0 = __float2half_rn(w0 - __half2float(hi0));
-        const __half lo1 = __float2half_rn(w1 - __half2float(hi1));
-        bw[f][nt][0] = movmatrix_trans(h2u(__halves2half2(hi0, lo0)));
-        bw[f][nt][1] = movmatrix_trans(h2u(__halves2half2(hi1, lo1)));
+        const float2 pp = make_float2(lg[ks][nt][0], lg[ks][nt][1]);
+        zs2[nt] = fma2(pp, zv, zs2[nt]);
+        const float2 w = mul2(pp, svc);
+        const __half2 hi = __floats2half2_rn(w.x, w.y);
+        const float2 r = sub2(w, __half22float2(hi));
+        const __half2 lo = __floats2half2_rn(r.x, r.y);
+        bw[f][nt][0] = movmatrix_trans(h2u(__lows2half2(hi, lo)));   // (hi, lo) of row g
+        bw[f][nt][1] = movmatrix_trans(h2u(__highs2half2(hi, lo)));  // (hi, lo) of row g + 8
       }
     }
 #pragma unroll
@@ -286,21 +289,24 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
       }
     }
   }
+  float zs[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    zs[nt] = zs2[nt].x + zs2[nt].y;
     zs[nt] += __shfl_xor_sync(0xffffffffu, zs[nt], 4);
     zs[nt] += __shfl_xor_sync(0xffffffffu, zs[nt], 8);
     zs[nt] += __shfl_xor_sync(0xffffffffu, zs[nt], 16);
   }
 #pragma unroll
   for (int mc = 0; mc < D / 16; ++mc) {
-    const float cj0 = __half2float(Vc[16 * mc + g]), cj1 = __half2float(Vc[16 * mc + g + 8]);
+    const float2 cj = make_float2(__half2float(Vc[16 * mc + g]), __half2float(Vc[16 * mc + g + 8]));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      st.o[mc][nt][0] = fmaf(st.o[mc][nt][0], alpha[nt],
-                             cj0 * fmaf(pacc[mc][nt][0] + pacc[mc][nt][1], kTwo24, zs[nt]));
-      st.o[mc][nt][1] = fmaf(st.o[mc][nt][1], alpha[nt],
-                             cj1 * fmaf(pacc[mc][nt][2] + pacc[mc][nt][3], kTwo24, zs[nt]));
+      float2 t = add2(make_float2(pacc[mc][nt][0], pacc[mc][nt][2]), make_float2(pacc[mc][nt][1], pacc[mc][nt][3]));
+      t = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(zs[nt], zs[nt])), cj);
+      const float2 o = fma2(make_float2(st.o[mc][nt][0], st.o[mc][nt][1]), make_float2(alpha[nt], alpha[nt]), t);
+      st.o[mc][nt][0] = o.x;
+      st.o[mc][nt][1] = o.y;
     }
   }
 }
@@ -317,8 +323,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
   extern __shared__ __align__(128) uint8_t smem_d[];
   uint8_t* recs = smem_d;
   float* qsm = reinterpret_cast<float*>(smem_d + S::kRecBytes);
-  __half2* qh2 = reinterpret_cast<__half2*>(smem_d + S::kRecBytes + S::kQBytes);
-  __half2* ql2 = qh2 + NH * QH;
+  uint2* qhl = reinterpret_cast<uint2*>(smem_d + S::kRecBytes + S::kQBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kQhBytes);
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -373,9 +378,10 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
         bulk_copy_g2s(vslot, src + KH, VH, vbar);
       }
     }
-    // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d): fp32 for q~.z',
-    // fp16 hi + lo for the B operand (channels 8..15 of every 16 pre-divided by 16, the
-    // subnormal scale of their codes)
+    // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d): fp32 for q~.z'
+    // (channels 16k + {2t, 2t+1, 2t+8, 2t+9} adjacent), fp16 hi + lo for the B operand
+    // (channels 8..15 of every 16 pre-divided by 16, the subnormal scale of their codes; one
+    // {hi pair, lo pair} entry per channel pair)
     for (int hl = warp; hl < NH; hl += kDecWarps) {
       float v[D / 32];
 #pragma unroll
@@ -387,17 +393,16 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
       }
       warp_fwht<D>(v, lane);
       const float sc = p.qscale * inv_sqrt_d<D>();
-      __half* qh = reinterpret_cast<__half*>(qh2 + hl * QH);
-      __half* ql = reinterpret_cast<__half*>(ql2 + hl * QH);
+      __half* qe = reinterpret_cast<__half*>(qhl + hl * QH);
 #pragma unroll
       for (int e = 0; e < D / 32; ++e) {
         const int j = lane * (D / 32) + e;
         const float x = v[e] * sc;
-        qsm[hl * QLD + j] = x;
+        qsm[hl * QLD + (j & ~15) + 4 * ((j & 7) >> 1) + 2 * ((j >> 3) & 1) + (j & 1)] = x;
         const float xb = (j & 15) >= 8 ? x * 0.0625f : x;
         const __half hi = __float2half_rn(xb);
-        qh[j] = hi;
-        ql[j] = __float2half_rn(xb - __half2float(hi));
+        qe[4 * (j >> 1) + (j & 1)] = hi;
+        qe[4 * (j >> 1) + 2 + (j & 1)] = __float2half_rn(xb - __half2float(hi));
       }
     }
     __syncthreads();  // q in shared memory for every warp
@@ -410,6 +415,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
 #pragma unroll
       for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
     }
+    // record of the warp's next page, looked up one page ahead so that issuing its copies
+    // never waits on the block-table load
+    const uint8_t* nxt = cnt > 1 ? page_src(1) : nullptr;
     for (int j = 0; j < cnt; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(kbar, j & 1))) {
         // a copy never arrived: report, drain this warp's copies still in flight, stop
@@ -421,10 +429,9 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
         break;
       }
       float lg[8][NT][2], alpha[NT];
-      qk_page<D, NT>(kslot, qsm, qh2, ql2, lane, st, lg, alpha);
+      qk_page<D, NT>(kslot, qsm, qhl, lane, st, lg, alpha);
       __syncwarp();
       const bool more = j + 1 < cnt;
-      const uint8_t* nxt = more ? page_src(j + 1) : nullptr;
       if (lane == 0 && more) {  // the K slot is free: fetch the next page's K half
         fence_proxy_async_smem();
         mbar_expect_tx(kbar, KH);
@@ -445,6 +452,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
         mbar_expect_tx(vbar, VH);
         bulk_copy_g2s(vslot, nxt + KH, VH, vbar);
       }
+      nxt = j + 2 < cnt ? page_src(j + 2) : nullptr;
     }
     // ---- merge the warps of this CTA ----
     __syncthreads();  // every warp is done with its slots

@@ -107,16 +107,6 @@ __device__ __forceinline__ void rs_chan2(float2 (&s)[N], float2 (&m2)[N], int ma
   }
 }
 
-__device__ __forceinline__ float fmin3(float a, float b, float c) {
-  float d;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 
 // Barrier among the `count` threads (a multiple of 32) that use barrier `id` (1..15).
 __device__ __forceinline__ void group_sync(int id, int count) {
