@@ -244,13 +244,71 @@ def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, s
     return statistics.median(ms), nbytes
 
 
-def _decode_configs(torch, kv, synth, peak):
+def _quality(torch, kv, synth):
+    """Attention-output cosine against full-precision attention over the raw fp16 K/V (float64,
+    torch), for the KVarN K4V2 cache decoded by the library, and, as an ablation, for plain
+    asymmetric round-to-nearest at the same bits on the raw 128-token tiles (K 4-bit per
+    channel, V 2-bit per token; no rotation, no variance normalisation)."""
+    dev = torch.device("cuda")
+    B, L, hkv, G, d = 4, 4096, HKV, HQ // HKV, D0
+    pages = L // 128
+    desc = kv.desc_from_preset(d, hkv)
+    k, v = synth.outlier_kv(B * L, hkv, d, seed=SEED + 100, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEED + 101)
+    q = torch.randn((B, hkv * G, d), generator=gen, device=dev).half()
+    table = torch.arange(B * pages, dtype=torch.int32, device=dev).view(B, pages)
+    pool = kv.alloc_pool(desc, B * pages, device=dev)
+    kv.quantize_tiles(desc, k, v, table.reshape(-1).contiguous(), pool)
+    out = torch.empty_like(q)
+    ws = kv.alloc_workspace(desc, B, hkv * G, pages, device=dev)
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    kv.decode_attention(desc, q, pool, table, lens, out, ws, softmax_scale=1 / math.sqrt(d))
+    torch.cuda.synchronize()
+    qq = q.double().view(B, hkv, G, d)
+
+    def attend(kk, vv):  # [B, L, hkv, d] -> [B, hkv * G, d]
+        p = torch.softmax(torch.einsum("bhgd,blhd->bhgl", qq, kk) / math.sqrt(d), dim=-1)
+        return torch.einsum("bhgl,blhd->bhgd", p, vv).reshape(B, hkv * G, d)
+
+    def rtn(x, bits, dim):
+        lo, hi = x.amin(dim=dim, keepdim=True), x.amax(dim=dim, keepdim=True)
+        s = ((hi - lo) / (2 ** bits - 1)).clamp_min(1e-8)
+        return torch.round((x - lo) / s).clamp(0, 2 ** bits - 1) * s + lo
+
+    kk, vv = k.double().view(B, L, hkv, d), v.double().view(B, L, hkv, d)
+    ref = attend(kk, vv)
+    k_rtn = rtn(kk.view(B, pages, 128, hkv, d), 4, 2).view(B, L, hkv, d)
+    v_rtn = rtn(vv.view(B, pages, 128, hkv, d), 2, 4).view(B, L, hkv, d)
+    naive = attend(k_rtn, v_rtn)
+
+    def cos(a):
+        return torch.nn.functional.cosine_similarity(a.reshape(-1, d), ref.reshape(-1, d), dim=-1)
+
+    c_kv, c_rtn = cos(out.double()), cos(naive)
+    return {
+        "cosine_vs_full_precision": float(c_kv.mean()), "cosine_min": float(c_kv.min()),
+        "naive_rtn_cosine": float(c_rtn.mean()), "naive_rtn_cosine_min": float(c_rtn.min()),
+        "sample": "%d sequences x %d tokens, %d q heads / %d kv heads, head_dim %d, outlier "
+                  "generator; reference: float64 softmax attention over the raw fp16 K/V"
+                  % (B, L, hkv * G, hkv, d),
+        "note": "a quality figure, not a target",
+    }
+
+
+def _decode_configs(torch, kv, synth, peak, args):
     """The 32B-class 64-layer decode step and the long-context shapes, each against bytes/peak."""
     res = {}
-    for key, cfg in (
-            ("decode_32b_step", dict(batch=32, seq_len=16384, hq=64, hkv=8, d0=128, layers=64, seed=4)),
-            ("decode_long_d256", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=256, layers=1, seed=5)),
-            ("decode_long_d96", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=96, layers=1, seed=5))):
+    for key, group, cfg in (
+            ("decode_32b_step", "32b", dict(batch=32, seq_len=16384, hq=64, hkv=8, d0=128, layers=64, seed=4)),
+            ("decode_long_d256", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=256, layers=1, seed=5)),
+            ("decode_long_d96", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=96, layers=1, seed=5))):
+        if args.extras not in ("all", group):
+            continue
+        if args.extra_batch:
+            cfg["batch"] = args.extra_batch
+        if args.extra_layers and cfg["layers"] > 1:
+            cfg["layers"] = args.extra_layers
         ms, nbytes = _time_decode_layers(torch, kv, synth, **cfg)
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[key] = {
@@ -378,7 +436,8 @@ def _run_kvarn(args, torch, world, rank):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     # ---- the 32B-class step (64 layers, GQA 8) and the long-context shapes (not timed steps)
-    extra = _decode_configs(torch, kv, synth, peak) if not args.no_extra else {}
+    extra = _decode_configs(torch, kv, synth, peak, args)
+    quality = _quality(torch, kv, synth)
 
     # ---- aggregate over ranks (replicas)
     if world > 1:
@@ -440,6 +499,7 @@ def _run_kvarn(args, torch, world, rank):
             },
         },
         **extra,
+        "quality": quality,
         "e2e": {"value": e2e_value, "unit": "KV tokens/s",
                 "h2d_bytes_per_step": (BATCH * HQ * D0 + 2 * BATCH * HKV * D0) * 2,
                 "d2h_bytes_per_step": BATCH * HQ * D0 * 2},
@@ -452,59 +512,125 @@ def _run_kvarn(args, torch, world, rank):
 # CPU oracle (baseline) arm
 # ------------------------------------------------------------------------------------------------
 
-def _oracle_sample(seconds: float, seed: int = SEED):
-    """Time the float64 oracle's decode attention on whole (sequence, kv head) caches of the
-    workload until `seconds` of CPU work: returns (KV tokens/s, description)."""
+_ORACLE_UNITS = None
+
+
+def _oracle_units(seed: int, n_units: int = 4):
+    """(q rows, oracle page records, L) of n_units whole (sequence, kv head) decode units of the
+    workload, quantised by the oracle (not timed)."""
     import numpy as np
-    import torch
     from calibration_free_kv_gb300 import synth
     from oracle import kvarn_oracle as ko
 
     shape = synth.decode_batch(BATCH, HQ, HKV, D0, seed=seed, min_pages=MIN_PAGES, max_pages=MAX_PAGES)
     lens = shape["seq_lens"].tolist()
     q = shape["q"].double().numpy()
-    done_tokens, done_units, t_total = 0, 0, 0.0
-    b = 0
     group = HQ // HKV
-    while t_total < seconds or done_units == 0:
-        L = lens[b % BATCH]
+    units = []
+    for b in range(n_units):
+        L = lens[b]
         k, v = synth.outlier_kv(L, 1, D0, seed=seed * 7 + b)
         n = L // 128
-        kt = k[:, 0].double().numpy().reshape(n, 128, D0)
-        vt = v[:, 0].double().numpy().reshape(n, 128, D0)
-        kq = ko.quantize_tile(kt, "K")
-        vq = ko.quantize_tile(vt, "V")
+        kq = ko.quantize_tile(k[:, 0].double().numpy().reshape(n, 128, D0), "K")
+        vq = ko.quantize_tile(v[:, 0].double().numpy().reshape(n, 128, D0), "V")
         fields = ("codes", "scale", "zero", "factor")
         recs = [ko.pack_record({f: kq[f][i] for f in fields}, {f: vq[f][i] for f in fields})
                 for i in range(n)]
-        t0 = time.perf_counter()
-        ko.decode_sequence(q[b % BATCH, :group], recs, None, None, 1 / math.sqrt(D0), D0)
-        t_total += time.perf_counter() - t0
-        done_tokens += L
-        done_units += 1
-        b += 1
-    # one (sequence, kv head) unit covers L tokens for 1 of the HKV heads
-    value = done_tokens / HKV / t_total
-    desc = ("%d whole (sequence, kv head) decode units (%d token-heads, 4 query heads each) of the "
-            "workload through the float64 oracle (dequantise + textbook attention); %.1f s"
-            % (done_units, done_tokens, t_total))
-    return value, desc, t_total
+        units.append((np.ascontiguousarray(q[b, :group]), recs, L))
+    return units
+
+
+def _oracle_init(units):
+    global _ORACLE_UNITS
+    _ORACLE_UNITS = units
+
+
+def _oracle_work(seconds: float):
+    """Decode the prepared units through the float64 oracle for `seconds`: (KV token-heads, s)."""
+    from oracle import kvarn_oracle as ko
+    tokens, i = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        q, recs, L = _ORACLE_UNITS[i % len(_ORACLE_UNITS)]
+        ko.decode_sequence(q, recs, None, None, 1 / math.sqrt(D0), D0)
+        tokens += L
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return tokens, el
+
+
+class OracleTimer:
+    """The float64 oracle's decode attention timed on the host cores: one spawned process per
+    core (single-threaded BLAS each), or one process alone."""
+
+    def __init__(self, seed: int = SEED):
+        import multiprocessing as mp
+        self.units = _oracle_units(seed)
+        self.cores = os.cpu_count() or 1
+        keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+        saved = {k: os.environ.get(k) for k in keys}
+        for k in keys:
+            os.environ[k] = "1"
+        try:
+            ctx = mp.get_context("spawn")
+            self.pool = ctx.Pool(self.cores, initializer=_oracle_init, initargs=(self.units,))
+            self.pool.map(_oracle_work, [0.0] * self.cores)  # workers up and warm
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, seconds: float, cores: int):
+        """KV tokens/s (all heads of a token) over `cores` processes working `seconds` each."""
+        res = self.pool.map(_oracle_work, [seconds] * cores, chunksize=1)
+        tokens = sum(t for t, _ in res)
+        wall = max(e for _, e in res)
+        return tokens / HKV / wall, wall
+
+    def describe(self):
+        pages = sum(len(r) for _, r, _ in self.units)
+        return ("%d whole (sequence, kv head) decode units of the workload (%d pages, 4 query heads "
+                "each), decoded repeatedly through the float64 oracle (dequantise + textbook "
+                "attention), one single-threaded process per core" % (len(self.units), pages))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def _cpu_baseline(seconds: float):
+    ot = OracleTimer()
+    try:
+        v_all, _ = ot.run(seconds / 2, ot.cores)
+        v_one, _ = ot.run(seconds / 2, 1)
+    finally:
+        ot.close()
+    return {"value": v_all, "unit": "KV tokens/s", "cores": ot.cores, "kind": "oracle",
+            "value_1core": v_one, "sample": ot.describe() + "; %.1f s on all cores, %.1f s on one"
+            % (seconds / 2, seconds / 2)}
 
 
 def _run_reference(args, world, rank):
     if rank != 0:
         return None
     per_step = max(1.0, 20.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        _oracle_sample(per_step * 0.25)
-    vals, total_t, descs = [], 0.0, []
-    for i in range(args.steps):
-        v, d, t = _oracle_sample(per_step, seed=SEED + i)
-        vals.append(v)
-        total_t += t
-        descs.append(d)
+    ot = OracleTimer()
+    try:
+        for _ in range(args.warmup):
+            ot.run(per_step * 0.25, ot.cores)
+        vals, total_t = [], 0.0
+        for i in range(args.steps):
+            v, t = ot.run(per_step, ot.cores)
+            vals.append(v)
+            total_t += t
+    finally:
+        ot.close()
+    descs = [ot.describe()]
     value = statistics.mean(vals)
-    cores = os.cpu_count()
+    cores = ot.cores
     return {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world,
@@ -529,8 +655,12 @@ def main():
                     help="decode batch (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="CPU work of the oracle baseline sample (kvarn arm)")
-    ap.add_argument("--no-extra", action="store_true",
-                    help="skip the 64-layer and long-context decode shapes (profiling runs)")
+    ap.add_argument("--extras", choices=("all", "none", "32b", "long"), default="all",
+                    help="which of the 64-layer and long-context decode shapes to time")
+    ap.add_argument("--extra-batch", type=int, default=0,
+                    help="batch of those shapes (0 = the workload's; smaller only for profiling)")
+    ap.add_argument("--extra-layers", type=int, default=0,
+                    help="layers of the 32B-class step (0 = 64; fewer only for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -552,9 +682,7 @@ def main():
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     res = _run_kvarn(args, torch, world, rank)
     if rank == 0 and res is not None:
-        value, desc, t = _oracle_sample(args.cpu_seconds)
-        res["cpu_baseline"] = {"value": value, "unit": "KV tokens/s", "cores": os.cpu_count(),
-                               "kind": "oracle", "sample": desc}
+        res["cpu_baseline"] = _cpu_baseline(args.cpu_seconds)
         print(json.dumps(res))
     if world > 1:
         torch.distributed.barrier()
