@@ -1,4 +1,4 @@
-"""Plain float64 CPU oracle for KVarN's K4V2 g128 KV-cache path.
+"""Plain float64 CPU oracle for KVarN's K4V2 g128 KV-cache path (and the other k/v bit presets).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this module.  The
@@ -19,7 +19,8 @@ Per 128-token tile of one KV head, K and V separately:
   2. rotate along head_dim: X = Z_pad . H / sqrt(d) [hotdry §Hadamard 旋转; vatt §四個步驟, Hadamard rotation]
   3. log-space Sinkhorn-style normalisation, channel std step then token std
      step, a fixed number of iterations           [hotdry §迭代方差归一化; vatt §四個步驟, iterative variance normalization]
-  4. asymmetric round-to-nearest: K 4-bit per channel, V 2-bit per token
+  4. asymmetric round-to-nearest: K 4-bit per channel, V 2-bit per token (other presets:
+     other widths, same steps)
                                                   [hotdry §非对称量化与尺度折叠; vatt §為什麼樸素的 2-bit…, worked example]
   5. normalisation factors folded into the stored scales ("scale folding")
                                                   [hotdry §非对称量化与尺度折叠; vatt §四個步驟, asymmetric quantization]
@@ -48,6 +49,11 @@ import numpy as np
 TILE_TOKENS = 128          # one tile == one paged-attention block  [vatt §怎麼用, knob table: tile=128]
 K_BITS = 4                 # preset kvarn_k4v2_g128                  [hotdry §核心配置参数]
 V_BITS = 2
+# Other presets run the same pipeline with other code widths [vatt §四個步驟, bit-width
+# assignment: other k/v bit presets take the same path; vatt §怎麼用, key/value bits knobs].
+# Reading: widths of 2 and 4 bits on either side; tiles stay 128 tokens.
+PRESETS = {"kvarn_k4v2_g128": (4, 2), "kvarn_k4v4_g128": (4, 4), "kvarn_k2v2_g128": (2, 2)}
+CODE_BITS = (2, 4)
 SINKHORN_ITERS = 4         # "usually 3-5 iterations"                [hotdry §迭代方差归一化, step 3]
 SINKHORN_EPS = 1e-6        # reading: stds below this are not normalised (pages give no value)
 SCALE_FLOOR = 1e-8         # reading: quantiser step floor for constant groups
@@ -178,14 +184,15 @@ def _f16(a):
 
 
 def quantize_tile(tile: np.ndarray, kind: str, d: int | None = None,
-                  iters: int = SINKHORN_ITERS, eps: float = SINKHORN_EPS):
+                  iters: int = SINKHORN_ITERS, eps: float = SINKHORN_EPS, bits: int | None = None):
     """Quantise a [..., 128, d0] tile of keys (kind 'K') or values (kind 'V').
 
-    K: 4-bit, scale/zero per channel over the 128 tokens; stored s'_j = s_j c_j,
+    K: 4-bit (default), scale/zero per channel over the 128 tokens; stored s'_j = s_j c_j,
        z'_j = m_j c_j (fp16) and the token factor r_i (fp16).
-    V: 2-bit, scale/zero per token over the channels; stored s'_i = s_i r_i,
+    V: 2-bit (default), scale/zero per token over the channels; stored s'_i = s_i r_i,
        z'_i = m_i r_i (fp16) and the channel factor c_j (fp16).
-    Returns dict(codes [...,T,d] uint8, scale fp16, zero fp16, factor fp16, pre f64).
+    `bits` overrides the width (2 or 4) for the other presets.
+    Returns dict(codes [...,T,d] uint8, scale fp16, zero fp16, factor fp16, pre f64, bits).
     [hotdry §非对称量化与尺度折叠: keys 4-bit, values 2-bit; key scales per channel,
      value scales per token, scales multiplied back on read; vatt §四個步驟 table:
      KEY per-channel 4-bit, VALUE per-token 2-bit]
@@ -197,14 +204,16 @@ def quantize_tile(tile: np.ndarray, kind: str, d: int | None = None,
     x = rotate(tile, d)
     n, r, c = sinkhorn_normalise(x, iters, eps)
     if kind == "K":
-        q, s, m, pre = rtn_asymmetric(n, K_BITS, axis=-2)
+        bits = K_BITS if bits is None else bits
+        q, s, m, pre = rtn_asymmetric(n, bits, axis=-2)
         scale, zero, factor = _f16(s * c), _f16(m * c), _f16(r)
     elif kind == "V":
-        q, s, m, pre = rtn_asymmetric(n, V_BITS, axis=-1)
+        bits = V_BITS if bits is None else bits
+        q, s, m, pre = rtn_asymmetric(n, bits, axis=-1)
         scale, zero, factor = _f16(s * r), _f16(m * r), _f16(c)
     else:
         raise ValueError("kind must be 'K' or 'V'")
-    return {"codes": q, "scale": scale, "zero": zero, "factor": factor, "pre": pre}
+    return {"codes": q, "scale": scale, "zero": zero, "factor": factor, "pre": pre, "bits": bits}
 
 
 def dequantize_tile(codes, scale, zero, factor, kind: str, d0: int) -> np.ndarray:
@@ -236,133 +245,150 @@ def dequantize_tile(codes, scale, zero, factor, kind: str, d0: int) -> np.ndarra
 #
 # The layout is this build's own contract (the pages fix only that the scales
 # live with the 128-token block: vatt §怎麼用, "scales hang on each block's
-# metadata").  Sections, all 16-byte aligned, T = 128, d = padded head_dim:
-#   K codes  T*d/2 bytes, uint32 words of eight 4-bit codes
+# metadata").  Sections, all 16-byte aligned, T = 128, d = padded head_dim,
+# kb / vb = K / V code bits (4 / 2 for kvarn_k4v2_g128):
+#   K codes  T*d*kb/8 bytes of uint32 words
 #   K scale[d], K zero[d], K token factor[T]  (fp16, little endian)
-#   V codes  T*d/4 bytes, uint32 words of sixteen 2-bit codes
+#   V codes  T*d*vb/8 bytes of uint32 words
 #   V scale[T], V zero[T], V channel factor[d] (fp16, little endian)
 #
-# K word (mi, kk, lane), mi in [0,8), kk in [0,d/16), lane in [0,32), g = lane//4,
-# tq = lane%4: word index ((mi*(d//64) + kk//4)*32 + lane)*4 + kk%4.  It holds
-# token t = 16mi + g + 8rho and channel j = 16kk + 8h + 2tq + p (rho, h, p in
-# {0,1}) at nibble h + 2rho + 4p.
-# V word (ks2, mc, lane), ks2 in [0,4), mc in [0,d/16): word index
-# ((ks2*(d//64) + mc//4)*32 + lane)*4 + mc%4.  It holds channel j = 16mc + g + 8rho
-# and token t = 16(2ks2+f) + 8h + 2tq + p (f, rho, h, p in {0,1}) at 2-bit slot
+# Every word carries m16n8k16 A-operand fragments (16 x 16 blocks, lane = 4g + tq,
+# g = lane//4, tq = lane%4; element (rho, h, p) of a fragment sits at row g + 8rho,
+# column 8h + 2tq + p of its block).  K's A operand is codes[token, channel]; V's is
+# codes^T[channel, token].  Blocks are indexed (o, i): K o = token block, i = channel
+# block; V o = token block, i = channel block; ni4 = d // 64.
+#   4-bit: word ((o*ni4 + i//4)*32 + lane)*4 + i%4 holds fragment (o, i), element
+#          (rho, h, p) at nibble h + 2rho + 4p.
+#   2-bit: word ((o//2*ni4 + i//4)*32 + lane)*4 + i%4 holds fragments (o, i) for both
+#          o of the pair, element (rho, h, p) of block o at slot 2(o%2) + h + 4rho + 8p.
+# For kvarn_k4v2_g128: K word (mi, kk, lane) holds token t = 16mi + g + 8rho and channel
+# j = 16kk + 8h + 2tq + p at nibble h + 2rho + 4p; V word (ks2, mc, lane) holds channel
+# j = 16mc + g + 8rho and token t = 16(2ks2+f) + 8h + 2tq + p at 2-bit slot
 # 2f + h + 4rho + 8p.
 
-def record_bytes(d: int, tokens: int = TILE_TOKENS) -> int:
-    """Bytes of one page record: codes at 4+2 bits per token-channel plus fp16 metadata.
+def record_bytes(d: int, tokens: int = TILE_TOKENS, k_bits: int = K_BITS, v_bits: int = V_BITS) -> int:
+    """Bytes of one page record: kb + vb bits of codes per token-channel plus fp16 metadata.
 
-    Pinned by: test_record_bytes (13824 B at d=128, ratio vs fp16 below 1/4, as the
-    vatt capacity widget's "<0.25x, about 4x" for kvarn_k4v2_g128).
+    Pinned by: test_record_bytes (13824 B at d=128 for K4V2, ratio vs fp16 below 1/4, as
+    the vatt capacity widget's "<0.25x, about 4x" for kvarn_k4v2_g128), test_record_bytes_presets.
     """
-    return tokens * d // 2 + tokens * d // 4 + 2 * (3 * d + 3 * tokens)
+    return tokens * d * k_bits // 8 + tokens * d * v_bits // 8 + 2 * (3 * d + 3 * tokens)
 
 
-def _section_offsets(d: int):
+def _section_offsets(d: int, k_bits: int = K_BITS, v_bits: int = V_BITS):
     """Byte offsets (K codes, V codes, K scale, K zero, K factor, V scale, V zero, V factor)."""
     t = TILE_TOKENS
     o_kc = 0
-    o_ks = t * d // 2
+    o_ks = t * d * k_bits // 8
     o_kz = o_ks + 2 * d
     o_kr = o_kz + 2 * d
     o_vc = o_kr + 2 * t
-    o_vs = o_vc + t * d // 4
+    o_vs = o_vc + t * d * v_bits // 8
     o_vz = o_vs + 2 * t
     o_vcf = o_vz + 2 * t
     return o_kc, o_vc, o_ks, o_kz, o_kr, o_vs, o_vz, o_vcf
 
 
-def _k_positions(d: int):
+def _code_positions(kind: str, bits: int, d: int):
+    """(word index, bit shift) for every (token, channel) of a K or V code section."""
+    t = np.arange(TILE_TOKENS)[:, None]
+    j = np.arange(d)[None, :]
+    if kind == "K":      # rows are tokens, columns channels
+        o, row, i, col = t // 16, t % 16, j // 16, j % 16
+    elif kind == "V":    # rows are channels, columns tokens
+        o, col, i, row = t // 16, t % 16, j // 16, j % 16
+    else:
+        raise ValueError("kind must be 'K' or 'V'")
+    g, rho = row % 8, row // 8
+    h, tq, p = col // 8, (col % 8) // 2, col % 2
+    lane = 4 * g + tq
+    ni4 = d // 64
+    if bits == 4:
+        word = ((o * ni4 + i // 4) * 32 + lane) * 4 + i % 4
+        shift = 4 * (h + 2 * rho + 4 * p)
+    elif bits == 2:
+        word = (((o // 2) * ni4 + i // 4) * 32 + lane) * 4 + i % 4
+        shift = 2 * (2 * (o % 2) + h + 4 * rho + 8 * p)
+    else:
+        raise ValueError("code bits must be 2 or 4")
+    return word, shift
+
+
+def _k_positions(d: int, bits: int = K_BITS):
     """(word index, bit shift) for every (token, channel) of the K code section."""
-    t = np.arange(TILE_TOKENS)[:, None]
-    j = np.arange(d)[None, :]
-    mi, rem_t = t // 16, t % 16
-    g, rho = rem_t % 8, rem_t // 8
-    kk, rem_j = j // 16, j % 16
-    h, rem_h = rem_j // 8, rem_j % 8
-    tq, p = rem_h // 2, rem_h % 2
-    lane = 4 * g + tq
-    word = ((mi * (d // 64) + kk // 4) * 32 + lane) * 4 + kk % 4
-    nib = h + 2 * rho + 4 * p
-    return word, 4 * nib
+    return _code_positions("K", bits, d)
 
 
-def _v_positions(d: int):
+def _v_positions(d: int, bits: int = V_BITS):
     """(word index, bit shift) for every (token, channel) of the V code section."""
-    t = np.arange(TILE_TOKENS)[:, None]
-    j = np.arange(d)[None, :]
-    ks, rem_t = t // 16, t % 16
-    ks2, f = ks // 2, ks % 2
-    h, rem_h = rem_t // 8, rem_t % 8
-    tq, p = rem_h // 2, rem_h % 2
-    mc, rem_j = j // 16, j % 16
-    rho, g = rem_j // 8, rem_j % 8
-    lane = 4 * g + tq
-    word = ((ks2 * (d // 64) + mc // 4) * 32 + lane) * 4 + mc % 4
-    slot = 2 * f + h + 4 * rho + 8 * p
-    return word, 2 * slot
+    return _code_positions("V", bits, d)
 
 
 def pack_record(k: dict, v: dict) -> bytes:
-    """Pack the quantised K and V tiles of one (page, kv head) into a page record.
+    """Pack the quantised K and V tiles of one (page, kv head) into a page record; the code
+    widths come from the dicts' "bits" (4 and 2 when absent).
 
-    Pinned by: test_pack_roundtrip, test_pack_is_bijective, test_record_bytes.
+    Pinned by: test_pack_roundtrip, test_pack_is_bijective, test_record_bytes,
+    test_code_words_are_mma_fragments.
     """
+    kb, vb = k.get("bits", K_BITS), v.get("bits", V_BITS)
     qk = np.asarray(k["codes"], dtype=np.uint32)
     qv = np.asarray(v["codes"], dtype=np.uint32)
+    if qk.max(initial=0) >= (1 << kb) or qv.max(initial=0) >= (1 << vb):
+        raise ValueError("code outside its bit width")
     d = qk.shape[-1]
-    kw = np.zeros(TILE_TOKENS * d // 8, dtype=np.uint32)
-    word, shift = _k_positions(d)
+    kw = np.zeros(TILE_TOKENS * d * kb // 32, dtype=np.uint32)
+    word, shift = _k_positions(d, kb)
     np.bitwise_or.at(kw, word.ravel(), (qk << shift.astype(np.uint32)).ravel())
-    vw = np.zeros(TILE_TOKENS * d // 16, dtype=np.uint32)
-    word, shift = _v_positions(d)
+    vw = np.zeros(TILE_TOKENS * d * vb // 32, dtype=np.uint32)
+    word, shift = _v_positions(d, vb)
     np.bitwise_or.at(vw, word.ravel(), (qv << shift.astype(np.uint32)).ravel())
+
     def f16(a):
         return np.asarray(a, dtype=np.float16).astype("<f2").tobytes()
 
     parts = [kw.astype("<u4").tobytes(), f16(k["scale"]), f16(k["zero"]), f16(k["factor"]),
              vw.astype("<u4").tobytes(), f16(v["scale"]), f16(v["zero"]), f16(v["factor"])]
     out = b"".join(parts)
-    assert len(out) == record_bytes(d)
+    assert len(out) == record_bytes(d, k_bits=kb, v_bits=vb)
     return out
 
 
-def unpack_record(rec, d: int):
+def unpack_record(rec, d: int, k_bits: int = K_BITS, v_bits: int = V_BITS):
     """Inverse of pack_record: returns (k dict, v dict) with codes and fp16 metadata."""
     buf = np.frombuffer(bytes(rec), dtype=np.uint8)
-    if buf.size != record_bytes(d):
-        raise ValueError("record size does not match head_dim")
-    o_kc, o_vc, o_ks, o_kz, o_kr, o_vs, o_vz, o_vcf = _section_offsets(d)
+    if buf.size != record_bytes(d, k_bits=k_bits, v_bits=v_bits):
+        raise ValueError("record size does not match head_dim and code bits")
+    o_kc, o_vc, o_ks, o_kz, o_kr, o_vs, o_vz, o_vcf = _section_offsets(d, k_bits, v_bits)
     t = TILE_TOKENS
     kw = buf[o_kc:o_ks].view("<u4").astype(np.uint32)
     vw = buf[o_vc:o_vs].view("<u4").astype(np.uint32)
-    word, shift = _k_positions(d)
-    qk = ((kw[word] >> shift.astype(np.uint32)) & 0xF).astype(np.uint8)
-    word, shift = _v_positions(d)
-    qv = ((vw[word] >> shift.astype(np.uint32)) & 0x3).astype(np.uint8)
+    word, shift = _k_positions(d, k_bits)
+    qk = ((kw[word] >> shift.astype(np.uint32)) & ((1 << k_bits) - 1)).astype(np.uint8)
+    word, shift = _v_positions(d, v_bits)
+    qv = ((vw[word] >> shift.astype(np.uint32)) & ((1 << v_bits) - 1)).astype(np.uint8)
 
     def f16(lo, n):
         return buf[lo:lo + 2 * n].view("<f2").astype(np.float16)
 
-    k = {"codes": qk, "scale": f16(o_ks, d), "zero": f16(o_kz, d), "factor": f16(o_kr, t)}
-    v = {"codes": qv, "scale": f16(o_vs, t), "zero": f16(o_vz, t), "factor": f16(o_vcf, d)}
+    k = {"codes": qk, "scale": f16(o_ks, d), "zero": f16(o_kz, d), "factor": f16(o_kr, t), "bits": k_bits}
+    v = {"codes": qv, "scale": f16(o_vs, t), "zero": f16(o_vz, t), "factor": f16(o_vcf, d), "bits": v_bits}
     return k, v
 
 
-def quantize_page(k_tile, v_tile, iters: int = SINKHORN_ITERS, eps: float = SINKHORN_EPS):
+def quantize_page(k_tile, v_tile, iters: int = SINKHORN_ITERS, eps: float = SINKHORN_EPS,
+                  k_bits: int = K_BITS, v_bits: int = V_BITS):
     """Quantise one (page, kv head): fp16 K/V tiles [128, d0] -> (record bytes, k, v)."""
     d = padded_head_dim(np.asarray(k_tile).shape[-1])
-    k = quantize_tile(k_tile, "K", d, iters, eps)
-    v = quantize_tile(v_tile, "V", d, iters, eps)
+    k = quantize_tile(k_tile, "K", d, iters, eps, bits=k_bits)
+    v = quantize_tile(v_tile, "V", d, iters, eps, bits=v_bits)
     return pack_record(k, v), k, v
 
 
-def dequantize_record(rec, d0: int):
+def dequantize_record(rec, d0: int, k_bits: int = K_BITS, v_bits: int = V_BITS):
     """Page record -> (K_hat [128, d0], V_hat [128, d0]) float64 in the original basis."""
     d = padded_head_dim(d0)
-    k, v = unpack_record(rec, d)
+    k, v = unpack_record(rec, d, k_bits, v_bits)
     kh = dequantize_tile(k["codes"], k["scale"], k["zero"], k["factor"], "K", d0)
     vh = dequantize_tile(v["codes"], v["scale"], v["zero"], v["factor"], "V", d0)
     return kh, vh
@@ -391,7 +417,8 @@ def softmax_attention(q: np.ndarray, keys: np.ndarray, values: np.ndarray,
 
 
 def decode_sequence(q_heads: np.ndarray, records, partial_k, partial_v,
-                    softmax_scale: float, d0: int) -> np.ndarray:
+                    softmax_scale: float, d0: int, k_bits: int = K_BITS,
+                    v_bits: int = V_BITS) -> np.ndarray:
     """Attention output of one sequence for all its query heads of ONE kv head.
 
     q_heads: [G, d0] queries sharing this kv head (grouped-query attention).
@@ -402,7 +429,7 @@ def decode_sequence(q_heads: np.ndarray, records, partial_k, partial_v,
     """
     ks, vs = [], []
     for rec in records:
-        kh, vh = dequantize_record(rec, d0)
+        kh, vh = dequantize_record(rec, d0, k_bits, v_bits)
         ks.append(kh)
         vs.append(vh)
     if partial_k is not None and len(partial_k):
@@ -427,7 +454,8 @@ def fp16_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int) -> int:
     return 2 * layers * kv_heads * head_dim * 2
 
 
-def packed_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int) -> float:
-    """Packed K4V2 bytes per token including the fp16 metadata of its page."""
+def packed_kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int,
+                              k_bits: int = K_BITS, v_bits: int = V_BITS) -> float:
+    """Packed bytes per token (K4V2 by default) including the fp16 metadata of its page."""
     d = padded_head_dim(head_dim)
-    return layers * kv_heads * record_bytes(d) / TILE_TOKENS
+    return layers * kv_heads * record_bytes(d, k_bits=k_bits, v_bits=v_bits) / TILE_TOKENS

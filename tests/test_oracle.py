@@ -404,6 +404,141 @@ def test_pack_roundtrip(d):
             np.testing.assert_array_equal(a[key], b[key])
 
 
+# --- other k/v bit presets (vatt §四個步驟, bit-width assignment: same pipeline) ----------
+
+_WIDTHS = [(4, 2), (4, 4), (2, 2), (2, 4)]
+
+
+def test_record_bytes_presets():
+    # T*d*(kb+vb)/8 code bytes + 2*(3d + 3T) fp16 metadata, by hand
+    assert ko.record_bytes(128, k_bits=4, v_bits=4) == 8192 + 8192 + 1536 == 17920
+    assert ko.record_bytes(128, k_bits=2, v_bits=2) == 4096 + 4096 + 1536 == 9728
+    assert ko.record_bytes(256, k_bits=4, v_bits=4) == 16384 + 16384 + 2304
+    assert ko.record_bytes(64, k_bits=2, v_bits=4) == 2048 + 4096 + 1152
+    assert set(ko.PRESETS.values()) <= set(_WIDTHS)
+    assert ko.PRESETS["kvarn_k4v2_g128"] == (ko.K_BITS, ko.V_BITS)
+    for kb, vb in _WIDTHS:
+        assert all(o % 16 == 0 for o in ko._section_offsets(128, kb, vb))
+
+
+@pytest.mark.parametrize("kind", ["K", "V"])
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("d", [64, 256])
+def test_code_positions_bijective(kind, bits, d):
+    word, shift = ko._code_positions(kind, bits, d)
+    keys = word.astype(np.int64) * 64 + shift
+    assert np.unique(keys).size == 128 * d
+    assert word.max() + 1 == 128 * d * bits // 32
+    assert set(np.unique(shift)) == set(range(0, 32, bits))
+
+
+@pytest.mark.parametrize("kb,vb", _WIDTHS)
+def test_code_words_are_mma_fragments_all_widths(kb, vb):
+    # the words of every width carry m16n8k16 A fragments (PTX fragment table): K's of
+    # codes[token, channel], V's of codes^T[channel, token]; 4-bit words one fragment with
+    # register r's (lo, hi) pair at nibbles (n, n+4), 2-bit words the fragments of two
+    # consecutive token blocks (K: rows, V: columns) with pairs at slots (n, n+8)
+    d = 64
+    rng = np.random.default_rng(kb * 10 + vb)
+    qk = rng.integers(0, 1 << kb, (128, d)).astype(np.uint8)
+    qv = rng.integers(0, 1 << vb, (128, d)).astype(np.uint8)
+    zd, zt = np.zeros(d, np.float16), np.zeros(128, np.float16)
+    rec = ko.pack_record({"codes": qk, "scale": zd, "zero": zd, "factor": zt, "bits": kb},
+                         {"codes": qv, "scale": zt, "zero": zt, "factor": zd, "bits": vb})
+    buf = np.frombuffer(rec, np.uint8)
+    o_kc, o_vc, o_ks, _, _, o_vs, _, _ = ko._section_offsets(d, kb, vb)
+    for kind, words, bits, codes in (("K", buf[o_kc:o_ks].view("<u4"), kb, qk),
+                                     ("V", buf[o_vc:o_vs].view("<u4"), vb, qv)):
+        mask = (1 << bits) - 1
+        for lane in range(32):
+            g, tq = lane // 4, lane % 4
+            for o in range(8):
+                for i in range(d // 16):
+                    blk = codes[16 * o:16 * o + 16, 16 * i:16 * i + 16]
+                    mat = blk if kind == "K" else blk.T
+                    want = _mma_a_fragment(mat, g, tq)
+                    if bits == 4:
+                        w = int(words[((o * (d // 64) + i // 4) * 32 + lane) * 4 + i % 4])
+                        got = [((w >> 4 * n) & mask, (w >> 4 * (n + 4)) & mask) for n in (0, 2, 1, 3)]
+                    else:
+                        w = int(words[(((o // 2) * (d // 64) + i // 4) * 32 + lane) * 4 + i % 4])
+                        f = o % 2
+                        got = [((w >> 2 * n) & mask, (w >> 2 * (n + 8)) & mask)
+                               for n in (2 * f, 2 * f + 4, 2 * f + 1, 2 * f + 5)]
+                    assert got == [tuple(int(x) for x in pr) for pr in want], (kind, bits, lane, o, i)
+
+
+@pytest.mark.parametrize("kb,vb", _WIDTHS)
+def test_pack_roundtrip_all_widths(kb, vb):
+    rng = np.random.default_rng(kb + 7 * vb)
+    d = 128
+    k = {"codes": rng.integers(0, 1 << kb, (128, d)).astype(np.uint8),
+         "scale": rng.standard_normal(d).astype(np.float16),
+         "zero": rng.standard_normal(d).astype(np.float16),
+         "factor": rng.standard_normal(128).astype(np.float16), "bits": kb}
+    v = {"codes": rng.integers(0, 1 << vb, (128, d)).astype(np.uint8),
+         "scale": rng.standard_normal(128).astype(np.float16),
+         "zero": rng.standard_normal(128).astype(np.float16),
+         "factor": rng.standard_normal(d).astype(np.float16), "bits": vb}
+    rec = ko.pack_record(k, v)
+    assert len(rec) == ko.record_bytes(d, k_bits=kb, v_bits=vb)
+    k2, v2 = ko.unpack_record(rec, d, kb, vb)
+    for a, b in ((k, k2), (v, v2)):
+        for key in a:
+            np.testing.assert_array_equal(a[key], b[key])
+    with pytest.raises(ValueError):   # a code wider than its section
+        ko.pack_record(dict(k, codes=np.full((128, d), 1 << kb, np.uint8)), v)
+
+
+def test_quantize_widths_closed_form_and_error_order():
+    # the closed-form tile quantises to the extreme levels 0 and 2^b - 1 at every width
+    r, c, x = _rank_one_scaled(128, 128, 11)
+    tile = ko.rotate(x, 128)
+    y = _checker(128, 128)
+    for bits in (2, 4):
+        for kind in ("K", "V"):
+            qd = ko.quantize_tile(tile, kind, bits=bits)
+            assert qd["bits"] == bits
+            np.testing.assert_array_equal(qd["codes"], ((2 ** bits - 1) * (y + 1) / 2).astype(np.uint8))
+    # on outlier data more bits give a smaller reconstruction error, within half a step
+    k, v = synth.outlier_kv(128, 1, 128, seed=14)
+    for kind, t in (("K", k), ("V", v)):
+        tile = t[:, 0].double().numpy()
+        errs = []
+        for bits in (2, 4):
+            qd = ko.quantize_tile(tile, kind, bits=bits)
+            assert qd["codes"].max() <= 2 ** bits - 1
+            back = ko.dequantize_tile(qd["codes"], qd["scale"], qd["zero"], qd["factor"], kind, 128)
+            errs.append(np.linalg.norm(back - tile) / np.linalg.norm(tile))
+            xr = ko.rotate(tile, 128)
+            br = ko.rotate(back, 128)
+            s = qd["scale"].astype(np.float64)
+            f = qd["factor"].astype(np.float64)
+            step = f[:, None] * s[None, :] if kind == "K" else s[:, None] * f[None, :]
+            assert np.all(np.abs(br - xr) <= 0.5 * step * 1.01 + 1e-3 * np.abs(xr) + 1e-6)
+        assert errs[1] < errs[0]
+
+
+def test_decode_sequence_presets_roundtrip():
+    # decode over records of each preset equals attention over that preset's dequantised
+    # tiles (pack/unpack/dequantise consistent at every width)
+    k, v = synth.outlier_kv(256, 1, 128, seed=15)
+    q = np.random.default_rng(15).standard_normal((2, 128))
+    for name, (kb, vb) in ko.PRESETS.items():
+        recs, ks, vs = [], [], []
+        for p in range(2):
+            kt = k[128 * p:128 * p + 128, 0].double().numpy()
+            vt = v[128 * p:128 * p + 128, 0].double().numpy()
+            rec, kq, vq = ko.quantize_page(kt, vt, k_bits=kb, v_bits=vb)
+            recs.append(rec)
+            ks.append(ko.dequantize_tile(kq["codes"], kq["scale"], kq["zero"], kq["factor"], "K", 128))
+            vs.append(ko.dequantize_tile(vq["codes"], vq["scale"], vq["zero"], vq["factor"], "V", 128))
+        got = ko.decode_sequence(q, recs, None, None, 0.1, 128, kb, vb)
+        keys, vals = np.concatenate(ks), np.concatenate(vs)
+        want = np.stack([ko.softmax_attention(qh, keys, vals, 0.1) for qh in q])
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12, err_msg=name)
+
+
 # --- attention ----------------------------------------------------------------
 
 def test_attention_single_token():
