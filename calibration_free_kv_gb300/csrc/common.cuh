@@ -17,16 +17,19 @@ struct RecordLayout {
   int kcodes, kscale, kzero, kfactor, vcodes, vscale, vzero, vfactor, bytes;
 };
 
-__host__ __device__ constexpr RecordLayout record_layout(int d) {
+// Page record of one (page, kv head) with kb-bit K codes and vb-bit V codes: the K half
+// (codes, scale[d], zero[d], token factor[128]) then the V half (codes, scale[128],
+// zero[128], channel factor[d]); metadata fp16, every section 16-byte aligned.
+__host__ __device__ constexpr RecordLayout record_layout(int d, int kb = 4, int vb = 2) {
   return RecordLayout{0,
-                      kTile * d / 2,
-                      kTile * d / 2 + 2 * d,
-                      kTile * d / 2 + 4 * d,
-                      kTile * d / 2 + 4 * d + 2 * kTile,
-                      kTile * d / 2 + 4 * d + 2 * kTile + kTile * d / 4,
-                      kTile * d / 2 + 4 * d + 4 * kTile + kTile * d / 4,
-                      kTile * d / 2 + 4 * d + 6 * kTile + kTile * d / 4,
-                      kTile * d / 2 + 6 * d + 6 * kTile + kTile * d / 4};
+                      kTile * d * kb / 8,
+                      kTile * d * kb / 8 + 2 * d,
+                      kTile * d * kb / 8 + 4 * d,
+                      kTile * d * kb / 8 + 4 * d + 2 * kTile,
+                      kTile * d * kb / 8 + 4 * d + 2 * kTile + kTile * d * vb / 8,
+                      kTile * d * kb / 8 + 4 * d + 4 * kTile + kTile * d * vb / 8,
+                      kTile * d * kb / 8 + 4 * d + 6 * kTile + kTile * d * vb / 8,
+                      kTile * d * kb / 8 + 6 * d + 6 * kTile + kTile * d * vb / 8};
 }
 
 __device__ __forceinline__ void flag_error(int32_t* status, int bits) {

@@ -29,20 +29,27 @@
 
 namespace kvarn {
 
-constexpr int kDecWarps = 8;
 constexpr float kTwo24 = 16777216.0f;
+constexpr int kMaxSmem = 232448;  // dynamic shared memory a CTA may opt in to
 
-template <int D, int NT>
+template <int D, int NT, int KB, int VB>
 struct DecodeShape {
+  static constexpr RecordLayout kRL = record_layout(D, KB, VB);
   static constexpr int kNH = 4 * NT;                 // head slots per kv head (G padded)
-  static constexpr int kRec = record_layout(D).bytes;
-  static constexpr int kKHalf = record_layout(D).vcodes;   // K codes + K metadata
-  static constexpr int kVHalf = kRec - kKHalf;             // V codes + V metadata
+  static constexpr int kRec = kRL.bytes;
+  static constexpr int kKHalf = kRL.vcodes;          // K codes + K metadata
+  static constexpr int kVHalf = kRec - kKHalf;       // V codes + V metadata
   static constexpr int kQld = D + 8;                 // fp32 row stride of q in shared memory
-  static constexpr int kRecBytes = kDecWarps * kRec; // one K slot + one V slot per warp
   static constexpr int kQBytes = kNH * kQld * 4;     // q~ (fp32) for q~ . z'
   static constexpr int kQhBytes = 2 * kNH * (D / 2 + 4) * 4;  // q~ as fp16 hi and lo, padded rows
-  static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + kDecWarps * 2 * 8;
+  // warps per CTA: 8, or 4 where 8 page slots would not fit in shared memory
+  static constexpr int kWarps = 8 * kRec + kQBytes + kQhBytes + 8 * 16 <= kMaxSmem ? 8 : 4;
+  static constexpr int kRecBytes = kWarps * kRec;    // one K slot + one V slot per warp
+  static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + kWarps * 2 * 8;
+  static_assert(kSmemBytes <= kMaxSmem, "page slots fit in shared memory");
+  static_assert(kRecBytes >= kWarps * kNH * (D + 2) * 4, "the merge scratch fits the page slots");
+  // two CTAs per SM where both their shared memory and 128 registers a thread suffice
+  static constexpr int kMinBlocks = (NT == 1 && 2 * (kSmemBytes + 1024) <= 233472) ? 2 : 1;
 };
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -140,12 +147,12 @@ __device__ __forceinline__ uint32_t b_split(__half2 qh, __half2 ql, __half2 s, b
 
 // QK of one whole page from its K half Rk: logits -> probabilities lg (tokens 16mi + g + 8r
 // of head 4nt + tq), online-softmax state updated, alpha = rescale of the previous state.
-template <int D, int NT>
+template <int D, int NT, int KB, int VB>
 __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const float* __restrict__ qsm,
                                         const uint2* __restrict__ qhl, int lane, WarpAcc<D, NT>& st,
                                         float (&lg)[8][NT][2], float (&alpha)[NT]) {
-  constexpr RecordLayout RL = record_layout(D);
-  constexpr int QLD = DecodeShape<D, NT>::kQld;
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
+  constexpr int QLD = DecodeShape<D, NT, KB, VB>::kQld;
   constexpr int QH = D / 2 + 4;  // row stride of qhl (one entry per channel pair)
   const int g = lane >> 2, tq = lane & 3;
   const __half2* Ks2 = reinterpret_cast<const __half2*>(Rk + RL.kscale);
@@ -181,31 +188,64 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     qzm[nt] = __shfl_sync(0xffffffffu, v, 8 * tq);  // head 4nt + tq lives in lanes g = 2tq
   }
-#pragma unroll
-  for (int mi = 0; mi < 8; ++mi) {
-    float acc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
-#pragma unroll
-    for (int kq = 0; kq < D / 64; ++kq) {
-      const uint4 w4 =
-          *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi * (D / 64) + kq) * 32 + lane) * 16);
-      const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint32_t a[4];
-        unpack_k(ws[e], a);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a, bq[4 * kq + e][nt][0], bq[4 * kq + e][nt][1]);
-      }
-    }
+  auto logits = [&](int mi, const float (&acc)[NT][4], float cf) {
     const float2 r = make_float2(__half2float(Kr[16 * mi + g]), __half2float(Kr[16 * mi + g + 8]));
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float2 t = add2(make_float2(acc[nt][0], acc[nt][2]), make_float2(acc[nt][1], acc[nt][3]));
-      const float2 u = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(qzm[nt], qzm[nt])), r);
+      const float2 u = mul2(fma2(t, make_float2(cf, cf), make_float2(qzm[nt], qzm[nt])), r);
       lg[mi][nt][0] = u.x;
       lg[mi][nt][1] = u.y;
+    }
+  };
+  if constexpr (KB == 4) {  // one word per fragment (token block mi, channel block kk)
+#pragma unroll
+    for (int mi = 0; mi < 8; ++mi) {
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+#pragma unroll
+      for (int kq = 0; kq < D / 64; ++kq) {
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi * (D / 64) + kq) * 32 + lane) * 16);
+        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a[4];
+          unpack_k(ws[e], a);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a, bq[4 * kq + e][nt][0], bq[4 * kq + e][nt][1]);
+        }
+      }
+      logits(mi, acc, kTwo24);
+    }
+  } else {  // 2-bit: one word per channel block kk holds token blocks 2mi2 and 2mi2 + 1
+    static_assert(KB == 2, "2- or 4-bit K codes");
+#pragma unroll
+    for (int mi2 = 0; mi2 < 4; ++mi2) {
+      float acc0[NT][4], acc1[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc0[nt][e] = acc1[nt][e] = 0.0f;
+#pragma unroll
+      for (int kq = 0; kq < D / 64; ++kq) {
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi2 * (D / 64) + kq) * 32 + lane) * 16);
+        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a0[4], a1[4];
+          unpack_v(ws[e], a0, a1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(acc0[nt], a0, bq[4 * kq + e][nt][0], bq[4 * kq + e][nt][1]);
+            mma16816(acc1[nt], a1, bq[4 * kq + e][nt][0], bq[4 * kq + e][nt][1]);
+          }
+        }
+      }
+      logits(2 * mi2, acc0, kTwo24);
+      logits(2 * mi2 + 1, acc1, kTwo24 * 0.0625f);  // the odd block's codes sit 4 bits higher
     }
   }
 #pragma unroll
@@ -233,10 +273,10 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
 }
 
 // PV of one whole page from its V half Rv with the probabilities of qk_page.
-template <int D, int NT>
+template <int D, int NT, int KB, int VB>
 __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const float (&lg)[8][NT][2],
                                         const float (&alpha)[NT], int lane, WarpAcc<D, NT>& st) {
-  constexpr RecordLayout RL = record_layout(D);
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
   const int g = lane >> 2;
   const __half* Vs = reinterpret_cast<const __half*>(Rv + (RL.vscale - RL.vcodes));
   const __half* Vz = reinterpret_cast<const __half*>(Rv + (RL.vzero - RL.vcodes));
@@ -255,9 +295,10 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
       const int ks = 2 * ks2 + f;
-      // token scales with the subnormal scale 2^(4f + 2h) of this block's codes compensated
-      // (h = 0: rows g); the powers of two keep the products exact
-      const float c0 = f ? 1.0f / 16.0f : 1.0f, c1 = f ? 1.0f / 64.0f : 0.25f;
+      // token scales with the subnormal scale of this block's codes compensated (h = 0: rows
+      // g): 2-bit 2^(4f + 2h), 4-bit 2^(4h); the powers of two keep the products exact
+      const float c0 = VB == 2 ? (f ? 1.0f / 16.0f : 1.0f) : 1.0f;
+      const float c1 = VB == 2 ? (f ? 1.0f / 64.0f : 0.25f) : 1.0f / 16.0f;
       const float2 svc = make_float2(__half2float(Vs[16 * ks + g]) * c0, __half2float(Vs[16 * ks + g + 8]) * c1);
       const float2 zv = make_float2(__half2float(Vz[16 * ks + g]), __half2float(Vz[16 * ks + g + 8]));
 #pragma unroll
@@ -274,13 +315,27 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
     }
 #pragma unroll
     for (int mq = 0; mq < D / 64; ++mq) {
-      const uint4 w4 = *reinterpret_cast<const uint4*>(Rv + ((ks2 * (D / 64) + mq) * 32 + lane) * 16);
-      const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+      uint32_t ws0[4], ws1[4];  // 2-bit: token blocks 2ks2 and 2ks2 + 1 share words; 4-bit: one each
+      if constexpr (VB == 2) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(Rv + ((ks2 * (D / 64) + mq) * 32 + lane) * 16);
+        ws0[0] = w4.x; ws0[1] = w4.y; ws0[2] = w4.z; ws0[3] = w4.w;
+      } else {
+        static_assert(VB == 4, "2- or 4-bit V codes");
+        const uint4 w0 = *reinterpret_cast<const uint4*>(Rv + (((2 * ks2) * (D / 64) + mq) * 32 + lane) * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(Rv + (((2 * ks2 + 1) * (D / 64) + mq) * 32 + lane) * 16);
+        ws0[0] = w0.x; ws0[1] = w0.y; ws0[2] = w0.z; ws0[3] = w0.w;
+        ws1[0] = w1.x; ws1[1] = w1.y; ws1[2] = w1.z; ws1[3] = w1.w;
+      }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int mc = 4 * mq + e;
         uint32_t a0[4], a1[4];
-        unpack_v(ws[e], a0, a1);
+        if constexpr (VB == 2) {
+          unpack_v(ws0[e], a0, a1);
+        } else {
+          unpack_k(ws0[e], a0);
+          unpack_k(ws1[e], a1);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma16816(pacc[mc][nt], a0, bw[0][nt][0], bw[0][nt][1]);
@@ -311,9 +366,11 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
   }
 }
 
-template <int D, int NT>
-__global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1) decode_kernel(DecodeParams p) {
-  using S = DecodeShape<D, NT>;
+template <int D, int NT, int KB, int VB>
+__global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, DecodeShape<D, NT, KB, VB>::kMinBlocks)
+    decode_kernel(DecodeParams p) {
+  using S = DecodeShape<D, NT, KB, VB>;
+  constexpr int kDecWarps = S::kWarps;
   constexpr int NH = S::kNH;
   constexpr int REC = S::kRec;
   constexpr int KH = S::kKHalf;
@@ -399,7 +456,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
         const int j = lane * (D / 32) + e;
         const float x = v[e] * sc;
         qsm[hl * QLD + (j & ~15) + 4 * ((j & 7) >> 1) + 2 * ((j >> 3) & 1) + (j & 1)] = x;
-        const float xb = (j & 15) >= 8 ? x * 0.0625f : x;
+        const float xb = (j & 15) >= 8 ? x * (KB == 4 ? 0.0625f : 0.25f) : x;
         const __half hi = __float2half_rn(xb);
         qe[4 * (j >> 1) + (j & 1)] = hi;
         qe[4 * (j >> 1) + 2 + (j & 1)] = __float2half_rn(xb - __half2float(hi));
@@ -429,7 +486,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
         break;
       }
       float lg[8][NT][2], alpha[NT];
-      qk_page<D, NT>(kslot, qsm, qhl, lane, st, lg, alpha);
+      qk_page<D, NT, KB, VB>(kslot, qsm, qhl, lane, st, lg, alpha);
       __syncwarp();
       const bool more = j + 1 < cnt;
       if (lane == 0 && more) {  // the K slot is free: fetch the next page's K half
@@ -445,7 +502,7 @@ __global__ void __launch_bounds__(kDecWarps * 32, (NT == 1 && D <= 128) ? 2 : 1)
         }
         break;
       }
-      pv_page<D, NT>(vslot, lg, alpha, lane, st);
+      pv_page<D, NT, KB, VB>(vslot, lg, alpha, lane, st);
       __syncwarp();
       if (lane == 0 && more) {  // the V slot is free: fetch the next page's V half
         fence_proxy_async_smem();
@@ -649,12 +706,12 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   }
 }
 
-template <int D, int NT>
+template <int D, int NT, int KB, int VB>
 static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
-  using S = DecodeShape<D, NT>;
+  using S = DecodeShape<D, NT, KB, VB>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_kernel<D, NT, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kSmemBytes) != cudaSuccess)
       return KVARN_ERR_CUDA;
     attr_set = true;
@@ -666,12 +723,12 @@ static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.max_splits, p.num_kv_heads, p.batch);
-  cfg.blockDim = dim3(kDecWarps * 32);
+  cfg.blockDim = dim3(S::kWarps * 32);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT>, p) != cudaSuccess) return KVARN_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess) return KVARN_ERR_CUDA;
   const int warps = p.batch * p.num_q_heads;
   cfg.gridDim = dim3((warps + 3) / 4);
   cfg.blockDim = dim3(128);
@@ -680,15 +737,23 @@ static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   return KVARN_OK;
 }
 
-int launch_decode_any(int d, int nt, const DecodeParams& p, cudaStream_t stream) {
+template <int KB, int VB>
+static int launch_decode_bits(int d, int nt, const DecodeParams& p, cudaStream_t stream) {
   if (nt == 1) {
-    if (d == 64) return launch_decode_t<64, 1>(p, stream);
-    if (d == 128) return launch_decode_t<128, 1>(p, stream);
-    if (d == 256) return launch_decode_t<256, 1>(p, stream);
+    if (d == 64) return launch_decode_t<64, 1, KB, VB>(p, stream);
+    if (d == 128) return launch_decode_t<128, 1, KB, VB>(p, stream);
+    if (d == 256) return launch_decode_t<256, 1, KB, VB>(p, stream);
   } else if (nt == 2) {
-    if (d == 64) return launch_decode_t<64, 2>(p, stream);
-    if (d == 128) return launch_decode_t<128, 2>(p, stream);
+    if (d == 64) return launch_decode_t<64, 2, KB, VB>(p, stream);
+    if (d == 128) return launch_decode_t<128, 2, KB, VB>(p, stream);
   }
+  return KVARN_ERR_UNSUPPORTED;
+}
+
+int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream) {
+  if (kb == 4 && vb == 2) return launch_decode_bits<4, 2>(d, nt, p, stream);
+  if (kb == 4 && vb == 4) return launch_decode_bits<4, 4>(d, nt, p, stream);
+  if (kb == 2 && vb == 2) return launch_decode_bits<2, 2>(d, nt, p, stream);
   return KVARN_ERR_UNSUPPORTED;
 }
 

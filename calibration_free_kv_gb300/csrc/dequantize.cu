@@ -18,9 +18,12 @@ struct DequantShape {
 };
 
 // grid.x = pages * Hkv * 2, block = 128 threads (one token row each while decoding codes).
-template <int D>
+// Code word positions as in kvarn.h: a 4-bit word holds one fragment, a 2-bit word the
+// fragments of two consecutive token blocks.
+template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
-  constexpr RecordLayout RL = record_layout(D);
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
+  constexpr int NI4 = D / 64;
   constexpr int LD = DequantShape<D>::kLd;
   extern __shared__ __align__(16) float smem_x[];
   const int unit = blockIdx.x >> 1;
@@ -45,11 +48,13 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
     for (int kk = 0; kk < D / 16; ++kk) {
       for (int tq = 0; tq < 4; ++tq) {
         const int lane = 4 * g_t + tq;
-        const uint32_t w = kw[((mi * (D / 64) + kk / 4) * 32 + lane) * 4 + (kk & 3)];
+        const int wo = KB == 4 ? mi : mi >> 1;
+        const uint32_t w = kw[((wo * NI4 + kk / 4) * 32 + lane) * 4 + (kk & 3)];
         for (int hh = 0; hh < 2; ++hh)
           for (int pp = 0; pp < 2; ++pp) {
             const int j = 16 * kk + 8 * hh + 2 * tq + pp;
-            const uint32_t code = (w >> (4 * (hh + 2 * rho + 4 * pp))) & 15u;
+            const int sh = KB == 4 ? 4 * (hh + 2 * rho + 4 * pp) : 2 * (2 * (mi & 1) + hh + 4 * rho + 8 * pp);
+            const uint32_t code = (w >> sh) & ((1u << KB) - 1u);
             smem_x[t * LD + j] =
                 r * fmaf((float)code, __half2float(ks[j]), __half2float(kz[j]));
           }
@@ -65,10 +70,12 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
     for (int mc = 0; mc < D / 16; ++mc)
       for (int g = 0; g < 8; ++g) {
         const int lane = 4 * g + tq;
-        const uint32_t w = vw[((ks2 * (D / 64) + mc / 4) * 32 + lane) * 4 + (mc & 3)];
+        const int wo = VB == 4 ? ks : ks2;
+        const uint32_t w = vw[((wo * NI4 + mc / 4) * 32 + lane) * 4 + (mc & 3)];
         for (int rho = 0; rho < 2; ++rho) {
           const int j = 16 * mc + g + 8 * rho;
-          const uint32_t code = (w >> (2 * (2 * f + hh + 4 * rho + 8 * pp))) & 3u;
+          const int sh = VB == 4 ? 4 * (hh + 2 * rho + 4 * pp) : 2 * (2 * f + hh + 4 * rho + 8 * pp);
+          const uint32_t code = (w >> sh) & ((1u << VB) - 1u);
           smem_x[t * LD + j] = __half2float(vc[j]) * fmaf((float)code, s, z);
         }
       }
@@ -93,28 +100,36 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
   }
 }
 
-template <int D>
+template <int D, int KB, int VB>
 static int launch_dequant_t(const DequantParams& p, int num_pages, cudaStream_t stream) {
   constexpr int kSmem = DequantShape<D>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(dequantize_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(dequantize_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmem) != cudaSuccess)
       return KVARN_ERR_CUDA;
     attr_set = true;
   }
-  dequantize_kernel<D><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
+  dequantize_kernel<D, KB, VB><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
-int launch_dequant_any(int d, const DequantParams& p, int num_pages, cudaStream_t stream) {
-  if (num_pages <= 0) return KVARN_OK;
+template <int KB, int VB>
+static int launch_dequant_bits(int d, const DequantParams& p, int num_pages, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_dequant_t<64>(p, num_pages, stream);
-    case 128: return launch_dequant_t<128>(p, num_pages, stream);
-    case 256: return launch_dequant_t<256>(p, num_pages, stream);
+    case 64: return launch_dequant_t<64, KB, VB>(p, num_pages, stream);
+    case 128: return launch_dequant_t<128, KB, VB>(p, num_pages, stream);
+    case 256: return launch_dequant_t<256, KB, VB>(p, num_pages, stream);
     default: return KVARN_ERR_UNSUPPORTED;
   }
+}
+
+int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pages, cudaStream_t stream) {
+  if (num_pages <= 0) return KVARN_OK;
+  if (kb == 4 && vb == 2) return launch_dequant_bits<4, 2>(d, p, num_pages, stream);
+  if (kb == 4 && vb == 4) return launch_dequant_bits<4, 4>(d, p, num_pages, stream);
+  if (kb == 2 && vb == 2) return launch_dequant_bits<2, 2>(d, p, num_pages, stream);
+  return KVARN_ERR_UNSUPPORTED;
 }
 
 }  // namespace kvarn

@@ -12,16 +12,32 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The presets: name -> K and V code bits, 128-token tiles.  kvarn_k4v2_g128 is the one the
+// pages ship; other k/v bit presets run the same pipeline [vatt §四個步驟, bit-width
+// assignment].
+struct Preset {
+  const char* name;
+  int k_bits, v_bits;
+};
+constexpr Preset kPresets[] = {
+    {"kvarn_k4v2_g128", 4, 2}, {"kvarn_k4v4_g128", 4, 4}, {"kvarn_k2v2_g128", 2, 2}};
+
+bool supported_bits(int kb, int vb) {
+  for (const Preset& pr : kPresets)
+    if (pr.k_bits == kb && pr.v_bits == vb) return true;
+  return false;
+}
+
 int check_desc(const kvarn_desc* d) {
   if (d == nullptr) return KVARN_ERR_INVALID_ARG;
-  if (d->tile_tokens != kTile || d->k_bits != 4 || d->v_bits != 2) return KVARN_ERR_UNSUPPORTED;
+  if (d->tile_tokens != kTile || !supported_bits(d->k_bits, d->v_bits)) return KVARN_ERR_UNSUPPORTED;
   if (d->head_dim < 8 || d->head_dim > 256 || d->head_dim % 8 != 0) return KVARN_ERR_UNSUPPORTED;
   const int dp = d->head_dim_padded;
   if (!(dp == 64 || dp == 128 || dp == 256) || d->head_dim > dp) return KVARN_ERR_UNSUPPORTED;
   if (d->num_kv_heads < 1) return KVARN_ERR_INVALID_ARG;
   if (d->sinkhorn_iters < 0 || d->sinkhorn_iters > 8) return KVARN_ERR_UNSUPPORTED;
   if (!(d->sinkhorn_eps > 0.0f)) return KVARN_ERR_INVALID_ARG;
-  if (d->page_record_bytes != record_layout(dp).bytes) return KVARN_ERR_INVALID_ARG;
+  if (d->page_record_bytes != record_layout(dp, d->k_bits, d->v_bits).bytes) return KVARN_ERR_INVALID_ARG;
   return KVARN_OK;
 }
 
@@ -37,7 +53,10 @@ extern "C" {
 
 int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, kvarn_desc* out) {
   if (preset == nullptr || out == nullptr) return KVARN_ERR_INVALID_ARG;
-  if (std::strcmp(preset, "kvarn_k4v2_g128") != 0) return KVARN_ERR_UNSUPPORTED;
+  const Preset* pr = nullptr;
+  for (const Preset& c : kPresets)
+    if (std::strcmp(preset, c.name) == 0) pr = &c;
+  if (pr == nullptr) return KVARN_ERR_UNSUPPORTED;
   if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0) return KVARN_ERR_UNSUPPORTED;
   if (num_kv_heads < 1) return KVARN_ERR_INVALID_ARG;
   kvarn_desc d;
@@ -45,11 +64,11 @@ int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, k
   d.head_dim_padded = padded_dim(head_dim);
   d.num_kv_heads = num_kv_heads;
   d.tile_tokens = kTile;
-  d.k_bits = 4;
-  d.v_bits = 2;
+  d.k_bits = pr->k_bits;
+  d.v_bits = pr->v_bits;
   d.sinkhorn_iters = 4;
   d.sinkhorn_eps = 1e-6f;
-  d.page_record_bytes = record_layout(d.head_dim_padded).bytes;
+  d.page_record_bytes = record_layout(d.head_dim_padded, d.k_bits, d.v_bits).bytes;
   *out = d;
   return KVARN_OK;
 }
@@ -89,7 +108,8 @@ int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, i
   p.eps = desc->sinkhorn_eps;
   p.status = dev_status;
   p.append = 0;
-  return launch_quantize_any(desc->head_dim_padded, p, num_tiles * desc->num_kv_heads,
+  return launch_quantize_any(desc->head_dim_padded, desc->k_bits, desc->v_bits, p,
+                             num_tiles * desc->num_kv_heads,
                              static_cast<cudaStream_t>(stream));
 }
 
@@ -129,7 +149,8 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
   p.eps = desc->sinkhorn_eps;
   p.status = dev_status;
   p.append = 1;
-  return launch_quantize_any(desc->head_dim_padded, p, batch * desc->num_kv_heads,
+  return launch_quantize_any(desc->head_dim_padded, desc->k_bits, desc->v_bits, p,
+                             batch * desc->num_kv_heads,
                              static_cast<cudaStream_t>(stream));
 }
 
@@ -191,7 +212,8 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
   p.pages_per_split = pps;
   p.max_splits = (max_pages + pps - 1) / pps + 1;
   p.status = dev_status;
-  return launch_decode_any(desc->head_dim_padded, nt, p, static_cast<cudaStream_t>(stream));
+  return launch_decode_any(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p,
+                           static_cast<cudaStream_t>(stream));
 }
 
 int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_t num_pool_pages,
@@ -213,7 +235,8 @@ int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_
   p.num_kv_heads = desc->num_kv_heads;
   p.d0 = desc->head_dim;
   p.status = dev_status;
-  return launch_dequant_any(desc->head_dim_padded, p, num_pages, static_cast<cudaStream_t>(stream));
+  return launch_dequant_any(desc->head_dim_padded, desc->k_bits, desc->v_bits, p, num_pages,
+                            static_cast<cudaStream_t>(stream));
 }
 
 const char* kvarn_status_string(int status) {

@@ -62,8 +62,8 @@ struct DequantParams {
   int32_t* status;
 };
 
-int launch_quantize_any(int d, const QuantizeParams& p, int units, cudaStream_t stream);
-int launch_decode_any(int d, int nt, const DecodeParams& p, cudaStream_t stream);
-int launch_dequant_any(int d, const DequantParams& p, int num_pages, cudaStream_t stream);
+int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int units, cudaStream_t stream);
+int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream);
+int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pages, cudaStream_t stream);
 
 }  // namespace kvarn

@@ -217,15 +217,16 @@ struct RotScratch {
 // single merging warp would need to hand its result out.  The partial buffers alternate between
 // two copies from one step to the next: a warp can only refill a copy after every warp of its
 // group has passed the barrier of the step in between, i.e. finished reading it.
-template <int D, bool TRANS>
+template <int D, bool TRANS, int KB, int VB>
 __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __restrict__ rec,
                                                  int iters, float eps, float* smem) {
   constexpr int LSIZE = TRANS ? D : kTile;
   constexpr int CSIZE = TRANS ? kTile : D;
   constexpr int NLQ = LSIZE / 32;
   constexpr int NCH = CSIZE / 64;
-  constexpr int QMAX = TRANS ? 3 : 15;
-  constexpr RecordLayout RL = record_layout(D);
+  constexpr int BITS = TRANS ? VB : KB;
+  constexpr int QMAX = (1 << BITS) - 1;
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
@@ -454,63 +455,95 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
   auto gather4 = [](uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x4000), 0x7610);
   };
-  if (!TRANS) {
-    // nibble h + 2 rho + 4 p of word j holds row 2 lh + rho, column 16 j + 8 h + 2 tq + p, so
-    // byte rho + 2 p holds h = 0 in its low and h = 1 in its high nibble
-    uint8_t* kc = rec + RL.kcodes;
+  // Words of BITS-bit codes (layout in kvarn.h).  A lane's codes form the fragments of row
+  // blocks 2lq + lh (from L) and column blocks 4ch + j (from C), element (rho, h, p) at row
+  // 2lh + rho, column 2(2j + h) + p of x.  K: token block = row block; V: token block =
+  // column block.
+  constexpr int NI4 = D / 64;
+  if constexpr (BITS == 4) {
+    // nibble h + 2rho + 4p: byte rho + 2p holds h = 0 in its low and h = 1 in its high nibble
+    uint32_t w[2][4];
 #pragma unroll
-    for (int lh = 0; lh < 2; ++lh) {
-      uint32_t w[4];
+    for (int lh = 0; lh < 2; ++lh)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c0 = 4 * j, c1 = 4 * j + 2, r0 = 2 * lh, r1 = 2 * lh + 1;
         const uint32_t lo = gather4(code[r0][c0], code[r1][c0], code[r0][c0 + 1], code[r1][c0 + 1]);
         const uint32_t hi = gather4(code[r0][c1], code[r1][c1], code[r0][c1 + 1], code[r1][c1 + 1]);
-        w[j] = (lo & 0x0F0F0F0Fu) | ((hi << 4) & 0xF0F0F0F0u);
+        w[lh][j] = (lo & 0x0F0F0F0Fu) | ((hi << 4) & 0xF0F0F0F0u);
       }
-      const int mi = 2 * lq + lh;
-      *reinterpret_cast<uint4*>(kc + ((mi * (D / 64) + ch) * 32 + lane) * 16) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+    if constexpr (!TRANS) {  // word (token block 2lq + lh, channel block 4ch + j)
+      uint8_t* kc = rec + RL.kcodes;
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh)
+        *reinterpret_cast<uint4*>(kc + (((2 * lq + lh) * NI4 + ch) * 32 + lane) * 16) =
+            make_uint4(w[lh][0], w[lh][1], w[lh][2], w[lh][3]);
+    } else {                 // word (token block 4ch + j, channel block 2lq + lh)
+      uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint2*>(vc + ((((4 * ch + j) * NI4 + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
+            make_uint2(w[0][j], w[1][j]);
     }
   } else {
-    // 2-bit slot uu + 4 rho + 8 p of word lh holds row 2 lh + rho, column 2 (4 uh + uu) + p
-    uint8_t* vc = rec + RL.vcodes;
+    static_assert(BITS == 2, "2- or 4-bit codes");
+    if constexpr (!TRANS) {
+      // word (token blocks 2lq and 2lq + 1, channel block 4ch + j): slot 2lh + h + 4rho + 8p,
+      // i.e. byte rho + 2p, bit pair 2lh + h
+      uint32_t w[4];
 #pragma unroll
-    for (int uh = 0; uh < 2; ++uh) {
-      uint32_t w[2];
-#pragma unroll
-      for (int lh = 0; lh < 2; ++lh) {
+      for (int j = 0; j < 4; ++j) {
         uint32_t acc = 0u;
 #pragma unroll
-        for (int uu = 3; uu >= 0; --uu) {
-          const int c = 2 * (4 * uh + uu), r0 = 2 * lh, r1 = 2 * lh + 1;
-          // byte rho + 2 p: row 2 lh + rho, column c + p
+        for (int s2 = 3; s2 >= 0; --s2) {
+          const int lh = s2 >> 1, c = 2 * (2 * j + (s2 & 1)), r0 = 2 * lh, r1 = 2 * lh + 1;
           const uint32_t b = gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
           acc = (acc << 2) | (b & 0x03030303u);
         }
-        w[lh] = acc;
+        w[j] = acc;
       }
-      const int ks2 = 2 * ch + uh;
-      *reinterpret_cast<uint2*>(vc + (((ks2 * (D / 64) + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
-          make_uint2(w[0], w[1]);
+      *reinterpret_cast<uint4*>(rec + RL.kcodes + ((lq * NI4 + ch) * 32 + lane) * 16) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      // word (token blocks 4ch + 2uh and + 1, channel block 2lq + lh): slot uu + 4rho + 8p for
+      // column 2(4uh + uu) + p, i.e. byte rho + 2p, bit pair uu
+      uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+      for (int uh = 0; uh < 2; ++uh) {
+        uint32_t w[2];
+#pragma unroll
+        for (int lh = 0; lh < 2; ++lh) {
+          uint32_t acc = 0u;
+#pragma unroll
+          for (int uu = 3; uu >= 0; --uu) {
+            const int c = 2 * (4 * uh + uu), r0 = 2 * lh, r1 = 2 * lh + 1;
+            const uint32_t b = gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
+            acc = (acc << 2) | (b & 0x03030303u);
+          }
+          w[lh] = acc;
+        }
+        const int ks2 = 2 * ch + uh;
+        *reinterpret_cast<uint2*>(vc + (((ks2 * NI4 + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
+            make_uint2(w[0], w[1]);
+      }
     }
   }
 }
 
-template <int D, bool TRANS>
+template <int D, bool TRANS, int KB, int VB>
 __device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, int64_t tok_stride,
                                               int d0, uint8_t* __restrict__ rec, int iters,
                                               float eps, float* smem) {
   float x[4][16];
   stage_and_rotate<D, TRANS>(src, tok_stride, d0, smem, x);
-  quantize_rotated<D, TRANS>(x, rec, iters, eps, smem);
+  quantize_rotated<D, TRANS, KB, VB>(x, rec, iters, eps, smem);
 }
 
 // ---- kernels --------------------------------------------------------------------------------
 
 
 // grid.x = units * 2 (K and V of one (tile or sequence, kv head)), block = 2*D threads.
-template <int D>
+template <int D, int KB, int VB>
 __global__ void __launch_bounds__(QuantShape<D>::kThreads)
     quantize_kernel(QuantizeParams p) {
   extern __shared__ __align__(16) float smem_q[];
@@ -553,22 +586,22 @@ __global__ void __launch_bounds__(QuantShape<D>::kThreads)
   }
   uint8_t* rec = p.pool + (page * p.num_kv_heads + h) * p.rec_bytes;
   if (is_v)
-    quantize_unit<D, true>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
+    quantize_unit<D, true, KB, VB>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
   else
-    quantize_unit<D, false>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
+    quantize_unit<D, false, KB, VB>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
 }
 
-template <int D>
+template <int D, int KB, int VB>
 static int launch_quantize(const QuantizeParams& p, int units, cudaStream_t stream) {
   constexpr int kSmem = QuantShape<D>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(quantize_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(quantize_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmem) != cudaSuccess)
       return KVARN_ERR_CUDA;
     attr_set = true;
   }
-  quantize_kernel<D><<<units * 2, QuantShape<D>::kThreads, kSmem, stream>>>(p);
+  quantize_kernel<D, KB, VB><<<units * 2, QuantShape<D>::kThreads, kSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
@@ -675,6 +708,7 @@ __device__ __forceinline__ void load_tile(uint32_t zbuf, const __half* src, int6
 
 }  // namespace tc
 
+template <int KB, int VB>
 __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizeParams p, int units) {
   extern __shared__ __align__(1024) uint8_t smem_tc[];
   using namespace tc;
@@ -845,9 +879,9 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
       uint8_t* rec;
       tc::unit_io(p, list[i], src, ts, rec);
       if ((list[i] & 1) != 0)
-        quantize_rotated<128, true>(x, rec, p.iters, p.eps, scratch);
+        quantize_rotated<128, true, KB, VB>(x, rec, p.iters, p.eps, scratch);
       else
-        quantize_rotated<128, false>(x, rec, p.iters, p.eps, scratch);
+        quantize_rotated<128, false, KB, VB>(x, rec, p.iters, p.eps, scratch);
     }
     __syncthreads();  // the scratch of this unit is dead before the next one starts
   }
@@ -864,10 +898,11 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
   }
 }
 
+template <int KB, int VB>
 static int launch_quantize_tc(const QuantizeParams& p, int units2, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(quantize_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(quantize_tc_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tc::kSmemBytes) != cudaSuccess)
       return KVARN_ERR_CUDA;
     attr_set = true;
@@ -878,18 +913,26 @@ static int launch_quantize_tc(const QuantizeParams& p, int units2, cudaStream_t 
   int grid = 2 * sms;
   grid = max(grid, (units2 + tc::kListCap - 1) / tc::kListCap);
   grid = min(grid, units2);
-  quantize_tc_kernel<<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(p, units2);
+  quantize_tc_kernel<KB, VB><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(p, units2);
   return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
-int launch_quantize_any(int d, const QuantizeParams& p, int units, cudaStream_t stream) {
-  if (units <= 0) return KVARN_OK;
+template <int KB, int VB>
+static int launch_quantize_bits(int d, const QuantizeParams& p, int units, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_quantize<64>(p, units, stream);
-    case 128: return launch_quantize_tc(p, units * 2, stream);
-    case 256: return launch_quantize<256>(p, units, stream);
+    case 64: return launch_quantize<64, KB, VB>(p, units, stream);
+    case 128: return launch_quantize_tc<KB, VB>(p, units * 2, stream);
+    case 256: return launch_quantize<256, KB, VB>(p, units, stream);
     default: return KVARN_ERR_UNSUPPORTED;
   }
+}
+
+int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int units, cudaStream_t stream) {
+  if (units <= 0) return KVARN_OK;
+  if (kb == 4 && vb == 2) return launch_quantize_bits<4, 2>(d, p, units, stream);
+  if (kb == 4 && vb == 4) return launch_quantize_bits<4, 4>(d, p, units, stream);
+  if (kb == 2 && vb == 2) return launch_quantize_bits<2, 2>(d, p, units, stream);
+  return KVARN_ERR_UNSUPPORTED;
 }
 
 }  // namespace kvarn

@@ -23,16 +23,23 @@ DEQUANT_RTOL = 1e-3
 DECODE_TOL = 2e-3
 
 
-def oracle_quantize(k_tiles: np.ndarray, v_tiles: np.ndarray, iters: int = ko.SINKHORN_ITERS):
+def oracle_quantize(k_tiles: np.ndarray, v_tiles: np.ndarray, iters: int = ko.SINKHORN_ITERS,
+                    k_bits: int = ko.K_BITS, v_bits: int = ko.V_BITS):
     """k_tiles, v_tiles: [n, 128, d0] float arrays -> (records list, kq dict, vq dict) batched."""
     d = ko.padded_head_dim(k_tiles.shape[-1])
-    kq = ko.quantize_tile(k_tiles, "K", d, iters)
-    vq = ko.quantize_tile(v_tiles, "V", d, iters)
+    kq = ko.quantize_tile(k_tiles, "K", d, iters, bits=k_bits)
+    vq = ko.quantize_tile(v_tiles, "V", d, iters, bits=v_bits)
+    fields = ("codes", "scale", "zero", "factor")
     recs = []
     for i in range(k_tiles.shape[0]):
-        recs.append(ko.pack_record({key: kq[key][i] for key in ("codes", "scale", "zero", "factor")},
-                                   {key: vq[key][i] for key in ("codes", "scale", "zero", "factor")}))
+        recs.append(ko.pack_record(dict({key: kq[key][i] for key in fields}, bits=k_bits),
+                                   dict({key: vq[key][i] for key in fields}, bits=v_bits)))
     return recs, kq, vq
+
+
+def tile_of(q: dict, i: int) -> dict:
+    """Tile i of a batched quantize_tile result (arrays sliced, the scalar code width kept)."""
+    return {key: (val if key == "bits" else val[i]) for key, val in q.items()}
 
 
 def record_bytes_of(pool: torch.Tensor, page: int, head: int) -> bytes:
@@ -66,9 +73,10 @@ def assert_f16_within_ulp(gpu, ora, what):
         what, int(bad.sum()), g[bad][:4], o[bad][:4])
 
 
-def compare_record(gpu_rec: bytes, kq_i: dict, vq_i: dict, d: int, stats: list):
+def compare_record(gpu_rec: bytes, kq_i: dict, vq_i: dict, d: int, stats: list,
+                   k_bits: int = ko.K_BITS, v_bits: int = ko.V_BITS):
     """Compare one GPU page record with the oracle's quantised K/V (dicts of one tile)."""
-    gk, gv = ko.unpack_record(gpu_rec, d)
+    gk, gv = ko.unpack_record(gpu_rec, d, k_bits, v_bits)
     stats.append(compare_codes(gk["codes"], kq_i["codes"], kq_i["pre"]))
     stats.append(compare_codes(gv["codes"], vq_i["codes"], vq_i["pre"]))
     for key in ("scale", "zero", "factor"):

@@ -114,8 +114,8 @@ def _check_sealed_pages(st, pages_per_seq=None):
             vt = v.double().numpy().transpose(1, 0, 2)
             _, kq, vq = H.oracle_quantize(kt, vt)
             for h in range(st.hkv):
-                H.compare_record(H.record_bytes_of(st.pool, page, h), {x: kq[x][h] for x in kq},
-                                 {x: vq[x][h] for x in vq}, desc.head_dim_padded, stats)
+                H.compare_record(H.record_bytes_of(st.pool, page, h), H.tile_of(kq, h),
+                                 H.tile_of(vq, h), desc.head_dim_padded, stats)
     if stats:
         H.assert_mismatch_budget(stats)
 

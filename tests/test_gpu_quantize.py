@@ -45,7 +45,7 @@ def _quantize_and_compare(kv, k, v, d0, page_ids=None, iters=None, check_units=N
     pids = page_ids.cpu().numpy()
     for i, (t, h) in enumerate(check_units):
         rec = H.record_bytes_of(pool, int(pids[t]), h)
-        H.compare_record(rec, {key: kq[key][i] for key in kq}, {key: vq[key][i] for key in vq}, d, stats)
+        H.compare_record(rec, H.tile_of(kq, i), H.tile_of(vq, i), d, stats)
     bad, total = H.assert_mismatch_budget(stats)
     return desc, pool, bad, total
 
