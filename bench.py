@@ -193,13 +193,38 @@ def _decode_bytes(lens, rec_bytes):
     return (sealed * HKV * rec_bytes + part * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2)
 
 
-def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, seed, reps=5):
+def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps=20):
+    """Median ms of kvarn_quantize_tiles on one layer (8 kv heads x 16384 tokens x d 128, K
+    and V), L2 flushed with a 512 MB write before every launch; and its algorithmic bytes."""
+    qdesc = kv.desc_from_preset(D0, Q_HEADS, preset=preset)
+    kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, D0, seed=2, device=dev)
+    qpool = kv.alloc_pool(qdesc, Q_TOKENS // 128, device=dev)
+    qids = torch.arange(Q_TOKENS // 128, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    q_ms = []
+    for rep in range(3 + reps):
+        flush.fill_(float(rep))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kv.quantize_tiles(qdesc, kq, vq, qids, qpool, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            q_ms.append(a.elapsed_time(b))
+    nbytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
+    del kq, vq, qpool, flush
+    torch.cuda.empty_cache()
+    return statistics.median(q_ms), nbytes
+
+
+def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, seed, reps=5,
+                        preset="kvarn_k4v2_g128"):
     """Decode over `layers` independent packed caches (one pool per layer, one shared permuted
     block table, every sequence at seq_len), launched back to back on one stream: median ms
     per pass over all layers, and the algorithmic bytes of one pass."""
     dev = torch.device("cuda")
     pages = seq_len // 128
-    desc = kv.desc_from_preset(d0, hkv)
+    desc = kv.desc_from_preset(d0, hkv, preset=preset)
     g = torch.Generator().manual_seed(seed)
     table = torch.randperm(batch * pages, generator=g).view(batch, pages).to(torch.int32).to(dev)
     page_ids = table.reshape(-1).contiguous()
@@ -302,7 +327,13 @@ def _decode_configs(torch, kv, synth, peak, args):
     for key, group, cfg in (
             ("decode_32b_step", "32b", dict(batch=32, seq_len=16384, hq=64, hkv=8, d0=128, layers=64, seed=4)),
             ("decode_long_d256", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=256, layers=1, seed=5)),
-            ("decode_long_d96", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=96, layers=1, seed=5))):
+            ("decode_long_d96", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=96, layers=1, seed=5)),
+            ("preset_kvarn_k4v2_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
+                                                       seed=6, preset="kvarn_k4v2_g128")),
+            ("preset_kvarn_k4v4_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
+                                                       seed=6, preset="kvarn_k4v4_g128")),
+            ("preset_kvarn_k2v2_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
+                                                       seed=6, preset="kvarn_k2v2_g128"))):
         if args.extras not in ("all", group):
             continue
         if args.extra_batch:
@@ -312,8 +343,9 @@ def _decode_configs(torch, kv, synth, peak, args):
         ms, nbytes = _time_decode_layers(torch, kv, synth, **cfg)
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[key] = {
-            "workload": "%d layer(s) x batch %d at %d tokens, %d q heads / %d kv heads, head_dim %d"
-                        % (cfg["layers"], cfg["batch"], cfg["seq_len"], cfg["hq"], cfg["hkv"], cfg["d0"]),
+            "workload": "%d layer(s) x batch %d at %d tokens, %d q heads / %d kv heads, head_dim %d, %s"
+                        % (cfg["layers"], cfg["batch"], cfg["seq_len"], cfg["hq"], cfg["hkv"], cfg["d0"],
+                           cfg.get("preset", "kvarn_k4v2_g128")),
             "ms_per_step": ms, "algorithmic_bytes": nbytes, "hbm_gbs": gbs, "frac": gbs / peak,
             "ideal_ms_at_peak": nbytes / (peak * 1e9) * 1e3,
             "kv_tokens_per_s": cfg["batch"] * cfg["seq_len"] / (ms * 1e-3),
@@ -408,24 +440,14 @@ def _run_kvarn(args, torch, world, rank):
     e2e_tokens = sum(int(lens_e.sum()) + BATCH * (i + 1) for i in range(e_steps))
 
     # ---- quantise throughput: one layer, 8 KV heads x 16384 tokens x head_dim 128
-    qdesc = kv.desc_from_preset(D0, Q_HEADS)
-    kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, D0, seed=2, device=dev)
-    qpool = kv.alloc_pool(qdesc, Q_TOKENS // 128, device=dev)
-    qids = torch.arange(Q_TOKENS // 128, dtype=torch.int32, device=dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    q_ms = []
-    for rep in range(3 + 20):
-        flush.fill_(float(rep))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        kv.quantize_tiles(qdesc, kq, vq, qids, qpool, stream=stream)
-        b.record(stream)
-        torch.cuda.synchronize()
-        if rep >= 3:
-            q_ms.append(a.elapsed_time(b))
-    q_med = statistics.median(q_ms)
-    q_bytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
+    q_med, q_bytes = _time_quantize(torch, kv, synth, dev, stream)
     q_gbs = q_bytes / (q_med * 1e-3) / 1e9
+    q_presets = {}
+    if args.extras in ("all", "presets"):
+        for name in ("kvarn_k4v4_g128", "kvarn_k2v2_g128"):
+            ms, nb = _time_quantize(torch, kv, synth, dev, stream, preset=name, reps=10)
+            q_presets[name] = {"us": ms * 1e3, "tokens_per_s": Q_TOKENS / (ms * 1e-3),
+                               "hbm_gbs": nb / (ms * 1e-3) / 1e9}
     # Quantisation is bound by fp32 arithmetic, not by HBM.  Per element it needs 37 fp32 ops:
     # 4 in each of the 8 std steps (product with the other axis' factor, its share of the sum,
     # minus the mean, square-accumulate) and 5 to quantise (two factor products, minus the zero
@@ -490,6 +512,7 @@ def _run_kvarn(args, torch, world, rank):
             "tokens_per_s": Q_TOKENS / (q_med * 1e-3),
             "us": q_med * 1e3, "hbm_gbs": q_gbs, "frac": q_gbs / peak,
             "algorithmic_bytes": q_bytes,
+            "other_presets": q_presets,
             "roofline": {
                 "kernel": "quantize_tc_kernel", "bound": "alu", "achieved": q_ops,
                 "peak": sms * 128 * (clk.get("sm_mhz") or SM_MAX_MHZ) * 1e-3, "unit": "Gop/s",
@@ -655,7 +678,7 @@ def main():
                     help="decode batch (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="CPU work of the oracle baseline sample (kvarn arm)")
-    ap.add_argument("--extras", choices=("all", "none", "32b", "long"), default="all",
+    ap.add_argument("--extras", choices=("all", "none", "32b", "long", "presets"), default="all",
                     help="which of the 64-layer and long-context decode shapes to time")
     ap.add_argument("--extra-batch", type=int, default=0,
                     help="batch of those shapes (0 = the workload's; smaller only for profiling)")
