@@ -539,6 +539,58 @@ def test_decode_sequence_presets_roundtrip():
         np.testing.assert_allclose(got, want, rtol=0, atol=1e-12, err_msg=name)
 
 
+# --- adaptive stop of the normalisation (hotdry §迭代方差归一化: usually 3-5 iterations) ---
+
+def _iteration_changes(x, iters):
+    """Largest |log factor change| of each iteration, recomputed from runs with fixed counts."""
+    out = []
+    prev_r, prev_c = np.ones(x.shape[-2]), np.ones(x.shape[-1])
+    for t in range(1, iters + 1):
+        _, r, c = ko.sinkhorn_normalise(x, t)
+        out.append(max(np.abs(np.log(r / prev_r)).max(), np.abs(np.log(c / prev_c)).max()))
+        prev_r, prev_c = r, c
+    return out
+
+
+def test_adaptive_stop_zero_tol_is_fixed():
+    x = ko.rotate(synth.outlier_kv(128, 1, 128, seed=16)[0][:, 0].double().numpy(), 128)
+    a = ko.sinkhorn_normalise(x, 4)
+    n, r, c, used = ko.sinkhorn_normalise(x, 4, tol=0.0, return_iters=True)
+    assert int(used) == 4
+    for u, w in zip(a, (n, r, c)):
+        np.testing.assert_array_equal(u, w)
+
+
+def test_adaptive_stop_closed_form():
+    # diag(r) Y diag(c) is normalised exactly by the first iteration, so the second moves
+    # nothing and the iteration stops there
+    _, _, x = _rank_one_scaled(128, 128, 21)
+    n, r, c, used = ko.sinkhorn_normalise(x, 8, tol=1e-9, return_iters=True)
+    assert int(used) == 2
+    np.testing.assert_allclose(np.abs(n), 1.0, rtol=1e-12)
+
+
+def test_adaptive_stop_rule_and_batching():
+    # each tile stops at the first iteration whose largest log-factor change is <= tol
+    # (changes recomputed independently from fixed-count runs); batched == one by one;
+    # a looser tol never uses more iterations
+    tiles = [ko.rotate(synth.outlier_kv(128, 1, 128, seed=30 + i)[j][:, 0].double().numpy(), 128)
+             for i in range(3) for j in (0, 1)]
+    for tol in (0.3, 0.05, 0.01):
+        _, _, _, used = ko.sinkhorn_normalise(np.stack(tiles), 8, tol=tol, return_iters=True)
+        for x, u in zip(tiles, used):
+            ch = _iteration_changes(x, 8)
+            want = next((t + 1 for t, v in enumerate(ch) if v <= tol), 8)
+            assert int(u) == want, (tol, ch)
+            _, _, _, u1 = ko.sinkhorn_normalise(x, 8, tol=tol, return_iters=True)
+            assert int(u1) == int(u)
+    u_loose = ko.sinkhorn_normalise(np.stack(tiles), 8, tol=0.3, return_iters=True)[3]
+    u_tight = ko.sinkhorn_normalise(np.stack(tiles), 8, tol=0.01, return_iters=True)[3]
+    assert np.all(u_loose <= u_tight)
+    q = ko.quantize_tile(np.stack([t[:, :128] for t in tiles]), "K", tol=0.05)
+    assert q["iters"].shape == (6,) and q["iters"].max() <= ko.SINKHORN_ITERS
+
+
 # --- attention ----------------------------------------------------------------
 
 def test_attention_single_token():
