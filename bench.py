@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "K4V2 g128 decode-attn KV tokens/s & HBM GB/s; quantize tokens/s (1 GB300)"
 QUANT_OPS_PER_ELEMENT = 37  # fp32 ops per quantised element (derivation at the quantize timing)
 SM_MAX_MHZ = 2070.0
+ADAPTIVE_TOL = 0.05  # early-stop tolerance of the normalisation (log-factor change per iteration)
 WORKLOAD = ("paged decode attention + append: batch 64, seq_len 128*U{8..128}, 32 q heads / 8 kv "
             "heads, head_dim 128, K4V2 g128 packed cache, permuted block table")
 BATCH, HQ, HKV, D0, MIN_PAGES, MAX_PAGES, SEED = 64, 32, 8, 128, 8, 128, 3
@@ -193,27 +194,32 @@ def _decode_bytes(lens, rec_bytes):
     return (sealed * HKV * rec_bytes + part * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2)
 
 
-def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps=20):
+def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps=20, tol=None):
     """Median ms of kvarn_quantize_tiles on one layer (8 kv heads x 16384 tokens x d 128, K
-    and V), L2 flushed with a 512 MB write before every launch; and its algorithmic bytes."""
+    and V), L2 flushed with a 512 MB write before every launch; and its algorithmic bytes.
+    With tol: kvarn_quantize_tiles_adaptive, and also the mean iterations used."""
     qdesc = kv.desc_from_preset(D0, Q_HEADS, preset=preset)
     kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, D0, seed=2, device=dev)
     qpool = kv.alloc_pool(qdesc, Q_TOKENS // 128, device=dev)
     qids = torch.arange(Q_TOKENS // 128, dtype=torch.int32, device=dev)
+    used = torch.zeros((Q_TOKENS // 128, Q_HEADS, 2), dtype=torch.int32, device=dev) if tol is not None else None
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     q_ms = []
     for rep in range(3 + reps):
         flush.fill_(float(rep))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        kv.quantize_tiles(qdesc, kq, vq, qids, qpool, stream=stream)
+        kv.quantize_tiles(qdesc, kq, vq, qids, qpool, stream=stream, sinkhorn_tol=tol, iters_used=used)
         b.record(stream)
         torch.cuda.synchronize()
         if rep >= 3:
             q_ms.append(a.elapsed_time(b))
     nbytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
+    mean_iters = float(used.double().mean()) if used is not None else None
     del kq, vq, qpool, flush
     torch.cuda.empty_cache()
+    if tol is not None:
+        return statistics.median(q_ms), nbytes, mean_iters
     return statistics.median(q_ms), nbytes
 
 
@@ -442,6 +448,9 @@ def _run_kvarn(args, torch, world, rank):
     # ---- quantise throughput: one layer, 8 KV heads x 16384 tokens x head_dim 128
     q_med, q_bytes = _time_quantize(torch, kv, synth, dev, stream)
     q_gbs = q_bytes / (q_med * 1e-3) / 1e9
+    a_ms, _, a_iters = _time_quantize(torch, kv, synth, dev, stream, reps=10, tol=ADAPTIVE_TOL)
+    q_adaptive = {"sinkhorn_tol": ADAPTIVE_TOL, "us": a_ms * 1e3, "tokens_per_s": Q_TOKENS / (a_ms * 1e-3),
+                  "mean_iterations": a_iters, "max_iterations": 4}
     q_presets = {}
     if args.extras in ("all", "presets"):
         for name in ("kvarn_k4v4_g128", "kvarn_k2v2_g128"):
@@ -513,6 +522,7 @@ def _run_kvarn(args, torch, world, rank):
             "us": q_med * 1e3, "hbm_gbs": q_gbs, "frac": q_gbs / peak,
             "algorithmic_bytes": q_bytes,
             "other_presets": q_presets,
+            "adaptive_stop": q_adaptive,
             "roofline": {
                 "kernel": "quantize_tc_kernel", "bound": "alu", "achieved": q_ops,
                 "peak": sms * 128 * (clk.get("sm_mhz") or SM_MAX_MHZ) * 1e-3, "unit": "Gop/s",

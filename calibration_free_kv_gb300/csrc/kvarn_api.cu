@@ -1,5 +1,6 @@
 // C ABI of the KVarN kernels: argument validation, launch configuration, status codes.
 // Nothing here allocates, synchronises or keeps state between calls.
+#include <cmath>
 #include <cstring>
 
 #include "common.cuh"
@@ -82,6 +83,16 @@ int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, i
                          int64_t head_stride, int num_tiles, const int32_t* page_ids,
                          void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
                          void* stream) {
+  return kvarn_quantize_tiles_adaptive(desc, k, v, tok_stride, head_stride, num_tiles, page_ids,
+                                       page_pool, num_pool_pages, 0.0f, nullptr, dev_status, stream);
+}
+
+int kvarn_quantize_tiles_adaptive(const kvarn_desc* desc, const void* k, const void* v,
+                                  int64_t tok_stride, int64_t head_stride, int num_tiles,
+                                  const int32_t* page_ids, void* page_pool, int64_t num_pool_pages,
+                                  float sinkhorn_tol, int32_t* iters_used, int32_t* dev_status,
+                                  void* stream) {
+  if (!(sinkhorn_tol >= 0.0f) || sinkhorn_tol > 10.0f) return KVARN_ERR_INVALID_ARG;
   int st = check_desc(desc);
   if (st != KVARN_OK) return st;
   if (num_tiles < 0) return KVARN_ERR_INVALID_ARG;
@@ -106,6 +117,11 @@ int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, i
   p.d0 = desc->head_dim;
   p.iters = desc->sinkhorn_iters;
   p.eps = desc->sinkhorn_eps;
+  if (sinkhorn_tol > 0.0f) {
+    p.tol_hi = std::exp(sinkhorn_tol);
+    p.tol_lo = std::exp(-sinkhorn_tol);
+  }
+  p.iters_out = iters_used;
   p.status = dev_status;
   p.append = 0;
   return launch_quantize_any(desc->head_dim_padded, desc->k_bits, desc->v_bits, p,

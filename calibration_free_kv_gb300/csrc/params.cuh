@@ -30,6 +30,10 @@ struct QuantizeParams {
   int d0;
   int iters;
   float eps;
+  // early stop: after an iteration in which every std step's sigma stayed within
+  // [tol_lo, tol_hi] = [e^-tol, e^tol]; tol_hi == 0 disables it
+  float tol_lo, tol_hi;
+  int32_t* iters_out;  // iterations used per unit [tile][head][K, V], or null
   int32_t* status;
   int append;  // 0: quantise whole tiles, 1: append one token and seal full tiles
 };

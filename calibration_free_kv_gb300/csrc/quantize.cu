@@ -117,10 +117,12 @@ __device__ __forceinline__ void group_sync(int id, int count) {
 // the std of the current normalised values) telescopes to f = 1 / sd; a std below eps has
 // nothing to normalise and the factor is kept.
 __device__ __forceinline__ float std_step_factor(float f_old, float m2, float inv_count,
-                                                 float eps) {
+                                                 float eps, float tol_lo, float tol_hi, bool& moved) {
   const float sd = sqrtf(fmaxf(m2 * inv_count, 0.0f));
   const float sigma = f_old * sd;
-  return sigma >= eps ? __frcp_rn(sd) : f_old;
+  if (sigma < eps) return f_old;
+  moved |= sigma > tol_hi || sigma < tol_lo;  // |ln sigma| beyond the early-stop tolerance
+  return __frcp_rn(sd);
 }
 
 template <int D, bool TRANS>
@@ -217,9 +219,12 @@ struct RotScratch {
 // single merging warp would need to hand its result out.  The partial buffers alternate between
 // two copies from one step to the next: a warp can only refill a copy after every warp of its
 // group has passed the barrier of the step in between, i.e. finished reading it.
+// Returns the iterations used: `iters`, or fewer when tol_hi > 0 and an iteration's std
+// steps all had sigma within [tol_lo, tol_hi] (decided for the whole CTA).
 template <int D, bool TRANS, int KB, int VB>
-__device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __restrict__ rec,
-                                                 int iters, float eps, float* smem) {
+__device__ __forceinline__ int quantize_rotated(float (&x)[4][16], uint8_t* __restrict__ rec,
+                                                int iters, float eps, float tol_lo, float tol_hi,
+                                                float* smem) {
   constexpr int LSIZE = TRANS ? D : kTile;
   constexpr int CSIZE = TRANS ? kTile : D;
   constexpr int NLQ = LSIZE / 32;
@@ -259,6 +264,7 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
   auto FL = [&](int l) { return make_float2(fL[l], fL[l]); };
 
   // std over L of each C column -> new C factors (the k-th such step uses buffer k % 2)
+  bool moved = false;  // a factor this thread computed moved beyond the early-stop tolerance
   auto update_c = [&](int k) {
     // Column pairs (2u, 2u + 1): sum and centred sum of squares of 4 rows.  The products are
     // rounded before a pairwise sum, so identical values give an exact mean and a zero sum of
@@ -299,8 +305,8 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
       m = pm[0];
     }
     float2 f = *reinterpret_cast<const float2*>(&fCw[ci]);
-    f.x = std_step_factor(f.x, m.x, 1.0f / LSIZE, eps);
-    f.y = std_step_factor(f.y, m.y, 1.0f / LSIZE, eps);
+    f.x = std_step_factor(f.x, m.x, 1.0f / LSIZE, eps, tol_lo, tol_hi, moved);
+    f.y = std_step_factor(f.y, m.y, 1.0f / LSIZE, eps, tol_lo, tol_hi, moved);
     *reinterpret_cast<float2*>(&fCw[ci]) = f;
     __syncwarp();
 #pragma unroll
@@ -360,13 +366,14 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
       }
       m = pm[0];
     }
-    fLw[ri] = std_step_factor(fLw[ri], m, 1.0f / CSIZE, eps);
+    fLw[ri] = std_step_factor(fLw[ri], m, 1.0f / CSIZE, eps, tol_lo, tol_hi, moved);
     __syncwarp();
 #pragma unroll
     for (int l = 0; l < 4; ++l) fL[l] = fLw[g + 8 * l];
   };
 
   // ---- 2. variance normalisation: channel-std step, then token-std step -------------------
+  int used = 0;
   for (int it = 0; it < iters; ++it) {
     if (!TRANS) {  // K: channels are C, tokens are L
       update_c(it);
@@ -375,12 +382,17 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
       update_l(it);
       update_c(it);
     }
+    ++used;
+    if (tol_hi > 0.0f) {  // one decision for the CTA: stop unless some factor still moved
+      if (!__syncthreads_or(moved ? 1 : 0)) break;
+      moved = false;
+    }
   }
 
   // ---- 3. per-column (along L) min / max, scale, zero-point ---------------------------------
   // N = (x fL) fC with fC > 0 fixed per column, and rounding is monotonic, so the extremes of N
   // are the extremes of z = x fL times fC, rounded once.
-  float4* qbuf = reinterpret_cast<float4*>(redA + ((iters + 1) & 1) * NLQ * CSIZE + lq * CSIZE + 64 * ch);
+  float4* qbuf = reinterpret_cast<float4*>(redA + ((used + 1) & 1) * NLQ * CSIZE + lq * CSIZE + 64 * ch);
   {
     float mn[16], mx[16];
 #pragma unroll
@@ -402,7 +414,7 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
     rs_minmax<4>(mn4, mx4, 4, (lane & 4) != 0);
     float2 zmin = make_float2(mn4[0], mn4[1]), zmax = make_float2(mx4[0], mx4[1]);
     if (NLQ > 1) {
-      float4* buf = reinterpret_cast<float4*>(redA + (iters & 1) * NLQ * CSIZE);
+      float4* buf = reinterpret_cast<float4*>(redA + (used & 1) * NLQ * CSIZE);
       buf[(lq * CSIZE + c_col) >> 1] = make_float4(zmin.x, zmin.y, zmax.x, zmax.y);
       group_sync(1 + ch, NLQ * 32);
 #pragma unroll
@@ -528,15 +540,16 @@ __device__ __forceinline__ void quantize_rotated(float (&x)[4][16], uint8_t* __r
       }
     }
   }
+  return used;
 }
 
 template <int D, bool TRANS, int KB, int VB>
-__device__ __forceinline__ void quantize_unit(const __half* __restrict__ src, int64_t tok_stride,
-                                              int d0, uint8_t* __restrict__ rec, int iters,
-                                              float eps, float* smem) {
+__device__ __forceinline__ int quantize_unit(const __half* __restrict__ src, int64_t tok_stride,
+                                             int d0, uint8_t* __restrict__ rec, const QuantizeParams& p,
+                                             float* smem) {
   float x[4][16];
   stage_and_rotate<D, TRANS>(src, tok_stride, d0, smem, x);
-  quantize_rotated<D, TRANS, KB, VB>(x, rec, iters, eps, smem);
+  return quantize_rotated<D, TRANS, KB, VB>(x, rec, p.iters, p.eps, p.tol_lo, p.tol_hi, smem);
 }
 
 // ---- kernels --------------------------------------------------------------------------------
@@ -585,10 +598,9 @@ __global__ void __launch_bounds__(QuantShape<D>::kThreads)
     return;
   }
   uint8_t* rec = p.pool + (page * p.num_kv_heads + h) * p.rec_bytes;
-  if (is_v)
-    quantize_unit<D, true, KB, VB>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
-  else
-    quantize_unit<D, false, KB, VB>(src, tok_stride, p.d0, rec, p.iters, p.eps, smem_q);
+  const int used = is_v ? quantize_unit<D, true, KB, VB>(src, tok_stride, p.d0, rec, p, smem_q)
+                        : quantize_unit<D, false, KB, VB>(src, tok_stride, p.d0, rec, p, smem_q);
+  if (p.iters_out != nullptr && !p.append && threadIdx.x == 0) p.iters_out[blockIdx.x] = used;
 }
 
 template <int D, int KB, int VB>
@@ -878,10 +890,10 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
       int64_t ts;
       uint8_t* rec;
       tc::unit_io(p, list[i], src, ts, rec);
-      if ((list[i] & 1) != 0)
-        quantize_rotated<128, true, KB, VB>(x, rec, p.iters, p.eps, scratch);
-      else
-        quantize_rotated<128, false, KB, VB>(x, rec, p.iters, p.eps, scratch);
+      const int used = (list[i] & 1) != 0
+                           ? quantize_rotated<128, true, KB, VB>(x, rec, p.iters, p.eps, p.tol_lo, p.tol_hi, scratch)
+                           : quantize_rotated<128, false, KB, VB>(x, rec, p.iters, p.eps, p.tol_lo, p.tol_hi, scratch);
+      if (p.iters_out != nullptr && !p.append && tid == 0) p.iters_out[list[i]] = used;
     }
     __syncthreads();  // the scratch of this unit is dead before the next one starts
   }

@@ -30,6 +30,7 @@ EXPORTED_SYMBOLS = (
     "kvarn_desc_from_preset",
     "kvarn_page_record_bytes",
     "kvarn_quantize_tiles",
+    "kvarn_quantize_tiles_adaptive",
     "kvarn_append_token",
     "kvarn_decode_workspace_bytes",
     "kvarn_decode_attention",
@@ -74,6 +75,7 @@ def _load():
         "kvarn_desc_from_preset": (i32, [ctypes.c_char_p, i32, i32, D]),
         "kvarn_page_record_bytes": (i64, [D]),
         "kvarn_quantize_tiles": (i32, [D, P, P, i64, i64, i32, P, P, i64, P, P]),
+        "kvarn_quantize_tiles_adaptive": (i32, [D, P, P, i64, i64, i32, P, P, i64, ctypes.c_float, P, P, P]),
         "kvarn_append_token": (i32, [D, i32, P, P, P, P, P, P, P, i32, P, i64, P, P]),
         "kvarn_decode_workspace_bytes": (ctypes.c_size_t, [D, i32, i32, i32]),
         "kvarn_decode_attention": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P, ctypes.c_float,
@@ -149,8 +151,11 @@ def alloc_pool(desc: KvarnDesc, num_pages: int, device="cuda") -> torch.Tensor:
 
 
 def quantize_tiles(desc: KvarnDesc, k: torch.Tensor, v: torch.Tensor, page_ids: torch.Tensor,
-                   pool: torch.Tensor, status: torch.Tensor | None = None, stream=None):
-    """k, v: fp16 [tokens, Hkv, d0] (token and head strides taken from the tensors)."""
+                   pool: torch.Tensor, status: torch.Tensor | None = None, stream=None,
+                   sinkhorn_tol: float | None = None, iters_used: torch.Tensor | None = None):
+    """k, v: fp16 [tokens, Hkv, d0] (token and head strides taken from the tensors).
+    With sinkhorn_tol or iters_used (int32 [tiles, Hkv, 2]) this calls
+    kvarn_quantize_tiles_adaptive."""
     _dev(k, torch.float16, "k")
     _dev(v, torch.float16, "v")
     _dev(page_ids, torch.int32, "page_ids")
@@ -159,6 +164,16 @@ def quantize_tiles(desc: KvarnDesc, k: torch.Tensor, v: torch.Tensor, page_ids: 
     num_tiles = k.shape[0] // 128
     if page_ids.numel() < num_tiles:
         raise ValueError("page_ids shorter than the number of tiles")
+    if sinkhorn_tol is not None or iters_used is not None:
+        if iters_used is not None:
+            _dev(iters_used, torch.int32, "iters_used")
+            if iters_used.numel() < num_tiles * desc.num_kv_heads * 2:
+                raise ValueError("iters_used holds fewer than tiles x Hkv x 2 entries")
+        _check(_lib.kvarn_quantize_tiles_adaptive(
+            ctypes.byref(desc), _ptr(k), _ptr(v), k.stride(0), k.stride(1), num_tiles, _ptr(page_ids),
+            _ptr(pool), pool.shape[0], float(sinkhorn_tol or 0.0), _ptr(iters_used), _ptr(status),
+            _stream(stream)), "kvarn_quantize_tiles_adaptive")
+        return
     _check(_lib.kvarn_quantize_tiles(ctypes.byref(desc), _ptr(k), _ptr(v), k.stride(0), k.stride(1),
                                      num_tiles, _ptr(page_ids), _ptr(pool), pool.shape[0],
                                      _ptr(status), _stream(stream)), "kvarn_quantize_tiles")

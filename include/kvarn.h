@@ -1,5 +1,6 @@
 /*
- * kvarn.h -- C ABI of the KVarN K4V2 g128 KV-cache path for GB300 (sm_103a).
+ * kvarn.h -- C ABI of the KVarN K4V2 g128 KV-cache path (and the other k/v bit presets) for
+ * GB300 (sm_103a).
  *
  * What is computed (sources cited by page title and section):
  *  - [hotdry]  blog.hotdry.top "KVarN Hadamard 旋转与方差归一化：KV-cache 量化的校准算法实现"
@@ -10,10 +11,11 @@
  * Every 128-token tile of every KV head is (1) zero-padded along head_dim to the next power of
  * two d [aifeeds §局限], (2) rotated along head_dim by the orthonormal Sylvester Hadamard
  * H_d / sqrt(d) [hotdry §Hadamard 旋转], (3) variance-normalised by alternating channel-std and
- * token-std steps whose factors live in log space, for a fixed iteration count [hotdry
- * §迭代方差归一化; vatt §四個步驟], (4) quantised by asymmetric round-to-nearest, keys to 4 bits
- * per channel and values to 2 bits per token, with the normalisation factors folded into the
- * stored fp16 scales [hotdry §非对称量化与尺度折叠].  Decode attention reads the packed cache
+ * token-std steps whose factors live in log space, for a fixed iteration count (or fewer,
+ * with kvarn_quantize_tiles_adaptive) [hotdry §迭代方差归一化; vatt §四個步驟], (4) quantised
+ * by asymmetric round-to-nearest, keys to 4 bits per channel and values to 2 bits per token
+ * (other presets: other widths, same steps [vatt §四個步驟, bit-width assignment]), with the
+ * normalisation factors folded into the stored fp16 scales [hotdry §非对称量化与尺度折叠].  Decode attention reads the packed cache
  * directly [vatt §怎麼用: one paged-attention block == one tile; attention computed in fp16
  * over the quantised cache].
  *
@@ -31,23 +33,30 @@
  *  - head_dim d0: 8..256 and a multiple of 8; it is padded to d = 64, 128 or 256.
  *  - GQA: query head hq reads KV head hq / G, G = num_q_heads / num_kv_heads in {1,2,4,8}.
  *
- * Page record: the packed K/V of one (page, kv head), record_bytes(d) bytes, 16-byte aligned
+ * Page record: the packed K/V of one (page, kv head), record_bytes bytes, 16-byte aligned
  * sections.  The page pool is [num_pool_pages][num_kv_heads][record_bytes]; record (p, h)
- * starts at byte ((p * num_kv_heads) + h) * record_bytes.  With T = 128:
- *    K codes  T*d/2 B   uint32 words of eight 4-bit codes
+ * starts at byte ((p * num_kv_heads) + h) * record_bytes.  With T = 128 and kb / vb the K / V
+ * code bits (4 / 2 for kvarn_k4v2_g128):
+ *    K codes  T*d*kb/8 B   uint32 words
  *    K scale s'[d], K zero z'[d], K token factor r[T]            (fp16)
- *    V codes  T*d/4 B   uint32 words of sixteen 2-bit codes
+ *    V codes  T*d*vb/8 B   uint32 words
  *    V scale s'[T], V zero z'[T], V channel factor c[d]          (fp16)
- * (the K half, T*d/2 + 4d + 2T bytes, precedes the V half, so each can be fetched alone).
+ * (the K half precedes the V half, so each can be fetched alone).
  * Dequantised rotated-domain values: K~[t][j] = r[t] (code*s'[j] + z'[j]),
  * V~[t][j] = c[j] (code*s'[t] + z'[t]); original basis = rows of (.) H_d / sqrt(d), first d0.
- * K word (mi, kk, lane) [mi < 8, kk < d/16, lane < 32, g = lane/4, tq = lane%4] is word
- * ((mi*(d/64) + kk/4)*32 + lane)*4 + kk%4; it holds token 16mi + g + 8rho, channel
- * 16kk + 8h + 2tq + p at nibble h + 2rho + 4p (rho, h, p in {0,1}).
- * V word (ks2, mc, lane) [ks2 < 4, mc < d/16] is word ((ks2*(d/64) + mc/4)*32 + lane)*4 + mc%4;
- * it holds channel 16mc + g + 8rho, token 16(2ks2 + f) + 8h + 2tq + p at 2-bit slot
- * 2f + h + 4rho + 8p.  (Each word is an m16n8k16 A-operand fragment: K as [token x channel],
- * V transposed as [channel x token].)  record_bytes = 13824 at d = 128, 26880 at d = 256.
+ * Code words carry m16n8k16 A-operand fragments of 16 x 16 blocks: K as [token x channel],
+ * V transposed as [channel x token]; lane = 4g + tq, element (rho, h, p) of a fragment is at
+ * row g + 8rho, column 8h + 2tq + p of its block.  Blocks (o, i): o = token block (< 8),
+ * i = channel block (< d/16).
+ *  4-bit: word ((o*(d/64) + i/4)*32 + lane)*4 + i%4 is fragment (o, i), element (rho, h, p)
+ *         at nibble h + 2rho + 4p.
+ *  2-bit: word ((o/2*(d/64) + i/4)*32 + lane)*4 + i%4 holds fragments (o, i) of both token
+ *         blocks o of a pair, element (rho, h, p) at 2-bit slot 2(o%2) + h + 4rho + 8p.
+ * For kvarn_k4v2_g128 K word (mi, kk, lane) holds token 16mi + g + 8rho, channel
+ * 16kk + 8h + 2tq + p at nibble h + 2rho + 4p; V word (ks2, mc, lane) holds channel
+ * 16mc + g + 8rho, token 16(2ks2 + f) + 8h + 2tq + p at slot 2f + h + 4rho + 8p.
+ * record_bytes (d = 128 / 256): kvarn_k4v2_g128 13824 / 26880, kvarn_k4v4_g128 17920 / 35072,
+ * kvarn_k2v2_g128 9728 / 18688.
  */
 #ifndef KVARN_H
 #define KVARN_H
@@ -76,16 +85,18 @@ typedef struct kvarn_desc {
   int32_t head_dim_padded;   /* d = 64, 128 or 256                                  */
   int32_t num_kv_heads;      /* Hkv                                                 */
   int32_t tile_tokens;       /* 128 (one tile == one page) [vatt §怎麼用 knob table]  */
-  int32_t k_bits;            /* 4                                                   */
-  int32_t v_bits;            /* 2                                                   */
+  int32_t k_bits;            /* 4 (kvarn_k4v2_g128, kvarn_k4v4_g128) or 2           */
+  int32_t v_bits;            /* 2 (kvarn_k4v2_g128, kvarn_k2v2_g128) or 4           */
   int32_t sinkhorn_iters;    /* 4 (0..8 accepted)                                   */
   float sinkhorn_eps;        /* 1e-6, floor of a std before its log                 */
   int64_t page_record_bytes; /* bytes of one (page, kv head) record                 */
 } kvarn_desc;
 
-/* Fill *out for preset "kvarn_k4v2_g128" [hotdry §核心配置参数: kv_cache_dtype
- * kvarn_k4v2_g128, block_size 128].  Host only.  UNSUPPORTED for another preset or a
- * head_dim outside 8..256 / not a multiple of 8; INVALID_ARG for NULL or Hkv < 1. */
+/* Fill *out for a preset: "kvarn_k4v2_g128" [hotdry §核心配置参数: kv_cache_dtype
+ * kvarn_k4v2_g128, block_size 128], or "kvarn_k4v4_g128" / "kvarn_k2v2_g128" (other k/v bit
+ * presets through the same pipeline [vatt §四個步驟, bit-width assignment]).  Host only.
+ * UNSUPPORTED for another name or a head_dim outside 8..256 / not a multiple of 8;
+ * INVALID_ARG for NULL or Hkv < 1. */
 int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, kvarn_desc* out);
 
 /* Bytes of one page record for this descriptor (host only). */
@@ -103,6 +114,22 @@ int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, i
                          int64_t head_stride, int num_tiles, const int32_t* page_ids,
                          void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
                          void* stream);
+
+/* kvarn_quantize_tiles with an early stop of the normalisation and per-unit telemetry
+ * [hotdry §迭代方差归一化: usually 3-5 iterations; vatt §四個步驟, Sinkhorn paragraph:
+ * alternate until both directions balance].
+ *  sinkhorn_tol  >= 0 (and <= 10).  0: always desc->sinkhorn_iters iterations, identical to
+ *                kvarn_quantize_tiles.  > 0: a unit (tile, head, K or V) stops after the
+ *                first iteration in which no std step moved a log factor by more than
+ *                sinkhorn_tol (every sigma within [e^-tol, e^tol]), at most sinkhorn_iters.
+ *  iters_used    device int32 [num_tiles][Hkv][2] (K, V) or NULL: iterations each unit used.
+ * Other arguments, layout and errors as kvarn_quantize_tiles; INVALID_ARG for a negative,
+ * NaN or too large sinkhorn_tol. */
+int kvarn_quantize_tiles_adaptive(const kvarn_desc* desc, const void* k, const void* v,
+                                  int64_t tok_stride, int64_t head_stride, int num_tiles,
+                                  const int32_t* page_ids, void* page_pool, int64_t num_pool_pages,
+                                  float sinkhorn_tol, int32_t* iters_used, int32_t* dev_status,
+                                  void* stream);
 
 /* Append one decode token per sequence and seal full tiles (tile filling implied by paging:
  * vatt §怎麼用, one block == one tile).
