@@ -116,7 +116,7 @@ int kvarn_quantize_tiles(const kvarn_desc* desc, const void* k, const void* v, i
                          void* stream);
 
 /* kvarn_quantize_tiles with an early stop of the normalisation and per-unit telemetry
- * [hotdry §迭代方差归一化: usually 3-5 iterations; vatt §四個步驟, Sinkhorn paragraph:
+ * [hotdry §迭代方差归一化: three to five iterations typical; vatt §四個步驟, Sinkhorn paragraph:
  * alternate until both directions balance].
  *  sinkhorn_tol  >= 0 (and <= 10).  0: always desc->sinkhorn_iters iterations, identical to
  *                kvarn_quantize_tiles.  > 0: a unit (tile, head, K or V) stops after the

@@ -54,7 +54,7 @@ V_BITS = 2
 # Reading: widths of 2 and 4 bits on either side; tiles stay 128 tokens.
 PRESETS = {"kvarn_k4v2_g128": (4, 2), "kvarn_k4v4_g128": (4, 4), "kvarn_k2v2_g128": (2, 2)}
 CODE_BITS = (2, 4)
-SINKHORN_ITERS = 4         # "usually 3-5 iterations"                [hotdry §迭代方差归一化, step 3]
+SINKHORN_ITERS = 4         # typical count three to five             [hotdry §迭代方差归一化, step 3]
 SINKHORN_EPS = 1e-6        # reading: stds below this are not normalised (pages give no value)
 SCALE_FLOOR = 1e-8         # reading: quantiser step floor for constant groups
 
@@ -125,7 +125,7 @@ def sinkhorn_normalise(x: np.ndarray, iters: int = SINKHORN_ITERS,
     Returns N = x / (r_i c_j), r = e^{lr}, c = e^{lc} (and the iterations each tile used
     when return_iters).
     With tol > 0 a tile stops after the first iteration in which no log factor moved by
-    more than tol (reading of "usually 3-5 iterations" and of the alternation approaching a
+    more than tol (reading of the typical count of three to five and of the alternation approaching a
     fixed point; at most `iters` iterations either way).
     [hotdry §迭代方差归一化 steps 1-3 and the log-space paragraph;
      vatt §四個步驟, the Sinkhorn paragraph: column then row, log domain, alternate until

@@ -539,7 +539,7 @@ def test_decode_sequence_presets_roundtrip():
         np.testing.assert_allclose(got, want, rtol=0, atol=1e-12, err_msg=name)
 
 
-# --- adaptive stop of the normalisation (hotdry §迭代方差归一化: usually 3-5 iterations) ---
+# --- adaptive stop of the normalisation (hotdry §迭代方差归一化: three to five iterations typical) ---
 
 def _iteration_changes(x, iters):
     """Largest |log factor change| of each iteration, recomputed from runs with fixed counts."""
