@@ -733,36 +733,39 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
   const int tid = threadIdx.x, warp = tid >> 5;
 
   // ---- this CTA's units (append mode: write every token first, keep the tiles that seal) ----
+  // Each warp takes every 8th of the CTA's units, so the dependent loads of different units
+  // (length, then token) overlap; the list order does not matter (units are independent).
   grid_launch_dependents();  // a dependent kernel still waits for this grid to complete
   if (tid == 0) *count = 0;
   __syncthreads();
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  const int lane = tid & 31;
+  constexpr int kWarps = kThreads / 32;
+  for (int u = blockIdx.x + gridDim.x * warp; u < units; u += gridDim.x * kWarps) {
     if (p.append) {
       const int h = (u >> 1) % p.num_kv_heads, b = (u >> 1) / p.num_kv_heads;
       const bool is_v = (u & 1) != 0;
       const int len = p.seq_lens[b];
       if (len < 0 || len >= p.max_pages * kTile) {
-        if (tid == 0 && !is_v && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
+        if (lane == 0 && !is_v && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
         continue;
       }
       __half* part = (is_v ? p.partial_v : p.partial_k) + ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
       const __half* nw = (is_v ? p.v_new : p.k_new) + ((int64_t)b * p.num_kv_heads + h) * p.d0;
-      for (int c = tid * 8; c < p.d0; c += kThreads * 8)
+      for (int c = lane * 8; c < p.d0; c += 32 * 8)
         *reinterpret_cast<uint4*>(part + (len % kTile) * p.d0 + c) = *reinterpret_cast<const uint4*>(nw + c);
-      if (tid == 0 && !is_v && h == 0 && p.seq_lens_out != nullptr) p.seq_lens_out[b] = len + 1;
+      if (lane == 0 && !is_v && h == 0 && p.seq_lens_out != nullptr) p.seq_lens_out[b] = len + 1;
       if (len % kTile != kTile - 1) continue;
     }
     const __half* src;
     int64_t ts;
     uint8_t* rec;
     if (!tc::unit_io(p, u, src, ts, rec)) {  // page id outside the pool: skip the unit
-      if (tid == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
+      if (lane == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
       continue;
     }
-    if (tid == 0) {
-      const int n = *count;
+    if (lane == 0) {
+      const int n = atomicAdd(count, 1);
       if (n < kListCap) list[n] = u;  // the grid is sized so that n stays below kListCap
-      *count = n + 1;
     }
   }
   __threadfence_block();
