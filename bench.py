@@ -327,6 +327,53 @@ def _quality(torch, kv, synth):
     }
 
 
+def _time_prefill(torch, kv, synth, batch=8, cache_len=8192, chunk=64, hq=32, hkv=8, d0=128, seed=7, reps=10):
+    """kvarn_prefill_attention: `chunk` new tokens per sequence over `cache_len` cached tokens
+    (sealed pages only) plus themselves, causal.  Returns median ms and the reported figures."""
+    dev = torch.device("cuda")
+    pages = cache_len // 128
+    desc = kv.desc_from_preset(d0, hkv)
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(batch * pages, generator=g).view(batch, pages).to(torch.int32).to(dev)
+    k, v = synth.outlier_kv(batch * cache_len, hkv, d0, seed=seed, device=dev)
+    pool = kv.alloc_pool(desc, batch * pages, device=dev)
+    kv.quantize_tiles(desc, k, v, table.reshape(-1).contiguous(), pool)
+    del k, v
+    q = torch.randn((batch, chunk, hq, d0), generator=g).half().to(dev)
+    ck = torch.randn((batch, chunk, hkv, d0), generator=g).half().to(dev)
+    cv = torch.randn((batch, chunk, hkv, d0), generator=g).half().to(dev)
+    out = torch.empty_like(q)
+    lens = torch.full((batch,), cache_len, dtype=torch.int32, device=dev)
+    ws = kv.alloc_prefill_workspace(desc, batch, hq, chunk, pages, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        kv.prefill_attention(desc, q, ck, cv, pool, table, lens, out, ws, status=status, stream=stream)
+    ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        kv.prefill_attention(desc, q, ck, cv, pool, table, lens, out, ws, status=status, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in prefill" % int(status.item()))
+    t = statistics.median(ms)
+    flops = 4.0 * batch * chunk * hq * (cache_len + (chunk + 1) / 2.0) * d0
+    cache_bytes = batch * pages * hkv * desc.page_record_bytes
+    del pool, ws
+    torch.cuda.empty_cache()
+    return {
+        "workload": "batch %d, %d new tokens each over %d cached tokens, %d q heads / %d kv heads, "
+                    "head_dim %d, K4V2" % (batch, chunk, cache_len, hq, hkv, d0),
+        "ms": t, "prefill_tokens_per_s": batch * chunk / (t * 1e-3),
+        "attention_tflops": flops / (t * 1e-3) / 1e12, "cache_bytes": cache_bytes,
+        "cache_gbs_once": cache_bytes / (t * 1e-3) / 1e9,
+    }
+
+
 def _decode_configs(torch, kv, synth, peak, args):
     """The 32B-class 64-layer decode step and the long-context shapes, each against bytes/peak."""
     res = {}
@@ -468,6 +515,8 @@ def _run_kvarn(args, torch, world, rank):
 
     # ---- the 32B-class step (64 layers, GQA 8) and the long-context shapes (not timed steps)
     extra = _decode_configs(torch, kv, synth, peak, args)
+    if args.extras in ("all", "prefill"):
+        extra["prefill"] = _time_prefill(torch, kv, synth)
     quality = _quality(torch, kv, synth)
 
     # ---- aggregate over ranks (replicas)
@@ -688,7 +737,7 @@ def main():
                     help="decode batch (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="CPU work of the oracle baseline sample (kvarn arm)")
-    ap.add_argument("--extras", choices=("all", "none", "32b", "long", "presets"), default="all",
+    ap.add_argument("--extras", choices=("all", "none", "32b", "long", "presets", "prefill"), default="all",
                     help="which of the 64-layer and long-context decode shapes to time")
     ap.add_argument("--extra-batch", type=int, default=0,
                     help="batch of those shapes (0 = the workload's; smaller only for profiling)")

@@ -383,8 +383,17 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   uint2* qhl = reinterpret_cast<uint2*>(smem_d + S::kRecBytes + S::kQBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kQhBytes);
 
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int h = blockIdx.y / p.vgroups, vg = blockIdx.y - h * p.vgroups;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // head slot hl of this CTA is query vector vh = vg * NH + hl of kv head h: chunk token
+  // vh / group, query head h * group + vh % group (decode: chunk 1, vh = group member)
+  const int n_vh = p.chunk * p.group;
+  auto valid = [&](int hl) { return vg * NH + hl < n_vh; };
+  auto vrow = [&](int hl) -> int64_t {
+    const int vh = vg * NH + hl;
+    return ((int64_t)b * p.chunk + vh / p.group) * p.num_q_heads + h * p.group + vh % p.group;
+  };
   const int g = lane >> 2, tq = lane & 3;
   grid_dependency_wait();  // lengths, partial tiles and pages come from the previous kernel
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
@@ -402,8 +411,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     return;
   }
 
-  float* part_base = p.part + ((int64_t)(b * p.num_q_heads + h * p.group) * p.max_splits + split) * (D + 4);
-  const int64_t head_stride = (int64_t)p.max_splits * (D + 4);
+  auto part_row = [&](int hl) { return p.part + (vrow(hl) * p.max_splits + split) * (D + 4); };
 
   if (!partial_split) {
     const int first = split * p.pages_per_split;
@@ -444,9 +452,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
 #pragma unroll
       for (int e = 0; e < D / 32; ++e) {
         const int j = lane * (D / 32) + e;
-        v[e] = (hl < p.group && j < p.d0)
-                   ? __half2float(p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + j])
-                   : 0.0f;
+        v[e] = (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) : 0.0f;
       }
       warp_fwht<D>(v, lane);
       const float sc = p.qscale * inv_sqrt_d<D>();
@@ -535,8 +541,9 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < NH * D; idx += blockDim.x) {
       const int hl = idx / D, j = idx - hl * D;
+      if (!valid(hl)) continue;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mS[w * NH + hl]);
@@ -547,7 +554,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
         o = fmaf(sc, oS[(w * NH + hl) * D + j], o);
         l = fmaf(sc, lS[w * NH + hl], l);
       }
-      float* dst = part_base + hl * head_stride;
+      float* dst = part_row(hl);
       dst[4 + j] = o;
       if (j == 0) {
         dst[0] = M;
@@ -563,8 +570,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     for (int e = 0; e < D / 32; ++e) {
       const int j = lane * (D / 32) + e;
       qsm[hl * QLD + j] =
-          (hl < p.group && j < p.d0)
-              ? __half2float(p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + j]) * p.qscale
+          (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) * p.qscale
               : 0.0f;
     }
   }
@@ -590,7 +596,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       }
 #pragma unroll
       for (int hl = 0; hl < NH; ++hl) {
-        if (hl >= p.group) break;
+        if (!valid(hl)) break;
         float dot = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; ++e) dot = fmaf(qsm[hl * QLD + lane + 32 * e], kv[e], dot);
@@ -618,7 +624,8 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     }
     __syncthreads();
     // merge warps, rotate o into the basis of the sealed splits, store
-    for (int hl = warp; hl < p.group; hl += kDecWarps) {
+    for (int hl = warp; hl < NH; hl += kDecWarps) {
+      if (!valid(hl)) break;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mS[w * NH + hl]);
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
         for (int e = 0; e < E; ++e) v[e] = fmaf(sc, oS[(w * NH + hl) * D + lane * E + e], v[e]);
       }
       warp_fwht<D>(v, lane);
-      float* dst = part_base + hl * head_stride;
+      float* dst = part_row(hl);
 #pragma unroll
       for (int e = 0; e < E; ++e) dst[4 + lane * E + e] = v[e] * inv_sqrt_d<D>();
       if (lane == 0) {
@@ -644,20 +651,22 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   }
 }
 
-// One warp per (sequence, query head): merge the splits, normalise, undo the rotation.
+// One warp per (sequence, chunk token, query head): merge the splits, normalise, undo the
+// rotation.
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  grid_dependency_wait();  // the split partials of decode_kernel
-  if (gw >= p.batch * p.num_q_heads) return;
-  const int b = gw / p.num_q_heads;
+  grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
+  if (gw >= p.batch * p.chunk * p.num_q_heads) return;
+  const int b = gw / (p.chunk * p.num_q_heads);
   const int cap = p.max_pages * kTile + (kTile - 1);
   int len = p.seq_lens[b];
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_sealed = len / kTile;
-  const int n_splits = (n_sealed + p.pages_per_split - 1) / p.pages_per_split + (len % kTile > 0 ? 1 : 0);
+  const int n_splits = (n_sealed + p.pages_per_split - 1) / p.pages_per_split + (len % kTile > 0 ? 1 : 0) +
+                       (p.chunk_k != nullptr ? 1 : 0);
   float v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) v[e] = 0.0f;
@@ -722,19 +731,98 @@ static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.max_splits, p.num_kv_heads, p.batch);
+  cfg.gridDim = dim3(p.max_splits, p.num_kv_heads * p.vgroups, p.batch);
   cfg.blockDim = dim3(S::kWarps * 32);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess) return KVARN_ERR_CUDA;
-  const int warps = p.batch * p.num_q_heads;
+  const int warps = p.batch * p.chunk * p.num_q_heads;
   cfg.gridDim = dim3((warps + 3) / 4);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   if (cudaLaunchKernelEx(&cfg, combine_kernel<D>, p) != cudaSuccess) return KVARN_ERR_CUDA;
   return KVARN_OK;
+}
+
+// Causal attention of each chunk query to the chunk's own raw fp16 tokens (prefill): one
+// warp per (sequence, chunk token c, query head), tokens 0..c, original basis, online
+// softmax in the log2 domain; the unnormalised output is rotated and written as the split
+// after the cache's splits [vatt §四個步驟: the rotation keeps q.k unchanged, so partials in
+// the rotated basis merge with the cache's].
+template <int D>
+__global__ void __launch_bounds__(128) chunk_kernel(DecodeParams p) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  grid_dependency_wait();
+  if (gw >= p.batch * p.chunk * p.num_q_heads) return;
+  const int hq = gw % p.num_q_heads, bc = gw / p.num_q_heads;
+  const int b = bc / p.chunk, c = bc - b * p.chunk;
+  const int h = hq / p.group;
+  float q[E], o[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int j = lane * E + e;
+    q[e] = j < p.d0 ? __half2float(p.q[(int64_t)gw * p.d0 + j]) * p.qscale : 0.0f;
+    o[e] = 0.0f;
+  }
+  float m = -INFINITY, l = 0.0f;
+  for (int t = 0; t <= c; ++t) {
+    const int64_t row = (((int64_t)b * p.chunk + t) * p.num_kv_heads + h) * p.d0;
+    float dot = 0.0f;
+    float vv[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int j = lane * E + e;
+      const float kx = j < p.d0 ? __half2float(p.chunk_k[row + j]) : 0.0f;
+      vv[e] = j < p.d0 ? __half2float(p.chunk_v[row + j]) : 0.0f;
+      dot = fmaf(q[e], kx, dot);
+    }
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, msk);
+    const float mnew = fmaxf(m, dot);
+    const float a = exp2f(m - mnew), pv = exp2f(dot - mnew);
+    m = mnew;
+    l = fmaf(l, a, pv);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] = fmaf(o[e], a, pv * vv[e]);
+  }
+  warp_fwht<D>(o, lane);
+  const int cap = p.max_pages * kTile + (kTile - 1);
+  int len = p.seq_lens[b];
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int split = (len / kTile + p.pages_per_split - 1) / p.pages_per_split + (len % kTile > 0 ? 1 : 0);
+  float* dst = p.part + ((int64_t)gw * p.max_splits + split) * (D + 4);
+#pragma unroll
+  for (int e = 0; e < E; ++e) dst[4 + lane * E + e] = o[e] * inv_sqrt_d<D>();
+  if (lane == 0) {
+    dst[0] = m;
+    dst[1] = l;
+  }
+}
+
+template <int D>
+static int launch_chunk_t(const DecodeParams& p, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  const int warps = p.batch * p.chunk * p.num_q_heads;
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_kernel<D>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
+int launch_chunk_any(int d, const DecodeParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_chunk_t<64>(p, stream);
+  if (d == 128) return launch_chunk_t<128>(p, stream);
+  if (d == 256) return launch_chunk_t<256>(p, stream);
+  return KVARN_ERR_UNSUPPORTED;
 }
 
 template <int KB, int VB>

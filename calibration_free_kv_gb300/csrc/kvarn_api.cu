@@ -227,9 +227,79 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
   p.d0 = desc->head_dim;
   p.pages_per_split = pps;
   p.max_splits = (max_pages + pps - 1) / pps + 1;
+  p.chunk = 1;
+  p.vgroups = 1;
   p.status = dev_status;
   return launch_decode_any(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p,
                            static_cast<cudaStream_t>(stream));
+}
+
+size_t kvarn_prefill_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
+                                     int chunk_len, int max_pages) {
+  if (check_desc(desc) != KVARN_OK || batch < 0 || num_q_heads < 1 || chunk_len < 1 || max_pages < 1)
+    return 0;
+  const int pps = decode_pages_per_split(max_pages);
+  const int64_t max_splits = (max_pages + pps - 1) / pps + 2;  // + partial tile + chunk
+  return (size_t)batch * chunk_len * num_q_heads * max_splits * (desc->head_dim_padded + 4) *
+         sizeof(float);
+}
+
+int kvarn_prefill_attention(const kvarn_desc* desc, int batch, int num_q_heads, int chunk_len,
+                            const void* q, const void* chunk_k, const void* chunk_v,
+                            const void* page_pool, int64_t num_pool_pages,
+                            const int32_t* block_table, int max_pages, const int32_t* cache_lens,
+                            const void* partial_k, const void* partial_v, float softmax_scale,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream) {
+  int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || num_q_heads < 1 || max_pages < 1 || chunk_len < 1) return KVARN_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return KVARN_ERR_UNSUPPORTED;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (!(group == 1 || group == 2 || group == 4 || group == 8)) return KVARN_ERR_UNSUPPORTED;
+  // query vectors of a kv head per CTA: 8 (4 at head_dim 256)
+  const int nt = desc->head_dim_padded <= 128 ? 2 : 1;
+  const int64_t vgroups = ((int64_t)chunk_len * group + 4 * nt - 1) / (4 * nt);
+  if (vgroups * desc->num_kv_heads > 65535 || (int64_t)batch > 65535) return KVARN_ERR_UNSUPPORTED;
+  if (batch == 0) return KVARN_OK;
+  if (q == nullptr || chunk_k == nullptr || chunk_v == nullptr || page_pool == nullptr ||
+      block_table == nullptr || cache_lens == nullptr || out == nullptr || workspace == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(page_pool) || !aligned16(workspace)) return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1 || !(softmax_scale > 0.0f)) return KVARN_ERR_INVALID_ARG;
+  const size_t need = kvarn_prefill_workspace_bytes(desc, batch, num_q_heads, chunk_len, max_pages);
+  if (workspace_bytes < need) return KVARN_ERR_WORKSPACE_TOO_SMALL;
+  const int pps = decode_pages_per_split(max_pages);
+  DecodeParams p{};
+  p.q = static_cast<const __half*>(q);
+  p.pool = static_cast<const uint8_t*>(page_pool);
+  p.num_pool_pages = num_pool_pages;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.seq_lens = cache_lens;
+  p.partial_k = static_cast<const __half*>(partial_k);
+  p.partial_v = static_cast<const __half*>(partial_v);
+  p.qscale = softmax_scale * kLog2e;
+  p.out = static_cast<__half*>(out);
+  p.part = static_cast<float*>(workspace);
+  p.batch = batch;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.num_q_heads = num_q_heads;
+  p.group = group;
+  p.d0 = desc->head_dim;
+  p.pages_per_split = pps;
+  p.max_splits = (max_pages + pps - 1) / pps + 2;
+  p.chunk = chunk_len;
+  p.vgroups = (int)vgroups;
+  p.chunk_k = static_cast<const __half*>(chunk_k);
+  p.chunk_v = static_cast<const __half*>(chunk_v);
+  p.status = dev_status;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the chunk's causal part first (its own split slot), then the cache splits and the merge
+  st = launch_chunk_any(desc->head_dim_padded, p, s);
+  if (st != KVARN_OK) return st;
+  return launch_decode_any(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p, s);
 }
 
 int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_t num_pool_pages,

@@ -49,9 +49,16 @@ struct DecodeParams {
   const __half* partial_v;
   float qscale;  // softmax_scale * log2(e)
   __half* out;
-  float* part;   // [batch][Hq][max_splits][D + 4]: m, l, -, -, o~[D]
+  float* part;   // [batch][chunk][Hq][max_splits][D + 4]: m, l, -, -, o~[D]
   int batch, num_kv_heads, num_q_heads, group, d0;
   int pages_per_split, max_splits;
+  // Prefill: `chunk` query tokens per sequence (1 for decode), q / out [batch][chunk][Hq][d0].
+  // The chunk * group query vectors of a kv head are split into `vgroups` CTAs of up to
+  // 4 * NT each; chunk_k / chunk_v [batch][chunk][Hkv][d0] (NULL for decode) are attended
+  // causally by the chunk kernel, whose partial is the split after the cache's.
+  int chunk, vgroups;
+  const __half* chunk_k;
+  const __half* chunk_v;
   int32_t* status;
 };
 
@@ -68,6 +75,7 @@ struct DequantParams {
 
 int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int units, cudaStream_t stream);
 int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream);
+int launch_chunk_any(int d, const DecodeParams& p, cudaStream_t stream);
 int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pages, cudaStream_t stream);
 
 }  // namespace kvarn

@@ -34,6 +34,8 @@ EXPORTED_SYMBOLS = (
     "kvarn_append_token",
     "kvarn_decode_workspace_bytes",
     "kvarn_decode_attention",
+    "kvarn_prefill_workspace_bytes",
+    "kvarn_prefill_attention",
     "kvarn_dequantize_tiles",
     "kvarn_status_string",
     "kvarn_decode_attention_noalloc",
@@ -81,6 +83,9 @@ def _load():
         "kvarn_decode_attention": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P, ctypes.c_float,
                                          P, P, ctypes.c_size_t, P, P]),
         "kvarn_dequantize_tiles": (i32, [D, P, i64, P, i32, P, P, P, P]),
+        "kvarn_prefill_workspace_bytes": (ctypes.c_size_t, [D, i32, i32, i32, i32]),
+        "kvarn_prefill_attention": (i32, [D, i32, i32, i32, P, P, P, P, i64, P, i32, P, P, P,
+                                          ctypes.c_float, P, P, ctypes.c_size_t, P, P]),
         "kvarn_status_string": (ctypes.c_char_p, [i32]),
         "kvarn_decode_attention_noalloc": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P,
                                                  ctypes.c_float, P, P, P]),
@@ -210,6 +215,36 @@ def decode_attention(desc: KvarnDesc, q, pool, block_table, seq_lens, out, works
                                        float(softmax_scale), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _ptr(status), _stream(stream)), "kvarn_decode_attention")
+
+
+def prefill_workspace_bytes(desc: KvarnDesc, batch: int, num_q_heads: int, chunk_len: int,
+                            max_pages: int) -> int:
+    return int(_lib.kvarn_prefill_workspace_bytes(ctypes.byref(desc), batch, num_q_heads, chunk_len,
+                                                  max_pages))
+
+
+def alloc_prefill_workspace(desc: KvarnDesc, batch: int, num_q_heads: int, chunk_len: int,
+                            max_pages: int, device="cuda"):
+    n = prefill_workspace_bytes(desc, batch, num_q_heads, chunk_len, max_pages)
+    return torch.empty((max(n, 16) + 15) // 16 * 4, dtype=torch.float32, device=device)
+
+
+def prefill_attention(desc: KvarnDesc, q, chunk_k, chunk_v, pool, block_table, cache_lens, out,
+                      workspace, partial_k=None, partial_v=None, softmax_scale=None, status=None,
+                      stream=None):
+    """q, out: fp16 [batch, chunk, Hq, d0]; chunk_k/v: fp16 [batch, chunk, Hkv, d0];
+    cache_lens: int32 [batch] tokens already cached (sealed pages + partial tile)."""
+    batch, chunk, hq, d0 = q.shape
+    if chunk_k.shape != (batch, chunk, desc.num_kv_heads, d0) or chunk_v.shape != chunk_k.shape:
+        raise ValueError("chunk_k / chunk_v must be [batch, chunk, Hkv, d0]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d0)
+    _check(_lib.kvarn_prefill_attention(ctypes.byref(desc), batch, hq, chunk, _ptr(q), _ptr(chunk_k),
+                                        _ptr(chunk_v), _ptr(pool), pool.shape[0], _ptr(block_table),
+                                        block_table.shape[1], _ptr(cache_lens), _ptr(partial_k),
+                                        _ptr(partial_v), float(softmax_scale), _ptr(out),
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        _ptr(status), _stream(stream)), "kvarn_prefill_attention")
 
 
 def decode_attention_noalloc(desc: KvarnDesc, q, pool, block_table, seq_lens, out, partial_k=None,

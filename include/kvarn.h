@@ -173,6 +173,29 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
 /* Size of the fixed device buffer used by kvarn_decode_attention_noalloc (16 MiB). */
 #define KVARN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 
+/* Workspace bytes kvarn_prefill_attention needs for this shape (host only; 0 if invalid). */
+size_t kvarn_prefill_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
+                                     int chunk_len, int max_pages);
+
+/* Chunked-prefill attention: a chunk of chunk_len new tokens per sequence attends to the
+ * packed cache and, causally, to itself (the step before decode; the cache side reads the
+ * same packed pages as decode [vatt §怎麼用: one block == one tile]).  Query token c of
+ * sequence b attends to the cache_lens[b] cached tokens (sealed pages + raw partial tile)
+ * and to chunk tokens 0..c.
+ *  q            fp16 [batch][chunk_len][Hq][d0];  out fp16 [batch][chunk_len][Hq][d0].
+ *  chunk_k/v    fp16 [batch][chunk_len][Hkv][d0]: the chunk's own keys and values (raw; quantise
+ *               them into the cache afterwards with kvarn_quantize_tiles / kvarn_append_token).
+ *  cache_lens   device int32 [batch]: cached tokens before the chunk (as seq_lens of decode).
+ *  Other arguments as kvarn_decode_attention; workspace >= kvarn_prefill_workspace_bytes.
+ *  UNSUPPORTED if chunk_len * G / 8 (/ 4 at head_dim 256) * Hkv exceeds 65535. */
+int kvarn_prefill_attention(const kvarn_desc* desc, int batch, int num_q_heads, int chunk_len,
+                            const void* q, const void* chunk_k, const void* chunk_v,
+                            const void* page_pool, int64_t num_pool_pages,
+                            const int32_t* block_table, int max_pages, const int32_t* cache_lens,
+                            const void* partial_k, const void* partial_v, float softmax_scale,
+                            void* out, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream);
+
 /* kvarn_decode_attention without a workspace argument, for callers that cannot allocate
  * device memory: plugins in engines that plan and own all device memory in advance, code
  * that must not call cudaMalloc on the decode path (it may synchronise the device), and

@@ -462,6 +462,42 @@ def decode_sequence(q_heads: np.ndarray, records, partial_k, partial_v,
                      for qh in np.asarray(q_heads, dtype=np.float64)])
 
 
+def prefill_sequence(q: np.ndarray, records, partial_k, partial_v, chunk_k: np.ndarray,
+                     chunk_v: np.ndarray, softmax_scale: float, d0: int,
+                     k_bits: int = K_BITS, v_bits: int = V_BITS) -> np.ndarray:
+    """Chunked-prefill attention of one sequence for the query heads of ONE kv head.
+
+    q: [C, G, d0] queries of the chunk's C tokens; chunk_k / chunk_v: [C, d0] the chunk's own
+    raw keys and values.  Query token c attends to every cached token (the dequantised sealed
+    pages, then the raw partial-tile tokens) and to chunk tokens 0..c: textbook causal
+    attention over the concatenation, in the original basis.  Returns [C, G, d0].
+    [vatt §怎麼用: the paged blocks hold the quantised cache; the step before decode reads
+     the same cache]
+    Pinned by: test_prefill_* (single token == decode with it appended, causal invariance,
+    full-precision cache limit).
+    """
+    ks, vs = [], []
+    for rec in records:
+        kh, vh = dequantize_record(rec, d0, k_bits, v_bits)
+        ks.append(kh)
+        vs.append(vh)
+    if partial_k is not None and len(partial_k):
+        ks.append(np.asarray(partial_k, dtype=np.float64)[:, :d0])
+        vs.append(np.asarray(partial_v, dtype=np.float64)[:, :d0])
+    cache_k = np.concatenate(ks, axis=0) if ks else np.zeros((0, d0))
+    cache_v = np.concatenate(vs, axis=0) if vs else np.zeros((0, d0))
+    ck = np.asarray(chunk_k, dtype=np.float64)[:, :d0]
+    cv = np.asarray(chunk_v, dtype=np.float64)[:, :d0]
+    q = np.asarray(q, dtype=np.float64)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for c in range(q.shape[0]):
+        keys = np.concatenate([cache_k, ck[:c + 1]], axis=0)
+        vals = np.concatenate([cache_v, cv[:c + 1]], axis=0)
+        for g in range(q.shape[1]):
+            out[c, g] = softmax_attention(q[c, g], keys, vals, softmax_scale)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # byte accounting
 # ----------------------------------------------------------------------------

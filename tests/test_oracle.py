@@ -669,3 +669,50 @@ def test_tiny_quality_figure():
     cos = float(o[0] @ ref / np.linalg.norm(o[0]) / np.linalg.norm(ref))
     print("tiny attention-output cosine vs fp16 cache: %.5f" % cos)
     assert cos > 0.9
+
+
+# --- chunked prefill (the step before decode over the same packed cache) -------------------
+
+def _small_cache(seed, pages, part):
+    k, v = synth.outlier_kv(128 * pages + part, 1, 128, seed=seed)
+    recs = [ko.quantize_page(k[128 * i:128 * i + 128, 0].double().numpy(),
+                             v[128 * i:128 * i + 128, 0].double().numpy())[0] for i in range(pages)]
+    pk = k[128 * pages:, 0].double().numpy()
+    pv = v[128 * pages:, 0].double().numpy()
+    return recs, pk, pv
+
+
+def test_prefill_single_token_is_decode_with_it_appended():
+    recs, pk, pv = _small_cache(70, 2, 5)
+    rng = np.random.default_rng(70)
+    q = rng.standard_normal((1, 3, 128))
+    ck, cv = rng.standard_normal((1, 128)), rng.standard_normal((1, 128))
+    got = ko.prefill_sequence(q, recs, pk, pv, ck, cv, 0.09, 128)
+    want = ko.decode_sequence(q[0], recs, np.concatenate([pk, ck]), np.concatenate([pv, cv]), 0.09, 128)
+    np.testing.assert_allclose(got[0], want, rtol=0, atol=1e-12)
+
+
+def test_prefill_is_causal():
+    # changing chunk token t changes no output before t, and changes the output at t
+    recs, pk, pv = _small_cache(71, 1, 0)
+    rng = np.random.default_rng(71)
+    q = rng.standard_normal((6, 2, 128))
+    ck, cv = rng.standard_normal((6, 128)), rng.standard_normal((6, 128))
+    a = ko.prefill_sequence(q, recs, pk, pv, ck, cv, 0.1, 128)
+    ck2, cv2 = ck.copy(), cv.copy()
+    ck2[3] = 400.0 * q[3, 0] / np.linalg.norm(q[3, 0])   # dominates query 3's first head
+    cv2[3] -= 3.0
+    b = ko.prefill_sequence(q, recs, pk, pv, ck2, cv2, 0.1, 128)
+    np.testing.assert_array_equal(a[:3], b[:3])
+    assert np.abs(a[3:] - b[3:]).max() > 1e-3
+
+
+def test_prefill_empty_cache_is_causal_self_attention():
+    # with nothing cached, token c attends to chunk tokens 0..c only: token 0 returns v_0
+    rng = np.random.default_rng(72)
+    q = rng.standard_normal((4, 1, 64))
+    ck, cv = rng.standard_normal((4, 64)), rng.standard_normal((4, 64))
+    out = ko.prefill_sequence(q, [], None, None, ck, cv, 0.125, 64)
+    np.testing.assert_allclose(out[0, 0], cv[0], rtol=0, atol=1e-12)
+    w = np.exp(0.125 * ck[:3] @ q[2, 0] - (0.125 * ck[:3] @ q[2, 0]).max())
+    np.testing.assert_allclose(out[2, 0], (w / w.sum()) @ cv[:3], rtol=1e-12, atol=1e-12)
