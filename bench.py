@@ -76,6 +76,17 @@ def _dist_env():
     return world, rank, local
 
 
+def _aggregate_over_ranks(torch, world, per_rank_ms, tokens_per_rank, device):
+    """Whole-job throughput of `world` independent replicas: every timing is the maximum over
+    ranks (the slowest replica ends the job) and the tokens are those of all ranks.
+    Returns (max timings in ms, throughputs per second)."""
+    t = torch.tensor([float(x) for x in per_rank_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = [float(x) for x in t]
+    return ms, [world * tok / (m * 1e-3) for tok, m in zip(tokens_per_rank, ms)]
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
 
@@ -520,12 +531,8 @@ def _run_kvarn(args, torch, world, rank):
     quality = _quality(torch, kv, synth)
 
     # ---- aggregate over ranks (replicas)
-    if world > 1:
-        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
-    value = world * tokens / (elapsed_ms * 1e-3)
-    e2e_value = world * e2e_tokens / (e2e_ms * 1e-3)
+    (elapsed_ms, e2e_ms), (value, e2e_value) = _aggregate_over_ranks(
+        torch, world, [elapsed_ms, e2e_ms], [tokens, e2e_tokens], dev)
     if rank != 0:
         return None
     return {
