@@ -64,6 +64,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t r;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
@@ -257,13 +263,13 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const float mnew = fmaxf(st.m[nt], mx);
-    alpha[nt] = exp2f(st.m[nt] - mnew);
+    alpha[nt] = ex2_approx(st.m[nt] - mnew);
     st.m[nt] = mnew;
     float2 ps = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int mi = 0; mi < 8; ++mi) {
       const float2 d = sub2(make_float2(lg[mi][nt][0], lg[mi][nt][1]), make_float2(mnew, mnew));
-      const float2 pv = make_float2(exp2f(d.x), exp2f(d.y));
+      const float2 pv = make_float2(ex2_approx(d.x), ex2_approx(d.y));
       lg[mi][nt][0] = pv.x;
       lg[mi][nt][1] = pv.y;
       ps = add2(ps, pv);
