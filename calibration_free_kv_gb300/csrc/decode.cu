@@ -1,4 +1,4 @@
-// KVarN paged decode attention over the packed K4/V2 cache (sm_103a).
+// KVarN paged decode (and chunked-prefill) attention over the packed cache (sm_103a).
 //
 // Math (rotated basis, R = H_d / sqrt(d) orthonormal and symmetric):
 //   logit_t = tau q . K_t = tau (qR) . (K_t R) = tau r_t ( sum_j q~_j s'_j code_tj + sum_j q~_j z'_j )
@@ -6,24 +6,27 @@
 // [vatt §四個步驟: the rotation is orthonormal so attention scores are unchanged;
 //  hotdry §非对称量化与尺度折叠: the folded scales are multiplied back at read time]
 //
-// decode_kernel: grid (split, kv head, sequence).  A CTA owns up to `pages_per_split` sealed
-// pages of one (sequence, kv head), or the raw fp16 partial tile.  Its 8 warps take whole
-// pages round-robin.  Every warp owns two shared-memory slots, one for the K half of a page
+// decode_kernel: grid (split, kv head x query block, sequence).  A CTA owns up to
+// `pages_per_split` sealed pages of one (sequence, kv head), or the raw fp16 partial tile, for
+// up to 4 * NT query vectors of that kv head (decode: its G query heads; prefill: blocks of
+// the chunk's C * G query vectors).  Its warps (8, or 4 where 8 page slots do not fit) take
+// whole pages round-robin.  Every warp owns two shared-memory slots, one for the K half of a page
 // record and one for the V half, each filled by a 1-D bulk copy completed on its own
 // mbarrier: the K half of the next page streams in while the warp works on the current
 // page's V half, and the V half of the next page while it works on the next K half.
-//   QK:  m16n8k16 MMAs, A = 4-bit codes [token x channel], B = q~ . s'_K split into fp16
+//   QK:  m16n8k16 MMAs, A = codes [token x channel] (4- or 2-bit), B = q~ . s'_K split into fp16
 //        hi + lo (columns: 4 heads x {hi, lo}); hi = fp16(qh s'), lo = fp16(ql s' + (qh s' -
 //        hi)) with q~ = qh + ql pre-split once per CTA and the product error taken exactly
 //        by an fp16 fma.
 //   softmax: online, log2 domain (tau log2(e) folded into q~).
-//   PV:  m16n8k16 MMAs, A = 2-bit codes^T [channel x token], B = p . s'_V split hi + lo,
+//   PV:  m16n8k16 MMAs, A = codes^T [channel x token] (2- or 4-bit), B = p . s'_V split hi + lo,
 //        moved from the QK accumulator layout with movmatrix.trans.
 // Codes enter the MMAs as exact fp16 subnormals: masking a code into the low mantissa bits
 // of a zero exponent gives code * 2^-24 (code * 2^-22 .. 2^-18 for higher bit positions), so
 // unpacking costs one AND per two codes; the powers of two are folded into B and into the
 // fp32 results.  The CTA merges its warps and writes (m, l, unnormalised o~) for its split;
 // combine_kernel merges the splits, divides by l, undoes the rotation and stores fp16.
+// chunk_kernel adds the causal part of a prefill chunk as one more split.
 #include "common.cuh"
 #include "params.cuh"
 
@@ -98,14 +101,6 @@ __device__ __forceinline__ void unpack_v(uint32_t x, uint32_t (&a0)[4], uint32_t
   a1[2] = x & 0x00C000C0u;
   a1[1] = y & 0x00300030u;
   a1[3] = y & 0x00C000C0u;
-}
-
-// fp32 pair -> fp16 hi (lo == false) or lo = x - hi (lo == true); hi + lo ~ x to ~22 bits.
-__device__ __forceinline__ uint32_t split_pick(float x0, float x1, bool lo) {
-  const __half2 hi = __floats2half2_rn(x0, x1);
-  const float2 hf = __half22float2(hi);
-  const __half2 lw = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-  return h2u(lo ? lw : hi);
 }
 
 // Walsh-Hadamard transform of D values spread over a warp, lane holding D/32 consecutive.

@@ -1,14 +1,19 @@
 // KVarN tile quantisation: rotate, variance-normalise, round, fold, pack (sm_103a).
 //
-// One CTA quantises one (tile, kv head, K-or-V) unit of 128 tokens x d channels.
+// Each (tile, kv head, K-or-V) unit of 128 tokens x d channels is quantised by one CTA
+// (quantize_tc_kernel, d = 128: persistent CTAs walking a list of units; quantize_kernel,
+// d = 64 / 256: one CTA per unit).
 //  1. rotate: every token row is zero-padded to d and multiplied by H_d / sqrt(d)
-//     [hotdry §Hadamard 旋转: FWHT, fused with the normalisation in one kernel]
-//  2. normalise: channel-std step then token-std step, `iters` times; the log-space factor
-//     updates of the pages telescope, so the kernel keeps the factors themselves
-//     (f_new = 1 / std of the un-normalised axis; unchanged when the std is below eps)
-//     [hotdry §迭代方差归一化; vatt §四個步驟, Sinkhorn paragraph]
-//  3. asymmetric RTN: K 4-bit per channel over tokens, V 2-bit per token over channels;
-//     normalisation factors folded into the fp16 scale/zero [hotdry §非对称量化与尺度折叠]
+//     [hotdry §Hadamard 旋转]: tcgen05.mma against H_128 (d = 128) or an FWHT in shared
+//     memory (d = 64, 256)
+//  2. normalise: channel-std step then token-std step, `iters` times (or fewer with an
+//     early-stop tolerance); the log-space factor updates of the pages telescope, so the
+//     kernel keeps the factors themselves (f_new = 1 / std of the un-normalised axis;
+//     unchanged when the std is below eps) [hotdry §迭代方差归一化; vatt §四個步驟, Sinkhorn
+//     paragraph]
+//  3. asymmetric RTN: K per channel over tokens, V per token over channels (4 / 2 bits for
+//     kvarn_k4v2_g128, other widths for the other presets); normalisation factors folded into
+//     the fp16 scale/zero [hotdry §非对称量化与尺度折叠]
 //  4. codes packed as m16n8k16 A-operand fragments (layout in kvarn.h).
 //
 // Thread layout.  The unit is viewed as L x C: K has L = tokens, C = channels; V is held
