@@ -288,3 +288,10 @@ def test_decode_32b_layer_sampled(kv):
         ref = ko.decode_sequence(q[b, h * group:(h + 1) * group].double().numpy(), rl, None, None, scale, d0)
         err = H.assert_decode_close(got[b, h * group:(h + 1) * group], ref, "32B layer b=%d h=%d" % (b, h))
         print("32B layer b=%d h=%d: max scaled err %.2e" % (b, h, err))
+
+
+def test_decode_longest_block_table(kv):
+    # 1024-page block tables (131072 tokens): one sequence with a 77-token partial tile, one
+    # exactly full; 32 splits plus the partial tile reach the combine step
+    err = _run_oracle_cache_case(kv, 2, 1, 4, 128, [1024 * 128 + 77, 1024 * 128], seed=11)
+    print("1024 pages: max scaled err %.2e" % err)
