@@ -127,6 +127,43 @@ __device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
   }
 }
 
+// E consecutive fp16 / fp32 values from shared memory (8, 16 or 32 bytes, aligned) as floats.
+template <int E>
+__device__ __forceinline__ void load_f16(const __half* src, float (&f)[E]) {
+  static_assert(E == 2 || E == 4 || E == 8, "2, 4 or 8 halves");
+  if constexpr (E == 2) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(src));
+    f[0] = a.x;
+    f[1] = a.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < E / 4; ++i) {
+      const uint2 u = reinterpret_cast<const uint2*>(src)[i];
+      const float2 a = __half22float2(u2h2(u.x)), c = __half22float2(u2h2(u.y));
+      f[4 * i] = a.x;
+      f[4 * i + 1] = a.y;
+      f[4 * i + 2] = c.x;
+      f[4 * i + 3] = c.y;
+    }
+  }
+}
+template <int E>
+__device__ __forceinline__ void load_f32(const float* src, float (&f)[E]) {
+  if constexpr (E % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < E / 4; ++i) {
+      const float4 a = reinterpret_cast<const float4*>(src)[i];
+      f[4 * i] = a.x;
+      f[4 * i + 1] = a.y;
+      f[4 * i + 2] = a.z;
+      f[4 * i + 3] = a.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) f[e] = src[e];
+  }
+}
+
 template <int D>
 __device__ __forceinline__ float inv_sqrt_d() {
   return D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
@@ -566,88 +603,150 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   }
 
   // ---- partial tile: raw fp16 tokens in the original basis ---------------------------------
+  // The n_part rows of K and of V are contiguous for one (sequence, kv head): two bulk copies
+  // bring them into the page-slot area, then logits, softmax and PV run from shared memory.
+  // Layout there: K rows [0, 256 D), V rows [256 D, 512 D) (row stride d0), probabilities
+  // [t][NH] after them, then the head maxima and sums; the PV warp sums later overlay K.
+  constexpr int E = D / 32;   // channels per lane, lane-contiguous
+  constexpr int R = 32 / NH;  // tokens per logit round: 32 (token, head slot) pairs
+  static_assert(S::kRecBytes >= 512 * D + 4 * NH * (kTile + 2), "partial tile fits the page slots");
+  static_assert(kDecWarps * NH * D * 4 <= 256 * D, "PV warp sums fit over the K rows");
+  const __half* Ks = reinterpret_cast<const __half*>(recs);
+  const __half* Vs = reinterpret_cast<const __half*>(recs + 256 * D);
+  float* pS = reinterpret_cast<float*>(recs + 512 * D);
+  float* mS = pS + kTile * NH;
+  float* lS = mS + NH;
+  const int c0 = lane * E;
+  const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
+  if (threadIdx.x == 0) {
+    const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
+    const uint32_t bytes = (uint32_t)(n_part * p.d0 * 2);  // a multiple of 16
+    mbar_init(bars, 1);
+    fence_mbar_init();
+    mbar_expect_tx(bars, 2 * bytes);
+    bulk_copy_g2s(recs, p.partial_k + base, bytes, bars);
+    bulk_copy_g2s(recs + 256 * D, p.partial_v + base, bytes, bars);
+  }
   for (int hl = warp; hl < NH; hl += kDecWarps) {
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      const int j = lane * (D / 32) + e;
+    for (int e = 0; e < E; ++e) {
+      const int j = c0 + e;
       qsm[hl * QLD + j] =
-          (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) * p.qscale
-              : 0.0f;
+          (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) * p.qscale : 0.0f;
     }
   }
-  __syncthreads();
-  {
-    constexpr int E = D / 32;
-    float m[NH], l[NH], acc[NH][E];
-#pragma unroll
-    for (int hl = 0; hl < NH; ++hl) {
-      m[hl] = -INFINITY;
-      l[hl] = 0.0f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[hl][e] = 0.0f;
+  __syncthreads();  // q staged, the barrier initialised
+  if (!__syncthreads_and(mbar_wait(bars, 0) ? 1 : 0)) {
+    if (threadIdx.x == 0) {
+      flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+      mbar_wait(bars, 0);  // the copies may still land: wait (bounded) before leaving
     }
-    const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
-    for (int t = warp; t < n_part; t += kDecWarps) {
-      float kv[E], vv[E];
+    return;
+  }
+  // logits: each lane sums its E channels for the 32 pairs of a round, then a halving
+  // butterfly leaves pair i = r * NH + hl complete in lane i
+  for (int tb = warp; tb * R < n_part; tb += kDecWarps) {
+    float v[32];
+    float qv[NH][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const int j = lane + 32 * e;
-        kv[e] = j < p.d0 ? __half2float(p.partial_k[base + (int64_t)t * p.d0 + j]) : 0.0f;
-        vv[e] = j < p.d0 ? __half2float(p.partial_v[base + (int64_t)t * p.d0 + j]) : 0.0f;
+    for (int hl = 0; hl < NH; ++hl) load_f32<E>(qsm + hl * QLD + c0, qv[hl]);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int t = tb * R + r;
+      float kf[E];
+      if (t < n_part && in) {
+        load_f16<E>(Ks + t * p.d0 + c0, kf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) kf[e] = 0.0f;
       }
 #pragma unroll
       for (int hl = 0; hl < NH; ++hl) {
-        if (!valid(hl)) break;
-        float dot = 0.0f;
+        float acc = 0.0f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) dot = fmaf(qsm[hl * QLD + lane + 32 * e], kv[e], dot);
-#pragma unroll
-        for (int msk = 16; msk > 0; msk >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, msk);
-        const float mnew = fmaxf(m[hl], dot);
-        const float a = exp2f(m[hl] - mnew), pv = exp2f(dot - mnew);
-        m[hl] = mnew;
-        l[hl] = fmaf(l[hl], a, pv);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[hl][e] = fmaf(acc[hl][e], a, pv * vv[e]);
+        for (int e = 0; e < E; ++e) acc = fmaf(qv[hl][e], kf[e], acc);
+        v[r * NH + hl] = acc;
       }
     }
-    float* mS = reinterpret_cast<float*>(recs);
-    float* lS = mS + kDecWarps * NH;
-    float* oS = lS + kDecWarps * NH;
 #pragma unroll
-    for (int hl = 0; hl < NH; ++hl) {
-      if (lane == 0) {
-        mS[warp * NH + hl] = m[hl];
-        lS[warp * NH + hl] = l[hl];
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float send = up ? v[i] : v[i + o];
+        const float keep = up ? v[i + o] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
-#pragma unroll
-      for (int e = 0; e < E; ++e) oS[(warp * NH + hl) * D + lane + 32 * e] = acc[hl][e];
     }
-    __syncthreads();
-    // merge warps, rotate o into the basis of the sealed splits, store
-    for (int hl = warp; hl < NH; hl += kDecWarps) {
-      if (!valid(hl)) break;
-      float M = -INFINITY;
+    const int t = tb * R + lane / NH;
+    if (t < n_part) pS[t * NH + lane % NH] = v[0];
+  }
+  __syncthreads();
+  // softmax over the partial tokens, one warp per head slot
+  for (int hl = warp; hl < NH; hl += kDecWarps) {
+    if (!valid(hl)) break;
+    float mx = -INFINITY;
+    for (int t = lane; t < n_part; t += 32) mx = fmaxf(mx, pS[t * NH + hl]);
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mS[w * NH + hl]);
-      float v[E], lsum = 0.0f;
+    for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+    float sum = 0.0f;
+    for (int t = lane; t < n_part; t += 32) {
+      const float pv = exp2f(pS[t * NH + hl] - mx);
+      pS[t * NH + hl] = pv;
+      sum += pv;
+    }
 #pragma unroll
-      for (int e = 0; e < E; ++e) v[e] = 0.0f;
+    for (int msk = 16; msk > 0; msk >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, msk);
+    if (lane == 0) {
+      mS[hl] = mx;
+      lS[hl] = sum;
+    }
+  }
+  __syncthreads();
+  // PV: warp w takes tokens w, w + kDecWarps, ...; the warp sums meet in shared memory
+  {
+    float acc[NH][E];
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float sc = exp2f(mS[w * NH + hl] - M);
-        lsum = fmaf(sc, lS[w * NH + hl], lsum);
+    for (int hl = 0; hl < NH; ++hl)
 #pragma unroll
-        for (int e = 0; e < E; ++e) v[e] = fmaf(sc, oS[(w * NH + hl) * D + lane * E + e], v[e]);
+      for (int e = 0; e < E; ++e) acc[hl][e] = 0.0f;
+    if (in) {
+      for (int t = warp; t < n_part; t += kDecWarps) {
+        float vf[E];
+        load_f16<E>(Vs + t * p.d0 + c0, vf);
+#pragma unroll
+        for (int hl = 0; hl < NH; ++hl) {
+          const float pw = pS[t * NH + hl];
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[hl][e] = fmaf(pw, vf[e], acc[hl][e]);
+        }
       }
-      warp_fwht<D>(v, lane);
-      float* dst = part_row(hl);
+    }
+    float* oS = reinterpret_cast<float*>(recs);  // K rows are no longer read
 #pragma unroll
-      for (int e = 0; e < E; ++e) dst[4 + lane * E + e] = v[e] * inv_sqrt_d<D>();
-      if (lane == 0) {
-        dst[0] = M;
-        dst[1] = lsum;
-      }
+    for (int hl = 0; hl < NH; ++hl)
+#pragma unroll
+      for (int e = 0; e < E; ++e) oS[(warp * NH + hl) * D + c0 + e] = acc[hl][e];
+  }
+  __syncthreads();
+  // sum the warps, rotate o into the basis of the sealed splits, store
+  for (int hl = warp; hl < NH; hl += kDecWarps) {
+    if (!valid(hl)) break;
+    const float* oS = reinterpret_cast<const float*>(recs);
+    float v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w)
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] += oS[(w * NH + hl) * D + c0 + e];
+    warp_fwht<D>(v, lane);
+    float* dst = part_row(hl);
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[4 + c0 + e] = v[e] * inv_sqrt_d<D>();
+    if (lane == 0) {
+      dst[0] = mS[hl];
+      dst[1] = lS[hl];
     }
   }
 }

@@ -203,7 +203,8 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
       out == nullptr || workspace == nullptr)
     return KVARN_ERR_INVALID_ARG;
   if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
-  if (!aligned16(page_pool) || !aligned16(workspace)) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(page_pool) || !aligned16(workspace) || !aligned16(partial_k) || !aligned16(partial_v))
+    return KVARN_ERR_INVALID_ARG;
   if (num_pool_pages < 1 || !(softmax_scale > 0.0f)) return KVARN_ERR_INVALID_ARG;
   const size_t need = kvarn_decode_workspace_bytes(desc, batch, num_q_heads, max_pages);
   if (workspace_bytes < need) return KVARN_ERR_WORKSPACE_TOO_SMALL;
@@ -266,7 +267,8 @@ int kvarn_prefill_attention(const kvarn_desc* desc, int batch, int num_q_heads, 
       block_table == nullptr || cache_lens == nullptr || out == nullptr || workspace == nullptr)
     return KVARN_ERR_INVALID_ARG;
   if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
-  if (!aligned16(page_pool) || !aligned16(workspace)) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(page_pool) || !aligned16(workspace) || !aligned16(partial_k) || !aligned16(partial_v))
+    return KVARN_ERR_INVALID_ARG;
   if (num_pool_pages < 1 || !(softmax_scale > 0.0f)) return KVARN_ERR_INVALID_ARG;
   const size_t need = kvarn_prefill_workspace_bytes(desc, batch, num_q_heads, chunk_len, max_pages);
   if (workspace_bytes < need) return KVARN_ERR_WORKSPACE_TOO_SMALL;

@@ -158,8 +158,9 @@ size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q
  *  q            fp16 [batch][Hq][d0] (one query per sequence and head).
  *  block_table  device int32 [batch][max_pages], seq_lens device int32 [batch]: TOTAL length,
  *               i.e. seq_lens[b]/128 sealed pages plus seq_lens[b]%128 raw tokens in the
- *               partial tile; seq_lens[b]/128 <= max_pages (else clamped and flagged).  partial_k/partial_v may be NULL only if no length has a
- *               remainder.
+ *               partial tile; seq_lens[b]/128 <= max_pages (else clamped and flagged).
+ *  partial_k/v  fp16 [batch][Hkv][128][d0] as for kvarn_append_token (16-byte aligned, else
+ *               INVALID_ARG); may be NULL only if no length has a remainder.
  *  softmax_scale  tau in softmax(tau q.k).
  *  out          fp16 [batch][Hq][d0]; a sequence of length 0 gives zeros.
  *  workspace    device scratch of at least kvarn_decode_workspace_bytes (16-byte aligned). */

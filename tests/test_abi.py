@@ -91,6 +91,12 @@ def test_validation_returns_before_launch(kv):
                                     ctypes.c_float(0.1), ctypes.c_void_p(16), ctypes.c_void_p(16), 8,
                                     null, null)
     assert st == kv.KVARN_ERR_WORKSPACE_TOO_SMALL
+    # partial tiles are staged with bulk copies: a misaligned one is refused before any launch
+    st = lib.kvarn_decode_attention(ctypes.byref(d), 2, 32, ctypes.c_void_p(16), ctypes.c_void_p(16), 8,
+                                    ctypes.c_void_p(16), 4, ctypes.c_void_p(16), ctypes.c_void_p(24),
+                                    ctypes.c_void_p(16), ctypes.c_float(0.1), ctypes.c_void_p(16),
+                                    ctypes.c_void_p(16), 1 << 30, null, null)
+    assert st == kv.KVARN_ERR_INVALID_ARG
     bad = kv.KvarnDesc.from_buffer_copy(d)
     bad.k_bits = 3
     assert lib.kvarn_dequantize_tiles(ctypes.byref(bad), null, 1, null, 1, null, null, null,
