@@ -759,6 +759,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
+  grid_launch_dependents();  // the next kernel (say, the next step's append) may start arriving
   if (gw >= p.batch * p.chunk * p.num_q_heads) return;
   const int b = gw / (p.chunk * p.num_q_heads);
   const int cap = p.max_pages * kTile + (kTile - 1);

@@ -26,6 +26,24 @@
 
 namespace kvarn {
 
+// Launch as a programmatic dependent of the previous kernel in the stream: the CTAs may be
+// scheduled while it drains and wait for it (griddepcontrol.wait) before reading anything.
+template <typename... KArgs, typename... Args>
+static int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                      Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
 template <int D>
 struct QuantShape {
   static constexpr int kThreads = 2 * D;       // D/16 warps, 64 values per thread
@@ -565,6 +583,8 @@ template <int D, int KB, int VB>
 __global__ void __launch_bounds__(QuantShape<D>::kThreads)
     quantize_kernel(QuantizeParams p) {
   extern __shared__ __align__(16) float smem_q[];
+  grid_dependency_wait();  // inputs, lengths and partial tiles may come from the previous kernel
+  grid_launch_dependents();
   const int unit = blockIdx.x >> 1;
   const bool is_v = (blockIdx.x & 1) != 0;
   const int h = unit % p.num_kv_heads;
@@ -618,8 +638,8 @@ static int launch_quantize(const QuantizeParams& p, int units, cudaStream_t stre
       return KVARN_ERR_CUDA;
     attr_set = true;
   }
-  quantize_kernel<D, KB, VB><<<units * 2, QuantShape<D>::kThreads, kSmem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  return launch_pdl(quantize_kernel<D, KB, VB>, dim3(units * 2), dim3(QuantShape<D>::kThreads), kSmem,
+                    stream, p);
 }
 
 // ---- head_dim 128: the rotation on the tensor cores -------------------------------------------
@@ -740,6 +760,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
   // ---- this CTA's units (append mode: write every token first, keep the tiles that seal) ----
   // Each warp takes every 8th of the CTA's units, so the dependent loads of different units
   // (length, then token) overlap; the list order does not matter (units are independent).
+  grid_dependency_wait();    // inputs, lengths and partial tiles may come from the previous kernel
   grid_launch_dependents();  // a dependent kernel still waits for this grid to complete
   if (tid == 0) *count = 0;
   __syncthreads();
@@ -933,8 +954,8 @@ static int launch_quantize_tc(const QuantizeParams& p, int units2, cudaStream_t 
   int grid = 2 * sms;
   grid = max(grid, (units2 + tc::kListCap - 1) / tc::kListCap);
   grid = min(grid, units2);
-  quantize_tc_kernel<KB, VB><<<grid, tc::kThreads, tc::kSmemBytes, stream>>>(p, units2);
-  return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  return launch_pdl(quantize_tc_kernel<KB, VB>, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, stream,
+                    p, units2);
 }
 
 template <int KB, int VB>
