@@ -385,6 +385,74 @@ def _time_prefill(torch, kv, synth, batch=8, cache_len=8192, chunk=64, hq=32, hk
     }
 
 
+def _time_fp16_baseline(torch, kv, S, stream, peak, reps=20, tail=64):
+    """Packed-cache decode against the uncompressed fp16 paged decode on the same lengths.
+
+    Both kernels run alone, back to back, on the decode workload's sequences with `tail` extra
+    tokens each (a partial tile for the packed cache, a partly filled last page for fp16); both
+    caches are larger than L2 (0.5 GB packed, 2.3 GB fp16)."""
+    dev = torch.device("cuda")
+    lens = (S["lens0"] + tail).to(torch.int32)
+    pages = ((lens + 127) // 128).tolist()
+    n_pool = sum(pages)
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED + 5)
+    pool = torch.randn((n_pool, HKV, 2, 128, D0), generator=g, device=dev).half()
+    table = torch.zeros((BATCH, max(pages)), dtype=torch.int32)
+    perm = torch.randperm(n_pool, generator=torch.Generator().manual_seed(SEED + 6)).to(torch.int32)
+    off = 0
+    for b in range(BATCH):
+        table[b, :pages[b]] = perm[off:off + pages[b]]
+        off += pages[b]
+    table = table.to(dev)
+    lens_d = lens.to(dev)
+    q = S["qs"][0]
+    out = torch.empty_like(S["out"])
+    ws = kv.alloc_fp16_workspace(D0, BATCH, HQ, table.shape[1], device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def fp16_call():
+        kv.fp16_decode_attention(HKV, q, pool, table, lens_d, out, ws, softmax_scale=1 / math.sqrt(D0),
+                                 status=status, stream=stream)
+
+    def kvarn_call():
+        kv.decode_attention(S["desc"], q, S["pool"], S["table"], lens_d, out, S["ws"],
+                            partial_k=S["pk"], partial_v=S["pv"], softmax_scale=1 / math.sqrt(D0),
+                            status=status, stream=stream)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    f_ms = timed(fp16_call)
+    k_ms = timed(kvarn_call)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the fp16 comparison" % int(status.item()))
+    tokens = int(lens.sum())
+    f_bytes = tokens * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2
+    k_bytes = _decode_bytes(lens.tolist(), S["rec_bytes"])
+    del pool
+    torch.cuda.empty_cache()
+    return {
+        "workload": "the decode workload's %d sequences at their lengths + %d tokens, alone, back to "
+                    "back (%d launches each)" % (BATCH, tail, reps),
+        "fp16_us": f_ms * 1e3, "fp16_tokens_per_s": tokens / (f_ms * 1e-3),
+        "fp16_hbm_gbs": f_bytes / (f_ms * 1e-3) / 1e9, "fp16_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peak,
+        "fp16_bytes": f_bytes,
+        "kvarn_us": k_ms * 1e3, "kvarn_tokens_per_s": tokens / (k_ms * 1e-3),
+        "kvarn_hbm_gbs": k_bytes / (k_ms * 1e-3) / 1e9, "kvarn_bytes": k_bytes,
+        "speedup_vs_fp16": f_ms / k_ms, "cache_bytes_ratio": f_bytes / k_bytes,
+    }
+
+
 def _decode_configs(torch, kv, synth, peak, args):
     """The 32B-class 64-layer decode step and the long-context shapes, each against bytes/peak."""
     res = {}
@@ -552,6 +620,8 @@ def _run_kvarn(args, torch, world, rank):
     extra = _decode_configs(torch, kv, synth, peak, args)
     if args.extras in ("all", "prefill"):
         extra["prefill"] = _time_prefill(torch, kv, synth)
+    if args.extras in ("all", "fp16"):
+        extra["fp16_baseline"] = _time_fp16_baseline(torch, kv, S, stream, peak)
     quality = _quality(torch, kv, synth)
 
     # ---- aggregate over ranks (replicas)
@@ -768,8 +838,9 @@ def main():
                     help="decode batch (64 = the benchmark workload; smaller only for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="CPU work of the oracle baseline sample (kvarn arm)")
-    ap.add_argument("--extras", choices=("all", "none", "32b", "long", "presets", "prefill"), default="all",
-                    help="which of the 64-layer and long-context decode shapes to time")
+    ap.add_argument("--extras", choices=("all", "none", "32b", "long", "presets", "prefill", "fp16"), default="all",
+                    help="which extra measurements to take: the 64-layer and long-context decode "
+                         "shapes, other presets, prefill, the fp16 paged decode baseline")
     ap.add_argument("--extra-batch", type=int, default=0,
                     help="batch of those shapes (0 = the workload's; smaller only for profiling)")
     ap.add_argument("--extra-layers", type=int, default=0,

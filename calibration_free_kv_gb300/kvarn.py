@@ -39,6 +39,9 @@ EXPORTED_SYMBOLS = (
     "kvarn_dequantize_tiles",
     "kvarn_status_string",
     "kvarn_decode_attention_noalloc",
+    "kvarn_fp16_page_bytes",
+    "kvarn_fp16_decode_workspace_bytes",
+    "kvarn_fp16_decode_attention",
 )
 
 # Size of the library's fixed decode scratch (KVARN_DECODE_NOALLOC_SCRATCH_BYTES in kvarn.h).
@@ -89,6 +92,10 @@ def _load():
         "kvarn_status_string": (ctypes.c_char_p, [i32]),
         "kvarn_decode_attention_noalloc": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P,
                                                  ctypes.c_float, P, P, P]),
+        "kvarn_fp16_page_bytes": (ctypes.c_size_t, [i32]),
+        "kvarn_fp16_decode_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32]),
+        "kvarn_fp16_decode_attention": (i32, [i32, i32, i32, i32, P, P, i64, P, i32, P, ctypes.c_float,
+                                              P, P, ctypes.c_size_t, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -260,6 +267,32 @@ def decode_attention_noalloc(desc: KvarnDesc, q, pool, block_table, seq_lens, ou
                                                _ptr(seq_lens), _ptr(partial_k), _ptr(partial_v),
                                                float(softmax_scale), _ptr(out), _ptr(status),
                                                _stream(stream)), "kvarn_decode_attention_noalloc")
+
+
+def fp16_page_bytes(head_dim: int) -> int:
+    """Bytes of one uncompressed fp16 (page, kv head) record: K rows then V rows [2][128][d]."""
+    return int(_lib.kvarn_fp16_page_bytes(head_dim))
+
+
+def alloc_fp16_workspace(head_dim: int, batch: int, num_q_heads: int, max_pages: int, device="cuda"):
+    n = int(_lib.kvarn_fp16_decode_workspace_bytes(head_dim, batch, num_q_heads, max_pages))
+    return torch.empty((max(n, 16) + 15) // 16 * 4, dtype=torch.float32, device=device)
+
+
+def fp16_decode_attention(num_kv_heads: int, q, pool, block_table, seq_lens, out, workspace,
+                          softmax_scale=None, status=None, stream=None):
+    """Uncompressed fp16 paged decode (the baseline): q, out fp16 [batch, Hq, d];
+    pool fp16 [pages, Hkv, 2, 128, d] (K rows then V rows per page and kv head)."""
+    batch, hq, d = q.shape
+    if pool.dim() != 5 or pool.shape[1:] != (num_kv_heads, 2, 128, d):
+        raise ValueError("pool must be fp16 [pages, Hkv, 2, 128, head_dim]")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    _check(_lib.kvarn_fp16_decode_attention(d, num_kv_heads, batch, hq, _ptr(q), _ptr(pool), pool.shape[0],
+                                            _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                            float(softmax_scale), _ptr(out), _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(), _ptr(status),
+                                            _stream(stream)), "kvarn_fp16_decode_attention")
 
 
 def dequantize_tiles(desc: KvarnDesc, pool, page_ids, k_out, v_out, status=None, stream=None):

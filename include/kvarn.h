@@ -226,6 +226,31 @@ int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_
                            const int32_t* page_ids, int num_pages, void* k_out, void* v_out,
                            int32_t* dev_status, void* stream);
 
+/* ---- Uncompressed fp16 paged decode: the baseline the packed cache is measured against ----
+ * [hotdry §监控要点: throughput is judged against fp16 KV caches; vatt §一次 16K context…:
+ *  every decode step reads every cached byte].  Same paging (128-token pages, block table,
+ *  seq_lens), split-K and merge as kvarn_decode_attention, no quantisation, no rotation.
+ *  Page record per (page, kv head): fp16 K rows then V rows, [2][128][head_dim], records laid
+ *  out [num_pool_pages][Hkv]; a length L uses ceil(L/128) pages, rows past L of the last page
+ *  are never read.  head_dim 64 or 128 (else UNSUPPORTED); G = Hq/Hkv in {1, 2, 4, 8}. */
+
+/* Bytes of one fp16 (page, kv head) record: 2 * 128 * head_dim * 2 (0 if unsupported). */
+size_t kvarn_fp16_page_bytes(int head_dim);
+
+/* Workspace bytes kvarn_fp16_decode_attention needs (host only; 0 if invalid). */
+size_t kvarn_fp16_decode_workspace_bytes(int head_dim, int batch, int num_q_heads, int max_pages);
+
+/*  q            fp16 [batch][Hq][head_dim] (4-byte aligned); out fp16 [batch][Hq][head_dim].
+ *  page_pool    16-byte aligned; block_table device int32 [batch][max_pages]; seq_lens device
+ *               int32 [batch] with ceil(L/128) <= max_pages (else clamped, KVARN_DEV_SEQ_TOO_LONG).
+ *  softmax_scale  tau in softmax(tau q.k); a sequence of length 0 gives zeros.
+ *  Device-side problems are OR-ed into *dev_status as for kvarn_decode_attention. */
+int kvarn_fp16_decode_attention(int head_dim, int num_kv_heads, int batch, int num_q_heads,
+                                const void* q, const void* page_pool, int64_t num_pool_pages,
+                                const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                float softmax_scale, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /* Static description of a KVARN_OK / KVARN_ERR_* code. */
 const char* kvarn_status_string(int status);
 

@@ -462,6 +462,23 @@ def decode_sequence(q_heads: np.ndarray, records, partial_k, partial_v,
                      for qh in np.asarray(q_heads, dtype=np.float64)])
 
 
+def fp16_decode_sequence(q_heads: np.ndarray, keys: np.ndarray, values: np.ndarray,
+                         softmax_scale: float) -> np.ndarray:
+    """Decode attention of the query heads of ONE kv head over an uncompressed fp16 cache.
+
+    keys, values: [L, d] the sequence's cached tokens as stored (fp16), no rotation and no
+    quantisation: the baseline the packed cache is compared with.  Returns [G, d].
+    [hotdry §监控要点: throughput is judged against an fp16 KV cache; vatt §一次 16K
+     context…: decode reads the whole cache every step]
+    Pinned by: test_fp16_decode_* (two-token closed form, paging invariance) and the
+    softmax_attention pins.
+    """
+    keys = np.asarray(keys, dtype=np.float64)
+    values = np.asarray(values, dtype=np.float64)
+    return np.stack([softmax_attention(qh, keys, values, softmax_scale)
+                     for qh in np.asarray(q_heads, dtype=np.float64)])
+
+
 def prefill_sequence(q: np.ndarray, records, partial_k, partial_v, chunk_k: np.ndarray,
                      chunk_v: np.ndarray, softmax_scale: float, d0: int,
                      k_bits: int = K_BITS, v_bits: int = V_BITS) -> np.ndarray:

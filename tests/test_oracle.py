@@ -641,6 +641,38 @@ def test_attention_large_logits_stay_finite():
     np.testing.assert_allclose(o[:4], [1 / (1 + w), 0, 0, w / (1 + w)], rtol=1e-12, atol=1e-300)
 
 
+def test_fp16_decode_two_tokens_closed_form():
+    # two keys whose scaled logits differ by ln 3: weights 3/4 and 1/4 for every query head
+    tau = 0.5
+    q = np.array([[1.0, 0.0, 0.0, 0.0], [2.0, 0.0, 0.0, 0.0]])
+    keys = np.array([[2 * np.log(3.0), 0.0, 0.0, 0.0], [0.0, 5.0, 0.0, 0.0]])
+    vals = np.array([[4.0, 0.0, -8.0, 1.0], [0.0, 4.0, 8.0, 1.0]])
+    o = ko.fp16_decode_sequence(q, keys, vals, tau)
+    np.testing.assert_allclose(o[0], [3.0, 1.0, -4.0, 1.0], rtol=1e-14)
+    # the second head doubles the logit gap: weights 9/10 and 1/10
+    np.testing.assert_allclose(o[1], [3.6, 0.4, -6.4, 1.0], rtol=1e-14)
+
+
+def test_fp16_decode_paging_invariance():
+    # the answer depends on the cached tokens only, not on how pages would split them: the
+    # log-sum-exp merge of per-128-token parts equals the whole (what split-K computes)
+    rng = np.random.default_rng(24)
+    q = rng.standard_normal((4, 64))
+    keys = rng.standard_normal((300, 64)) * 2
+    vals = rng.standard_normal((300, 64))
+    whole = ko.fp16_decode_sequence(q, keys, vals, 0.125)
+    for gi in range(4):
+        parts = []
+        for a in range(0, 300, 128):
+            lg = 0.125 * keys[a:a + 128] @ q[gi]
+            w = np.exp(lg - lg.max())
+            parts.append((lg.max(), w.sum(), w @ vals[a:a + 128]))
+        m = max(p[0] for p in parts)
+        num = sum(np.exp(p[0] - m) * p[2] for p in parts)
+        den = sum(np.exp(p[0] - m) * p[1] for p in parts)
+        np.testing.assert_allclose(whole[gi], num / den, rtol=1e-12, atol=1e-14)
+
+
 def test_attention_empty_is_zero():
     o = ko.softmax_attention(np.ones(8), np.zeros((0, 8)), np.zeros((0, 8)), 1.0)
     np.testing.assert_array_equal(o, np.zeros(8))
