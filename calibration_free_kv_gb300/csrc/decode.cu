@@ -404,6 +404,292 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
   }
 }
 
+// ---- eight query vectors per warp (NT = 2): the heads on the MMA's M axis --------------------
+// Rows g and g + 8 of a 16-row A operand hold head g's fp16 hi and lo parts and the page's codes
+// are the B operand: an A-fragment word of 16 tokens (or 16 channels, for V) holds exactly the
+// B fragments of two 8-wide blocks.  QK then leaves head g's logits of tokens 2tq, 2tq + 1 of
+// each 8-token block in lane (g, tq), which is the layout of PV's A operand: no transposes, and
+// each lane splits one head's operands instead of building a B column pair per head slot.
+
+template <int D>
+struct WarpAccT {
+  float m[1], l[1];   // head g; l is this lane's share until the CTA merge sums the tq lanes
+  float o[D / 8][2];  // head g, channels 8cb + 2tq, +1 (rotated basis)
+};
+
+// qh s (rounded) and the rest of (qh + ql) s, with the rounding error of qh s taken exactly.
+__device__ __forceinline__ void split_hi_lo(__half2 qh, __half2 ql, __half2 s, uint32_t& hi,
+                                            uint32_t& lo) {
+  const __half2 h = __hmul2(qh, s);
+  hi = h2u(h);
+  lo = h2u(__hfma2(ql, s, __hfma2(qh, s, __hneg2(h))));
+}
+
+// QK of one page for head g: probabilities of tokens 8b + 2tq, +1 in lg[b][0], online state
+// updated, alpha = rescale of the previous state.
+template <int D, int KB, int VB>
+__device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const float* __restrict__ qsm,
+                                          const uint2* __restrict__ qhl, int lane, WarpAccT<D>& st,
+                                          float (&lg)[16][1][2], float (&alpha)[1]) {
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
+  constexpr int QLD = DecodeShape<D, 2, KB, VB>::kQld;
+  constexpr int QH = D / 2 + 4;
+  const int g = lane >> 2, tq = lane & 3;
+  const __half2* Ks2 = reinterpret_cast<const __half2*>(Rk + RL.kscale);
+  const __half2* Kz2 = reinterpret_cast<const __half2*>(Rk + RL.kzero);
+  const __half2* Kr2 = reinterpret_cast<const __half2*>(Rk + RL.kfactor);
+  uint32_t aq[D / 16][4];  // head g: rows g = hi, g + 8 = lo; channels 2tq.. and 2tq + 8..
+  float2 qz2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const int jp = 8 * kk + tq;
+    const __half2 s0 = Ks2[jp], s1 = Ks2[jp + 4];
+    const float2 z0 = __half22float2(Kz2[jp]), z1 = __half22float2(Kz2[jp + 4]);
+    const float4 q4 = *reinterpret_cast<const float4*>(qsm + g * QLD + 16 * kk + 4 * tq);
+    qz2 = fma2(make_float2(q4.x, q4.y), z0, qz2);
+    qz2 = fma2(make_float2(q4.z, q4.w), z1, qz2);
+    const uint2 u0 = qhl[g * QH + jp], u1 = qhl[g * QH + jp + 4];
+    split_hi_lo(u2h2(u0.x), u2h2(u0.y), s0, aq[kk][0], aq[kk][1]);
+    split_hi_lo(u2h2(u1.x), u2h2(u1.y), s1, aq[kk][2], aq[kk][3]);
+  }
+  float qz = qz2.x + qz2.y;
+  qz += __shfl_xor_sync(0xffffffffu, qz, 1);
+  qz += __shfl_xor_sync(0xffffffffu, qz, 2);
+  // 8-token block b: rows g (hi) + g + 8 (lo) of columns 2tq, 2tq + 1
+  auto logits = [&](int b, const float (&acc)[4], float cf) {
+    const float2 r = __half22float2(Kr2[4 * b + tq]);
+    const float2 t = add2(make_float2(acc[0], acc[1]), make_float2(acc[2], acc[3]));
+    const float2 u = mul2(fma2(t, make_float2(cf, cf), make_float2(qz, qz)), r);
+    lg[b][0][0] = u.x;
+    lg[b][0][1] = u.y;
+  };
+  if constexpr (KB == 4) {  // word (16 tokens x 16 channels): tokens g -> a0, a2; g + 8 -> a1, a3
+#pragma unroll
+    for (int mi = 0; mi < 8; ++mi) {
+      float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kq = 0; kq < D / 64; ++kq) {
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi * (D / 64) + kq) * 32 + lane) * 16);
+        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a[4];
+          unpack_k(ws[e], a);
+          mma16816(acc0, aq[4 * kq + e], a[0], a[2]);
+          mma16816(acc1, aq[4 * kq + e], a[1], a[3]);
+        }
+      }
+      logits(2 * mi, acc0, kTwo24);
+      logits(2 * mi + 1, acc1, kTwo24);
+    }
+  } else {  // 2-bit: one word holds 16-token blocks 2mi2 and 2mi2 + 1 of a channel block
+    static_assert(KB == 2, "2- or 4-bit K codes");
+#pragma unroll
+    for (int mi2 = 0; mi2 < 4; ++mi2) {
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+#pragma unroll
+      for (int kq = 0; kq < D / 64; ++kq) {
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi2 * (D / 64) + kq) * 32 + lane) * 16);
+        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t a0[4], a1[4];
+          unpack_v(ws[e], a0, a1);
+          mma16816(acc[0], aq[4 * kq + e], a0[0], a0[2]);
+          mma16816(acc[1], aq[4 * kq + e], a0[1], a0[3]);
+          mma16816(acc[2], aq[4 * kq + e], a1[0], a1[2]);
+          mma16816(acc[3], aq[4 * kq + e], a1[1], a1[3]);
+        }
+      }
+      logits(4 * mi2, acc[0], kTwo24);
+      logits(4 * mi2 + 1, acc[1], kTwo24);
+      logits(4 * mi2 + 2, acc[2], kTwo24 * 0.0625f);  // the odd 16-token block sits 4 bits higher
+      logits(4 * mi2 + 3, acc[3], kTwo24 * 0.0625f);
+    }
+  }
+  float mx = fmaxf(lg[0][0][0], lg[0][0][1]);
+#pragma unroll
+  for (int b = 1; b < 16; ++b) mx = fmax3(mx, lg[b][0][0], lg[b][0][1]);
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float mnew = fmaxf(st.m[0], mx);
+  alpha[0] = ex2_approx(st.m[0] - mnew);
+  st.m[0] = mnew;
+  float2 ps = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int b = 0; b < 16; ++b) {
+    const float2 d = sub2(make_float2(lg[b][0][0], lg[b][0][1]), make_float2(mnew, mnew));
+    const float2 pv = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+    lg[b][0][0] = pv.x;
+    lg[b][0][1] = pv.y;
+    ps = add2(ps, pv);
+  }
+  st.l[0] = fmaf(st.l[0], alpha[0], ps.x + ps.y);
+}
+
+// PV of one page for head g with the probabilities of qk_page_t.
+template <int D, int KB, int VB>
+__device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const float (&lg)[16][1][2],
+                                          const float (&alpha)[1], int lane, WarpAccT<D>& st) {
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
+  const int tq = lane & 3;
+  const __half2* Vs2 = reinterpret_cast<const __half2*>(Rv + (RL.vscale - RL.vcodes));
+  const __half2* Vz2 = reinterpret_cast<const __half2*>(Rv + (RL.vzero - RL.vcodes));
+  const __half2* Vc2 = reinterpret_cast<const __half2*>(Rv + (RL.vfactor - RL.vcodes));
+  float pacc[D / 8][4];  // 8-channel block cb: rows g (hi) / g + 8 (lo), channels 2tq, 2tq + 1
+#pragma unroll
+  for (int cb = 0; cb < D / 8; ++cb) pacc[cb][0] = pacc[cb][1] = pacc[cb][2] = pacc[cb][3] = 0.0f;
+  float2 zs2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int ks2 = 0; ks2 < 4; ++ks2) {
+    uint32_t ap[2][4];  // 16-token blocks 2ks2 + f: rows g = hi, g + 8 = lo of p s'_V
+#pragma unroll
+    for (int f = 0; f < 2; ++f) {
+      const int k = 2 * ks2 + f;
+      // the codes' subnormal scale compensated: 2-bit 2^(4f + 2h), 4-bit 2^(4h), h = token half
+      const float c0 = VB == 2 ? (f ? 1.0f / 16.0f : 1.0f) : 1.0f;
+      const float c1 = VB == 2 ? (f ? 1.0f / 64.0f : 0.25f) : 1.0f / 16.0f;
+      const float2 pa = make_float2(lg[2 * k][0][0], lg[2 * k][0][1]);          // tokens 16k + 2tq, +1
+      const float2 pb = make_float2(lg[2 * k + 1][0][0], lg[2 * k + 1][0][1]);  // tokens 16k + 8 + 2tq, +1
+      zs2 = fma2(pa, __half22float2(Vz2[8 * k + tq]), zs2);
+      zs2 = fma2(pb, __half22float2(Vz2[8 * k + 4 + tq]), zs2);
+      const float2 wa = mul2(pa, mul2(__half22float2(Vs2[8 * k + tq]), make_float2(c0, c0)));
+      const float2 wb = mul2(pb, mul2(__half22float2(Vs2[8 * k + 4 + tq]), make_float2(c1, c1)));
+      const __half2 ha = __floats2half2_rn(wa.x, wa.y), hb = __floats2half2_rn(wb.x, wb.y);
+      const float2 ra = sub2(wa, __half22float2(ha)), rb = sub2(wb, __half22float2(hb));
+      ap[f][0] = h2u(ha);
+      ap[f][1] = h2u(__floats2half2_rn(ra.x, ra.y));
+      ap[f][2] = h2u(hb);
+      ap[f][3] = h2u(__floats2half2_rn(rb.x, rb.y));
+    }
+#pragma unroll
+    for (int mq = 0; mq < D / 64; ++mq) {
+      uint32_t ws0[4], ws1[4];
+      if constexpr (VB == 2) {
+        const uint4 w4 = *reinterpret_cast<const uint4*>(Rv + ((ks2 * (D / 64) + mq) * 32 + lane) * 16);
+        ws0[0] = w4.x; ws0[1] = w4.y; ws0[2] = w4.z; ws0[3] = w4.w;
+      } else {
+        static_assert(VB == 4, "2- or 4-bit V codes");
+        const uint4 w0 = *reinterpret_cast<const uint4*>(Rv + (((2 * ks2) * (D / 64) + mq) * 32 + lane) * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(Rv + (((2 * ks2 + 1) * (D / 64) + mq) * 32 + lane) * 16);
+        ws0[0] = w0.x; ws0[1] = w0.y; ws0[2] = w0.z; ws0[3] = w0.w;
+        ws1[0] = w1.x; ws1[1] = w1.y; ws1[2] = w1.z; ws1[3] = w1.w;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int mc = 4 * mq + e;  // channels 16mc..: 8-channel blocks 2mc (a0, a2), 2mc + 1 (a1, a3)
+        uint32_t a0[4], a1[4];
+        if constexpr (VB == 2) {
+          unpack_v(ws0[e], a0, a1);
+        } else {
+          unpack_k(ws0[e], a0);
+          unpack_k(ws1[e], a1);
+        }
+        mma16816(pacc[2 * mc], ap[0], a0[0], a0[2]);
+        mma16816(pacc[2 * mc + 1], ap[0], a0[1], a0[3]);
+        mma16816(pacc[2 * mc], ap[1], a1[0], a1[2]);
+        mma16816(pacc[2 * mc + 1], ap[1], a1[1], a1[3]);
+      }
+    }
+  }
+  float zs = zs2.x + zs2.y;
+  zs += __shfl_xor_sync(0xffffffffu, zs, 1);
+  zs += __shfl_xor_sync(0xffffffffu, zs, 2);
+#pragma unroll
+  for (int cb = 0; cb < D / 8; ++cb) {
+    const float2 cj = __half22float2(Vc2[4 * cb + tq]);
+    float2 t = add2(make_float2(pacc[cb][0], pacc[cb][1]), make_float2(pacc[cb][2], pacc[cb][3]));
+    t = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(zs, zs)), cj);
+    const float2 o = fma2(make_float2(st.o[cb][0], st.o[cb][1]), make_float2(alpha[0], alpha[0]), t);
+    st.o[cb][0] = o.x;
+    st.o[cb][1] = o.y;
+  }
+}
+
+// The per-warp decode path of NT head slots: NT = 2 takes the heads-on-M form above.
+template <int D, int NT, int KB, int VB>
+struct PagePath {
+  using State = WarpAcc<D, NT>;
+  static constexpr int kLgBlocks = 8, kLgNt = NT;
+  __device__ static void init(State& st) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      st.m[nt] = -INFINITY;
+      st.l[nt] = 0.0f;
+#pragma unroll
+      for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
+    }
+  }
+  __device__ static void qk(const uint8_t* Rk, const float* qsm, const uint2* qhl, int lane, State& st,
+                            float (&lg)[kLgBlocks][kLgNt][2], float (&alpha)[kLgNt]) {
+    qk_page<D, NT, KB, VB>(Rk, qsm, qhl, lane, st, lg, alpha);
+  }
+  __device__ static void pv(const uint8_t* Rv, const float (&lg)[kLgBlocks][kLgNt][2],
+                            const float (&alpha)[kLgNt], int lane, State& st) {
+    pv_page<D, NT, KB, VB>(Rv, lg, alpha, lane, st);
+  }
+  // (m, l, o) of every head slot of this warp into the CTA's merge scratch
+  __device__ static void store(const State& st, int warp, int lane, float* mS, float* lS, float* oS) {
+    constexpr int NH = 4 * NT;
+    const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float l = st.l[nt];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      const int hl = 4 * nt + tq;
+      if (g == 0) {
+        mS[warp * NH + hl] = st.m[nt];
+        lS[warp * NH + hl] = l;
+      }
+#pragma unroll
+      for (int mc = 0; mc < D / 16; ++mc) {
+        oS[(warp * NH + hl) * D + 16 * mc + g] = st.o[mc][nt][0];
+        oS[(warp * NH + hl) * D + 16 * mc + g + 8] = st.o[mc][nt][1];
+      }
+    }
+  }
+};
+
+template <int D, int KB, int VB>
+struct PagePath<D, 2, KB, VB> {
+  using State = WarpAccT<D>;
+  static constexpr int kLgBlocks = 16, kLgNt = 1;
+  __device__ static void init(State& st) {
+    st.m[0] = -INFINITY;
+    st.l[0] = 0.0f;
+#pragma unroll
+    for (int cb = 0; cb < D / 8; ++cb) st.o[cb][0] = st.o[cb][1] = 0.0f;
+  }
+  __device__ static void qk(const uint8_t* Rk, const float* qsm, const uint2* qhl, int lane, State& st,
+                            float (&lg)[kLgBlocks][kLgNt][2], float (&alpha)[kLgNt]) {
+    qk_page_t<D, KB, VB>(Rk, qsm, qhl, lane, st, lg, alpha);
+  }
+  __device__ static void pv(const uint8_t* Rv, const float (&lg)[kLgBlocks][kLgNt][2],
+                            const float (&alpha)[kLgNt], int lane, State& st) {
+    pv_page_t<D, KB, VB>(Rv, lg, alpha, lane, st);
+  }
+  __device__ static void store(const State& st, int warp, int lane, float* mS, float* lS, float* oS) {
+    constexpr int NH = 8;
+    const int g = lane >> 2, tq = lane & 3;
+    float l = st.l[0];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (tq == 0) {
+      mS[warp * NH + g] = st.m[0];
+      lS[warp * NH + g] = l;
+    }
+#pragma unroll
+    for (int cb = 0; cb < D / 8; ++cb)
+      *reinterpret_cast<float2*>(&oS[(warp * NH + g) * D + 8 * cb + 2 * tq]) = make_float2(st.o[cb][0], st.o[cb][1]);
+  }
+};
+
 template <int D, int NT, int KB, int VB>
 __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, DecodeShape<D, NT, KB, VB>::kMinBlocks)
     decode_kernel(DecodeParams p) {
@@ -508,14 +794,9 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     }
     __syncthreads();  // q in shared memory for every warp
 
-    WarpAcc<D, NT> st;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      st.m[nt] = -INFINITY;
-      st.l[nt] = 0.0f;
-#pragma unroll
-      for (int mc = 0; mc < D / 16; ++mc) st.o[mc][nt][0] = st.o[mc][nt][1] = 0.0f;
-    }
+    using Path = PagePath<D, NT, KB, VB>;
+    typename Path::State st;
+    Path::init(st);
     // record of the warp's next page, looked up one page ahead so that issuing its copies
     // never waits on the block-table load
     const uint8_t* nxt = cnt > 1 ? page_src(1) : nullptr;
@@ -529,8 +810,8 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
         }
         break;
       }
-      float lg[8][NT][2], alpha[NT];
-      qk_page<D, NT, KB, VB>(kslot, qsm, qhl, lane, st, lg, alpha);
+      float lg[Path::kLgBlocks][Path::kLgNt][2], alpha[Path::kLgNt];
+      Path::qk(kslot, qsm, qhl, lane, st, lg, alpha);
       __syncwarp();
       const bool more = j + 1 < cnt;
       if (lane == 0 && more) {  // the K slot is free: fetch the next page's K half
@@ -546,7 +827,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
         }
         break;
       }
-      pv_page<D, NT, KB, VB>(vslot, lg, alpha, lane, st);
+      Path::pv(vslot, lg, alpha, lane, st);
       __syncwarp();
       if (lane == 0 && more) {  // the V slot is free: fetch the next page's V half
         fence_proxy_async_smem();
@@ -561,23 +842,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float l = st.l[nt];
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      const int hl = 4 * nt + tq;
-      if (g == 0) {
-        mS[warp * NH + hl] = st.m[nt];
-        lS[warp * NH + hl] = l;
-      }
-#pragma unroll
-      for (int mc = 0; mc < D / 16; ++mc) {
-        oS[(warp * NH + hl) * D + 16 * mc + g] = st.o[mc][nt][0];
-        oS[(warp * NH + hl) * D + 16 * mc + g + 8] = st.o[mc][nt][1];
-      }
-    }
+    Path::store(st, warp, lane, mS, lS, oS);
     __syncthreads();
     for (int idx = threadIdx.x; idx < NH * D; idx += blockDim.x) {
       const int hl = idx / D, j = idx - hl * D;
