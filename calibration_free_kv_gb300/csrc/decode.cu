@@ -28,11 +28,11 @@
 // combine_kernel merges the splits, divides by l, undoes the rotation and stores fp16.
 // chunk_kernel adds the causal part of a prefill chunk as one more split.
 #include "common.cuh"
+#include "decode_util.cuh"
 #include "params.cuh"
 
 namespace kvarn {
 
-constexpr float kTwo24 = 16777216.0f;
 constexpr int kMaxSmem = 232448;  // dynamic shared memory a CTA may opt in to
 
 template <int D, int NT, int KB, int VB>
@@ -54,120 +54,6 @@ struct DecodeShape {
   // two CTAs per SM where both their shared memory and 128 registers a thread suffice
   static constexpr int kMinBlocks = (NT == 1 && 2 * (kSmemBytes + 1024) <= 233472) ? 2 : 1;
 };
-
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u2h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
-
-// K word -> A fragment as fp16 subnormals: a0/a1 (channels 2tq..) = code * 2^-24,
-// a2/a3 (channels 2tq+8..) = code * 2^-20.
-__device__ __forceinline__ void unpack_k(uint32_t x, uint32_t (&a)[4]) {
-  const uint32_t y = x >> 8;
-  a[0] = x & 0x000F000Fu;
-  a[2] = x & 0x00F000F0u;
-  a[1] = y & 0x000F000Fu;
-  a[3] = y & 0x00F000F0u;
-}
-
-// V word -> the A fragments of token blocks 2ks2 (a0) and 2ks2+1 (a1) as fp16 subnormals:
-// block f, token half h -> code * 2^(-24 + 4f + 2h).
-__device__ __forceinline__ void unpack_v(uint32_t x, uint32_t (&a0)[4], uint32_t (&a1)[4]) {
-  const uint32_t y = x >> 8;
-  a0[0] = x & 0x00030003u;
-  a0[2] = x & 0x000C000Cu;
-  a0[1] = y & 0x00030003u;
-  a0[3] = y & 0x000C000Cu;
-  a1[0] = x & 0x00300030u;
-  a1[2] = x & 0x00C000C0u;
-  a1[1] = y & 0x00300030u;
-  a1[3] = y & 0x00C000C0u;
-}
-
-// Walsh-Hadamard transform of D values spread over a warp, lane holding D/32 consecutive.
-template <int D>
-__device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
-  constexpr int E = D / 32;
-#pragma unroll
-  for (int h = 1; h < E; h <<= 1)
-#pragma unroll
-    for (int i = 0; i < E; ++i)
-      if ((i & h) == 0) {
-        const float a = v[i], b = v[i + h];
-        v[i] = a + b;
-        v[i + h] = a - b;
-      }
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-      v[i] = upper ? (o - v[i]) : (v[i] + o);
-    }
-  }
-}
-
-// E consecutive fp16 / fp32 values from shared memory (8, 16 or 32 bytes, aligned) as floats.
-template <int E>
-__device__ __forceinline__ void load_f16(const __half* src, float (&f)[E]) {
-  static_assert(E == 2 || E == 4 || E == 8, "2, 4 or 8 halves");
-  if constexpr (E == 2) {
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(src));
-    f[0] = a.x;
-    f[1] = a.y;
-  } else {
-#pragma unroll
-    for (int i = 0; i < E / 4; ++i) {
-      const uint2 u = reinterpret_cast<const uint2*>(src)[i];
-      const float2 a = __half22float2(u2h2(u.x)), c = __half22float2(u2h2(u.y));
-      f[4 * i] = a.x;
-      f[4 * i + 1] = a.y;
-      f[4 * i + 2] = c.x;
-      f[4 * i + 3] = c.y;
-    }
-  }
-}
-template <int E>
-__device__ __forceinline__ void load_f32(const float* src, float (&f)[E]) {
-  if constexpr (E % 4 == 0) {
-#pragma unroll
-    for (int i = 0; i < E / 4; ++i) {
-      const float4 a = reinterpret_cast<const float4*>(src)[i];
-      f[4 * i] = a.x;
-      f[4 * i + 1] = a.y;
-      f[4 * i + 2] = a.z;
-      f[4 * i + 3] = a.w;
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < E; ++e) f[e] = src[e];
-  }
-}
-
-template <int D>
-__device__ __forceinline__ float inv_sqrt_d() {
-  return D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
-}
 
 template <int D, int NT>
 struct WarpAcc {
