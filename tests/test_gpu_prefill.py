@@ -104,3 +104,10 @@ def test_prefill_long_chunk(kv):
     # a 33-token chunk over one long cached sequence, GQA 4
     err = _prefill_case(kv, [16384 + 40], 33, 1, 4, 128, seed=12)
     print("prefill chunk 33 over 16424 cached tokens: max scaled error %.2e" % err)
+
+
+def test_prefill_chunk64(kv):
+    # the bench's prefill shape at a smaller batch: 64-token chunks, GQA 4 (256 query vectors
+    # per kv head, four CTAs of 64), 8195 and 2000 cached tokens
+    err = _prefill_case(kv, [8192 + 3, 2000], 64, 2, 4, 128, seed=13)
+    print("prefill chunk 64: max scaled error %.2e" % err)
