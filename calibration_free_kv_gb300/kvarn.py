@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "kvarn_fp16_page_bytes",
     "kvarn_fp16_decode_workspace_bytes",
     "kvarn_fp16_decode_attention",
+    "kvarn_selftest_wait_timeout",
 )
 
 # Size of the library's fixed decode scratch (KVARN_DECODE_NOALLOC_SCRATCH_BYTES in kvarn.h).
@@ -96,6 +97,7 @@ def _load():
         "kvarn_fp16_decode_workspace_bytes": (ctypes.c_size_t, [i32, i32, i32, i32]),
         "kvarn_fp16_decode_attention": (i32, [i32, i32, i32, i32, P, P, i64, P, i32, P, ctypes.c_float,
                                               P, P, ctypes.c_size_t, P, P]),
+        "kvarn_selftest_wait_timeout": (i32, [P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -293,6 +295,11 @@ def fp16_decode_attention(num_kv_heads: int, q, pool, block_table, seq_lens, out
                                             float(softmax_scale), _ptr(out), _ptr(workspace),
                                             workspace.numel() * workspace.element_size(), _ptr(status),
                                             _stream(stream)), "kvarn_fp16_decode_attention")
+
+
+def selftest_wait_timeout(status, stream=None):
+    """Launch the bounded-wait self-test: ~2 s later DEV_WAIT_TIMEOUT is set in `status`."""
+    _check(_lib.kvarn_selftest_wait_timeout(_ptr(status), _stream(stream)), "kvarn_selftest_wait_timeout")
 
 
 def dequantize_tiles(desc: KvarnDesc, pool, page_ids, k_out, v_out, status=None, stream=None):

@@ -251,6 +251,12 @@ int kvarn_fp16_decode_attention(int head_dim, int num_kv_heads, int batch, int n
                                 float softmax_scale, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* Self-test of the kernels' bounded waits: one thread waits on an mbarrier that nothing
+ * completes; after ~2 s the wait gives up and KVARN_DEV_WAIT_TIMEOUT is OR-ed into
+ * *dev_status (device int32, required).  Launches on `stream` and returns; the GPU context
+ * stays usable.  INVALID_ARG if dev_status is NULL. */
+int kvarn_selftest_wait_timeout(int32_t* dev_status, void* stream);
+
 /* Static description of a KVARN_OK / KVARN_ERR_* code. */
 const char* kvarn_status_string(int status);
 

@@ -295,3 +295,18 @@ def test_decode_longest_block_table(kv):
     # exactly full; 32 splits plus the partial tile reach the combine step
     err = _run_oracle_cache_case(kv, 2, 1, 4, 128, [1024 * 128 + 77, 1024 * 128], seed=11)
     print("1024 pages: max scaled err %.2e" % err)
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(kv):
+    # a wait on an mbarrier that nothing completes gives up (~2 s) with a status bit; a decode
+    # launched afterwards on the same context still runs and matches the oracle
+    import time
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    kv.selftest_wait_timeout(status)
+    torch.cuda.synchronize()
+    waited = time.time() - t0
+    assert int(status.item()) == kv.DEV_WAIT_TIMEOUT
+    assert 0.5 < waited < 30.0
+    err = _run_oracle_cache_case(kv, 2, 1, 4, 128, [300, 129], seed=21)
+    print("wait gave up after %.2f s; decode afterwards: max scaled err %.2e" % (waited, err))
