@@ -43,7 +43,8 @@ struct DecodeShape {
   static constexpr int kKHalf = kRL.vcodes;          // K codes + K metadata
   static constexpr int kVHalf = kRec - kKHalf;       // V codes + V metadata
   static constexpr int kQld = D + 8;                 // fp32 row stride of q in shared memory
-  static constexpr int kQBytes = kNH * kQld * 4;     // q~ (fp32) for q~ . z'
+  // q~ (fp32) for q~ . z'; 8 heads per warp take q~ . z' from the fp16 hi + lo parts instead
+  static constexpr int kQBytes = NT == 2 ? 0 : kNH * kQld * 4;
   static constexpr int kQhBytes = 2 * kNH * (D / 2 + 4) * 4;  // q~ as fp16 hi and lo, padded rows
   // warps per CTA: 8, or 4 where 8 page slots would not fit in shared memory
   static constexpr int kWarps = 8 * kRec + kQBytes + kQhBytes + 8 * 16 <= kMaxSmem ? 8 : 4;
@@ -51,8 +52,8 @@ struct DecodeShape {
   static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + kWarps * 2 * 8;
   static_assert(kSmemBytes <= kMaxSmem, "page slots fit in shared memory");
   static_assert(kRecBytes >= kWarps * kNH * (D + 2) * 4, "the merge scratch fits the page slots");
-  // two CTAs per SM where both their shared memory and 128 registers a thread suffice
-  static constexpr int kMinBlocks = (NT == 1 && 2 * (kSmemBytes + 1024) <= 233472) ? 2 : 1;
+  // two CTAs per SM where their shared memory fits (registers then capped at 128 a thread)
+  static constexpr int kMinBlocks = 2 * (kSmemBytes + 1024) <= 233472 ? 2 : 1;
 };
 
 template <int D, int NT>
@@ -314,27 +315,28 @@ __device__ __forceinline__ void split_hi_lo(__half2 qh, __half2 ql, __half2 s, u
 // QK of one page for head g: probabilities of tokens 8b + 2tq, +1 in lg[b][0], online state
 // updated, alpha = rescale of the previous state.
 template <int D, int KB, int VB>
-__device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const float* __restrict__ qsm,
+__device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const float* __restrict__ /* no fp32 q~ */,
                                           const uint2* __restrict__ qhl, int lane, WarpAccT<D>& st,
                                           float (&lg)[16][1][2], float (&alpha)[1]) {
   constexpr RecordLayout RL = record_layout(D, KB, VB);
-  constexpr int QLD = DecodeShape<D, 2, KB, VB>::kQld;
   constexpr int QH = D / 2 + 4;
   const int g = lane >> 2, tq = lane & 3;
   const __half2* Ks2 = reinterpret_cast<const __half2*>(Rk + RL.kscale);
   const __half2* Kz2 = reinterpret_cast<const __half2*>(Rk + RL.kzero);
   const __half2* Kr2 = reinterpret_cast<const __half2*>(Rk + RL.kfactor);
   uint32_t aq[D / 16][4];  // head g: rows g = hi, g + 8 = lo; channels 2tq.. and 2tq + 8..
+  // q~ . z' from q~ = hi + lo (channels 8..15 of each 16 carry the codes' 2^-4 / 2^-2 scale)
+  constexpr float kUndo = KB == 4 ? 16.0f : 4.0f;
   float2 qz2 = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const int jp = 8 * kk + tq;
     const __half2 s0 = Ks2[jp], s1 = Ks2[jp + 4];
     const float2 z0 = __half22float2(Kz2[jp]), z1 = __half22float2(Kz2[jp + 4]);
-    const float4 q4 = *reinterpret_cast<const float4*>(qsm + g * QLD + 16 * kk + 4 * tq);
-    qz2 = fma2(make_float2(q4.x, q4.y), z0, qz2);
-    qz2 = fma2(make_float2(q4.z, q4.w), z1, qz2);
     const uint2 u0 = qhl[g * QH + jp], u1 = qhl[g * QH + jp + 4];
+    qz2 = fma2(add2(__half22float2(u2h2(u0.x)), __half22float2(u2h2(u0.y))), z0, qz2);
+    qz2 = fma2(mul2(add2(__half22float2(u2h2(u1.x)), __half22float2(u2h2(u1.y))), make_float2(kUndo, kUndo)),
+               z1, qz2);
     split_hi_lo(u2h2(u0.x), u2h2(u0.y), s0, aq[kk][0], aq[kk][1]);
     split_hi_lo(u2h2(u1.x), u2h2(u1.y), s1, aq[kk][2], aq[kk][3]);
   }
@@ -417,7 +419,9 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
   st.l[0] = fmaf(st.l[0], alpha[0], ps.x + ps.y);
 }
 
-// PV of one page for head g with the probabilities of qk_page_t.
+// PV of one page for head g with the probabilities of qk_page_t.  The A operands of all
+// eight 16-token blocks are built first; the channels are then taken 64 at a time, so only
+// one slice of accumulators is live (two CTAs of 8 warps fit an SM).
 template <int D, int KB, int VB>
 __device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const float (&lg)[16][1][2],
                                           const float (&alpha)[1], int lane, WarpAccT<D>& st) {
@@ -426,34 +430,37 @@ __device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const 
   const __half2* Vs2 = reinterpret_cast<const __half2*>(Rv + (RL.vscale - RL.vcodes));
   const __half2* Vz2 = reinterpret_cast<const __half2*>(Rv + (RL.vzero - RL.vcodes));
   const __half2* Vc2 = reinterpret_cast<const __half2*>(Rv + (RL.vfactor - RL.vcodes));
-  float pacc[D / 8][4];  // 8-channel block cb: rows g (hi) / g + 8 (lo), channels 2tq, 2tq + 1
-#pragma unroll
-  for (int cb = 0; cb < D / 8; ++cb) pacc[cb][0] = pacc[cb][1] = pacc[cb][2] = pacc[cb][3] = 0.0f;
+  uint32_t ap[8][4];  // 16-token block k: rows g = hi, g + 8 = lo of p s'_V
   float2 zs2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-  for (int ks2 = 0; ks2 < 4; ++ks2) {
-    uint32_t ap[2][4];  // 16-token blocks 2ks2 + f: rows g = hi, g + 8 = lo of p s'_V
+  for (int k = 0; k < 8; ++k) {
+    const int f = k & 1;
+    // the codes' subnormal scale compensated: 2-bit 2^(4f + 2h), 4-bit 2^(4h), h = token half
+    const float c0 = VB == 2 ? (f ? 1.0f / 16.0f : 1.0f) : 1.0f;
+    const float c1 = VB == 2 ? (f ? 1.0f / 64.0f : 0.25f) : 1.0f / 16.0f;
+    const float2 pa = make_float2(lg[2 * k][0][0], lg[2 * k][0][1]);          // tokens 16k + 2tq, +1
+    const float2 pb = make_float2(lg[2 * k + 1][0][0], lg[2 * k + 1][0][1]);  // tokens 16k + 8 + 2tq, +1
+    zs2 = fma2(pa, __half22float2(Vz2[8 * k + tq]), zs2);
+    zs2 = fma2(pb, __half22float2(Vz2[8 * k + 4 + tq]), zs2);
+    const float2 wa = mul2(pa, mul2(__half22float2(Vs2[8 * k + tq]), make_float2(c0, c0)));
+    const float2 wb = mul2(pb, mul2(__half22float2(Vs2[8 * k + 4 + tq]), make_float2(c1, c1)));
+    const __half2 ha = __floats2half2_rn(wa.x, wa.y), hb = __floats2half2_rn(wb.x, wb.y);
+    const float2 ra = sub2(wa, __half22float2(ha)), rb = sub2(wb, __half22float2(hb));
+    ap[k][0] = h2u(ha);
+    ap[k][1] = h2u(__floats2half2_rn(ra.x, ra.y));
+    ap[k][2] = h2u(hb);
+    ap[k][3] = h2u(__floats2half2_rn(rb.x, rb.y));
+  }
+  float zs = zs2.x + zs2.y;
+  zs += __shfl_xor_sync(0xffffffffu, zs, 1);
+  zs += __shfl_xor_sync(0xffffffffu, zs, 2);
 #pragma unroll
-    for (int f = 0; f < 2; ++f) {
-      const int k = 2 * ks2 + f;
-      // the codes' subnormal scale compensated: 2-bit 2^(4f + 2h), 4-bit 2^(4h), h = token half
-      const float c0 = VB == 2 ? (f ? 1.0f / 16.0f : 1.0f) : 1.0f;
-      const float c1 = VB == 2 ? (f ? 1.0f / 64.0f : 0.25f) : 1.0f / 16.0f;
-      const float2 pa = make_float2(lg[2 * k][0][0], lg[2 * k][0][1]);          // tokens 16k + 2tq, +1
-      const float2 pb = make_float2(lg[2 * k + 1][0][0], lg[2 * k + 1][0][1]);  // tokens 16k + 8 + 2tq, +1
-      zs2 = fma2(pa, __half22float2(Vz2[8 * k + tq]), zs2);
-      zs2 = fma2(pb, __half22float2(Vz2[8 * k + 4 + tq]), zs2);
-      const float2 wa = mul2(pa, mul2(__half22float2(Vs2[8 * k + tq]), make_float2(c0, c0)));
-      const float2 wb = mul2(pb, mul2(__half22float2(Vs2[8 * k + 4 + tq]), make_float2(c1, c1)));
-      const __half2 ha = __floats2half2_rn(wa.x, wa.y), hb = __floats2half2_rn(wb.x, wb.y);
-      const float2 ra = sub2(wa, __half22float2(ha)), rb = sub2(wb, __half22float2(hb));
-      ap[f][0] = h2u(ha);
-      ap[f][1] = h2u(__floats2half2_rn(ra.x, ra.y));
-      ap[f][2] = h2u(hb);
-      ap[f][3] = h2u(__floats2half2_rn(rb.x, rb.y));
-    }
+  for (int mq = 0; mq < D / 64; ++mq) {  // channels 64mq..64mq + 63: 8-channel blocks 8mq + cl
+    float pacc[8][4];
 #pragma unroll
-    for (int mq = 0; mq < D / 64; ++mq) {
+    for (int cl = 0; cl < 8; ++cl) pacc[cl][0] = pacc[cl][1] = pacc[cl][2] = pacc[cl][3] = 0.0f;
+#pragma unroll
+    for (int ks2 = 0; ks2 < 4; ++ks2) {
       uint32_t ws0[4], ws1[4];
       if constexpr (VB == 2) {
         const uint4 w4 = *reinterpret_cast<const uint4*>(Rv + ((ks2 * (D / 64) + mq) * 32 + lane) * 16);
@@ -466,8 +473,7 @@ __device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const 
         ws1[0] = w1.x; ws1[1] = w1.y; ws1[2] = w1.z; ws1[3] = w1.w;
       }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int mc = 4 * mq + e;  // channels 16mc..: 8-channel blocks 2mc (a0, a2), 2mc + 1 (a1, a3)
+      for (int e = 0; e < 4; ++e) {  // channels 16(4mq + e)..: 8-channel blocks 2e (a0, a2), 2e + 1 (a1, a3)
         uint32_t a0[4], a1[4];
         if constexpr (VB == 2) {
           unpack_v(ws0[e], a0, a1);
@@ -475,24 +481,22 @@ __device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const 
           unpack_k(ws0[e], a0);
           unpack_k(ws1[e], a1);
         }
-        mma16816(pacc[2 * mc], ap[0], a0[0], a0[2]);
-        mma16816(pacc[2 * mc + 1], ap[0], a0[1], a0[3]);
-        mma16816(pacc[2 * mc], ap[1], a1[0], a1[2]);
-        mma16816(pacc[2 * mc + 1], ap[1], a1[1], a1[3]);
+        mma16816(pacc[2 * e], ap[2 * ks2], a0[0], a0[2]);
+        mma16816(pacc[2 * e + 1], ap[2 * ks2], a0[1], a0[3]);
+        mma16816(pacc[2 * e], ap[2 * ks2 + 1], a1[0], a1[2]);
+        mma16816(pacc[2 * e + 1], ap[2 * ks2 + 1], a1[1], a1[3]);
       }
     }
-  }
-  float zs = zs2.x + zs2.y;
-  zs += __shfl_xor_sync(0xffffffffu, zs, 1);
-  zs += __shfl_xor_sync(0xffffffffu, zs, 2);
 #pragma unroll
-  for (int cb = 0; cb < D / 8; ++cb) {
-    const float2 cj = __half22float2(Vc2[4 * cb + tq]);
-    float2 t = add2(make_float2(pacc[cb][0], pacc[cb][1]), make_float2(pacc[cb][2], pacc[cb][3]));
-    t = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(zs, zs)), cj);
-    const float2 o = fma2(make_float2(st.o[cb][0], st.o[cb][1]), make_float2(alpha[0], alpha[0]), t);
-    st.o[cb][0] = o.x;
-    st.o[cb][1] = o.y;
+    for (int cl = 0; cl < 8; ++cl) {
+      const int cb = 8 * mq + cl;
+      const float2 cj = __half22float2(Vc2[4 * cb + tq]);
+      float2 t = add2(make_float2(pacc[cl][0], pacc[cl][1]), make_float2(pacc[cl][2], pacc[cl][3]));
+      t = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(zs, zs)), cj);
+      const float2 o = fma2(make_float2(st.o[cb][0], st.o[cb][1]), make_float2(alpha[0], alpha[0]), t);
+      st.o[cb][0] = o.x;
+      st.o[cb][1] = o.y;
+    }
   }
 }
 
@@ -604,7 +608,6 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     const int vh = vg * NH + hl;
     return ((int64_t)b * p.chunk + vh / p.group) * p.num_q_heads + h * p.group + vh % p.group;
   };
-  const int g = lane >> 2, tq = lane & 3;
   grid_dependency_wait();  // lengths, partial tiles and pages come from the previous kernel
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
   int len = p.seq_lens[b];
@@ -671,7 +674,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       for (int e = 0; e < D / 32; ++e) {
         const int j = lane * (D / 32) + e;
         const float x = v[e] * sc;
-        qsm[hl * QLD + (j & ~15) + 4 * ((j & 7) >> 1) + 2 * ((j >> 3) & 1) + (j & 1)] = x;
+        if constexpr (S::kQBytes > 0) qsm[hl * QLD + (j & ~15) + 4 * ((j & 7) >> 1) + 2 * ((j >> 3) & 1) + (j & 1)] = x;
         const float xb = (j & 15) >= 8 ? x * (KB == 4 ? 0.0625f : 0.25f) : x;
         const __half hi = __float2half_rn(xb);
         qe[4 * (j >> 1) + (j & 1)] = hi;
@@ -767,6 +770,10 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   float* pS = reinterpret_cast<float*>(recs + 512 * D);
   float* mS = pS + kTile * NH;
   float* lS = mS + NH;
+  // q in the original basis: the fp32 q~ area, or after the softmax scratch where there is none
+  constexpr int kPartQ = (512 * D + 4 * NH * (kTile + 2) + 15) & ~15;
+  static_assert(S::kQBytes > 0 || S::kRecBytes >= kPartQ + NH * QLD * 4, "partial q fits");
+  float* qp = S::kQBytes > 0 ? qsm : reinterpret_cast<float*>(recs + kPartQ);
   const int c0 = lane * E;
   const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
   if (threadIdx.x == 0) {
@@ -782,7 +789,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int j = c0 + e;
-      qsm[hl * QLD + j] =
+      qp[hl * QLD + j] =
           (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) * p.qscale : 0.0f;
     }
   }
@@ -800,7 +807,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     float v[32];
     float qv[NH][E];
 #pragma unroll
-    for (int hl = 0; hl < NH; ++hl) load_f32<E>(qsm + hl * QLD + c0, qv[hl]);
+    for (int hl = 0; hl < NH; ++hl) load_f32<E>(qp + hl * QLD + c0, qv[hl]);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int t = tb * R + r;
