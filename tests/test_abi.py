@@ -102,3 +102,21 @@ def test_validation_returns_before_launch(kv):
     assert lib.kvarn_dequantize_tiles(ctypes.byref(bad), null, 1, null, 1, null, null, null,
                                       null) == kv.KVARN_ERR_UNSUPPORTED
     assert "workspace" in kv.status_string(kv.KVARN_ERR_WORKSPACE_TOO_SMALL)
+
+
+def test_fp16_baseline_validation(kv):
+    # the fp16 baseline decode refuses unsupported shapes and bad arguments before any launch
+    lib = kv._lib
+    null = ctypes.c_void_p(0)
+    p16 = ctypes.c_void_p(16)
+    assert kv.fp16_page_bytes(128) == 2 * 128 * 128 * 2
+    assert kv.fp16_page_bytes(96) == 0
+    assert lib.kvarn_fp16_decode_workspace_bytes(128, 2, 32, 4) == 2 * 32 * 1 * (128 + 4) * 4
+    args = lambda hd, hkv, hq, ws_bytes, pool=p16: (hd, hkv, 2, hq, p16, pool, 8, p16, 4, p16,
+                                                     ctypes.c_float(0.1), p16, p16, ws_bytes, null, null)
+    assert lib.kvarn_fp16_decode_attention(*args(96, 8, 32, 1 << 20)) == kv.KVARN_ERR_UNSUPPORTED
+    assert lib.kvarn_fp16_decode_attention(*args(128, 8, 24, 1 << 20)) == kv.KVARN_ERR_UNSUPPORTED
+    assert lib.kvarn_fp16_decode_attention(*args(128, 8, 32, 16)) == kv.KVARN_ERR_WORKSPACE_TOO_SMALL
+    assert lib.kvarn_fp16_decode_attention(*args(128, 8, 32, 1 << 20, ctypes.c_void_p(24))) == \
+        kv.KVARN_ERR_INVALID_ARG
+    assert lib.kvarn_selftest_wait_timeout(null, null) == kv.KVARN_ERR_INVALID_ARG
