@@ -105,7 +105,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.device_id, "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -115,9 +115,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def mark(self):
+        """Host time, to bracket the timed region."""
+        return time.time()
+
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -129,7 +133,14 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
+        lines = self.lines
+        inside = [ln for t, ln in lines if window is None or window[0] <= t <= window[1]]
+        where = "during the timed region"
+        if not inside and window is not None and lines:  # a region shorter than the sampling interval
+            mid = 0.5 * (window[0] + window[1])
+            inside = [ln for t, ln in sorted(lines, key=lambda x: abs(x[0] - mid))[:3]]
+            where = "nearest the timed region (shorter than the 50 ms sampling interval)"
+        for line in inside:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
@@ -143,7 +154,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "sampled": where}
 
 
 def _device_id(torch):
@@ -532,12 +543,14 @@ def _run_kvarn(args, torch, world, rank):
     clocks.start()
     time.sleep(0.3)
     torch.cuda.synchronize()
+    w0 = clocks.mark()
     t0.record(stream)
     for i in range(args.steps):
         step(ev=dec_ev.get(i))
     t1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    w1 = clocks.mark()
+    clk = clocks.stop(window=(w0, w1))
     elapsed_ms = t0.elapsed_time(t1)
     dec_ms = [a.elapsed_time(b) for a, b in dec_ev.values()]
     status = int(S["status"].item())
@@ -653,6 +666,9 @@ def _run_kvarn(args, torch, world, rank):
             "workload": WORKLOAD.replace("batch 64", "batch %d" % BATCH),
             "batch": BATCH, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D0,
             "seq_len": "128*U{8..128}", "mean_seq_len": float(lens_before.double().mean()),
+            "growth": "each step appends one token per sequence (a tile seals every 128 steps per "
+                      "sequence); mean length over the timed steps %.0f"
+                      % (float(lens_before.double().mean()) + (args.steps + 1) / 2),
             "preset": "kvarn_k4v2_g128",
             "l2": "inputs larger than L2: each decode reads %.0f MB of packed cache" % (dec_bytes[0] / 1e6),
         },
@@ -837,7 +853,7 @@ def _run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("kvarn", "reference"), default="kvarn")
     ap.add_argument("--batch", type=int, default=64,
