@@ -36,7 +36,7 @@ METRIC = "K4V2 g128 decode-attn KV tokens/s & HBM GB/s; quantize tokens/s (1 GB3
 QUANT_OPS_PER_ELEMENT = 37  # fp32 ops per quantised element (derivation at the quantize timing)
 SM_MAX_MHZ = 2070.0
 ADAPTIVE_TOL = 0.05  # early-stop tolerance of the normalisation (log-factor change per iteration)
-DEC_EVENT_EVERY = 5  # timed steps between two live samples of the decode call's duration
+DEC_EVENT_SAMPLES = 40  # live samples of the decode call's duration, spread over the timed steps
 WORKLOAD = ("paged decode attention + append: batch 64, seq_len 128*U{8..128}, 32 q heads / 8 kv "
             "heads, head_dim 128, K4V2 g128 packed cache, permuted block table")
 BATCH, HQ, HKV, D0, MIN_PAGES, MAX_PAGES, SEED = 64, 32, 8, 128, 8, 128, 3
@@ -533,10 +533,11 @@ def _run_kvarn(args, torch, world, rank):
     if world > 1:
         torch.distributed.barrier()
     lens_before = S["lens"][state["cur"]].to(torch.int64).cpu()
-    # The decode call's own duration is sampled live on every DEC_EVENT_EVERY-th timed step: an
-    # event recorded between append and decode ends their programmatic-launch overlap, so the
-    # other steps run without it.
-    sampled = [i for i in range(args.steps) if i % DEC_EVENT_EVERY == 0]
+    # The decode call's own duration is sampled live on DEC_EVENT_SAMPLES evenly spaced timed
+    # steps: an event recorded between append and decode ends their programmatic-launch
+    # overlap, so the other steps run without it.
+    every = max(1, args.steps // DEC_EVENT_SAMPLES)
+    sampled = [i for i in range(args.steps) if i % every == 0]
     dec_ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(_device_id(torch))
@@ -686,7 +687,7 @@ def _run_kvarn(args, torch, world, rank):
                               "when decode.cu changed since that capture",
             "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
             "duration_source": "CUDA events on the launching stream around the decode call on every "
-                               "%dth timed step (%d of %d)" % (DEC_EVENT_EVERY, len(dec_ms), args.steps),
+                               "%dth timed step (%d of %d)" % (every, len(dec_ms), args.steps),
         },
         "quantize": {
             "workload": "one layer, 8 KV heads x 16384 tokens x head_dim 128 (K and V), L2 flushed",
