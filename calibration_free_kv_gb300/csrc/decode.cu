@@ -1020,33 +1020,72 @@ __global__ void __launch_bounds__(128) chunk_kernel(DecodeParams p) {
   const int hq = gw % p.num_q_heads, bc = gw / p.num_q_heads;
   const int b = bc / p.chunk, c = bc - b * p.chunk;
   const int h = hq / p.group;
+  const int c0 = lane * E;
+  const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
   float q[E], o[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    const int j = lane * E + e;
-    q[e] = j < p.d0 ? __half2float(p.q[(int64_t)gw * p.d0 + j]) * p.qscale : 0.0f;
+    q[e] = in ? __half2float(p.q[(int64_t)gw * p.d0 + c0 + e]) * p.qscale : 0.0f;
     o[e] = 0.0f;
   }
   float m = -INFINITY, l = 0.0f;
-  for (int t = 0; t <= c; ++t) {
-    const int64_t row = (((int64_t)b * p.chunk + t) * p.num_kv_heads + h) * p.d0;
-    float dot = 0.0f;
-    float vv[E];
+  const int n_tok = c + 1;  // chunk tokens 0..c
+  const int64_t rstride = (int64_t)p.num_kv_heads * p.d0;
+  const __half* kbase = p.chunk_k + ((int64_t)b * p.chunk * p.num_kv_heads + h) * p.d0 + c0;
+  const __half* vbase = p.chunk_v + ((int64_t)b * p.chunk * p.num_kv_heads + h) * p.d0 + c0;
+  for (int t0 = 0; t0 < n_tok; t0 += 32) {
+    // logits of tokens t0 + i: each lane sums its channels for 32 tokens, a halving shuffle
+    // butterfly leaves token t0 + i complete in lane i
+    float v[32];
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int j = lane * E + e;
-      const float kx = j < p.d0 ? __half2float(p.chunk_k[row + j]) : 0.0f;
-      vv[e] = j < p.d0 ? __half2float(p.chunk_v[row + j]) : 0.0f;
-      dot = fmaf(q[e], kx, dot);
+    for (int i = 0; i < 32; ++i) {
+      float kf[E];
+      if (t0 + i < n_tok && in) {
+        load_f16<E>(kbase + (t0 + i) * rstride, kf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) kf[e] = 0.0f;
+      }
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc = fmaf(q[e], kf[e], acc);
+      v[i] = acc;
     }
 #pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, msk);
-    const float mnew = fmaxf(m, dot);
-    const float a = exp2f(m - mnew), pv = exp2f(dot - mnew);
-    m = mnew;
-    l = fmaf(l, a, pv);
+    for (int w = 16; w >= 1; w >>= 1) {
+      const bool up = (lane & w) != 0;
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = fmaf(o[e], a, pv * vv[e]);
+      for (int i = 0; i < w; ++i) {
+        const float send = up ? v[i] : v[i + w];
+        const float keep = up ? v[i + w] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
+    }
+    const bool live = t0 + lane < n_tok;
+    float mx = live ? v[0] : -INFINITY;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+    const float mnew = fmaxf(m, mx);
+    const float a = exp2f(m - mnew);
+    const float pv = live ? exp2f(v[0] - mnew) : 0.0f;
+    float ps = pv;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, msk);
+    m = mnew;
+    l = fmaf(l, a, ps);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] *= a;
+    const int cnt = min(32, n_tok - t0);
+#pragma unroll 8
+    for (int i = 0; i < cnt; ++i) {
+      const float pw = __shfl_sync(0xffffffffu, pv, i);
+      if (in) {
+        float vf[E];
+        load_f16<E>(vbase + (t0 + i) * rstride, vf);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = fmaf(pw, vf[e], o[e]);
+      }
+    }
   }
   warp_fwht<D>(o, lane);
   const int cap = p.max_pages * kTile + (kTile - 1);

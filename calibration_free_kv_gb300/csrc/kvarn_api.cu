@@ -266,6 +266,7 @@ int kvarn_prefill_attention(const kvarn_desc* desc, int batch, int num_q_heads, 
   if (q == nullptr || chunk_k == nullptr || chunk_v == nullptr || page_pool == nullptr ||
       block_table == nullptr || cache_lens == nullptr || out == nullptr || workspace == nullptr)
     return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(chunk_k) || !aligned16(chunk_v)) return KVARN_ERR_INVALID_ARG;
   if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
   if (!aligned16(page_pool) || !aligned16(workspace) || !aligned16(partial_k) || !aligned16(partial_v))
     return KVARN_ERR_INVALID_ARG;

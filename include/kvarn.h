@@ -184,8 +184,9 @@ size_t kvarn_prefill_workspace_bytes(const kvarn_desc* desc, int batch, int num_
  * sequence b attends to the cache_lens[b] cached tokens (sealed pages + raw partial tile)
  * and to chunk tokens 0..c.
  *  q            fp16 [batch][chunk_len][Hq][d0];  out fp16 [batch][chunk_len][Hq][d0].
- *  chunk_k/v    fp16 [batch][chunk_len][Hkv][d0]: the chunk's own keys and values (raw; quantise
- *               them into the cache afterwards with kvarn_quantize_tiles / kvarn_append_token).
+ *  chunk_k/v    fp16 [batch][chunk_len][Hkv][d0], 16-byte aligned: the chunk's own keys and
+ *               values (raw; quantise them into the cache afterwards with kvarn_quantize_tiles /
+ *               kvarn_append_token).
  *  cache_lens   device int32 [batch]: cached tokens before the chunk (as seq_lens of decode).
  *  Other arguments as kvarn_decode_attention; workspace >= kvarn_prefill_workspace_bytes.
  *  UNSUPPORTED if chunk_len * G / 8 (/ 4 at head_dim 256) * Hkv exceeds 65535. */
