@@ -51,9 +51,10 @@ K_BITS = 4                 # preset kvarn_k4v2_g128                  [hotdry Â§æ
 V_BITS = 2
 # Other presets run the same pipeline with other code widths [vatt Â§å››å€‹æ­¥é©Ÿ, bit-width
 # assignment: other k/v bit presets take the same path; vatt Â§æ€Žéº¼ç”¨, key/value bits knobs].
-# Reading: widths of 2 and 4 bits on either side; tiles stay 128 tokens.
-PRESETS = {"kvarn_k4v2_g128": (4, 2), "kvarn_k4v4_g128": (4, 4), "kvarn_k2v2_g128": (2, 2)}
-CODE_BITS = (2, 4)
+# Reading: widths of 2, 4 and 8 bits on either side; tiles stay 128 tokens.
+PRESETS = {"kvarn_k4v2_g128": (4, 2), "kvarn_k4v4_g128": (4, 4), "kvarn_k2v2_g128": (2, 2),
+           "kvarn_k8v4_g128": (8, 4)}
+CODE_BITS = (2, 4, 8)
 SINKHORN_ITERS = 4         # typical count three to five             [hotdry Â§è¿­ä»£æ–¹å·®å½’ä¸€åŒ–, step 3]
 SINKHORN_EPS = 1e-6        # reading: stds below this are not normalised (pages give no value)
 SCALE_FLOOR = 1e-8         # reading: quantiser step floor for constant groups
@@ -209,7 +210,7 @@ def quantize_tile(tile: np.ndarray, kind: str, d: int | None = None,
        z'_j = m_j c_j (fp16) and the token factor r_i (fp16).
     V: 2-bit (default), scale/zero per token over the channels; stored s'_i = s_i r_i,
        z'_i = m_i r_i (fp16) and the channel factor c_j (fp16).
-    `bits` overrides the width (2 or 4) for the other presets; `tol` > 0 stops the
+    `bits` overrides the width (2, 4 or 8) for the other presets; `tol` > 0 stops the
     normalisation early (see sinkhorn_normalise).
     Returns dict(codes [...,T,d] uint8, scale fp16, zero fp16, factor fp16, pre f64, bits,
     iters = iterations used per tile).
@@ -282,6 +283,8 @@ def dequantize_tile(codes, scale, zero, factor, kind: str, d0: int) -> np.ndarra
 #          (rho, h, p) at nibble h + 2rho + 4p.
 #   2-bit: word ((o//2*ni4 + i//4)*32 + lane)*4 + i%4 holds fragments (o, i) for both
 #          o of the pair, element (rho, h, p) of block o at slot 2(o%2) + h + 4rho + 8p.
+#   8-bit: words ((o*ni2 + i//2)*32 + lane)*4 + 2(i%2) + h, h = 0, 1, hold fragment (o, i),
+#          element (rho, h, p) at byte rho + 2p of word h; ni2 = d // 32.
 # For kvarn_k4v2_g128: K word (mi, kk, lane) holds token t = 16mi + g + 8rho and channel
 # j = 16kk + 8h + 2tq + p at nibble h + 2rho + 4p; V word (ks2, mc, lane) holds channel
 # j = 16mc + g + 8rho and token t = 16(2ks2+f) + 8h + 2tq + p at 2-bit slot
@@ -330,8 +333,11 @@ def _code_positions(kind: str, bits: int, d: int):
     elif bits == 2:
         word = (((o // 2) * ni4 + i // 4) * 32 + lane) * 4 + i % 4
         shift = 2 * (2 * (o % 2) + h + 4 * rho + 8 * p)
+    elif bits == 8:
+        word = ((o * (d // 32) + i // 2) * 32 + lane) * 4 + 2 * (i % 2) + h
+        shift = 8 * (rho + 2 * p)
     else:
-        raise ValueError("code bits must be 2 or 4")
+        raise ValueError("code bits must be 2, 4 or 8")
     return word, shift
 
 

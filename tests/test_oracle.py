@@ -127,7 +127,7 @@ def test_worked_2bit_example():
     assert ko.rtn_dequantize(np.array([3]), s, m, axis=0)[0] == pytest.approx(28.0, abs=1e-12)
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_rtn_matches_brute_force(bits):
     # round-to-nearest == the nearest of the 2^b grid points (ties aside)
     rng = np.random.default_rng(10 + bits)
@@ -406,7 +406,7 @@ def test_pack_roundtrip(d):
 
 # --- other k/v bit presets (vatt §四個步驟, bit-width assignment: same pipeline) ----------
 
-_WIDTHS = [(4, 2), (4, 4), (2, 2), (2, 4)]
+_WIDTHS = [(4, 2), (4, 4), (2, 2), (2, 4), (8, 4), (4, 8)]
 
 
 def test_record_bytes_presets():
@@ -415,6 +415,8 @@ def test_record_bytes_presets():
     assert ko.record_bytes(128, k_bits=2, v_bits=2) == 4096 + 4096 + 1536 == 9728
     assert ko.record_bytes(256, k_bits=4, v_bits=4) == 16384 + 16384 + 2304
     assert ko.record_bytes(64, k_bits=2, v_bits=4) == 2048 + 4096 + 1152
+    assert ko.record_bytes(128, k_bits=8, v_bits=4) == 16384 + 8192 + 1536 == 26112
+    assert ko.record_bytes(256, k_bits=8, v_bits=4) == 32768 + 16384 + 2304
     assert set(ko.PRESETS.values()) <= set(_WIDTHS)
     assert ko.PRESETS["kvarn_k4v2_g128"] == (ko.K_BITS, ko.V_BITS)
     for kb, vb in _WIDTHS:
@@ -422,7 +424,7 @@ def test_record_bytes_presets():
 
 
 @pytest.mark.parametrize("kind", ["K", "V"])
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 @pytest.mark.parametrize("d", [64, 256])
 def test_code_positions_bijective(kind, bits, d):
     word, shift = ko._code_positions(kind, bits, d)
@@ -437,7 +439,9 @@ def test_code_words_are_mma_fragments_all_widths(kb, vb):
     # the words of every width carry m16n8k16 A fragments (PTX fragment table): K's of
     # codes[token, channel], V's of codes^T[channel, token]; 4-bit words one fragment with
     # register r's (lo, hi) pair at nibbles (n, n+4), 2-bit words the fragments of two
-    # consecutive token blocks (K: rows, V: columns) with pairs at slots (n, n+8)
+    # consecutive token blocks (K: rows, V: columns) with pairs at slots (n, n+8), 8-bit
+    # fragments two consecutive words (registers 0, 1 in the first, 2, 3 in the second) with
+    # pairs at bytes (n, n+2)
     d = 64
     rng = np.random.default_rng(kb * 10 + vb)
     qk = rng.integers(0, 1 << kb, (128, d)).astype(np.uint8)
@@ -460,6 +464,11 @@ def test_code_words_are_mma_fragments_all_widths(kb, vb):
                     if bits == 4:
                         w = int(words[((o * (d // 64) + i // 4) * 32 + lane) * 4 + i % 4])
                         got = [((w >> 4 * n) & mask, (w >> 4 * (n + 4)) & mask) for n in (0, 2, 1, 3)]
+                    elif bits == 8:
+                        base = ((o * (d // 32) + i // 2) * 32 + lane) * 4 + 2 * (i % 2)
+                        got = []
+                        for w in (int(words[base]), int(words[base + 1])):
+                            got += [((w >> 8 * n) & mask, (w >> 8 * (n + 2)) & mask) for n in (0, 1)]
                     else:
                         w = int(words[(((o // 2) * (d // 64) + i // 4) * 32 + lane) * 4 + i % 4])
                         f = o % 2
@@ -487,7 +496,7 @@ def test_pack_roundtrip_all_widths(kb, vb):
         for key in a:
             np.testing.assert_array_equal(a[key], b[key])
     with pytest.raises(ValueError):   # a code wider than its section
-        ko.pack_record(dict(k, codes=np.full((128, d), 1 << kb, np.uint8)), v)
+        ko.pack_record(dict(k, codes=np.full((128, d), 1 << kb, np.uint16)), v)
 
 
 def test_quantize_widths_closed_form_and_error_order():
@@ -495,7 +504,7 @@ def test_quantize_widths_closed_form_and_error_order():
     r, c, x = _rank_one_scaled(128, 128, 11)
     tile = ko.rotate(x, 128)
     y = _checker(128, 128)
-    for bits in (2, 4):
+    for bits in (2, 4, 8):
         for kind in ("K", "V"):
             qd = ko.quantize_tile(tile, kind, bits=bits)
             assert qd["bits"] == bits
@@ -505,7 +514,7 @@ def test_quantize_widths_closed_form_and_error_order():
     for kind, t in (("K", k), ("V", v)):
         tile = t[:, 0].double().numpy()
         errs = []
-        for bits in (2, 4):
+        for bits in (2, 4, 8):
             qd = ko.quantize_tile(tile, kind, bits=bits)
             assert qd["codes"].max() <= 2 ** bits - 1
             back = ko.dequantize_tile(qd["codes"], qd["scale"], qd["zero"], qd["factor"], kind, 128)
@@ -515,8 +524,14 @@ def test_quantize_widths_closed_form_and_error_order():
             s = qd["scale"].astype(np.float64)
             f = qd["factor"].astype(np.float64)
             step = f[:, None] * s[None, :] if kind == "K" else s[:, None] * f[None, :]
-            assert np.all(np.abs(br - xr) <= 0.5 * step * 1.01 + 1e-3 * np.abs(xr) + 1e-6)
-        assert errs[1] < errs[0]
+            # half a step of rounding, plus the fp16 storage of factor, scale and zero (each
+            # within 2^-11 relative): |f16(f)(q f16(s) + f16(z)) - f(q s + z)| <= 2^-10 f (q s + |z|)
+            q = qd["codes"].astype(np.float64)
+            z = np.abs(qd["zero"].astype(np.float64))
+            meta = f[:, None] * (q * s[None, :] + z[None, :]) if kind == "K" else \
+                f[None, :] * (q * s[:, None] + z[:, None])
+            assert np.all(np.abs(br - xr) <= (0.5 * step + 2.0 ** -10 * meta) * 1.01 + 1e-6)
+        assert errs[2] < errs[1] < errs[0]
 
 
 def test_decode_sequence_presets_roundtrip():
