@@ -477,7 +477,9 @@ def _decode_configs(torch, kv, synth, peak, args):
             ("preset_kvarn_k4v4_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
                                                        seed=6, preset="kvarn_k4v4_g128")),
             ("preset_kvarn_k2v2_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
-                                                       seed=6, preset="kvarn_k2v2_g128"))):
+                                                       seed=6, preset="kvarn_k2v2_g128")),
+            ("preset_kvarn_k8v4_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
+                                                       seed=6, preset="kvarn_k8v4_g128"))):
         if args.extras not in ("all", group):
             continue
         if args.extra_batch:
@@ -621,7 +623,7 @@ def _run_kvarn(args, torch, world, rank):
                   "mean_iterations": a_iters, "max_iterations": 4}
     q_presets = {}
     if args.extras in ("all", "presets"):
-        for name in ("kvarn_k4v4_g128", "kvarn_k2v2_g128"):
+        for name in ("kvarn_k4v4_g128", "kvarn_k2v2_g128", "kvarn_k8v4_g128"):
             ms, nb = _time_quantize(torch, kv, synth, dev, stream, preset=name, reps=10)
             q_presets[name] = {"us": ms * 1e3, "tokens_per_s": Q_TOKENS / (ms * 1e-3),
                                "hbm_gbs": nb / (ms * 1e-3) / 1e9}

@@ -56,6 +56,18 @@ struct DecodeShape {
   static constexpr int kMinBlocks = 2 * (kSmemBytes + 1024) <= 233472 ? 2 : 1;
 };
 
+// Power-of-two factors on the fp16 hi + lo query of the QK operand for channels 0..7 (kH0) and
+// 8..15 (kH1) of every 16, and on the MMA sum (kAcc).  4- and 2-bit codes of channels 8..15 sit
+// 4 / 2 bits higher in their fp16 subnormals.  8-bit codes have a small scale s' against their
+// zero point (the sum cancels against q~ . z'), so q is lifted by 2^8 to keep the lo parts of q
+// and of q s' out of the fp16 subnormal range.
+template <int KB>
+struct QkScale {
+  static constexpr float kH0 = KB == 8 ? 256.0f : 1.0f;
+  static constexpr float kH1 = KB == 4 ? 0.0625f : (KB == 2 ? 0.25f : 256.0f);
+  static constexpr float kAcc = KB == 8 ? kTwo24 / 256.0f : kTwo24;
+};
+
 template <int D, int NT>
 struct WarpAcc {
   float m[NT], l[NT];
@@ -144,8 +156,29 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
       }
       logits(mi, acc, kTwo24);
     }
+  } else if constexpr (KB == 8) {  // two words per fragment; a 16-byte load holds two
+#pragma unroll
+    for (int mi = 0; mi < 8; ++mi) {
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+#pragma unroll
+      for (int kp = 0; kp < D / 32; ++kp) {
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi * (D / 32) + kp) * 32 + lane) * 16);
+        uint32_t a0[4], a1[4];
+        unpack_k8(w4.x, w4.y, a0);
+        unpack_k8(w4.z, w4.w, a1);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(acc[nt], a0, bq[2 * kp][nt][0], bq[2 * kp][nt][1]);
+          mma16816(acc[nt], a1, bq[2 * kp + 1][nt][0], bq[2 * kp + 1][nt][1]);
+        }
+      }
+      logits(mi, acc, QkScale<KB>::kAcc);
+    }
   } else {  // 2-bit: one word per channel block kk holds token blocks 2mi2 and 2mi2 + 1
-    static_assert(KB == 2, "2- or 4-bit K codes");
+    static_assert(KB == 2, "2-, 4- or 8-bit K codes");
 #pragma unroll
     for (int mi2 = 0; mi2 < 4; ++mi2) {
       float acc0[NT][4], acc1[NT][4];
@@ -325,8 +358,8 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
   const __half2* Kz2 = reinterpret_cast<const __half2*>(Rk + RL.kzero);
   const __half2* Kr2 = reinterpret_cast<const __half2*>(Rk + RL.kfactor);
   uint32_t aq[D / 16][4];  // head g: rows g = hi, g + 8 = lo; channels 2tq.. and 2tq + 8..
-  // q~ . z' from q~ = hi + lo (channels 8..15 of each 16 carry the codes' 2^-4 / 2^-2 scale)
-  constexpr float kUndo = KB == 4 ? 16.0f : 4.0f;
+  // q~ . z' from q~ = hi + lo, with the operand factors of QkScale undone
+  constexpr float kUndo0 = 1.0f / QkScale<KB>::kH0, kUndo1 = 1.0f / QkScale<KB>::kH1;
   float2 qz2 = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
@@ -334,8 +367,10 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
     const __half2 s0 = Ks2[jp], s1 = Ks2[jp + 4];
     const float2 z0 = __half22float2(Kz2[jp]), z1 = __half22float2(Kz2[jp + 4]);
     const uint2 u0 = qhl[g * QH + jp], u1 = qhl[g * QH + jp + 4];
-    qz2 = fma2(add2(__half22float2(u2h2(u0.x)), __half22float2(u2h2(u0.y))), z0, qz2);
-    qz2 = fma2(mul2(add2(__half22float2(u2h2(u1.x)), __half22float2(u2h2(u1.y))), make_float2(kUndo, kUndo)),
+    float2 q0 = add2(__half22float2(u2h2(u0.x)), __half22float2(u2h2(u0.y)));
+    if constexpr (QkScale<KB>::kH0 != 1.0f) q0 = mul2(q0, make_float2(kUndo0, kUndo0));
+    qz2 = fma2(q0, z0, qz2);
+    qz2 = fma2(mul2(add2(__half22float2(u2h2(u1.x)), __half22float2(u2h2(u1.y))), make_float2(kUndo1, kUndo1)),
                z1, qz2);
     split_hi_lo(u2h2(u0.x), u2h2(u0.y), s0, aq[kk][0], aq[kk][1]);
     split_hi_lo(u2h2(u1.x), u2h2(u1.y), s1, aq[kk][2], aq[kk][3]);
@@ -371,8 +406,27 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
       logits(2 * mi, acc0, kTwo24);
       logits(2 * mi + 1, acc1, kTwo24);
     }
+  } else if constexpr (KB == 8) {  // two words per 16 x 16 block; a 16-byte load holds two blocks
+#pragma unroll
+    for (int mi = 0; mi < 8; ++mi) {
+      float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kp = 0; kp < D / 32; ++kp) {
+        const uint4 w4 =
+            *reinterpret_cast<const uint4*>(Rk + RL.kcodes + ((mi * (D / 32) + kp) * 32 + lane) * 16);
+        uint32_t a[4];
+        unpack_k8(w4.x, w4.y, a);
+        mma16816(acc0, aq[2 * kp], a[0], a[2]);
+        mma16816(acc1, aq[2 * kp], a[1], a[3]);
+        unpack_k8(w4.z, w4.w, a);
+        mma16816(acc0, aq[2 * kp + 1], a[0], a[2]);
+        mma16816(acc1, aq[2 * kp + 1], a[1], a[3]);
+      }
+      logits(2 * mi, acc0, QkScale<KB>::kAcc);
+      logits(2 * mi + 1, acc1, QkScale<KB>::kAcc);
+    }
   } else {  // 2-bit: one word holds 16-token blocks 2mi2 and 2mi2 + 1 of a channel block
-    static_assert(KB == 2, "2- or 4-bit K codes");
+    static_assert(KB == 2, "2-, 4- or 8-bit K codes");
 #pragma unroll
     for (int mi2 = 0; mi2 < 4; ++mi2) {
       float acc[4][4];
@@ -658,8 +712,8 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     }
     // rotated queries of this kv head's group, scaled by tau log2(e) / sqrt(d): fp32 for q~.z'
     // (channels 16k + {2t, 2t+1, 2t+8, 2t+9} adjacent), fp16 hi + lo for the B operand
-    // (channels 8..15 of every 16 pre-divided by 16, the subnormal scale of their codes; one
-    // {hi pair, lo pair} entry per channel pair)
+    // (times the QkScale factors of the code width; one {hi pair, lo pair} entry per channel
+    // pair)
     for (int hl = warp; hl < NH; hl += kDecWarps) {
       float v[D / 32];
 #pragma unroll
@@ -675,7 +729,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
         const int j = lane * (D / 32) + e;
         const float x = v[e] * sc;
         if constexpr (S::kQBytes > 0) qsm[hl * QLD + (j & ~15) + 4 * ((j & 7) >> 1) + 2 * ((j >> 3) & 1) + (j & 1)] = x;
-        const float xb = (j & 15) >= 8 ? x * (KB == 4 ? 0.0625f : 0.25f) : x;
+        const float xb = x * ((j & 15) >= 8 ? QkScale<KB>::kH1 : QkScale<KB>::kH0);
         const __half hi = __float2half_rn(xb);
         qe[4 * (j >> 1) + (j & 1)] = hi;
         qe[4 * (j >> 1) + 2 + (j & 1)] = __float2half_rn(xb - __half2float(hi));
@@ -1140,6 +1194,7 @@ int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cuda
   if (kb == 4 && vb == 2) return launch_decode_bits<4, 2>(d, nt, p, stream);
   if (kb == 4 && vb == 4) return launch_decode_bits<4, 4>(d, nt, p, stream);
   if (kb == 2 && vb == 2) return launch_decode_bits<2, 2>(d, nt, p, stream);
+  if (kb == 8 && vb == 4) return launch_decode_bits<8, 4>(d, nt, p, stream);
   return KVARN_ERR_UNSUPPORTED;
 }
 

@@ -41,6 +41,15 @@ __device__ __forceinline__ void unpack_k(uint32_t x, uint32_t (&a)[4]) {
   a[3] = y & 0x00F000F0u;
 }
 
+// 8-bit fragment words w0, w1 -> A fragment as fp16 subnormals code * 2^-24: register rho + 2h
+// takes bytes rho and rho + 2 of word h (every code below 2^10, so each is exact).
+__device__ __forceinline__ void unpack_k8(uint32_t w0, uint32_t w1, uint32_t (&a)[4]) {
+  a[0] = __byte_perm(w0, 0u, 0x4240);
+  a[1] = __byte_perm(w0, 0u, 0x4341);
+  a[2] = __byte_perm(w1, 0u, 0x4240);
+  a[3] = __byte_perm(w1, 0u, 0x4341);
+}
+
 // V word -> the A fragments of token blocks 2ks2 (a0) and 2ks2+1 (a1) as fp16 subnormals:
 // block f, token half h -> code * 2^(-24 + 4f + 2h).
 __device__ __forceinline__ void unpack_v(uint32_t x, uint32_t (&a0)[4], uint32_t (&a1)[4]) {

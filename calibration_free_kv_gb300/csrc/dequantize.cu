@@ -17,13 +17,31 @@ struct DequantShape {
   static constexpr int kSmemBytes = kTile * kLd * 4;
 };
 
+// Code of element (rho, h, p) of fragment (o, i) for lane `lane` (layout in kvarn.h): a 4-bit
+// word holds one fragment, a 2-bit word the fragments of token blocks o and o ^ 1, an 8-bit
+// fragment two words.
+template <int D, int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t* w, int o, int i, int lane, int rho, int h,
+                                            int pp) {
+  int word, sh;
+  if constexpr (BITS == 4) {
+    word = ((o * (D / 64) + i / 4) * 32 + lane) * 4 + (i & 3);
+    sh = 4 * (h + 2 * rho + 4 * pp);
+  } else if constexpr (BITS == 8) {
+    word = ((o * (D / 32) + i / 2) * 32 + lane) * 4 + 2 * (i & 1) + h;
+    sh = 8 * (rho + 2 * pp);
+  } else {
+    static_assert(BITS == 2, "2-, 4- or 8-bit codes");
+    word = (((o >> 1) * (D / 64) + i / 4) * 32 + lane) * 4 + (i & 3);
+    sh = 2 * (2 * (o & 1) + h + 4 * rho + 8 * pp);
+  }
+  return (w[word] >> sh) & ((1u << BITS) - 1u);
+}
+
 // grid.x = pages * Hkv * 2, block = 128 threads (one token row each while decoding codes).
-// Code word positions as in kvarn.h: a 4-bit word holds one fragment, a 2-bit word the
-// fragments of two consecutive token blocks.
 template <int D, int KB, int VB>
 __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
   constexpr RecordLayout RL = record_layout(D, KB, VB);
-  constexpr int NI4 = D / 64;
   constexpr int LD = DequantShape<D>::kLd;
   extern __shared__ __align__(16) float smem_x[];
   const int unit = blockIdx.x >> 1;
@@ -48,13 +66,10 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
     for (int kk = 0; kk < D / 16; ++kk) {
       for (int tq = 0; tq < 4; ++tq) {
         const int lane = 4 * g_t + tq;
-        const int wo = KB == 4 ? mi : mi >> 1;
-        const uint32_t w = kw[((wo * NI4 + kk / 4) * 32 + lane) * 4 + (kk & 3)];
         for (int hh = 0; hh < 2; ++hh)
           for (int pp = 0; pp < 2; ++pp) {
             const int j = 16 * kk + 8 * hh + 2 * tq + pp;
-            const int sh = KB == 4 ? 4 * (hh + 2 * rho + 4 * pp) : 2 * (2 * (mi & 1) + hh + 4 * rho + 8 * pp);
-            const uint32_t code = (w >> sh) & ((1u << KB) - 1u);
+            const uint32_t code = code_at<D, KB>(kw, mi, kk, lane, rho, hh, pp);
             smem_x[t * LD + j] =
                 r * fmaf((float)code, __half2float(ks[j]), __half2float(kz[j]));
           }
@@ -65,17 +80,14 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
     const float s = __half2float(reinterpret_cast<const __half*>(rec + RL.vscale)[t]);
     const float z = __half2float(reinterpret_cast<const __half*>(rec + RL.vzero)[t]);
     const __half* vc = reinterpret_cast<const __half*>(rec + RL.vfactor);
-    const int ks = t >> 4, ks2 = ks >> 1, f = ks & 1, hh = rho_or_h;
+    const int ks = t >> 4, hh = rho_or_h;
     const int tq = (t & 7) >> 1, pp = t & 1;
     for (int mc = 0; mc < D / 16; ++mc)
       for (int g = 0; g < 8; ++g) {
         const int lane = 4 * g + tq;
-        const int wo = VB == 4 ? ks : ks2;
-        const uint32_t w = vw[((wo * NI4 + mc / 4) * 32 + lane) * 4 + (mc & 3)];
         for (int rho = 0; rho < 2; ++rho) {
           const int j = 16 * mc + g + 8 * rho;
-          const int sh = VB == 4 ? 4 * (hh + 2 * rho + 4 * pp) : 2 * (2 * f + hh + 4 * rho + 8 * pp);
-          const uint32_t code = (w >> sh) & ((1u << VB) - 1u);
+          const uint32_t code = code_at<D, VB>(vw, ks, mc, lane, rho, hh, pp);
           smem_x[t * LD + j] = __half2float(vc[j]) * fmaf((float)code, s, z);
         }
       }
@@ -129,6 +141,7 @@ int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pa
   if (kb == 4 && vb == 2) return launch_dequant_bits<4, 2>(d, p, num_pages, stream);
   if (kb == 4 && vb == 4) return launch_dequant_bits<4, 4>(d, p, num_pages, stream);
   if (kb == 2 && vb == 2) return launch_dequant_bits<2, 2>(d, p, num_pages, stream);
+  if (kb == 8 && vb == 4) return launch_dequant_bits<8, 4>(d, p, num_pages, stream);
   return KVARN_ERR_UNSUPPORTED;
 }
 

@@ -21,7 +21,8 @@ struct Preset {
   int k_bits, v_bits;
 };
 constexpr Preset kPresets[] = {
-    {"kvarn_k4v2_g128", 4, 2}, {"kvarn_k4v4_g128", 4, 4}, {"kvarn_k2v2_g128", 2, 2}};
+    {"kvarn_k4v2_g128", 4, 2}, {"kvarn_k4v4_g128", 4, 4}, {"kvarn_k2v2_g128", 2, 2},
+    {"kvarn_k8v4_g128", 8, 4}};
 
 bool supported_bits(int kb, int vb) {
   for (const Preset& pr : kPresets)

@@ -520,8 +520,31 @@ __device__ __forceinline__ int quantize_rotated(float (&x)[4][16], uint8_t* __re
         *reinterpret_cast<uint2*>(vc + ((((4 * ch + j) * NI4 + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
             make_uint2(w[0][j], w[1][j]);
     }
+  } else if constexpr (BITS == 8) {
+    // fragment (row block 2lq + lh, column block 4ch + j) in two words h = 0, 1: element
+    // (rho, h, p) at byte rho + 2p of word h, which is gather4's order
+    auto w8 = [&](int lh, int j, int hh) {
+      const int c = 2 * (2 * j + hh), r0 = 2 * lh, r1 = 2 * lh + 1;
+      return gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
+    };
+    constexpr int NI2 = D / 32;
+    if constexpr (!TRANS) {  // words of (token block 2lq + lh, channel blocks 4ch + 2jj, + 1)
+      uint8_t* kc = rec + RL.kcodes;
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+          *reinterpret_cast<uint4*>(kc + (((2 * lq + lh) * NI2 + 2 * ch + jj) * 32 + lane) * 16) =
+              make_uint4(w8(lh, 2 * jj, 0), w8(lh, 2 * jj, 1), w8(lh, 2 * jj + 1, 0), w8(lh, 2 * jj + 1, 1));
+    } else {                 // words of (token block 4ch + j, channel blocks 2lq, 2lq + 1)
+      uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(vc + (((4 * ch + j) * NI2 + lq) * 32 + lane) * 16) =
+            make_uint4(w8(0, j, 0), w8(0, j, 1), w8(1, j, 0), w8(1, j, 1));
+    }
   } else {
-    static_assert(BITS == 2, "2- or 4-bit codes");
+    static_assert(BITS == 2, "2-, 4- or 8-bit codes");
     if constexpr (!TRANS) {
       // word (token blocks 2lq and 2lq + 1, channel block 4ch + j): slot 2lh + h + 4rho + 8p,
       // i.e. byte rho + 2p, bit pair 2lh + h
@@ -973,6 +996,7 @@ int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int unit
   if (kb == 4 && vb == 2) return launch_quantize_bits<4, 2>(d, p, units, stream);
   if (kb == 4 && vb == 4) return launch_quantize_bits<4, 4>(d, p, units, stream);
   if (kb == 2 && vb == 2) return launch_quantize_bits<2, 2>(d, p, units, stream);
+  if (kb == 8 && vb == 4) return launch_quantize_bits<8, 4>(d, p, units, stream);
   return KVARN_ERR_UNSUPPORTED;
 }
 

@@ -52,11 +52,13 @@
  *         at nibble h + 2rho + 4p.
  *  2-bit: word ((o/2*(d/64) + i/4)*32 + lane)*4 + i%4 holds fragments (o, i) of both token
  *         blocks o of a pair, element (rho, h, p) at 2-bit slot 2(o%2) + h + 4rho + 8p.
+ *  8-bit: words ((o*(d/32) + i/2)*32 + lane)*4 + 2(i%2) + h, h = 0, 1, hold fragment (o, i),
+ *         element (rho, h, p) at byte rho + 2p of word h.
  * For kvarn_k4v2_g128 K word (mi, kk, lane) holds token 16mi + g + 8rho, channel
  * 16kk + 8h + 2tq + p at nibble h + 2rho + 4p; V word (ks2, mc, lane) holds channel
  * 16mc + g + 8rho, token 16(2ks2 + f) + 8h + 2tq + p at slot 2f + h + 4rho + 8p.
  * record_bytes (d = 128 / 256): kvarn_k4v2_g128 13824 / 26880, kvarn_k4v4_g128 17920 / 35072,
- * kvarn_k2v2_g128 9728 / 18688.
+ * kvarn_k2v2_g128 9728 / 18688, kvarn_k8v4_g128 26112 / 51456.
  */
 #ifndef KVARN_H
 #define KVARN_H
@@ -85,7 +87,7 @@ typedef struct kvarn_desc {
   int32_t head_dim_padded;   /* d = 64, 128 or 256                                  */
   int32_t num_kv_heads;      /* Hkv                                                 */
   int32_t tile_tokens;       /* 128 (one tile == one page) [vatt §怎麼用 knob table]  */
-  int32_t k_bits;            /* 4 (kvarn_k4v2_g128, kvarn_k4v4_g128) or 2           */
+  int32_t k_bits;            /* 4 (kvarn_k4v2_g128, kvarn_k4v4_g128), 2 or 8        */
   int32_t v_bits;            /* 2 (kvarn_k4v2_g128, kvarn_k2v2_g128) or 4           */
   int32_t sinkhorn_iters;    /* 4 (0..8 accepted)                                   */
   float sinkhorn_eps;        /* 1e-6, floor of a std before its log                 */
@@ -93,8 +95,9 @@ typedef struct kvarn_desc {
 } kvarn_desc;
 
 /* Fill *out for a preset: "kvarn_k4v2_g128" [hotdry §核心配置参数: kv_cache_dtype
- * kvarn_k4v2_g128, block_size 128], or "kvarn_k4v4_g128" / "kvarn_k2v2_g128" (other k/v bit
- * presets through the same pipeline [vatt §四個步驟, bit-width assignment]).  Host only.
+ * kvarn_k4v2_g128, block_size 128], or "kvarn_k4v4_g128" / "kvarn_k2v2_g128" /
+ * "kvarn_k8v4_g128" (other k/v bit presets through the same pipeline [vatt §四個步驟,
+ * bit-width assignment]).  Host only.
  * UNSUPPORTED for another name or a head_dim outside 8..256 / not a multiple of 8;
  * INVALID_ARG for NULL or Hkv < 1. */
 int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, kvarn_desc* out);

@@ -3,6 +3,9 @@
 Tolerances (stated once, used by every GPU test):
   * codes: bit-exact, except codes whose oracle float64 pre-round value lies within 1e-5 of
     a k+0.5 boundary; those may differ by one level, and at most 1e-4 of all codes may.
+    Both figures grow with (2^b - 1) / 15 above 4 bits: the kernel's fp32 pre-round value
+    (N - m) / s with s = (M - m) / (2^b - 1) moves by (2^b - 1) eps for an fp32 error of
+    eps (M - m) in N or m, so its band around a boundary widens with the level count.
   * stored fp16 scale / zero / factor: within one fp16 ulp of the oracle's.
   * dequantised fp16 values: |gpu - oracle| <= 1e-3 |oracle| + 1e-5 max|tile| (same bytes).
   * decode output (fp16): |gpu - oracle| <= 2e-3 max(1, max_j |oracle_j|) per query head.
@@ -46,21 +49,27 @@ def record_bytes_of(pool: torch.Tensor, page: int, head: int) -> bytes:
     return bytes(pool[page, head].cpu().numpy().tobytes())
 
 
-def compare_codes(gpu_codes, ora_codes, ora_pre):
-    """Returns (mismatches, total); asserts every mismatch is an exempt boundary case."""
+def _width_factor(bits: int) -> float:
+    return max(1.0, ((1 << bits) - 1) / 15.0)
+
+
+def compare_codes(gpu_codes, ora_codes, ora_pre, bits: int = 4):
+    """Returns (mismatches, total, allowed mismatches); asserts every mismatch is an exempt
+    boundary case."""
     g = np.asarray(gpu_codes).astype(np.int64)
     o = np.asarray(ora_codes).astype(np.int64)
     bad = g != o
     n_bad = int(bad.sum())
+    band = CODE_BOUNDARY * _width_factor(bits)
     if n_bad:
         pre = np.asarray(ora_pre)[bad]
         dist = np.abs(pre - (np.floor(pre) + 0.5))
-        assert np.all(dist < CODE_BOUNDARY), (
-            "code mismatch away from a rounding boundary: %s" % list(zip(pre[dist >= CODE_BOUNDARY][:5],
-                                                                   g[bad][dist >= CODE_BOUNDARY][:5],
-                                                                   o[bad][dist >= CODE_BOUNDARY][:5])))
+        assert np.all(dist < band), (
+            "code mismatch away from a rounding boundary: %s" % list(zip(pre[dist >= band][:5],
+                                                                   g[bad][dist >= band][:5],
+                                                                   o[bad][dist >= band][:5])))
         assert np.all(np.abs(g[bad] - o[bad]) == 1)
-    return n_bad, g.size
+    return n_bad, g.size, CODE_MISMATCH_FRACTION * _width_factor(bits) * g.size
 
 
 def assert_f16_within_ulp(gpu, ora, what):
@@ -77,8 +86,8 @@ def compare_record(gpu_rec: bytes, kq_i: dict, vq_i: dict, d: int, stats: list,
                    k_bits: int = ko.K_BITS, v_bits: int = ko.V_BITS):
     """Compare one GPU page record with the oracle's quantised K/V (dicts of one tile)."""
     gk, gv = ko.unpack_record(gpu_rec, d, k_bits, v_bits)
-    stats.append(compare_codes(gk["codes"], kq_i["codes"], kq_i["pre"]))
-    stats.append(compare_codes(gv["codes"], vq_i["codes"], vq_i["pre"]))
+    stats.append(compare_codes(gk["codes"], kq_i["codes"], kq_i["pre"], k_bits))
+    stats.append(compare_codes(gv["codes"], vq_i["codes"], vq_i["pre"], v_bits))
     for key in ("scale", "zero", "factor"):
         assert_f16_within_ulp(gk[key], kq_i[key], "K " + key)
         assert_f16_within_ulp(gv[key], vq_i[key], "V " + key)
@@ -87,7 +96,8 @@ def compare_record(gpu_rec: bytes, kq_i: dict, vq_i: dict, d: int, stats: list,
 def assert_mismatch_budget(stats):
     bad = sum(s[0] for s in stats)
     total = sum(s[1] for s in stats)
-    assert bad <= CODE_MISMATCH_FRACTION * total, "%d of %d codes differ" % (bad, total)
+    allowed = sum(s[2] for s in stats)
+    assert bad <= allowed, "%d of %d codes differ" % (bad, total)
     return bad, total
 
 

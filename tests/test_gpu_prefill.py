@@ -94,7 +94,7 @@ def test_prefill_parity(kv, chunk, group, d0):
     print("prefill chunk=%d G=%d d0=%d: max scaled error %.2e" % (chunk, group, d0, err))
 
 
-@pytest.mark.parametrize("preset", ["kvarn_k4v4_g128", "kvarn_k2v2_g128"])
+@pytest.mark.parametrize("preset", ["kvarn_k4v4_g128", "kvarn_k2v2_g128", "kvarn_k8v4_g128"])
 def test_prefill_other_presets(kv, preset):
     err = _prefill_case(kv, [300, 4096], 8, 2, 4, 128, seed=11, preset=preset)
     print("prefill %s: max scaled error %.2e" % (preset, err))

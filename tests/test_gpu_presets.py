@@ -1,6 +1,7 @@
-"""The other k/v bit presets (kvarn_k4v4_g128, kvarn_k2v2_g128) through the same GPU pipeline,
-against the float64 oracle at the same widths: quantisation, dequantisation, decode over an
-oracle-built cache (with raw partial tiles, GQA 4 and 8), and append sealing."""
+"""The other k/v bit presets (kvarn_k4v4_g128, kvarn_k2v2_g128, kvarn_k8v4_g128) through the
+same GPU pipeline, against the float64 oracle at the same widths: quantisation,
+dequantisation, decode over an oracle-built cache (with raw partial tiles, GQA 4 and 8), and
+append sealing."""
 
 import math
 
@@ -14,7 +15,7 @@ from tests import helpers as H
 
 pytestmark = pytest.mark.gpu
 
-OTHER = ["kvarn_k4v4_g128", "kvarn_k2v2_g128"]
+OTHER = ["kvarn_k4v4_g128", "kvarn_k2v2_g128", "kvarn_k8v4_g128"]
 
 
 @pytest.fixture(scope="module")
