@@ -58,14 +58,30 @@ struct DecodeShape {
 
 // Power-of-two factors on the fp16 hi + lo query of the QK operand for channels 0..7 (kH0) and
 // 8..15 (kH1) of every 16, and on the MMA sum (kAcc).  4- and 2-bit codes of channels 8..15 sit
-// 4 / 2 bits higher in their fp16 subnormals.  8-bit codes have a small scale s' against their
-// zero point (the sum cancels against q~ . z'), so q is lifted by 2^8 to keep the lo parts of q
-// and of q s' out of the fp16 subnormal range.
+// 4 / 2 bits higher in their fp16 subnormals, so those channels take 1/16 / 1/4 of the others'
+// factor.  q is lifted so that the lo parts of q and of q s' stay out of the fp16 subnormal
+// range (the code sum cancels against q~ . z', so their precision shows in the logits): by
+// 2^4 / 2^2 at 4 / 2 bits (channels 8..15 at 1), by 2^8 at 8 bits, whose scale s' is smallest.
 template <int KB>
 struct QkScale {
-  static constexpr float kH0 = KB == 8 ? 256.0f : 1.0f;
-  static constexpr float kH1 = KB == 4 ? 0.0625f : (KB == 2 ? 0.25f : 256.0f);
-  static constexpr float kAcc = KB == 8 ? kTwo24 / 256.0f : kTwo24;
+  static constexpr float kH0 = KB == 8 ? 256.0f : (KB == 4 ? 16.0f : 4.0f);
+  static constexpr float kH1 = KB == 8 ? 256.0f : 1.0f;
+  static constexpr float kAcc = kTwo24 / kH0;
+};
+
+// Power-of-two factors on the PV weights p s' of tokens 0..7 (h = 0) and 8..15 (h = 1) of
+// 16-token block f of a pair, and on the MMA sum (kAcc).  2-bit codes of token half h of block
+// f sit 4f + 2h bits higher in their fp16 subnormals, 4-bit codes of half 1 four bits higher:
+// those weights take the inverse.  No lift (kLift = 1): unlike the QK operand, lifting the
+// weights by 2^4 left every decode error unchanged, and the weights keep the full fp16 range.
+template <int VB>
+struct PvScale {
+  static_assert(VB == 2 || VB == 4, "2- or 4-bit V codes");
+  static constexpr float kLift = 1.0f;
+  static constexpr float kAcc = kTwo24 / kLift;
+  __device__ static constexpr float c(int f, int h) {
+    return kLift * (VB == 2 ? 1.0f / float(1 << (4 * f + 2 * h)) : (h ? 1.0f / 16.0f : 1.0f));
+  }
 };
 
 template <int D, int NT>
@@ -154,7 +170,7 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
           for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a, bq[4 * kq + e][nt][0], bq[4 * kq + e][nt][1]);
         }
       }
-      logits(mi, acc, kTwo24);
+      logits(mi, acc, QkScale<KB>::kAcc);
     }
   } else if constexpr (KB == 8) {  // two words per fragment; a 16-byte load holds two
 #pragma unroll
@@ -202,8 +218,8 @@ __device__ __forceinline__ void qk_page(const uint8_t* __restrict__ Rk, const fl
           }
         }
       }
-      logits(2 * mi2, acc0, kTwo24);
-      logits(2 * mi2 + 1, acc1, kTwo24 * 0.0625f);  // the odd block's codes sit 4 bits higher
+      logits(2 * mi2, acc0, QkScale<KB>::kAcc);
+      logits(2 * mi2 + 1, acc1, QkScale<KB>::kAcc * 0.0625f);  // the odd block's codes sit 4 bits higher
     }
   }
 #pragma unroll
@@ -253,10 +269,9 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
 #pragma unroll
     for (int f = 0; f < 2; ++f) {
       const int ks = 2 * ks2 + f;
-      // token scales with the subnormal scale of this block's codes compensated (h = 0: rows
-      // g): 2-bit 2^(4f + 2h), 4-bit 2^(4h); the powers of two keep the products exact
-      const float c0 = VB == 2 ? (f ? 1.0f / 16.0f : 1.0f) : 1.0f;
-      const float c1 = VB == 2 ? (f ? 1.0f / 64.0f : 0.25f) : 1.0f / 16.0f;
+      // token scales times the PvScale factors of this block (h = 0: rows g); powers of two
+      // keep the products exact
+      const float c0 = PvScale<VB>::c(f, 0), c1 = PvScale<VB>::c(f, 1);
       const float2 svc = make_float2(__half2float(Vs[16 * ks + g]) * c0, __half2float(Vs[16 * ks + g + 8]) * c1);
       const float2 zv = make_float2(__half2float(Vz[16 * ks + g]), __half2float(Vz[16 * ks + g + 8]));
 #pragma unroll
@@ -316,7 +331,7 @@ __device__ __forceinline__ void pv_page(const uint8_t* __restrict__ Rv, const fl
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float2 t = add2(make_float2(pacc[mc][nt][0], pacc[mc][nt][2]), make_float2(pacc[mc][nt][1], pacc[mc][nt][3]));
-      t = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(zs[nt], zs[nt])), cj);
+      t = mul2(fma2(t, make_float2(PvScale<VB>::kAcc, PvScale<VB>::kAcc), make_float2(zs[nt], zs[nt])), cj);
       const float2 o = fma2(make_float2(st.o[mc][nt][0], st.o[mc][nt][1]), make_float2(alpha[nt], alpha[nt]), t);
       st.o[mc][nt][0] = o.x;
       st.o[mc][nt][1] = o.y;
@@ -368,10 +383,11 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
     const float2 z0 = __half22float2(Kz2[jp]), z1 = __half22float2(Kz2[jp + 4]);
     const uint2 u0 = qhl[g * QH + jp], u1 = qhl[g * QH + jp + 4];
     float2 q0 = add2(__half22float2(u2h2(u0.x)), __half22float2(u2h2(u0.y)));
+    float2 q1 = add2(__half22float2(u2h2(u1.x)), __half22float2(u2h2(u1.y)));
     if constexpr (QkScale<KB>::kH0 != 1.0f) q0 = mul2(q0, make_float2(kUndo0, kUndo0));
+    if constexpr (QkScale<KB>::kH1 != 1.0f) q1 = mul2(q1, make_float2(kUndo1, kUndo1));
     qz2 = fma2(q0, z0, qz2);
-    qz2 = fma2(mul2(add2(__half22float2(u2h2(u1.x)), __half22float2(u2h2(u1.y))), make_float2(kUndo1, kUndo1)),
-               z1, qz2);
+    qz2 = fma2(q1, z1, qz2);
     split_hi_lo(u2h2(u0.x), u2h2(u0.y), s0, aq[kk][0], aq[kk][1]);
     split_hi_lo(u2h2(u1.x), u2h2(u1.y), s1, aq[kk][2], aq[kk][3]);
   }
@@ -403,8 +419,8 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
           mma16816(acc1, aq[4 * kq + e], a[1], a[3]);
         }
       }
-      logits(2 * mi, acc0, kTwo24);
-      logits(2 * mi + 1, acc1, kTwo24);
+      logits(2 * mi, acc0, QkScale<KB>::kAcc);
+      logits(2 * mi + 1, acc1, QkScale<KB>::kAcc);
     }
   } else if constexpr (KB == 8) {  // two words per 16 x 16 block; a 16-byte load holds two blocks
 #pragma unroll
@@ -447,10 +463,10 @@ __device__ __forceinline__ void qk_page_t(const uint8_t* __restrict__ Rk, const 
           mma16816(acc[3], aq[4 * kq + e], a1[1], a1[3]);
         }
       }
-      logits(4 * mi2, acc[0], kTwo24);
-      logits(4 * mi2 + 1, acc[1], kTwo24);
-      logits(4 * mi2 + 2, acc[2], kTwo24 * 0.0625f);  // the odd 16-token block sits 4 bits higher
-      logits(4 * mi2 + 3, acc[3], kTwo24 * 0.0625f);
+      logits(4 * mi2, acc[0], QkScale<KB>::kAcc);
+      logits(4 * mi2 + 1, acc[1], QkScale<KB>::kAcc);
+      logits(4 * mi2 + 2, acc[2], QkScale<KB>::kAcc * 0.0625f);  // the odd 16-token block sits 4 bits higher
+      logits(4 * mi2 + 3, acc[3], QkScale<KB>::kAcc * 0.0625f);
     }
   }
   float mx = fmaxf(lg[0][0][0], lg[0][0][1]);
@@ -489,9 +505,8 @@ __device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const 
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int f = k & 1;
-    // the codes' subnormal scale compensated: 2-bit 2^(4f + 2h), 4-bit 2^(4h), h = token half
-    const float c0 = VB == 2 ? (f ? 1.0f / 16.0f : 1.0f) : 1.0f;
-    const float c1 = VB == 2 ? (f ? 1.0f / 64.0f : 0.25f) : 1.0f / 16.0f;
+    // the PvScale factors of this block, h = token half
+    const float c0 = PvScale<VB>::c(f, 0), c1 = PvScale<VB>::c(f, 1);
     const float2 pa = make_float2(lg[2 * k][0][0], lg[2 * k][0][1]);          // tokens 16k + 2tq, +1
     const float2 pb = make_float2(lg[2 * k + 1][0][0], lg[2 * k + 1][0][1]);  // tokens 16k + 8 + 2tq, +1
     zs2 = fma2(pa, __half22float2(Vz2[8 * k + tq]), zs2);
@@ -546,7 +561,7 @@ __device__ __forceinline__ void pv_page_t(const uint8_t* __restrict__ Rv, const 
       const int cb = 8 * mq + cl;
       const float2 cj = __half22float2(Vc2[4 * cb + tq]);
       float2 t = add2(make_float2(pacc[cl][0], pacc[cl][1]), make_float2(pacc[cl][2], pacc[cl][3]));
-      t = mul2(fma2(t, make_float2(kTwo24, kTwo24), make_float2(zs, zs)), cj);
+      t = mul2(fma2(t, make_float2(PvScale<VB>::kAcc, PvScale<VB>::kAcc), make_float2(zs, zs)), cj);
       const float2 o = fma2(make_float2(st.o[cb][0], st.o[cb][1]), make_float2(alpha[0], alpha[0]), t);
       st.o[cb][0] = o.x;
       st.o[cb][1] = o.y;
