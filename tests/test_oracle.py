@@ -142,9 +142,10 @@ def test_rtn_matches_brute_force(bits):
         clear = (srt[:, 1] - srt[:, 0]) > 1e-9 * float(s)
         np.testing.assert_array_equal(q[clear], best[clear])
 
-    # round to nearest on a grid of step s: |z - z_hat| <= s / 2 inside [min, max] (vatt §為什麼樸素的 2-bit…)
+
 def test_rtn_error_bound():
-    # the benchmark spec bound |z - z_hat| <= scale / 2 in the quantised domain
+    # round to nearest on a grid of step s: |z - z_hat| <= s / 2 inside [min, max]
+    # (vatt §為什麼樸素的 2-bit…: the range split into 2^bits - 1 steps, nearest level)
     rng = np.random.default_rng(3)
     x = rng.standard_normal((128, 64)) * 3.0
     for bits, axis in ((4, 0), (2, 1)):
