@@ -27,7 +27,7 @@ Per 128-token tile of one KV head, K and V separately:
 Decode attention is the textbook softmax attention over the dequantised cache
 (plus the raw fp16 tokens of the unsealed partial tile), in the original basis.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * Sylvester Hadamard in natural order, no random signs; scaled by 1/sqrt(d).
   * std is the population std (ddof 0, mean subtracted).  A row or column whose std is
     below EPS=1e-6 has nothing to normalise and keeps its factor (its log factor gains 0);
