@@ -58,6 +58,17 @@ def test_record_bytes_match_oracle(kv):
         assert desc.page_record_bytes == ko.record_bytes(ko.padded_head_dim(d0))
 
 
+def test_every_oracle_preset_has_a_descriptor(kv):
+    # the library's preset table and the oracle's agree on names, widths and record sizes
+    from oracle import kvarn_oracle as ko
+    for name, (kb, vb) in ko.PRESETS.items():
+        for d0 in (64, 96, 128, 256):
+            desc = kv.desc_from_preset(d0, 3, preset=name)
+            assert (desc.k_bits, desc.v_bits) == (kb, vb)
+            assert desc.page_record_bytes == kv.page_record_bytes(desc) == \
+                ko.record_bytes(ko.padded_head_dim(d0), k_bits=kb, v_bits=vb)
+
+
 def test_preset_rejections(kv):
     with pytest.raises(kv.KvarnError) as e:
         kv.desc_from_preset(128, 8, preset="kvarn_k2v2_g64")
