@@ -72,7 +72,7 @@ def test_preset_quantize_and_dequantize(kv, preset, d0, hkv, tiles):
     print("%s d0=%d: %d of %d codes on a boundary differ" % (preset, d0, bad, total))
 
 
-def _oracle_cache_decode(kv, preset, d0, group, seq_lens, seed):
+def _oracle_cache_decode(kv, preset, d0, group, seq_lens, seed, **synth_kw):
     kb, vb = ko.PRESETS[preset]
     hkv = 2
     batch = len(seq_lens)
@@ -89,7 +89,7 @@ def _oracle_cache_decode(kv, preset, d0, group, seq_lens, seed):
     recs, tails = {}, {}
     off = 0
     for b, L in enumerate(seq_lens):
-        k, v = synth.outlier_kv(max(L, 1), hkv, d0, seed=seed * 100 + b)
+        k, v = synth.outlier_kv(max(L, 1), hkv, d0, seed=seed * 100 + b, **synth_kw)
         k, v = k[:L], v[:L]
         n = pages[b]
         table[b, :n] = perm[off:off + n]
@@ -136,6 +136,16 @@ def _oracle_cache_decode(kv, preset, d0, group, seq_lens, seed):
 def test_preset_decode_parity(kv, preset, d0, group):
     err = _oracle_cache_decode(kv, preset, d0, group, [0, 77, 128, 1000, 4096 + 5, 300], seed=7 + d0)
     print("%s d0=%d G=%d: max scaled error %.2e" % (preset, d0, group, err))
+
+
+@pytest.mark.parametrize("preset", ["kvarn_k4v2_g128"] + OTHER)
+@pytest.mark.parametrize("d0,group", [(128, 4), (128, 8)])
+def test_preset_decode_extreme_outliers(kv, preset, d0, group):
+    # outlier channels x1000..x4000 (values up to the fp16 clamp of 60000): the lifted QK
+    # operand and the PV weights stay finite and the output matches the oracle
+    err = _oracle_cache_decode(kv, preset, d0, group, [77, 1000, 4096 + 5], seed=21 + d0,
+                               scale_lo=1000.0, scale_hi=4000.0)
+    print("%s d0=%d G=%d, outliers x1000..x4000: max scaled error %.2e" % (preset, d0, group, err))
 
 
 @pytest.mark.parametrize("preset", OTHER)
