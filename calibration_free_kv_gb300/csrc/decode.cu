@@ -998,7 +998,36 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   float v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) v[e] = 0.0f;
-  if (n_splits > 0) {
+  if (n_splits > 0 && n_splits <= 4) {
+    // up to four splits (the common case): every load issued before the first use
+    const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
+    float2 ml[4];
+    float o[4][E];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s < n_splits) {
+        ml[s] = *reinterpret_cast<const float2*>(base + s * (D + 4));
+        load_f32<E>(base + s * (D + 4) + 4 + lane * E, o[s]);
+      } else {
+        ml[s] = make_float2(-INFINITY, 0.0f);
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[s][e] = 0.0f;
+      }
+    }
+    const float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
+    float lsum = 0.0f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const float w = s < n_splits ? exp2f(ml[s].x - M) : 0.0f;
+      lsum = fmaf(w, ml[s].y, lsum);
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = fmaf(w, o[s][e], v[e]);
+    }
+    const float inv = inv_sqrt_d<D>() / lsum;
+    warp_fwht<D>(v, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] *= inv;
+  } else if (n_splits > 0) {
     const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
     // split statistics, one split per lane, 32 per pass
     float M = -INFINITY;
