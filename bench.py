@@ -723,9 +723,10 @@ def _run_kvarn(args, torch, world, rank):
 _ORACLE_UNITS = None
 
 
-def _oracle_units(seed: int, n_units: int = 4):
-    """(q rows, oracle page records, L) of n_units whole (sequence, kv head) decode units of the
-    workload, quantised by the oracle (not timed)."""
+def _oracle_units(seed: int, n_units: int = 4, max_pages=None):
+    """(q rows, oracle page records, L) of n_units (sequence, kv head) decode units of the
+    workload, quantised by the oracle (not timed); with max_pages, each unit keeps its first
+    max_pages pages (a shorter sequence of the same data)."""
     import numpy as np
     from calibration_free_kv_gb300 import synth
     from oracle import kvarn_oracle as ko
@@ -744,6 +745,8 @@ def _oracle_units(seed: int, n_units: int = 4):
         fields = ("codes", "scale", "zero", "factor")
         recs = [ko.pack_record({f: kq[f][i] for f in fields}, {f: vq[f][i] for f in fields})
                 for i in range(n)]
+        if max_pages is not None and len(recs) > max_pages:
+            recs, L = recs[:max_pages], 128 * max_pages
         units.append((np.ascontiguousarray(q[b, :group]), recs, L))
     return units
 
@@ -772,9 +775,10 @@ class OracleTimer:
     """The float64 oracle's decode attention timed on the host cores: one spawned process per
     core (single-threaded BLAS each), or one process alone."""
 
-    def __init__(self, seed: int = SEED):
+    def __init__(self, seed: int = SEED, max_pages=None):
         import multiprocessing as mp
-        self.units = _oracle_units(seed)
+        self.max_pages = max_pages
+        self.units = _oracle_units(seed, max_pages=max_pages)
         self.cores = os.cpu_count() or 1
         keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
         saved = {k: os.environ.get(k) for k in keys}
@@ -800,9 +804,11 @@ class OracleTimer:
 
     def describe(self):
         pages = sum(len(r) for _, r, _ in self.units)
-        return ("%d whole (sequence, kv head) decode units of the workload (%d pages, 4 query heads "
+        which = ("whole" if self.max_pages is None else
+                 "first-%d-page (short steps)" % self.max_pages)
+        return ("%d %s (sequence, kv head) decode units of the workload (%d pages, 4 query heads "
                 "each), decoded repeatedly through the float64 oracle (dequantise + textbook "
-                "attention), one single-threaded process per core" % (len(self.units), pages))
+                "attention), one single-threaded process per core" % (len(self.units), which, pages))
 
     def close(self):
         self.pool.close()
@@ -824,8 +830,11 @@ def _cpu_baseline(seconds: float):
 def _run_reference(args, world, rank):
     if rank != 0:
         return None
-    per_step = max(1.0, 20.0 / max(1, args.steps + args.warmup))
-    ot = OracleTimer()
+    # about a minute of oracle work in all: 1 s a step for short runs, down to one decode unit
+    # a step (a few tens of ms) when many steps are asked for
+    per_step = min(1.0, max(0.02, 60.0 / max(1, args.steps + args.warmup)))
+    # a whole unit (tens of pages) takes a few tenths of a second: short steps take 4-page units
+    ot = OracleTimer(max_pages=None if per_step >= 0.5 else 4)
     try:
         for _ in range(args.warmup):
             ot.run(per_step * 0.25, ot.cores)
