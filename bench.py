@@ -285,6 +285,9 @@ def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, s
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        # keep the GPU busy (~100 us) while the host enqueues the pass, so that the events
+        # time the kernels and not the host's launch latency of the first one
+        torch.cuda._sleep(200000)
         a.record(stream)
         one_pass()
         b.record(stream)

@@ -1088,7 +1088,10 @@ static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.max_splits, p.num_kv_heads * p.vgroups, p.batch);
+  // the sealed splits at this split size plus the partial tile's (the workspace stride
+  // max_splits is laid out for the smallest size and may be larger)
+  const int splits = min(p.max_splits, (p.max_pages + p.pages_per_split - 1) / p.pages_per_split + 1);
+  cfg.gridDim = dim3(splits, p.num_kv_heads * p.vgroups, p.batch);
   cfg.blockDim = dim3(S::kWarps * 32);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
@@ -1219,6 +1222,55 @@ int launch_chunk_any(int d, const DecodeParams& p, cudaStream_t stream) {
   if (d == 128) return launch_chunk_t<128>(p, stream);
   if (d == 256) return launch_chunk_t<256>(p, stream);
   return KVARN_ERR_UNSUPPORTED;
+}
+
+// Split size for long block tables.  Their sequences are long and, in a batch, of similar
+// length, so the CTAs of sequences at the full table length are taken as the work: the cost
+// of a size is its waves of CTAs over the GPU's CTA slots times the page rounds of one warp
+// (ceil(pages / warps)); the cheapest size wins, ties going to the larger (fewer CTAs and
+// partials to merge).  Tables up to 256 pages, whose lengths vary, keep 32.
+template <int D, int NT, int KB, int VB>
+static int split_pages_t(int64_t units, int max_pages) {
+  using S = DecodeShape<D, NT, KB, VB>;
+  constexpr int kBase = 32, kMax = 128;
+  if (max_pages <= 256 || units < 1) return kBase;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return kBase;
+  const int64_t slots = (int64_t)sms * S::kMinBlocks;
+  int best = kBase;
+  int64_t best_cost = INT64_MAX;
+  for (int pps = kBase; pps <= kMax; ++pps) {
+    const int64_t ctas = units * ((max_pages + pps - 1) / pps);
+    const int64_t cost = ((ctas + slots - 1) / slots) * ((pps + S::kWarps - 1) / S::kWarps);
+    if (cost <= best_cost) {
+      best_cost = cost;
+      best = pps;
+    }
+  }
+  return best;
+}
+
+template <int KB, int VB>
+static int split_pages_bits(int d, int nt, int64_t units, int max_pages) {
+  if (nt == 1) {
+    if (d == 64) return split_pages_t<64, 1, KB, VB>(units, max_pages);
+    if (d == 128) return split_pages_t<128, 1, KB, VB>(units, max_pages);
+    if (d == 256) return split_pages_t<256, 1, KB, VB>(units, max_pages);
+  } else if (nt == 2) {
+    if (d == 64) return split_pages_t<64, 2, KB, VB>(units, max_pages);
+    if (d == 128) return split_pages_t<128, 2, KB, VB>(units, max_pages);
+  }
+  return 32;
+}
+
+int decode_split_pages(int d, int nt, int kb, int vb, int64_t units, int max_pages) {
+  if (kb == 4 && vb == 2) return split_pages_bits<4, 2>(d, nt, units, max_pages);
+  if (kb == 4 && vb == 4) return split_pages_bits<4, 4>(d, nt, units, max_pages);
+  if (kb == 2 && vb == 2) return split_pages_bits<2, 2>(d, nt, units, max_pages);
+  if (kb == 8 && vb == 4) return split_pages_bits<8, 4>(d, nt, units, max_pages);
+  return 32;
 }
 
 template <int KB, int VB>

@@ -171,12 +171,10 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
                              static_cast<cudaStream_t>(stream));
 }
 
-// Sealed pages per decode CTA (its warps take them round-robin).
-static int decode_pages_per_split(const kvarn_desc* desc, int max_pages) {
-  // Long block tables at head_dim <= 128 take 64-page splits: half the CTA starts and the
-  // splits to merge (long context at head_dim 96: 136 -> 122 us); everything else 32.
-  return (max_pages > 256 && desc->head_dim_padded <= 128) ? 64 : 32;
-}
+// Smallest split size (sealed pages per decode CTA, its warps taking them round-robin): the
+// workspace holds the partials of this many splits per row.  A launch may take a larger size
+// (decode_split_pages), which needs fewer.
+static int decode_pages_per_split(const kvarn_desc*, int) { return 32; }
 
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
                                     int max_pages) {
@@ -228,8 +226,9 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
   p.num_q_heads = num_q_heads;
   p.group = group;
   p.d0 = desc->head_dim;
-  p.pages_per_split = pps;
-  p.max_splits = (max_pages + pps - 1) / pps + 1;
+  p.max_splits = (max_pages + pps - 1) / pps + 1;  // workspace stride at the smallest size
+  p.pages_per_split = decode_split_pages(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits,
+                                         (int64_t)batch * desc->num_kv_heads, max_pages);
   p.chunk = 1;
   p.vgroups = 1;
   p.status = dev_status;
@@ -293,8 +292,9 @@ int kvarn_prefill_attention(const kvarn_desc* desc, int batch, int num_q_heads, 
   p.num_q_heads = num_q_heads;
   p.group = group;
   p.d0 = desc->head_dim;
-  p.pages_per_split = pps;
-  p.max_splits = (max_pages + pps - 1) / pps + 2;
+  p.max_splits = (max_pages + pps - 1) / pps + 2;  // workspace stride at the smallest size
+  p.pages_per_split = decode_split_pages(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits,
+                                         (int64_t)batch * desc->num_kv_heads * vgroups, max_pages);
   p.chunk = chunk_len;
   p.vgroups = (int)vgroups;
   p.chunk_k = static_cast<const __half*>(chunk_k);

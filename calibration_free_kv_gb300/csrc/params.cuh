@@ -75,6 +75,10 @@ struct DequantParams {
 
 int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int units, cudaStream_t stream);
 int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream);
+// Sealed pages per decode CTA for `units` (sequence, kv head, vector group) rows of a block
+// table `max_pages` wide: 32, or for tables over 256 pages the size in [32, 128] that fills
+// the GPU's CTA slots best.  Never below 32, the size the workspace is laid out for.
+int decode_split_pages(int d, int nt, int kb, int vb, int64_t units, int max_pages);
 int launch_chunk_any(int d, const DecodeParams& p, cudaStream_t stream);
 int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pages, cudaStream_t stream);
 
