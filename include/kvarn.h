@@ -152,7 +152,10 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
                        void* page_pool, int64_t num_pool_pages, int32_t* dev_status,
                        void* stream);
 
-/* Workspace bytes kvarn_decode_attention needs for this batch shape (host only). */
+/* Workspace bytes kvarn_decode_attention needs for this batch shape (host only): fp32 split
+ * partials laid out for 32-page splits, the smallest split size; a launch over a block table
+ * wider than 256 pages may take larger splits (chosen from the GPU's SM count) and fills fewer
+ * of them.  Needs no GPU. */
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
                                     int max_pages);
 
