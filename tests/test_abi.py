@@ -131,3 +131,46 @@ def test_fp16_baseline_validation(kv):
     assert lib.kvarn_fp16_decode_attention(*args(128, 8, 32, 1 << 20, ctypes.c_void_p(24))) == \
         kv.KVARN_ERR_INVALID_ARG
     assert lib.kvarn_selftest_wait_timeout(null, null) == kv.KVARN_ERR_INVALID_ARG
+
+
+_C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "kvarn.h"
+
+int main(void) {
+  kvarn_desc d;
+  if (kvarn_desc_from_preset("kvarn_k4v2_g128", 128, 8, &d) != KVARN_OK) return 1;
+  if (d.page_record_bytes != 13824 || kvarn_page_record_bytes(&d) != 13824) return 2;
+  if (kvarn_desc_from_preset("no_such_preset", 128, 8, &d) != KVARN_ERR_UNSUPPORTED) return 3;
+  if (kvarn_desc_from_preset("kvarn_k4v2_g128", 128, 8, &d) != KVARN_OK) return 4;
+  if (kvarn_decode_workspace_bytes(&d, 64, 32, 128) == 0) return 5;
+  /* argument errors return before any CUDA call */
+  if (kvarn_decode_attention(NULL, 1, 4, NULL, NULL, 1, NULL, 1, NULL, NULL, NULL, 0.1f, NULL,
+                             NULL, 0, NULL, NULL) != KVARN_ERR_INVALID_ARG) return 6;
+  if (strlen(kvarn_status_string(KVARN_ERR_WORKSPACE_TOO_SMALL)) == 0) return 7;
+  printf("ok %lld\n", (long long)d.page_record_bytes);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(kv, tmp_path):
+    # a C11 client compiles against kvarn.h alone (no C++ in the declarations) and links the
+    # shared library by its exported C names
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(_C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(kv.library_path())
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lkvarn", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip() == "ok 13824"
