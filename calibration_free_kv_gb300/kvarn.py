@@ -123,10 +123,14 @@ def _check(status: int, where: str):
 
 
 def _ptr(t):
+    """Device pointer of a tensor argument (None -> NULL).  Every buffer the library takes is
+    device memory, so a host tensor is refused here rather than handed to a kernel."""
     if t is None:
         return None
     if not isinstance(t, torch.Tensor):
         raise TypeError("expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError("every tensor argument must be a CUDA tensor (got one on %s)" % t.device)
     return ctypes.c_void_p(t.data_ptr())
 
 

@@ -174,3 +174,33 @@ def test_header_is_plain_c_and_links(kv, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.strip() == "ok 13824"
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    # the binding has no fallback: without libkvarn.so importing it raises
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "calibration_free_kv_gb300"
+    pkg.mkdir()
+    for name in ("__init__.py", "kvarn.py", "synth.py", "build.py"):
+        shutil.copy(os.path.join(ROOT, "calibration_free_kv_gb300", name), pkg / name)
+    r = subprocess.run([sys.executable, "-c", "from calibration_free_kv_gb300 import kvarn"],
+                       cwd=str(tmp_path), capture_output=True, text=True, timeout=300,
+                       env=dict(os.environ, PYTHONPATH=str(tmp_path)))
+    assert r.returncode != 0
+    assert "libkvarn.so is not built" in r.stderr and "no fallback" in r.stderr
+
+
+def test_binding_rejects_host_tensors(kv):
+    # every tensor argument must be device memory: a CPU tensor is refused before any call
+    import torch
+    d = kv.desc_from_preset(128, 2)
+    q = torch.zeros((1, 8, 128), dtype=torch.float16)
+    pool = torch.zeros((2, 2, d.page_record_bytes), dtype=torch.uint8)
+    table = torch.zeros((1, 1), dtype=torch.int32)
+    lens = torch.zeros(1, dtype=torch.int32)
+    out = torch.zeros_like(q)
+    ws = torch.zeros(kv.decode_workspace_bytes(d, 1, 8, 1), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kv.decode_attention(d, q, pool, table, lens, out, ws)

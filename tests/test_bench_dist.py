@@ -37,7 +37,7 @@ def _worker(rank, world, port, out):
 def test_aggregate_takes_the_slowest_rank():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
