@@ -4,6 +4,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kvarn.h"
 
 namespace kvarn {
@@ -30,6 +32,24 @@ __host__ __device__ constexpr RecordLayout record_layout(int d, int kb = 4, int 
                       kTile * d * kb / 8 + 4 * d + 4 * kTile + kTile * d * vb / 8,
                       kTile * d * kb / 8 + 4 * d + 6 * kTile + kTile * d * vb / 8,
                       kTile * d * kb / 8 + 6 * d + 6 * kTile + kTile * d * vb / 8};
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device.  The attribute
+// belongs to the device's context, so a process that launches on several GPUs sets it on each:
+// `once` (one static object per kernel) remembers the devices done, 0..63; devices beyond that
+// set it on every launch.  Concurrent first calls both set it, which is harmless.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+};
+inline int set_smem_limit(PerDeviceOnce& once, const void* kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return KVARN_ERR_CUDA;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (once.done.load(std::memory_order_acquire) & bit) != 0ull) return KVARN_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return KVARN_ERR_CUDA;
+  if (bit != 0ull) once.done.fetch_or(bit, std::memory_order_release);
+  return KVARN_OK;
 }
 
 __device__ __forceinline__ void flag_error(int32_t* status, int bits) {

@@ -1075,13 +1075,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
 template <int D, int NT, int KB, int VB>
 static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   using S = DecodeShape<D, NT, KB, VB>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_kernel<D, NT, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             S::kSmemBytes) != cudaSuccess)
-      return KVARN_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce smem_once;  // the attribute is set once per device
+  const void* fn = reinterpret_cast<const void*>(decode_kernel<D, NT, KB, VB>);
+  if (const int st = set_smem_limit(smem_once, fn, S::kSmemBytes); st != KVARN_OK) return st;
   // both kernels may start while their predecessor in the stream drains; each waits for it
   // (griddepcontrol.wait) before touching its results
   cudaLaunchAttribute attr[1];

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "params.cuh"
 
 namespace {
 
@@ -23,7 +24,9 @@ constexpr int kMaxDevices = 128;
 std::mutex g_scratch_lock;
 void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of the scratch buffer on the current device, looked up once per device.
+// Device address of the scratch buffer on the current device, looked up once per device and
+// kept for the life of the process (cudaDeviceReset would unload the module and leave the kept
+// address stale; the header tells callers not to reset a device they use this entry point on).
 int scratch_on_current_device(void** addr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVARN_ERR_CUDA;
@@ -47,13 +50,20 @@ extern "C" int kvarn_decode_attention_noalloc(const kvarn_desc* desc, int batch,
                                               const void* partial_k, const void* partial_v,
                                               float softmax_scale, void* out, int32_t* dev_status,
                                               void* stream) {
-  void* scratch = nullptr;
-  const int st = scratch_on_current_device(&scratch);
+  // The argument checks of kvarn_decode_attention come first, so that a bad argument gives the
+  // same status as there and an empty batch returns without touching the GPU.
+  int st = kvarn::decode_args_check(desc, batch, num_q_heads, q, page_pool, num_pool_pages,
+                                    block_table, max_pages, seq_lens, partial_k, partial_v,
+                                    softmax_scale, out);
+  if (st == kvarn::kDecodeNothingToDo) return KVARN_OK;
   if (st != KVARN_OK) return st;
-  // Same kernels as kvarn_decode_attention; a shape whose partials exceed the buffer is
-  // rejected there with KVARN_ERR_WORKSPACE_TOO_SMALL before anything is launched.  No part
-  // of the buffer has to start at zero: every partial the merge reads is written earlier in
-  // the same call.
+  if (kvarn_decode_workspace_bytes(desc, batch, num_q_heads, max_pages) > kScratchBytes)
+    return KVARN_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  st = scratch_on_current_device(&scratch);
+  if (st != KVARN_OK) return st;
+  // Same kernels as kvarn_decode_attention.  No part of the buffer has to start at zero: every
+  // partial the merge reads is written earlier in the same call.
   return kvarn_decode_attention(desc, batch, num_q_heads, q, page_pool, num_pool_pages,
                                 block_table, max_pages, seq_lens, partial_k, partial_v,
                                 softmax_scale, out, scratch, kScratchBytes, dev_status, stream);

@@ -115,13 +115,9 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
 template <int D, int KB, int VB>
 static int launch_dequant_t(const DequantParams& p, int num_pages, cudaStream_t stream) {
   constexpr int kSmem = DequantShape<D>::kSmemBytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(dequantize_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem) != cudaSuccess)
-      return KVARN_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce smem_once;  // the attribute is set once per device
+  const void* fn = reinterpret_cast<const void*>(dequantize_kernel<D, KB, VB>);
+  if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
   dequantize_kernel<D, KB, VB><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }

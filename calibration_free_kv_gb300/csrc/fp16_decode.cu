@@ -312,13 +312,9 @@ __global__ void __launch_bounds__(128) combine_f16_kernel(DecodeParams p) {
 
 template <int D, int NT>
 static int launch(const DecodeParams& p, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_f16_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Shape<D>::kSmem) != cudaSuccess)
-      return KVARN_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce smem_once;  // the attribute is set once per device
+  const void* fn = reinterpret_cast<const void*>(decode_f16_kernel<D, NT>);
+  if (const int st = set_smem_limit(smem_once, fn, Shape<D>::kSmem); st != KVARN_OK) return st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

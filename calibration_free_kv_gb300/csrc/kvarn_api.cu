@@ -30,23 +30,30 @@ bool supported_bits(int kb, int vb) {
   return false;
 }
 
+// Next power of two >= d0 [aifeeds §局限: a head_dim that is not a power of two is padded up to
+// the nearest one].
+int padded_dim(int d0) {
+  int d = 1;
+  while (d < d0) d *= 2;
+  return d;
+}
+
+// head_dim 40..256 in steps of 8: padded to 64, 128 or 256, the widths a page record exists for
+// (its code words tile 64-channel groups).  head_dim <= 32 would pad to itself (8, 16, 32) and
+// is refused.
+bool supported_head_dim(int d0) { return d0 > 32 && d0 <= 256 && d0 % 8 == 0; }
+
 int check_desc(const kvarn_desc* d) {
   if (d == nullptr) return KVARN_ERR_INVALID_ARG;
   if (d->tile_tokens != kTile || !supported_bits(d->k_bits, d->v_bits)) return KVARN_ERR_UNSUPPORTED;
-  if (d->head_dim < 8 || d->head_dim > 256 || d->head_dim % 8 != 0) return KVARN_ERR_UNSUPPORTED;
-  const int dp = d->head_dim_padded;
-  if (!(dp == 64 || dp == 128 || dp == 256) || d->head_dim > dp) return KVARN_ERR_UNSUPPORTED;
+  if (!supported_head_dim(d->head_dim)) return KVARN_ERR_UNSUPPORTED;
+  if (d->head_dim_padded != padded_dim(d->head_dim)) return KVARN_ERR_UNSUPPORTED;
   if (d->num_kv_heads < 1) return KVARN_ERR_INVALID_ARG;
   if (d->sinkhorn_iters < 0 || d->sinkhorn_iters > 8) return KVARN_ERR_UNSUPPORTED;
   if (!(d->sinkhorn_eps > 0.0f)) return KVARN_ERR_INVALID_ARG;
-  if (d->page_record_bytes != record_layout(dp, d->k_bits, d->v_bits).bytes) return KVARN_ERR_INVALID_ARG;
+  if (d->page_record_bytes != record_layout(d->head_dim_padded, d->k_bits, d->v_bits).bytes)
+    return KVARN_ERR_INVALID_ARG;
   return KVARN_OK;
-}
-
-int padded_dim(int d0) {
-  int d = 64;
-  while (d < d0) d *= 2;
-  return d;
 }
 
 }  // namespace
@@ -59,7 +66,7 @@ int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, k
   for (const Preset& c : kPresets)
     if (std::strcmp(preset, c.name) == 0) pr = &c;
   if (pr == nullptr) return KVARN_ERR_UNSUPPORTED;
-  if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0) return KVARN_ERR_UNSUPPORTED;
+  if (!supported_head_dim(head_dim)) return KVARN_ERR_UNSUPPORTED;
   if (num_kv_heads < 1) return KVARN_ERR_INVALID_ARG;
   kvarn_desc d;
   d.head_dim = head_dim;
@@ -184,30 +191,54 @@ size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q
   return (size_t)batch * num_q_heads * max_splits * (desc->head_dim_padded + 4) * sizeof(float);
 }
 
+}  // extern "C"
+
+namespace kvarn {
+
+// Host-side checks of a decode call's arguments other than its workspace: a KVARN_ERR_* code,
+// KVARN_OK, or kDecodeNothingToDo for an empty batch (a valid call that launches nothing).
+int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                      const void* page_pool, int64_t num_pool_pages, const int32_t* block_table,
+                      int max_pages, const int32_t* seq_lens, const void* partial_k,
+                      const void* partial_v, float softmax_scale, const void* out) {
+  const int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || num_q_heads < 1 || max_pages < 1) return KVARN_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return KVARN_ERR_UNSUPPORTED;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (!(group == 1 || group == 2 || group == 4 || group == 8)) return KVARN_ERR_UNSUPPORTED;
+  if (group == 8 && desc->head_dim_padded == 256) return KVARN_ERR_UNSUPPORTED;
+  if (batch == 0) return kDecodeNothingToDo;
+  if (q == nullptr || page_pool == nullptr || block_table == nullptr || seq_lens == nullptr ||
+      out == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(page_pool) || !aligned16(partial_k) || !aligned16(partial_v))
+    return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1 || !(softmax_scale > 0.0f)) return KVARN_ERR_INVALID_ARG;
+  return KVARN_OK;
+}
+
+}  // namespace kvarn
+
+extern "C" {
+
 int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
                            const void* page_pool, int64_t num_pool_pages,
                            const int32_t* block_table, int max_pages, const int32_t* seq_lens,
                            const void* partial_k, const void* partial_v, float softmax_scale,
                            void* out, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, void* stream) {
-  int st = check_desc(desc);
+  const int st = decode_args_check(desc, batch, num_q_heads, q, page_pool, num_pool_pages,
+                                   block_table, max_pages, seq_lens, partial_k, partial_v,
+                                   softmax_scale, out);
+  if (st == kDecodeNothingToDo) return KVARN_OK;
   if (st != KVARN_OK) return st;
-  if (batch < 0 || num_q_heads < 1 || max_pages < 1) return KVARN_ERR_INVALID_ARG;
-  if (num_q_heads % desc->num_kv_heads != 0) return KVARN_ERR_UNSUPPORTED;
-  const int group = num_q_heads / desc->num_kv_heads;
-  if (!(group == 1 || group == 2 || group == 4 || group == 8)) return KVARN_ERR_UNSUPPORTED;
-  const int nt = group <= 4 ? 1 : 2;
-  if (nt == 2 && desc->head_dim_padded == 256) return KVARN_ERR_UNSUPPORTED;
-  if (batch == 0) return KVARN_OK;
-  if (q == nullptr || page_pool == nullptr || block_table == nullptr || seq_lens == nullptr ||
-      out == nullptr || workspace == nullptr)
-    return KVARN_ERR_INVALID_ARG;
-  if ((partial_k == nullptr) != (partial_v == nullptr)) return KVARN_ERR_INVALID_ARG;
-  if (!aligned16(page_pool) || !aligned16(workspace) || !aligned16(partial_k) || !aligned16(partial_v))
-    return KVARN_ERR_INVALID_ARG;
-  if (num_pool_pages < 1 || !(softmax_scale > 0.0f)) return KVARN_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace)) return KVARN_ERR_INVALID_ARG;
   const size_t need = kvarn_decode_workspace_bytes(desc, batch, num_q_heads, max_pages);
   if (workspace_bytes < need) return KVARN_ERR_WORKSPACE_TOO_SMALL;
+  const int group = num_q_heads / desc->num_kv_heads;
+  const int nt = group <= 4 ? 1 : 2;
   const int pps = decode_pages_per_split(desc, max_pages);
   DecodeParams p{};
   p.q = static_cast<const __half*>(q);

@@ -4,6 +4,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "kvarn.h"
+
 namespace kvarn {
 
 struct QuantizeParams {
@@ -72,6 +74,15 @@ struct DequantParams {
   int d0;
   int32_t* status;
 };
+
+// decode_args_check: a valid decode call with nothing to launch (batch 0).
+constexpr int kDecodeNothingToDo = 1;
+// Host-side checks of a decode call's arguments other than its workspace (kvarn_api.cu):
+// KVARN_OK, kDecodeNothingToDo or a KVARN_ERR_* code.
+int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                      const void* page_pool, int64_t num_pool_pages, const int32_t* block_table,
+                      int max_pages, const int32_t* seq_lens, const void* partial_k,
+                      const void* partial_v, float softmax_scale, const void* out);
 
 int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int units, cudaStream_t stream);
 int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream);

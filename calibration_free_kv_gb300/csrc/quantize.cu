@@ -654,13 +654,9 @@ __global__ void __launch_bounds__(QuantShape<D>::kThreads)
 template <int D, int KB, int VB>
 static int launch_quantize(const QuantizeParams& p, int units, cudaStream_t stream) {
   constexpr int kSmem = QuantShape<D>::kSmemBytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(quantize_kernel<D, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmem) != cudaSuccess)
-      return KVARN_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce smem_once;  // the attribute is set once per device
+  const void* fn = reinterpret_cast<const void*>(quantize_kernel<D, KB, VB>);
+  if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
   return launch_pdl(quantize_kernel<D, KB, VB>, dim3(units * 2), dim3(QuantShape<D>::kThreads), kSmem,
                     stream, p);
 }
@@ -964,13 +960,9 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
 
 template <int KB, int VB>
 static int launch_quantize_tc(const QuantizeParams& p, int units2, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(quantize_tc_kernel<KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             tc::kSmemBytes) != cudaSuccess)
-      return KVARN_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce smem_once;  // the attribute is set once per device
+  const void* fn = reinterpret_cast<const void*>(quantize_tc_kernel<KB, VB>);
+  if (const int st = set_smem_limit(smem_once, fn, tc::kSmemBytes); st != KVARN_OK) return st;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -30,7 +30,9 @@
  *    OR-ed as KVARN_DEV_* bits into *dev_status when dev_status is non-NULL (a device
  *    int32 the caller zeroes and reads); the kernels then clamp to in-bounds data and
  *    never trap.
- *  - head_dim d0: 8..256 and a multiple of 8; it is padded to d = 64, 128 or 256.
+ *  - head_dim d0: 40..256 and a multiple of 8; it is padded to the next power of two,
+ *    d = 64, 128 or 256 [aifeeds §局限].  d0 <= 32 would pad to 8, 16 or 32, widths that have
+ *    no page record layout, and is refused (KVARN_ERR_UNSUPPORTED).
  *  - GQA: query head hq reads KV head hq / G, G = num_q_heads / num_kv_heads in {1,2,4,8}.
  *
  * Page record: the packed K/V of one (page, kv head), record_bytes bytes, 16-byte aligned
@@ -98,7 +100,7 @@ typedef struct kvarn_desc {
  * kvarn_k4v2_g128, block_size 128], or "kvarn_k4v4_g128" / "kvarn_k2v2_g128" /
  * "kvarn_k8v4_g128" (other k/v bit presets through the same pipeline [vatt §四個步驟,
  * bit-width assignment]).  Host only.
- * UNSUPPORTED for another name or a head_dim outside 8..256 / not a multiple of 8;
+ * UNSUPPORTED for another name or a head_dim outside 40..256 / not a multiple of 8;
  * INVALID_ARG for NULL or Hkv < 1. */
 int kvarn_desc_from_preset(const char* preset, int head_dim, int num_kv_heads, kvarn_desc* out);
 
@@ -213,9 +215,12 @@ int kvarn_prefill_attention(const kvarn_desc* desc, int batch, int num_q_heads, 
  *    KVARN_DECODE_NOALLOC_SCRATCH_BYTES per GPU, held from the library's load until exit.
  *    A shape whose kvarn_decode_workspace_bytes exceeds it returns
  *    KVARN_ERR_WORKSPACE_TOO_SMALL before anything is launched.
- *  - The first call on each device looks up the buffer's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call before any
- *    stream capture.  The current device must own stream and pointers.
+ *  - Arguments are checked first, with the same results as kvarn_decode_attention (an
+ *    empty batch returns KVARN_OK without touching the GPU).  Then the first call on each
+ *    device looks up the buffer's device address (cudaGetSymbolAddress) with that device
+ *    current; make that first call before any stream capture.  The address is kept until
+ *    the process exits: do not use this entry point on a device after cudaDeviceReset on it.
+ *    The current device must own stream and pointers.
  *  - All calls on a device share the buffer and it keeps the last call's contents; nothing
  *    in it needs to start at zero.  Calls that overlap on the GPU (other streams, other
  *    threads) race on it: order them on one stream or serialise them. */

@@ -65,13 +65,14 @@ SCALE_FLOOR = 1e-8         # reading: quantiser step floor for constant groups
 # ----------------------------------------------------------------------------
 
 def padded_head_dim(d0: int) -> int:
-    """Next power of two >= d0 (at least 64).  [aifeeds §局限: pad to nearest power]
+    """Next power of two >= d0.  [aifeeds §局限: a head_dim that is not a power of two is
+    padded up to the nearest one]
 
     Pinned by: test_padded_head_dim.
     """
     if d0 < 1:
         raise ValueError("head_dim must be positive")
-    d = 64
+    d = 1
     while d < d0:
         d *= 2
     return d
@@ -293,10 +294,18 @@ def dequantize_tile(codes, scale, zero, factor, kind: str, d0: int) -> np.ndarra
 def record_bytes(d: int, tokens: int = TILE_TOKENS, k_bits: int = K_BITS, v_bits: int = V_BITS) -> int:
     """Bytes of one page record: kb + vb bits of codes per token-channel plus fp16 metadata.
 
+    The record layout is defined for padded head_dim 64, 128 and 256 (its code words tile
+    64-channel groups); smaller padded widths have no record (ValueError).
     Pinned by: test_record_bytes (13824 B at d=128 for K4V2, ratio vs fp16 below 1/4, as
     the vatt capacity widget's "<0.25x, about 4x" for kvarn_k4v2_g128), test_record_bytes_presets.
     """
+    _check_record_dim(d)
     return tokens * d * k_bits // 8 + tokens * d * v_bits // 8 + 2 * (3 * d + 3 * tokens)
+
+
+def _check_record_dim(d: int) -> None:
+    if d not in (64, 128, 256):
+        raise ValueError("page records exist for padded head_dim 64, 128 and 256 only")
 
 
 def _section_offsets(d: int, k_bits: int = K_BITS, v_bits: int = V_BITS):
@@ -323,6 +332,7 @@ def _code_positions(kind: str, bits: int, d: int):
         o, col, i, row = t // 16, t % 16, j // 16, j % 16
     else:
         raise ValueError("kind must be 'K' or 'V'")
+    _check_record_dim(d)
     g, rho = row % 8, row // 8
     h, tq, p = col // 8, (col % 8) // 2, col % 2
     lane = 4 * g + tq

@@ -76,6 +76,12 @@ def test_preset_rejections(kv):
     for bad in (0, 7, 100, 264):
         with pytest.raises(kv.KvarnError):
             kv.desc_from_preset(bad, 8)
+    # head_dim <= 32 pads to itself (8, 16, 32 or 32 for 24), which has no page record
+    for small in (8, 16, 24, 32):
+        with pytest.raises(kv.KvarnError) as e:
+            kv.desc_from_preset(small, 8)
+        assert e.value.status == kv.KVARN_ERR_UNSUPPORTED
+    assert kv.desc_from_preset(40, 8).head_dim_padded == 64
 
 
 def test_workspace_size(kv):
@@ -113,6 +119,36 @@ def test_validation_returns_before_launch(kv):
     assert lib.kvarn_dequantize_tiles(ctypes.byref(bad), null, 1, null, 1, null, null, null,
                                       null) == kv.KVARN_ERR_UNSUPPORTED
     assert "workspace" in kv.status_string(kv.KVARN_ERR_WORKSPACE_TOO_SMALL)
+
+
+def test_noalloc_argument_errors_match_the_workspace_entry_point(kv):
+    # the allocation-free decode checks its arguments before it looks up its buffer (no CUDA
+    # call): the same bad arguments give the same codes as kvarn_decode_attention, and an empty
+    # batch is a no-op; host only
+    lib = kv._lib
+    d = kv.desc_from_preset(128, 8)
+    null = ctypes.c_void_p(0)
+    p16 = ctypes.c_void_p(16)
+    bad_bits = kv.KvarnDesc.from_buffer_copy(d)
+    bad_bits.k_bits = 3
+    cases = [
+        (None, 2, 32, p16, p16, 8, p16, 4, p16, null, null, 0.1, p16),          # no descriptor
+        (bad_bits, 2, 32, p16, p16, 8, p16, 4, p16, null, null, 0.1, p16),      # unsupported bits
+        (d, 2, 24, p16, p16, 8, p16, 4, p16, null, null, 0.1, p16),             # G = 3
+        (d, -1, 32, p16, p16, 8, p16, 4, p16, null, null, 0.1, p16),            # negative batch
+        (d, 2, 32, null, p16, 8, p16, 4, p16, null, null, 0.1, p16),            # no q
+        (d, 2, 32, p16, p16, 8, p16, 4, p16, ctypes.c_void_p(24), p16, 0.1, p16),  # misaligned partial
+        (d, 2, 32, p16, p16, 8, p16, 4, p16, p16, null, 0.1, p16),              # one partial only
+        (d, 2, 32, p16, p16, 8, p16, 4, p16, null, null, 0.0, p16),             # softmax scale 0
+        (d, 0, 32, null, null, 8, null, 4, null, null, null, 0.1, null),        # empty batch: ok
+    ]
+    for c in cases:
+        desc = ctypes.POINTER(kv.KvarnDesc)() if c[0] is None else ctypes.byref(c[0])
+        args = (desc,) + c[1:11] + (ctypes.c_float(c[11]), c[12])
+        want = lib.kvarn_decode_attention(*args, ctypes.c_void_p(16), 1 << 30, null, null)
+        got = lib.kvarn_decode_attention_noalloc(*args, null, null)
+        assert got == want, (c, got, want)
+    assert want == kv.KVARN_OK
 
 
 def test_fp16_baseline_validation(kv):

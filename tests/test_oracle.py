@@ -50,11 +50,24 @@ def _checker(t, d):
 # --- padding and rotation ----------------------------------------------------
 
 def test_padded_head_dim():
-    # aifeeds §局限: non power-of-two head_dim is padded to the next power of two
-    assert ko.padded_head_dim(96) == 128
-    assert ko.padded_head_dim(128) == 128
-    assert ko.padded_head_dim(129) == 256
-    assert ko.padded_head_dim(256) == 256
+    # aifeeds §局限: a head_dim that is not a power of two is padded up to the next power of
+    # two; a power of two is kept as it is, however small
+    for d0, want in ((1, 1), (3, 4), (8, 8), (16, 16), (32, 32), (33, 64), (64, 64), (96, 128),
+                     (128, 128), (129, 256), (256, 256)):
+        assert ko.padded_head_dim(d0) == want, d0
+
+
+@pytest.mark.parametrize("d0", [8, 16, 32])
+def test_small_head_dims_rotate_by_their_own_order(d0):
+    # aifeeds §局限: d0 = 8/16/32 are powers of two, so the rotation is H_d0 / sqrt(d0) itself
+    # (no padding): a unit vector e_0 becomes the constant row 1/sqrt(d0)
+    x = np.zeros((1, d0))
+    x[0, 0] = 1.0
+    np.testing.assert_allclose(ko.rotate(x, ko.padded_head_dim(d0)), np.full((1, d0), d0 ** -0.5),
+                               rtol=0, atol=1e-15)
+    # and such widths have no page record (the record's code words tile 64-channel groups)
+    with pytest.raises(ValueError):
+        ko.record_bytes(d0)
 
 
 @pytest.mark.parametrize("n", [1, 2, 4, 8, 16, 32, 64, 128, 256])
