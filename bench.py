@@ -37,6 +37,7 @@ QUANT_OPS_PER_ELEMENT = 37  # fp32 ops per quantised element (derivation at the 
 SM_MAX_MHZ = 2070.0
 ADAPTIVE_TOL = 0.05  # early-stop tolerance of the normalisation (log-factor change per iteration)
 DEC_EVENT_SAMPLES = 40  # live samples of the decode call's duration, spread over the timed steps
+DEC_EVENT_EVERY_MIN = 5  # ... on at most one step in five, so most steps keep their launch overlap
 WORKLOAD = ("paged decode attention + append: batch 64, seq_len 128*U{8..128}, 32 q heads / 8 kv "
             "heads, head_dim 128, K4V2 g128 packed cache, permuted block table")
 BATCH, HQ, HKV, D0, MIN_PAGES, MAX_PAGES, SEED = 64, 32, 8, 128, 8, 128, 3
@@ -53,21 +54,24 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# DRAM traffic / algorithmic bytes of one decode_kernel launch, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum at batch 24), valid only for the decode.cu source
+# it was taken on: the traffic is reported as null once that file changes.
+DECODE_TRAFFIC = {"decode_cu_sha256": "", "dram_over_algorithmic": None}
+
+
 def _decode_traffic_ratio():
-    """DRAM bytes / algorithmic bytes of the decode kernel from the committed ncu summary, or
-    None when decode.cu changed since that capture."""
+    """DRAM bytes / algorithmic bytes of the decode kernel, or None when decode.cu changed since
+    the capture DECODE_TRAFFIC records."""
     import hashlib
-    import re
     try:
-        with open(os.path.join(ROOT, "profiles", "decode_kernel_batch24_d128.md")) as fh:
-            text = fh.read()
         with open(os.path.join(ROOT, "calibration_free_kv_gb300", "csrc", "decode.cu"), "rb") as fh:
             digest = hashlib.sha256(fh.read()).hexdigest()
-        want = re.search(r"source_sha256:\s*([0-9a-f]{64})", text).group(1)
-        ratio = float(re.search(r"traffic_ratio_dram_over_algorithmic:\s*([0-9.]+)", text).group(1))
-        return ratio if want == digest else None
-    except Exception:
+    except OSError:
         return None
+    if DECODE_TRAFFIC["dram_over_algorithmic"] is None or digest != DECODE_TRAFFIC["decode_cu_sha256"]:
+        return None
+    return float(DECODE_TRAFFIC["dram_over_algorithmic"])
 
 
 def _dist_env():
@@ -171,7 +175,8 @@ def _device_id(torch):
 def _setup_decode(torch, kv, synth, steps_total):
     dev = torch.device("cuda")
     shape = synth.decode_batch(BATCH, HQ, HKV, D0, seed=SEED, min_pages=MIN_PAGES, max_pages=MAX_PAGES)
-    lens0 = shape["seq_lens"].to(torch.int64)
+    lens0 = _initial_lens()  # sealed pages + raw tokens of the open tile
+    phase = lens0 % 128
     base_table = shape["block_table"]
     n_seal_pages = int((lens0 // 128).sum())
     grow = steps_total // 128 + 2                    # pages each sequence may seal while timed
@@ -184,13 +189,19 @@ def _setup_decode(torch, kv, synth, steps_total):
         table[b, :n] = base_table[b, :n]
         table[b, n:n + grow] = extra[b]
     desc = kv.desc_from_preset(D0, HKV)
+    assert desc.page_record_bytes == REC_BYTES
     pool = kv.alloc_pool(desc, n_pool, device=dev)
-    total = int(lens0.sum())
+    total = 128 * n_seal_pages  # the sealed tokens (the open tiles come from another draw)
     k_all, v_all = synth.outlier_kv(total, HKV, D0, seed=SEED, device=dev)
     page_ids = torch.cat([base_table[b, :int(lens0[b]) // 128] for b in range(BATCH)]).to(dev)
     kv.quantize_tiles(desc, k_all, v_all, page_ids, pool)
+    # the open tile of sequence b holds phase[b] raw fp16 tokens of the same generator
+    kp, vp = synth.outlier_kv(BATCH * 128, HKV, D0, seed=SEED + 9, device=dev)
+    rows = (torch.arange(128, device=dev)[None, :] < phase.to(dev)[:, None]).to(torch.float16)
+    pk = (kp.view(BATCH, 128, HKV, D0).transpose(1, 2) * rows[:, None, :, None]).contiguous()
+    pv = (vp.view(BATCH, 128, HKV, D0).transpose(1, 2) * rows[:, None, :, None]).contiguous()
     torch.cuda.synchronize()
-    del k_all, v_all
+    del k_all, v_all, kp, vp
     torch.cuda.empty_cache()
     g = torch.Generator(device=dev)
     g.manual_seed(SEED + 1)
@@ -200,13 +211,42 @@ def _setup_decode(torch, kv, synth, steps_total):
     vn = [torch.randn((BATCH, HKV, D0), generator=g, device=dev).half() for _ in range(n_sets)]
     return {
         "desc": desc, "pool": pool, "table": table.to(dev), "lens0": lens0, "qs": qs, "kn": kn, "vn": vn,
-        "pk": torch.zeros((BATCH, HKV, 128, D0), dtype=torch.float16, device=dev),
-        "pv": torch.zeros((BATCH, HKV, 128, D0), dtype=torch.float16, device=dev),
+        "pk": pk, "pv": pv,
         "lens": [lens0.to(torch.int32).to(dev), torch.zeros(BATCH, dtype=torch.int32, device=dev)],
         "out": torch.empty((BATCH, HQ, D0), dtype=torch.float16, device=dev),
         "ws": kv.alloc_workspace(desc, BATCH, HQ, width, device=dev),
         "status": torch.zeros(1, dtype=torch.int32, device=dev),
         "rec_bytes": desc.page_record_bytes,
+    }
+
+
+REC_BYTES = 13824  # one kvarn_k4v2_g128 page record at head_dim 128 (checked against the library)
+
+
+def _initial_lens():
+    """Lengths of the decode workload before its first step: 128 * U{8..128} sealed tokens plus
+    U{0..127} raw tokens in each sequence's open tile (CPU int64 [BATCH])."""
+    import torch
+    from calibration_free_kv_gb300 import synth
+    shape = synth.decode_batch(BATCH, HQ, HKV, D0, seed=SEED, min_pages=MIN_PAGES, max_pages=MAX_PAGES)
+    return shape["seq_lens"].to(torch.int64) + synth.partial_phases(BATCH, SEED + 7)
+
+
+def _workload_config(lens_before, steps):
+    """The `config` object of the bench line, the same for both arms: lens_before are the
+    lengths when the timed steps start (CPU int64 [BATCH])."""
+    mean0 = float(lens_before.double().mean())
+    return {
+        "workload": WORKLOAD.replace("batch 64", "batch %d" % BATCH),
+        "batch": BATCH, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D0,
+        "seq_len": "128*U{8..128} sealed + U{0..127} raw tokens in the open tile",
+        "mean_seq_len": mean0,
+        "growth": "each step appends one token per sequence (a tile seals every 128 steps per "
+                  "sequence, at random phases); mean length over the timed steps %.0f"
+                  % (mean0 + (steps + 1) / 2),
+        "preset": "kvarn_k4v2_g128",
+        "l2": "inputs larger than L2: each decode reads %.0f MB of packed cache"
+              % (_decode_bytes((lens_before + 1).tolist(), REC_BYTES) / 1e6),
     }
 
 
@@ -217,12 +257,12 @@ def _decode_bytes(lens, rec_bytes):
     return (sealed * HKV * rec_bytes + part * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2)
 
 
-def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps=20, tol=None):
-    """Median ms of kvarn_quantize_tiles on one layer (8 kv heads x 16384 tokens x d 128, K
-    and V), L2 flushed with a 512 MB write before every launch; and its algorithmic bytes.
+def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps=20, tol=None, d0=D0):
+    """Median ms of kvarn_quantize_tiles on one layer (8 kv heads x 16384 tokens x head_dim d0,
+    K and V), L2 flushed with a 512 MB write before every launch; and its algorithmic bytes.
     With tol: kvarn_quantize_tiles_adaptive, and also the mean iterations used."""
-    qdesc = kv.desc_from_preset(D0, Q_HEADS, preset=preset)
-    kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, D0, seed=2, device=dev)
+    qdesc = kv.desc_from_preset(d0, Q_HEADS, preset=preset)
+    kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, d0, seed=2, device=dev)
     qpool = kv.alloc_pool(qdesc, Q_TOKENS // 128, device=dev)
     qids = torch.arange(Q_TOKENS // 128, dtype=torch.int32, device=dev)
     used = torch.zeros((Q_TOKENS // 128, Q_HEADS, 2), dtype=torch.int32, device=dev) if tol is not None else None
@@ -237,13 +277,46 @@ def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps
         torch.cuda.synchronize()
         if rep >= 3:
             q_ms.append(a.elapsed_time(b))
-    nbytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
+    nbytes = 2 * Q_TOKENS * Q_HEADS * d0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
     mean_iters = float(used.double().mean()) if used is not None else None
     del kq, vq, qpool, flush
     torch.cuda.empty_cache()
     if tol is not None:
         return statistics.median(q_ms), nbytes, mean_iters
     return statistics.median(q_ms), nbytes
+
+
+def _time_error_telemetry(torch, kv, synth, dev, stream, reps=10):
+    """kvarn_quantization_error over the quantise layer (8 kv heads x 16384 tokens x d 128): every
+    record checked against its fp16 tiles, L2 flushed before each launch.  Returns us and the
+    bytes it reads (fp16 tiles + records)."""
+    qdesc = kv.desc_from_preset(D0, Q_HEADS)
+    kq, vq = synth.outlier_kv(Q_TOKENS, Q_HEADS, D0, seed=2, device=dev)
+    qpool = kv.alloc_pool(qdesc, Q_TOKENS // 128, device=dev)
+    qids = torch.arange(Q_TOKENS // 128, dtype=torch.int32, device=dev)
+    kv.quantize_tiles(qdesc, kq, vq, qids, qpool, stream=stream)
+    err = torch.zeros((Q_TOKENS // 128, Q_HEADS, 2, 4), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    ms = []
+    for rep in range(3 + reps):
+        flush.fill_(float(rep))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        kv.quantization_error(qdesc, kq, vq, qids, qpool, err, stream=stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if rep >= 3:
+            ms.append(a.elapsed_time(b))
+    e = err.double()
+    rel_k = torch.sqrt(e[:, :, 0, 0] / e[:, :, 0, 1])
+    rel_v = torch.sqrt(e[:, :, 1, 0] / e[:, :, 1, 1])
+    nbytes = 2 * Q_TOKENS * Q_HEADS * D0 * 2 + (Q_TOKENS // 128) * Q_HEADS * qdesc.page_record_bytes
+    t = statistics.median(ms)
+    del kq, vq, qpool, flush
+    torch.cuda.empty_cache()
+    return {"us": t * 1e3, "algorithmic_bytes": nbytes, "hbm_gbs": nbytes / (t * 1e-3) / 1e9,
+            "rel_frobenius_error_k_mean": float(rel_k.mean()), "rel_frobenius_error_k_max": float(rel_k.max()),
+            "rel_frobenius_error_v_mean": float(rel_v.mean()), "rel_frobenius_error_v_max": float(rel_v.max())}
 
 
 def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, seed, reps=5,
@@ -342,15 +415,33 @@ def _quality(torch, kv, synth):
     def cos(a):
         return torch.nn.functional.cosine_similarity(a.reshape(-1, d), ref.reshape(-1, d), dim=-1)
 
+    def dist(c):  # per (sequence, query head) cosines
+        qs = torch.quantile(c, torch.tensor([0.01, 0.05, 0.25, 0.5], dtype=c.dtype, device=c.device))
+        return {"mean": float(c.mean()), "min": float(c.min()), "p1": float(qs[0]), "p5": float(qs[1]),
+                "p25": float(qs[2]), "median": float(qs[3])}
+
     c_kv, c_rtn = cos(out.double()), cos(naive)
-    return {
+    res = {
         "cosine_vs_full_precision": float(c_kv.mean()), "cosine_min": float(c_kv.min()),
         "naive_rtn_cosine": float(c_rtn.mean()), "naive_rtn_cosine_min": float(c_rtn.min()),
-        "sample": "%d sequences x %d tokens, %d q heads / %d kv heads, head_dim %d, outlier "
-                  "generator; reference: float64 softmax attention over the raw fp16 K/V"
-                  % (B, L, hkv * G, hkv, d),
-        "note": "a quality figure, not a target",
+        "q_unit_normal": {"kvarn": dist(c_kv), "naive_rtn": dist(c_rtn)},
     }
+    # the same caches with q / sqrt(d) (the tiny configuration's query scale): softer
+    # attention, so fewer heads sit on a near-tie between two keys
+    qs = (q.float() / math.sqrt(d)).half()
+    out2 = torch.empty_like(q)
+    kv.decode_attention(desc, qs, pool, table, lens, out2, ws, softmax_scale=1 / math.sqrt(d))
+    torch.cuda.synchronize()
+    qq = qs.double().view(B, hkv, G, d)
+    ref = attend(kk, vv)
+    c_kv2, c_rtn2 = cos(out2.double()), cos(attend(k_rtn, v_rtn))
+    res["q_over_sqrt_d"] = {"kvarn": dist(c_kv2), "naive_rtn": dist(c_rtn2)}
+    res["sample"] = ("%d sequences x %d tokens, %d q heads / %d kv heads, head_dim %d, outlier "
+                     "generator; q ~ N(0,1) and q ~ N(0,1)/sqrt(d); per (sequence, query head) "
+                     "cosines; reference: float64 softmax attention over the raw fp16 K/V"
+                     % (B, L, hkv * G, hkv, d))
+    res["note"] = "a quality figure, not a target"
+    return res
 
 
 def _time_prefill(torch, kv, synth, batch=8, cache_len=8192, chunk=64, hq=32, hkv=8, d0=128, seed=7, reps=10):
@@ -468,6 +559,102 @@ def _time_fp16_baseline(torch, kv, S, stream, peak, reps=20, tail=64):
     }
 
 
+def _time_long_stream(torch, kv, synth, d0, peak, steps=512, batch=4, hq=32, hkv=8, seed=5):
+    """Streaming decode at long context: `steps` steps of append + decode for `batch` sequences
+    starting at 130560 + {0, 1, 64, 127} tokens (1020 sealed pages each plus an open tile),
+    head_dim d0 (96 is zero-padded to 128); every tile that fills seals into a packed page inside
+    the timed steps.  The steps run twice from the same state: the first pass warms up, the
+    second (which rewrites the same sealed pages with the same bytes) is timed."""
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    desc = kv.desc_from_preset(d0, hkv)
+    rec = desc.page_record_bytes
+    starts = torch.tensor([130560, 130561, 130624, 130687][:batch], dtype=torch.int64)
+    sealed0 = starts // 128
+    width = int((starts.max() + steps) // 128) + 1
+    n_pool = batch * width
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(n_pool, generator=g).view(batch, width).to(torch.int32)
+    k, v = synth.outlier_kv(int(sealed0.sum()) * 128, hkv, d0, seed=seed, device=dev)
+    ids = torch.cat([table[b, :int(sealed0[b])] for b in range(batch)]).to(dev)
+    pool = kv.alloc_pool(desc, n_pool, device=dev)
+    kv.quantize_tiles(desc, k, v, ids, pool)
+    del k, v
+    kp, vp = synth.outlier_kv(batch * 128, hkv, d0, seed=seed + 1, device=dev)
+    rows = (torch.arange(128, device=dev)[None, :] < (starts % 128).to(dev)[:, None]).to(torch.float16)
+    pk0 = (kp.view(batch, 128, hkv, d0).transpose(1, 2) * rows[:, None, :, None]).contiguous()
+    pv0 = (vp.view(batch, 128, hkv, d0).transpose(1, 2) * rows[:, None, :, None]).contiguous()
+    pk, pv = pk0.clone(), pv0.clone()
+    gd = torch.Generator(device=dev)
+    gd.manual_seed(seed + 2)
+    qs = [torch.randn((batch, hq, d0), generator=gd, device=dev).half() for _ in range(4)]
+    kn = [torch.randn((batch, hkv, d0), generator=gd, device=dev).half() for _ in range(4)]
+    vn = [torch.randn((batch, hkv, d0), generator=gd, device=dev).half() for _ in range(4)]
+    lens = [torch.empty(batch, dtype=torch.int32, device=dev) for _ in range(2)]
+    out = torch.empty((batch, hq, d0), dtype=torch.float16, device=dev)
+    table = table.to(dev)
+    ws = kv.alloc_workspace(desc, batch, hq, width, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(d0)
+    every = 5
+    for rep in range(2):
+        lens[0].copy_(starts.to(torch.int32))
+        pk.copy_(pk0)
+        pv.copy_(pv0)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(0, steps, every)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(200000)  # the host enqueues the first steps while the GPU waits
+        t0.record(stream)
+        for i in range(steps):
+            c = i % 2
+            kv.append_token(desc, kn[i % 4], vn[i % 4], pk, pv, lens[c], table, pool,
+                            seq_lens_out=lens[1 - c], status=status, stream=stream)
+            if i % every == 0:
+                ev[i // every][0].record(stream)
+            kv.decode_attention(desc, qs[i % 4], pool, table, lens[1 - c], out, ws, partial_k=pk,
+                                partial_v=pv, softmax_scale=scale, status=status, stream=stream)
+            if i % every == 0:
+                ev[i // every][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the long-context stream" % int(status.item()))
+    total_ms = t0.elapsed_time(t1)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    d_pad = desc.head_dim_padded
+    new_tok = 2 * batch * hkv * d0 * 2            # k_new + v_new
+    dec_bytes, step_bytes, seals = [], 0, 0
+    for i in range(steps):
+        L = starts + i + 1                          # lengths the step's decode attends to
+        sealed = int((L // 128).sum())
+        part = int((L % 128).sum())
+        db = sealed * hkv * rec + part * hkv * d0 * 2 * 2 + 2 * batch * hq * d0 * 2
+        n_seal = int(((starts + i) % 128 == 127).sum())   # tiles that fill in this step's append
+        seals += n_seal
+        ab = 2 * new_tok + n_seal * hkv * (2 * 128 * d0 * 2 + rec)  # read + write the token; seal
+        step_bytes += db + ab
+        if i % every == 0:
+            dec_bytes.append(db)
+    dec_gbs = statistics.mean(dec_bytes) / (statistics.mean(dec_ms) * 1e-3) / 1e9
+    step_gbs = step_bytes / (total_ms * 1e-3) / 1e9
+    del pool, ws
+    torch.cuda.empty_cache()
+    return {
+        "workload": "%d steps of append + decode, batch %d from %s tokens, %d q heads / %d kv heads, "
+                    "head_dim %d (padded %d), K4V2; %d tiles sealed inside the timed steps"
+                    % (steps, batch, "/".join(str(int(x)) for x in starts), hq, hkv, d0, d_pad,
+                       seals * hkv),
+        "us_per_step": total_ms * 1e3 / steps,
+        "algorithmic_bytes_per_step": step_bytes / steps,
+        "hbm_gbs": step_gbs, "frac": step_gbs / peak,
+        "decode_us": statistics.mean(dec_ms) * 1e3, "decode_hbm_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
+        "decode_duration_source": "CUDA events around the decode call on every %dth step" % every,
+        "kv_tokens_per_s": sum(int((starts + i + 1).sum()) for i in range(steps)) / (total_ms * 1e-3),
+    }
+
+
 def _decode_configs(torch, kv, synth, peak, args):
     """The 32B-class 64-layer decode step and the long-context shapes, each against bytes/peak."""
     res = {}
@@ -499,6 +686,9 @@ def _decode_configs(torch, kv, synth, peak, args):
             "ideal_ms_at_peak": nbytes / (peak * 1e9) * 1e3,
             "kv_tokens_per_s": cfg["batch"] * cfg["seq_len"] / (ms * 1e-3),
         }
+    if args.extras in ("all", "long"):
+        for d0 in (256, 96):
+            res["decode_long_stream_d%d" % d0] = _time_long_stream(torch, kv, synth, d0, peak)
     return res
 
 
@@ -538,10 +728,10 @@ def _run_kvarn(args, torch, world, rank):
     if world > 1:
         torch.distributed.barrier()
     lens_before = S["lens"][state["cur"]].to(torch.int64).cpu()
-    # The decode call's own duration is sampled live on DEC_EVENT_SAMPLES evenly spaced timed
-    # steps: an event recorded between append and decode ends their programmatic-launch
-    # overlap, so the other steps run without it.
-    every = max(1, args.steps // DEC_EVENT_SAMPLES)
+    # The decode call's own duration is sampled live on at most DEC_EVENT_SAMPLES evenly spaced
+    # timed steps, at most one in DEC_EVENT_EVERY_MIN: an event recorded between append and
+    # decode ends their programmatic-launch overlap, so the other steps run without it.
+    every = max(DEC_EVENT_EVERY_MIN, args.steps // DEC_EVENT_SAMPLES)
     sampled = [i for i in range(args.steps) if i % every == 0]
     dec_ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -624,6 +814,13 @@ def _run_kvarn(args, torch, world, rank):
     a_ms, _, a_iters = _time_quantize(torch, kv, synth, dev, stream, reps=10, tol=ADAPTIVE_TOL)
     q_adaptive = {"sinkhorn_tol": ADAPTIVE_TOL, "us": a_ms * 1e3, "tokens_per_s": Q_TOKENS / (a_ms * 1e-3),
                   "mean_iterations": a_iters, "max_iterations": 4}
+    q_telemetry = _time_error_telemetry(torch, kv, synth, dev, stream)
+    q_dims = {}
+    for d0 in (64, 256):  # the CUDA-core rotation path (head_dim 64 and 256)
+        ms, nb = _time_quantize(torch, kv, synth, dev, stream, reps=10, d0=d0)
+        q_dims["head_dim_%d" % d0] = {"us": ms * 1e3, "tokens_per_s": Q_TOKENS / (ms * 1e-3),
+                                      "algorithmic_bytes": nb, "hbm_gbs": nb / (ms * 1e-3) / 1e9,
+                                      "frac": nb / (ms * 1e-3) / 1e9 / peak}
     q_presets = {}
     if args.extras in ("all", "presets"):
         for name in ("kvarn_k4v4_g128", "kvarn_k2v2_g128", "kvarn_k8v4_g128"):
@@ -668,16 +865,7 @@ def _run_kvarn(args, torch, world, rank):
                         "accumulation; f32 quantisation; u4/u2 packed cache",
         "data": "synthetic (outlier generator: N(0,1), 4 channels x20-50 per head, lognormal token "
                 "scales; seeds 3 and 2)",
-        "config": {
-            "workload": WORKLOAD.replace("batch 64", "batch %d" % BATCH),
-            "batch": BATCH, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D0,
-            "seq_len": "128*U{8..128}", "mean_seq_len": float(lens_before.double().mean()),
-            "growth": "each step appends one token per sequence (a tile seals every 128 steps per "
-                      "sequence); mean length over the timed steps %.0f"
-                      % (float(lens_before.double().mean()) + (args.steps + 1) / 2),
-            "preset": "kvarn_k4v2_g128",
-            "l2": "inputs larger than L2: each decode reads %.0f MB of packed cache" % (dec_bytes[0] / 1e6),
-        },
+        "config": _workload_config(lens_before, args.steps),
         "decode_hbm_gbs": achieved,
         "decode_us": avg_dec * 1e3,
         "roofline": {
@@ -700,6 +888,8 @@ def _run_kvarn(args, torch, world, rank):
             "us": q_med * 1e3, "hbm_gbs": q_gbs, "frac": q_gbs / peak,
             "algorithmic_bytes": q_bytes,
             "other_presets": q_presets,
+            "other_head_dims": q_dims,
+            "error_telemetry": q_telemetry,
             "adaptive_stop": q_adaptive,
             "roofline": {
                 "kernel": "quantize_tc_kernel", "bound": "alu", "achieved": q_ops,
@@ -857,8 +1047,7 @@ def _run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (outlier generator)",
-        "config": {"workload": WORKLOAD, "batch": BATCH, "num_q_heads": HQ, "num_kv_heads": HKV,
-                   "head_dim": D0, "seq_len": "128*U{8..128}", "preset": "kvarn_k4v2_g128"},
+        "config": _workload_config(_initial_lens() + args.warmup, args.steps),
         "cpu_baseline": {"value": value, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
                          "sample": descs[0] if descs else ""},
         "e2e": {"value": value, "unit": "KV tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

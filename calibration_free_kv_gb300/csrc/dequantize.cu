@@ -39,7 +39,9 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t* w, int o, int i, int
 }
 
 // grid.x = pages * Hkv * 2, block = 128 threads (one token row each while decoding codes).
-template <int D, int KB, int VB>
+// ERR: instead of storing fp16, compare the dequantised tile (fp32) with the fp16 tile it was
+// quantised from and write the unit's four error statistics (kvarn_quantization_error).
+template <int D, int KB, int VB, bool ERR>
 __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
   constexpr RecordLayout RL = record_layout(D, KB, VB);
   constexpr int LD = DequantShape<D>::kLd;
@@ -105,20 +107,63 @@ __global__ void __launch_bounds__(128) dequantize_kernel(DequantParams p) {
     __syncthreads();
   }
   const float isd = D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
-  __half* dst = (is_v ? p.v_out : p.k_out) + ((int64_t)pi * p.num_kv_heads + h) * kTile * p.d0;
-  for (int idx = threadIdx.x; idx < kTile * p.d0; idx += blockDim.x) {
-    const int row = idx / p.d0, j = idx - row * p.d0;
-    dst[idx] = __float2half_rn(smem_x[row * LD + j] * isd);
+  if constexpr (!ERR) {
+    __half* dst = (is_v ? p.v_out : p.k_out) + ((int64_t)pi * p.num_kv_heads + h) * kTile * p.d0;
+    for (int idx = threadIdx.x; idx < kTile * p.d0; idx += blockDim.x) {
+      const int row = idx / p.d0, j = idx - row * p.d0;
+      dst[idx] = __float2half_rn(smem_x[row * LD + j] * isd);
+    }
+  } else {
+    // sum (x - x^)^2, sum x^2, max |x - x^|, max |x| over the 128 x d0 values of the unit
+    const __half* src = (is_v ? p.v_src : p.k_src) + (int64_t)pi * kTile * p.tok_stride +
+                        (int64_t)h * p.head_stride;
+    float se = 0.0f, sx = 0.0f, me = 0.0f, mx = 0.0f;
+    for (int idx = threadIdx.x; idx < kTile * p.d0; idx += blockDim.x) {
+      const int row = idx / p.d0, j = idx - row * p.d0;
+      const float x = __half2float(src[row * p.tok_stride + j]);
+      const float e = x - smem_x[row * LD + j] * isd;
+      se = fmaf(e, e, se);
+      sx = fmaf(x, x, sx);
+      me = fmaxf(me, fabsf(e));
+      mx = fmaxf(mx, fabsf(x));
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+      se += __shfl_xor_sync(0xffffffffu, se, m);
+      sx += __shfl_xor_sync(0xffffffffu, sx, m);
+      me = fmaxf(me, __shfl_xor_sync(0xffffffffu, me, m));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    }
+    __syncthreads();  // smem_x is read by every thread above; reuse its head for the warps' sums
+    float4* part = reinterpret_cast<float4*>(smem_x);
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = make_float4(se, sx, me, mx);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float4 a = part[0];
+#pragma unroll
+      for (int w = 1; w < 4; ++w) {
+        const float4 b = part[w];
+        a = make_float4(a.x + b.x, a.y + b.y, fmaxf(a.z, b.z), fmaxf(a.w, b.w));
+      }
+      reinterpret_cast<float4*>(p.err_out)[((int64_t)pi * p.num_kv_heads + h) * 2 + (is_v ? 1 : 0)] = a;
+    }
   }
 }
 
 template <int D, int KB, int VB>
 static int launch_dequant_t(const DequantParams& p, int num_pages, cudaStream_t stream) {
   constexpr int kSmem = DequantShape<D>::kSmemBytes;
-  static PerDeviceOnce smem_once;  // the attribute is set once per device
-  const void* fn = reinterpret_cast<const void*>(dequantize_kernel<D, KB, VB>);
-  if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
-  dequantize_kernel<D, KB, VB><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
+  if (p.err_out == nullptr) {
+    static PerDeviceOnce smem_once;  // the attribute is set once per device
+    const void* fn = reinterpret_cast<const void*>(dequantize_kernel<D, KB, VB, false>);
+    if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
+    dequantize_kernel<D, KB, VB, false><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
+  } else {
+    static PerDeviceOnce smem_once;
+    const void* fn = reinterpret_cast<const void*>(dequantize_kernel<D, KB, VB, true>);
+    if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
+    dequantize_kernel<D, KB, VB, true><<<num_pages * p.num_kv_heads * 2, 128, kSmem, stream>>>(p);
+  }
   return cudaGetLastError() == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 

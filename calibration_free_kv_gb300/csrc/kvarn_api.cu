@@ -361,6 +361,37 @@ int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_
                             static_cast<cudaStream_t>(stream));
 }
 
+int kvarn_quantization_error(const kvarn_desc* desc, const void* k, const void* v,
+                             int64_t tok_stride, int64_t head_stride, int num_tiles,
+                             const int32_t* page_ids, const void* page_pool, int64_t num_pool_pages,
+                             float* err_stats, int32_t* dev_status, void* stream) {
+  int st = check_desc(desc);
+  if (st != KVARN_OK) return st;
+  if (num_tiles < 0) return KVARN_ERR_INVALID_ARG;
+  if (num_tiles == 0) return KVARN_OK;
+  if (k == nullptr || v == nullptr || page_ids == nullptr || page_pool == nullptr ||
+      err_stats == nullptr)
+    return KVARN_ERR_INVALID_ARG;
+  if (!aligned16(err_stats)) return KVARN_ERR_INVALID_ARG;
+  if (tok_stride <= 0 || head_stride < 0) return KVARN_ERR_INVALID_ARG;
+  if (num_pool_pages < 1) return KVARN_ERR_INVALID_ARG;
+  if ((int64_t)num_tiles * desc->num_kv_heads * 2 > 0x7fffffffLL) return KVARN_ERR_INVALID_ARG;
+  DequantParams p{};
+  p.pool = static_cast<const uint8_t*>(page_pool);
+  p.num_pool_pages = num_pool_pages;
+  p.page_ids = page_ids;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.d0 = desc->head_dim;
+  p.status = dev_status;
+  p.k_src = static_cast<const __half*>(k);
+  p.v_src = static_cast<const __half*>(v);
+  p.tok_stride = tok_stride;
+  p.head_stride = head_stride;
+  p.err_out = err_stats;
+  return launch_dequant_any(desc->head_dim_padded, desc->k_bits, desc->v_bits, p, num_tiles,
+                            static_cast<cudaStream_t>(stream));
+}
+
 const char* kvarn_status_string(int status) {
   switch (status) {
     case KVARN_OK: return "ok";

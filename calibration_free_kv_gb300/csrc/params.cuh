@@ -73,6 +73,12 @@ struct DequantParams {
   int num_kv_heads;
   int d0;
   int32_t* status;
+  // error telemetry (err_out non-null): the fp16 tiles the records were quantised from, laid
+  // out as kvarn_quantize_tiles' inputs, and four floats per (tile, kv head, K or V)
+  const __half* k_src;
+  const __half* v_src;
+  int64_t tok_stride, head_stride;
+  float* err_out;
 };
 
 // decode_args_check: a valid decode call with nothing to launch (batch 0).

@@ -43,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "kvarn_fp16_decode_workspace_bytes",
     "kvarn_fp16_decode_attention",
     "kvarn_selftest_wait_timeout",
+    "kvarn_quantization_error",
 )
 
 # Size of the library's fixed decode scratch (KVARN_DECODE_NOALLOC_SCRATCH_BYTES in kvarn.h).
@@ -98,6 +99,7 @@ def _load():
         "kvarn_fp16_decode_attention": (i32, [i32, i32, i32, i32, P, P, i64, P, i32, P, ctypes.c_float,
                                               P, P, ctypes.c_size_t, P, P]),
         "kvarn_selftest_wait_timeout": (i32, [P, P]),
+        "kvarn_quantization_error": (i32, [D, P, P, i64, i64, i32, P, P, i64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -310,3 +312,22 @@ def dequantize_tiles(desc: KvarnDesc, pool, page_ids, k_out, v_out, status=None,
     _check(_lib.kvarn_dequantize_tiles(ctypes.byref(desc), _ptr(pool), pool.shape[0],
                                        _ptr(page_ids), page_ids.numel(), _ptr(k_out), _ptr(v_out),
                                        _ptr(status), _stream(stream)), "kvarn_dequantize_tiles")
+
+
+def quantization_error(desc: KvarnDesc, k, v, page_ids, pool, err_stats, status=None, stream=None):
+    """Error telemetry of the records page_ids[i] against the fp16 tiles of k, v ([tokens, Hkv,
+    d0], as given to quantize_tiles): err_stats float32 [tiles, Hkv, 2, 4] receives, per unit,
+    sum (x - x^)^2, sum x^2, max |x - x^|, max |x|."""
+    _dev(k, torch.float16, "k")
+    _dev(v, torch.float16, "v")
+    _dev(page_ids, torch.int32, "page_ids")
+    _dev(err_stats, torch.float32, "err_stats")
+    if k.shape != v.shape or k.stride() != v.stride() or k.dim() != 3 or k.stride(2) != 1:
+        raise ValueError("k and v must be [tokens, Hkv, d0] with matching strides, channels contiguous")
+    num_tiles = k.shape[0] // 128
+    if page_ids.numel() < num_tiles or err_stats.numel() < num_tiles * desc.num_kv_heads * 8:
+        raise ValueError("page_ids or err_stats too short for the tiles")
+    _check(_lib.kvarn_quantization_error(ctypes.byref(desc), _ptr(k), _ptr(v), k.stride(0), k.stride(1),
+                                         num_tiles, _ptr(page_ids), _ptr(pool), pool.shape[0],
+                                         _ptr(err_stats), _ptr(status), _stream(stream)),
+           "kvarn_quantization_error")

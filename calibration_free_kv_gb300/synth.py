@@ -100,3 +100,10 @@ def decode_batch(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
     q = torch.randn((batch, num_q_heads, head_dim), generator=g).to(torch.float16)
     return {"seq_lens": seq_lens.to(torch.int32).to(device), "block_table": table.to(device),
             "q": q.to(device), "pool_pages": n_pool}
+
+
+def partial_phases(batch: int, seed: int) -> torch.Tensor:
+    """Raw tokens already in each sequence's unsealed tile, U{0..127} (int64 [batch], CPU):
+    a decode loop meets its sequences at random points of their current 128-token tile."""
+    g = _gen(seed, "cpu")
+    return torch.randint(0, 128, (batch,), generator=g)

@@ -238,6 +238,22 @@ int kvarn_dequantize_tiles(const kvarn_desc* desc, const void* page_pool, int64_
                            const int32_t* page_ids, int num_pages, void* k_out, void* v_out,
                            int32_t* dev_status, void* stream);
 
+/* Quantisation-error telemetry: page records checked against the fp16 tiles they were
+ * quantised from [hotdry §监控要点: sample the dequantised values periodically and watch the
+ * quantisation error].  Tiles and pages are given as to kvarn_quantize_tiles (the same k, v,
+ * strides, num_tiles and page_ids; pass a subset of the tiles to sample).  For each tile i,
+ * kv head h and half (0 = K, 1 = V) it writes four floats at err_stats[((i*Hkv + h)*2 + half)*4]:
+ *    sum over the 128 x d0 values of (x - x^)^2,   sum of x^2,   max |x - x^|,   max |x|
+ * with x the fp16 source value and x^ the record's dequantised value in the original basis
+ * (float32, before the fp16 rounding of kvarn_dequantize_tiles).  The relative Frobenius error
+ * of the unit is sqrt(first / second).
+ *  err_stats  device float [num_tiles][Hkv][2][4], 16-byte aligned.
+ * Reads the records and the source tiles once; launches one kernel. */
+int kvarn_quantization_error(const kvarn_desc* desc, const void* k, const void* v,
+                             int64_t tok_stride, int64_t head_stride, int num_tiles,
+                             const int32_t* page_ids, const void* page_pool, int64_t num_pool_pages,
+                             float* err_stats, int32_t* dev_status, void* stream);
+
 /* ---- Uncompressed fp16 paged decode: the baseline the packed cache is measured against ----
  * [hotdry §监控要点: throughput is judged against fp16 KV caches; vatt §一次 16K context…:
  *  every decode step reads every cached byte].  Same paging (128-token pages, block table,

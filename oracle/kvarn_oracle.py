@@ -262,6 +262,24 @@ def dequantize_tile(codes, scale, zero, factor, kind: str, d0: int) -> np.ndarra
     return rotate(xt, d)[..., :d0]
 
 
+def quantization_error(tile: np.ndarray, codes, scale, zero, factor, kind: str) -> np.ndarray:
+    """Error statistics of one quantised tile against the tile it came from.
+
+    tile: [128, d0] source values; codes / scale / zero / factor: one K or V half of a page
+    record (as quantize_tile returns or unpack_record gives back).  With x the source and
+    x^ = dequantize_tile(...) the dequantised tile in the original basis, returns
+    [sum (x - x^)^2, sum x^2, max |x - x^|, max |x|] over the 128 x d0 values.
+    [hotdry §监控要点: sample the dequantised values periodically and watch the quantisation
+     error]
+    Pinned by: test_quantization_error_* (rotated-domain equality, power-of-two scaling,
+    bit-width order, zero tile).
+    """
+    x = np.asarray(tile, dtype=np.float64)
+    d0 = x.shape[-1]
+    e = x - dequantize_tile(codes, scale, zero, factor, kind, d0)
+    return np.array([np.sum(e * e), np.sum(x * x), np.max(np.abs(e)), np.max(np.abs(x))])
+
+
 # ----------------------------------------------------------------------------
 # page record: byte layout of one (page, kv head) in the packed cache
 # ----------------------------------------------------------------------------

@@ -777,3 +777,53 @@ def test_prefill_empty_cache_is_causal_self_attention():
     np.testing.assert_allclose(out[0, 0], cv[0], rtol=0, atol=1e-12)
     w = np.exp(0.125 * ck[:3] @ q[2, 0] - (0.125 * ck[:3] @ q[2, 0]).max())
     np.testing.assert_allclose(out[2, 0], (w / w.sum()) @ cv[:3], rtol=1e-12, atol=1e-12)
+
+
+# --- quantisation-error telemetry (hotdry §监控要点) ----------------------------------------
+
+def _stats(tile, kind, bits=None):
+    q = ko.quantize_tile(tile, kind, bits=bits)
+    return ko.quantization_error(tile, q["codes"], q["scale"], q["zero"], q["factor"], kind), q
+
+
+@pytest.mark.parametrize("kind", ["K", "V"])
+def test_quantization_error_equals_rotated_domain_error(kind):
+    # the rotation is orthonormal, so at d0 = d the original-basis error equals the error of
+    # the stored values against X = rotate(tile) in the rotated domain, computed here without
+    # any inverse rotation
+    k, v = synth.outlier_kv(128, 1, 128, seed=31)
+    tile = (k if kind == "K" else v)[:, 0].double().numpy()
+    st, q = _stats(tile, kind)
+    x = ko.rotate(tile, 128)
+    s, z, f = (q[n].astype(np.float64) for n in ("scale", "zero", "factor"))
+    if kind == "K":
+        xt = f[:, None] * (q["codes"] * s[None, :] + z[None, :])
+    else:
+        xt = f[None, :] * (q["codes"] * s[:, None] + z[:, None])
+    np.testing.assert_allclose(st[0], np.sum((x - xt) ** 2), rtol=1e-10)
+    np.testing.assert_allclose(st[1], np.sum(tile ** 2), rtol=1e-12)
+    assert st[3] == np.max(np.abs(tile))
+    assert 0 < st[0] < st[1] and 0 < st[2] <= st[3]
+
+
+def test_quantization_error_scales_with_powers_of_two():
+    # every step is equivariant under x -> 2^k x (fp16 metadata rounding included), so the two
+    # sums scale by 4^k and the two maxima by 2^k
+    k, _ = synth.outlier_kv(128, 1, 96, seed=32)
+    tile = k[:, 0].double().numpy()
+    a, _ = _stats(tile, "K")
+    b, _ = _stats(tile * 8.0, "K")
+    np.testing.assert_allclose(b, a * np.array([64.0, 64.0, 8.0, 8.0]), rtol=1e-9)
+
+
+def test_quantization_error_falls_with_code_width():
+    # more code bits on the same tile give a smaller reconstruction error
+    _, v = synth.outlier_kv(128, 1, 128, seed=33)
+    tile = v[:, 0].double().numpy()
+    e2, e4, e8 = (_stats(tile, "V", bits=b)[0][0] for b in (2, 4, 8))
+    assert e8 < e4 < e2
+
+
+def test_quantization_error_of_a_zero_tile():
+    st, _ = _stats(np.zeros((128, 128)), "K")
+    np.testing.assert_array_equal(st, np.zeros(4))
