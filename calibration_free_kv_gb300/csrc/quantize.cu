@@ -661,15 +661,24 @@ static int launch_quantize(const QuantizeParams& p, int units, cudaStream_t stre
                     stream, p);
 }
 
-// ---- head_dim 128: the rotation on the tensor cores -------------------------------------------
+// ---- head_dim 128: the rotation on the tensor cores, the statistics one line per thread -------
 //
-// Persistent CTAs of 256 threads walk a list of units.  Each CTA builds H_128 once in shared
-// memory and rotates every unit with tcgen05.mma (fp16 operands, exact +-1 entries, fp32
-// accumulation in tensor memory): K as D[token][channel] = Z . H, V as D[channel][token] =
-// H . Z^T, so in both cases the quantisation axis lies along TMEM lanes.  tcgen05.ld with the
-// 16x256b shape hands every thread exactly its 4 x 16 block of the layout used by
-// quantize_rotated.  The next unit's fp16 tile is fetched with cp.async and rotated into the
-// second TMEM buffer while the current unit is normalised and quantised.
+// Persistent CTAs of 256 threads (two per SM) walk a list of units.  Each CTA builds H_128 once
+// in shared memory.  Per unit, two tcgen05.mma rotations (fp16 operands, exact +-1 entries, fp32
+// accumulation) put the tile into tensor memory twice: A = Z.H (TMEM lanes = tokens, columns =
+// channels) and B = H.Z^T (lanes = channels, columns = tokens).  The rotation's 1/sqrt(d) is
+// folded into the initial token factors instead of being applied to the values.
+//
+// A std step normalises the lines of one orientation: the channel step the lines of B, the
+// token step the lines of A.  Thread (warp w, lane t) owns line 32(w % 4) + t and its columns
+// [64(w / 4), +64): it streams its 64 values out of tensor memory and scales them by the other
+// axis' factors (broadcast from shared memory); the half line gets an exact two-pass mean and
+// centred sum of squares, and one shared-memory exchange with the partner thread that holds
+// the other 64 columns merges the halves (Chan's formula).
+//
+// Quantisation: the min / max of each group is taken one group per line (K: lines of B, V:
+// lines of A) and the codes are formed in the 16x256b layout of the other orientation (K: A,
+// V: B), where every thread holds exactly the fragments it packs.
 namespace tc {
 constexpr int kThreads = 256;
 constexpr int kOpBytes = 128 * 128 * 2;              // one 128 x 128 fp16 operand
@@ -677,15 +686,18 @@ constexpr uint32_t kLbo = 128;                       // K-adjacent 8x8 core matr
 constexpr uint32_t kSbo = 2048;                      // row-band-adjacent core matrices
 constexpr int kHOff = 0;
 constexpr int kZOff = kOpBytes;                      // two tile buffers
-constexpr int kScrOff = 3 * kOpBytes;
-constexpr int kScrBytes = RotScratch<128>::kFloats * 4;  // scratch of quantize_rotated
+constexpr int kFOff = 3 * kOpBytes;                  // token factors fT[128], channel factors fC[128]
+constexpr int kXOff = kFOff + 2 * 128 * 4;           // partner exchange, float4 [256]
+constexpr int kQOff = kXOff + kThreads * 16;         // group (m, 1/s), float2 [128]
 constexpr int kListCap = 256;                        // units per CTA
-constexpr int kListOff = kScrOff + kScrBytes;
+constexpr int kIoOff = kQOff + 64 * 16;                // per listed unit: tile source, record
+constexpr int kListOff = kIoOff + kListCap * 16;
 constexpr int kBarOff = kListOff + kListCap * 4;
 constexpr int kSmemBytes = kBarOff + 64;
-constexpr int kTmemCols = 256;                       // two 128-column fp32 accumulators
+constexpr int kTmemCols = 256;                       // A (columns 0..127) and B (128..255)
 // kind::f16 instruction descriptor: f32 accumulate, f16 A and B, both K-major, N = 128, M = 128
 constexpr uint32_t kIdesc = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr float kInvSqrt128 = 0.08838834764831845f;
 
 __device__ __forceinline__ uint32_t canon(int r, int k) {  // byte offset of element (r, k)
   return (uint32_t)((r >> 3) * kSbo + (k >> 3) * kLbo + (r & 7) * 16 + (k & 7) * 2);
@@ -712,6 +724,7 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 consecutive accumulator columns of 16 TMEM lanes (16x256b, 8 repetitions).
 __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
@@ -724,6 +737,29 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)
         "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
         "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+}
+
+// 32 consecutive columns of the warp's 32 TMEM lanes (32x32b, 32 repetitions): lane t of the
+// warp receives its own lane's values.
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+
+// The thread's 64 values of its line: columns [64 hf, +64) of TMEM lane `line`.
+__device__ __forceinline__ void load_line(uint32_t taddr, uint32_t (&r)[64]) {
+  uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[0]);
+  uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&r[32]);
+  tmem_ld_32x32b_x32(taddr, lo);
+  tmem_ld_32x32b_x32(taddr + 32, hi);
+  tmem_wait_ld();
 }
 
 // Source tile and destination record of a unit; false if the unit has nothing to do.
@@ -749,17 +785,366 @@ __device__ __forceinline__ bool unit_io(const QuantizeParams& p, int u, const __
   return true;
 }
 
-// Stage one fp16 tile (128 tokens x d0, zero-padded to 128) into a canonical K-major buffer.
+// Stage one fp16 tile (128 tokens x d0, zero-padded to 128) into a canonical K-major buffer:
+// thread t copies the 16-byte chunk c8 = (t / 8) % 16 of tokens t0 + 16j, t0 = t % 8 + 8 (t / 128),
+// j < 8 (16-byte chunks past d0 are zero-filled).
 __device__ __forceinline__ void load_tile(uint32_t zbuf, const __half* src, int64_t tok_stride,
                                           int d0) {
+  const int tid = threadIdx.x;
+  const int c8 = (tid >> 3) & 15, t0 = (tid & 7) | ((tid >> 7) << 3);
+  const bool in = c8 * 8 < d0;
+  const __half* g = src + t0 * tok_stride + c8 * 8;
+  const int64_t step = 16 * tok_stride;
+  const uint32_t s = zbuf + canon(t0, c8 * 8);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int q = threadIdx.x + kThreads * j;        // bits: [t & 7][c8][t >> 3]
-    const int t = (q & 7) | ((q >> 7) << 3), c8 = (q >> 3) & 15;
-    const bool in = c8 * 8 < d0;
-    cp_async16(zbuf + canon(t, c8 * 8), in ? (const void*)(src + t * tok_stride + c8 * 8) : (const void*)src,
-               in ? 16u : 0u);
+  for (int j = 0; j < 8; ++j)
+    cp_async16(s + j * 2 * kSbo, in ? (const void*)(g + j * step) : (const void*)src, in ? 16u : 0u);
+}
+
+// reciprocal square root (MUFU, relative error below 2^-22; +inf at 0)
+__device__ __forceinline__ float rsqrt_approx(float x) {
+  float r;
+  asm("rsqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// New factor of a line from its variance: 1 / sd, or the old factor where the line's std under
+// the old factor (sigma = f_old sd) is below eps.  `moved`: |ln sigma| beyond the early-stop
+// tolerance.
+__device__ __forceinline__ float line_factor(float f_old, float var, float eps, float tol_lo, float tol_hi,
+                                             bool& moved) {
+  const float v = fmaxf(var, 0.0f);
+  const float rs = rsqrt_approx(v);
+  const float sigma = v > 0.0f ? f_old * (v * rs) : 0.0f;
+  if (!(sigma >= eps)) return f_old;
+  moved = sigma > tol_hi || sigma < tol_lo;
+  return rs;
+}
+
+// y = x f for the thread's 64 values, in place, each product rounded toward zero.  A product
+// in another rounding mode than the adds that follow is never fused into them, so a later
+// y - mean sees exactly the stored product: a line of identical y has centred values of
+// exactly 0.  (Round-toward-zero is one unit in the last place at most, well inside the
+// precision the normalisation needs.)
+__device__ __forceinline__ float2 mul2_rz(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack_f2(a)), "l"(pack_f2(b)));
+  return unpack_f2(d);
+}
+__device__ __forceinline__ void scale_line(uint32_t (&r)[64], const float4* f4) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float4 f = f4[k];
+    const float2 y0 = mul2_rz(make_float2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1])),
+                              make_float2(f.x, f.y));
+    const float2 y1 = mul2_rz(make_float2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])),
+                              make_float2(f.z, f.w));
+    r[4 * k] = __float_as_uint(y0.x);
+    r[4 * k + 1] = __float_as_uint(y0.y);
+    r[4 * k + 2] = __float_as_uint(y1.x);
+    r[4 * k + 3] = __float_as_uint(y1.y);
   }
+}
+
+// One std step over the lines of one orientation (TMEM columns at taddr): every line's values
+// scaled by the column factors `fcol`, its own factor in `fline[line]` replaced by the new one.
+// Returns whether the factor moved beyond the early-stop tolerance.  Every thread of the CTA
+// calls it; it ends with a CTA barrier, after which the new factors are visible.
+//
+// Each thread takes its half line (64 values) in an exact two-pass form: y = x f rounded, a
+// pairwise sum (so a half line of identical values has a mean equal to its values), then the
+// centred squares.  The two halves are merged with Chan's formula after one exchange with the
+// partner thread: a line of identical values gets a std of exactly 0, and a large mean costs no
+// precision.
+__device__ __forceinline__ bool std_step(uint32_t taddr, const float* fcol, float* fline, float4* xbuf,
+                                         int line, int hf, float eps, float tol_lo, float tol_hi) {
+  const int tid = threadIdx.x;
+  const float4* f4 = reinterpret_cast<const float4*>(fcol + 64 * hf);
+  const float f_old = fline[line];
+  uint32_t r[64];
+  load_line(taddr, r);
+  scale_line(r, f4);
+  // pairwise sum of the 64 rounded y (as 32 pairs)
+  float2 ps[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    ps[i] = add2(make_float2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
+                 make_float2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) ps[i] = add2(ps[2 * i], ps[2 * i + 1]);
+  const float mean_h = (ps[0].x + ps[0].y) * (1.0f / 64.0f);
+  float2 q[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) q[a] = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    const float2 d = sub2(make_float2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])),
+                          make_float2(mean_h, mean_h));
+    q[k & 3] = fma2(d, d, q[k & 3]);
+  }
+  const float2 tq = add2(add2(q[0], q[1]), add2(q[2], q[3]));
+  const float m2_h = tq.x + tq.y;
+  float2* x2 = reinterpret_cast<float2*>(xbuf);
+  x2[2 * tid] = make_float2(mean_h, m2_h);
+  __syncthreads();
+  const float2 o = x2[2 * (tid ^ 128)];
+  // Chan's merge of two halves of 64, the lower column half first (both partners agree)
+  const float mean_lo = hf ? o.x : mean_h, m2_lo = hf ? o.y : m2_h;
+  const float mean_hi = hf ? mean_h : o.x, m2_hi = hf ? m2_h : o.y;
+  const float delta = mean_hi - mean_lo;
+  const float var = fmaf(delta * delta, 32.0f, m2_lo + m2_hi) * (1.0f / 128.0f);
+  bool moved = false;
+  const float f_new = line_factor(f_old, var, eps, tol_lo, tol_hi, moved);
+  if (hf == 0) fline[line] = f_new;
+  __syncthreads();
+  return moved;
+}
+
+// Codes of a 4 x 16 block in the 16x256b layout (rows g + 8l of the warp's 32-lane quarter,
+// columns 8u + 2tq + p of its 64-column half): v = (x fL_l fC_c - m_c) / s_c, rounded half to
+// even by the 1.5 * 2^23 addition (the code is the low byte of the float's bits), then packed
+// as mma fragments into the record (layout in kvarn.h).
+template <bool TRANS, int KB, int VB>
+__device__ __forceinline__ void codes_and_pack(const float (&x)[4][16], const float (&fl)[4], const float* fcol,
+                                               const float4* qpair, uint8_t* __restrict__ rec) {
+  constexpr int D = 128;
+  constexpr int BITS = TRANS ? VB : KB;
+  constexpr RecordLayout RL = record_layout(D, KB, VB);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tq = lane & 3;
+  const int lq = warp & 3, ch = warp >> 2;
+  uint32_t code[4][16];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int c = 64 * ch + 8 * u + 2 * tq;
+    const float4 q = qpair[c >> 1];                 // (m_c, 1/s_c, m_c+1, 1/s_c+1)
+    const float2 fc = *reinterpret_cast<const float2*>(fcol + c);
+    const float2 nm = make_float2(-q.x, -q.z), inv = make_float2(q.y, q.w);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+      const float2 z = mul2(make_float2(x[l][2 * u], x[l][2 * u + 1]), make_float2(fl[l], fl[l]));
+      const float2 dlt = fma2(z, fc, nm);
+      const float2 v = fma2(dlt, inv, make_float2(12582912.0f, 12582912.0f));
+      code[l][2 * u] = __float_as_uint(v.x);
+      code[l][2 * u + 1] = __float_as_uint(v.y);
+    }
+  }
+  // low bytes of four code registers -> one word, byte i from register i
+  auto gather4 = [](uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x4000), 0x7610);
+  };
+  // A lane's codes form the fragments of row blocks 2lq + lh and column blocks 4ch + j, element
+  // (rho, h, p) at row 2lh + rho, column 2(2j + h) + p of code[][].  K: token block = row
+  // block; V: token block = column block.
+  constexpr int NI4 = D / 64;
+  if constexpr (BITS == 4) {
+    uint32_t w[2][4];
+#pragma unroll
+    for (int lh = 0; lh < 2; ++lh)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c0 = 4 * j, c1 = 4 * j + 2, r0 = 2 * lh, r1 = 2 * lh + 1;
+        const uint32_t lo = gather4(code[r0][c0], code[r1][c0], code[r0][c0 + 1], code[r1][c0 + 1]);
+        const uint32_t hi = gather4(code[r0][c1], code[r1][c1], code[r0][c1 + 1], code[r1][c1 + 1]);
+        w[lh][j] = (lo & 0x0F0F0F0Fu) | ((hi << 4) & 0xF0F0F0F0u);
+      }
+    if constexpr (!TRANS) {
+      uint8_t* kc = rec + RL.kcodes;
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh)
+        *reinterpret_cast<uint4*>(kc + (((2 * lq + lh) * NI4 + ch) * 32 + lane) * 16) =
+            make_uint4(w[lh][0], w[lh][1], w[lh][2], w[lh][3]);
+    } else {
+      uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint2*>(vc + ((((4 * ch + j) * NI4 + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
+            make_uint2(w[0][j], w[1][j]);
+    }
+  } else if constexpr (BITS == 8) {
+    auto w8 = [&](int lh, int j, int hh) {
+      const int c = 2 * (2 * j + hh), r0 = 2 * lh, r1 = 2 * lh + 1;
+      return gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
+    };
+    constexpr int NI2 = D / 32;
+    if constexpr (!TRANS) {
+      uint8_t* kc = rec + RL.kcodes;
+#pragma unroll
+      for (int lh = 0; lh < 2; ++lh)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+          *reinterpret_cast<uint4*>(kc + (((2 * lq + lh) * NI2 + 2 * ch + jj) * 32 + lane) * 16) =
+              make_uint4(w8(lh, 2 * jj, 0), w8(lh, 2 * jj, 1), w8(lh, 2 * jj + 1, 0), w8(lh, 2 * jj + 1, 1));
+    } else {
+      uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(vc + (((4 * ch + j) * NI2 + lq) * 32 + lane) * 16) =
+            make_uint4(w8(0, j, 0), w8(0, j, 1), w8(1, j, 0), w8(1, j, 1));
+    }
+  } else {
+    static_assert(BITS == 2, "2-, 4- or 8-bit codes");
+    if constexpr (!TRANS) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t acc = 0u;
+#pragma unroll
+        for (int s2 = 3; s2 >= 0; --s2) {
+          const int lh = s2 >> 1, c = 2 * (2 * j + (s2 & 1)), r0 = 2 * lh, r1 = 2 * lh + 1;
+          const uint32_t b = gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
+          acc = (acc << 2) | (b & 0x03030303u);
+        }
+        w[j] = acc;
+      }
+      *reinterpret_cast<uint4*>(rec + RL.kcodes + ((lq * NI4 + ch) * 32 + lane) * 16) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      uint8_t* vc = rec + RL.vcodes;
+#pragma unroll
+      for (int uh = 0; uh < 2; ++uh) {
+        uint32_t w[2];
+#pragma unroll
+        for (int lh = 0; lh < 2; ++lh) {
+          uint32_t acc = 0u;
+#pragma unroll
+          for (int uu = 3; uu >= 0; --uu) {
+            const int c = 2 * (4 * uh + uu), r0 = 2 * lh, r1 = 2 * lh + 1;
+            const uint32_t b = gather4(code[r0][c], code[r1][c], code[r0][c + 1], code[r1][c + 1]);
+            acc = (acc << 2) | (b & 0x03030303u);
+          }
+          w[lh] = acc;
+        }
+        const int ks2 = 2 * ch + uh;
+        *reinterpret_cast<uint2*>(vc + (((ks2 * NI4 + lq / 2) * 32 + lane) * 4 + 2 * (lq & 1)) * 4) =
+            make_uint2(w[0], w[1]);
+      }
+    }
+  }
+}
+
+// Normalise, quantise, fold and pack one unit.  Its rotation B is in TMEM columns bufB when
+// this is called; A (columns bufA) may still be in flight: wait_a() (CTA-uniform, idempotent,
+// false on a timeout) is called before A's first use.  Between the group pass and the codes
+// pass, once every thread has finished reading the buffer the group pass used, group_done(
+// freed columns) runs (the caller may rotate the next unit into it).  Returns the iterations
+// used, or -1 after a timeout.  fT / fC: the CTA's token and channel factor arrays.
+template <int KB, int VB, class WaitA, class GroupDone>
+__device__ __forceinline__ int quantize_unit_tc(bool is_v, uint32_t tmem_base, uint32_t bufB, uint32_t bufA,
+                                                uint8_t* __restrict__ rec, const QuantizeParams& p, float* fT,
+                                                float* fC, float4* xbuf, float4* qpair, WaitA wait_a,
+                                                GroupDone group_done) {
+  constexpr RecordLayout RL = record_layout(128, KB, VB);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lg = warp & 3, hf = warp >> 2;
+  const int line = 32 * lg + lane;
+  // token factors start at 1/sqrt(d): the values in TMEM are Z.H without the rotation's scale
+  if (tid < 128) fT[tid] = kInvSqrt128; else fC[tid - 128] = 1.0f;
+  __syncthreads();
+  const uint32_t lanes = ((uint32_t)(32 * lg) << 16) + 64 * hf;
+  const uint32_t tA = tmem_base + bufA + lanes;  // lines = tokens
+  const uint32_t tB = tmem_base + bufB + lanes;  // lines = channels
+
+  // ---- variance normalisation: channel-std step (lines of B), then token-std step (lines of A)
+  int used = 0;
+  for (int it = 0; it < p.iters; ++it) {
+    bool moved = std_step(tB, fT, fC, xbuf, line, hf, p.eps, p.tol_lo, p.tol_hi);
+    if (!wait_a()) return -1;
+    moved |= std_step(tA, fC, fT, xbuf, line, hf, p.eps, p.tol_lo, p.tol_hi);
+    ++used;
+    if (p.tol_hi > 0.0f && !__syncthreads_or(moved ? 1 : 0)) break;
+  }
+  if (!wait_a()) return -1;
+
+  // ---- group extremes, one group per line: K groups are channels (lines of B, over tokens),
+  // V groups are tokens (lines of A, over channels).  N = x fL fC with positive factors and
+  // monotonic rounding, so the extremes of N are those of x f_other times the group's factor.
+  constexpr int QMAXK = (1 << KB) - 1, QMAXV = (1 << VB) - 1;
+  {
+    const float* fo = is_v ? fC : fT;  // factors of the columns of the group's line
+    const float4* f4 = reinterpret_cast<const float4*>(fo + 64 * hf);
+    uint32_t r[64];
+    load_line(is_v ? tA : tB, r);
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float4 f = f4[k];
+      const float2 y0 = mul2(make_float2(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1])),
+                             make_float2(f.x, f.y));
+      const float2 y1 = mul2(make_float2(__uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])),
+                             make_float2(f.z, f.w));
+      mn = fmin3(fmin3(mn, y0.x, y0.y), y1.x, y1.y);
+      mx = fmax3(fmax3(mx, y0.x, y0.y), y1.x, y1.y);
+    }
+    xbuf[tid] = make_float4(mn, mx, 0.0f, 0.0f);
+    __syncthreads();
+    const float4 o = xbuf[tid ^ 128];
+    mn = fminf(mn, o.x);
+    mx = fmaxf(mx, o.y);
+    const float fg = (is_v ? fT : fC)[line];  // the group's own factor
+    const float m = mn * fg, M = mx * fg;
+    const float s = fmaxf(__fdiv_rn(__fsub_rn(M, m), (float)(is_v ? QMAXV : QMAXK)), 1e-8f);
+    if (hf == 0) reinterpret_cast<float2*>(qpair)[line] = make_float2(m, __frcp_rn(s));
+    if (rec == nullptr) {
+      // page id outside the pool (flagged): computed, not stored
+    } else if (hf == 0) {
+      // folded metadata: K s' = s c, z' = m c with c = 1 / fC (fp16); V s' = s r, z' = m r with
+      // r = 1 / (sqrt(d) fT) (the token factors carry the rotation's 1/sqrt(d))
+      const float fold = is_v ? fg * 11.313708498984761f : fg;
+      __half* scale_out = reinterpret_cast<__half*>(rec + (is_v ? RL.vscale : RL.kscale));
+      __half* zero_out = reinterpret_cast<__half*>(rec + (is_v ? RL.vzero : RL.kzero));
+      scale_out[line] = __float2half_rn(__fdiv_rn(s, fold));
+      zero_out[line] = __float2half_rn(__fdiv_rn(m, fold));
+    } else {
+      // the other axis' factor record: K token factor r = 1 / (sqrt(d) fT), V channel factor
+      // c = 1 / fC
+      __half* fac_out = reinterpret_cast<__half*>(rec + (is_v ? RL.vfactor : RL.kfactor));
+      fac_out[line] = __float2half_rn(is_v ? __frcp_rn(fC[line]) : __fdiv_rn(kInvSqrt128, fT[line]));
+    }
+  }
+  // group parameters visible ((m, 1/s) stored as float2 per group); every thread is done with
+  // the group pass' TMEM buffer
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  group_done(is_v ? bufA : bufB);
+
+  // ---- codes in the 16x256b layout: K from A (rows tokens, columns = channel groups), V from B
+  // (rows channels, columns = token groups)
+  {
+    const int g = lane >> 2;
+    float x[4][16];
+    const uint32_t col = tmem_base + (is_v ? bufB : bufA) + 64 * hf;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[32];
+      tmem_ld_16x256b_x8(col + ((uint32_t)(32 * lg + 16 * half) << 16), r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        x[2 * half][2 * u] = __uint_as_float(r[4 * u]);
+        x[2 * half][2 * u + 1] = __uint_as_float(r[4 * u + 1]);
+        x[2 * half + 1][2 * u] = __uint_as_float(r[4 * u + 2]);
+        x[2 * half + 1][2 * u + 1] = __uint_as_float(r[4 * u + 3]);
+      }
+    }
+    const float* frow = is_v ? fC : fT;  // factors of the rows (L axis)
+    const float* fcol = is_v ? fT : fC;  // factors of the columns (the groups)
+    float fl[4];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) fl[l] = frow[32 * lg + g + 8 * l];
+    // (m, 1/s) of groups c and c + 1 as one float4
+    const float4* q4 = reinterpret_cast<const float4*>(qpair);
+    if (rec == nullptr) {
+    } else if (is_v) {
+      codes_and_pack<true, KB, VB>(x, fl, fcol, q4, rec);
+    } else {
+      codes_and_pack<false, KB, VB>(x, fl, fcol, q4, rec);
+    }
+  }
+  return used;
 }
 
 }  // namespace tc
@@ -770,23 +1155,58 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
   using namespace tc;
   const uint32_t sbase = smem_u32(smem_tc);
   int* list = reinterpret_cast<int*>(smem_tc + kListOff);
+  const __half** srcs = reinterpret_cast<const __half**>(smem_tc + kIoOff);
+  uint8_t** recs = reinterpret_cast<uint8_t**>(smem_tc + kIoOff + kListCap * 8);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem_tc + kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_tc + kBarOff + 16);
   int* count = reinterpret_cast<int*>(smem_tc + kBarOff + 24);
-  float* scratch = reinterpret_cast<float*>(smem_tc + kScrOff);
+  float* fT = reinterpret_cast<float*>(smem_tc + kFOff);
+  float* fC = fT + 128;
+  float4* xbuf = reinterpret_cast<float4*>(smem_tc + kXOff);
+  float4* qpair = reinterpret_cast<float4*>(smem_tc + kQOff);
   const int tid = threadIdx.x, warp = tid >> 5;
 
-  // ---- this CTA's units (append mode: write every token first, keep the tiles that seal) ----
-  // Each warp takes every 8th of the CTA's units, so the dependent loads of different units
-  // (length, then token) overlap; the list order does not matter (units are independent).
+  // ---- this CTA's units ----
+  // Tile mode: units blockIdx.x + k gridDim.x, in that order, so that the first tile can be
+  // requested before anything else; a unit whose page id is outside the pool is flagged and
+  // computed without writing its record (rec = null).  Append mode: every token is written
+  // first, and only the tiles that seal are listed; each warp takes every 8th of the CTA's units
+  // so that the dependent loads of different units (length, then token) overlap.
   grid_dependency_wait();    // inputs, lengths and partial tiles may come from the previous kernel
   grid_launch_dependents();  // a dependent kernel still waits for this grid to complete
-  if (tid == 0) *count = 0;
-  __syncthreads();
+  const int64_t tstride = p.append ? (int64_t)p.d0 : p.tok_stride;  // token stride of every tile
   const int lane = tid & 31;
   constexpr int kWarps = kThreads / 32;
-  for (int u = blockIdx.x + gridDim.x * warp; u < units; u += gridDim.x * kWarps) {
-    if (p.append) {
+  int n_my;
+  if (!p.append) {
+    n_my = blockIdx.x < units ? min((units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1, kListCap) : 0;
+    if (n_my == 0) return;
+    {
+      const int u = blockIdx.x;
+      const int h = (u >> 1) % p.num_kv_heads, t = (u >> 1) / p.num_kv_heads;
+      load_tile(sbase + kZOff,
+                ((u & 1) ? p.v : p.k) + (int64_t)t * kTile * p.tok_stride + (int64_t)h * p.head_stride,
+                tstride, p.d0);
+      cp_async_commit();
+    }
+    for (int k = tid; k < n_my; k += kThreads) {
+      const int u = blockIdx.x + k * gridDim.x;
+      const __half* src;
+      int64_t ts;
+      uint8_t* rec;
+      if (!tc::unit_io(p, u, src, ts, rec)) {
+        flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
+        rec = nullptr;
+      }
+      list[k] = u;
+      srcs[k] = src;
+      recs[k] = rec;
+    }
+    __syncthreads();
+  } else {
+    if (tid == 0) *count = 0;
+    __syncthreads();
+    for (int u = blockIdx.x + gridDim.x * warp; u < units; u += gridDim.x * kWarps) {
       const int h = (u >> 1) % p.num_kv_heads, b = (u >> 1) / p.num_kv_heads;
       const bool is_v = (u & 1) != 0;
       const int len = p.seq_lens[b];
@@ -800,25 +1220,29 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
         *reinterpret_cast<uint4*>(part + (len % kTile) * p.d0 + c) = *reinterpret_cast<const uint4*>(nw + c);
       if (lane == 0 && !is_v && h == 0 && p.seq_lens_out != nullptr) p.seq_lens_out[b] = len + 1;
       if (len % kTile != kTile - 1) continue;
+      const __half* src;
+      int64_t ts;
+      uint8_t* rec;
+      if (!tc::unit_io(p, u, src, ts, rec)) {  // page id outside the pool: skip the unit
+        if (lane == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
+        continue;
+      }
+      if (lane == 0) {
+        const int n = atomicAdd(count, 1);
+        if (n < kListCap) {  // the grid is sized so that n stays below kListCap
+          list[n] = u;
+          srcs[n] = src;
+          recs[n] = rec;
+        }
+      }
     }
-    const __half* src;
-    int64_t ts;
-    uint8_t* rec;
-    if (!tc::unit_io(p, u, src, ts, rec)) {  // page id outside the pool: skip the unit
-      if (lane == 0) flag_error(p.status, KVARN_DEV_BAD_PAGE_ID);
-      continue;
-    }
-    if (lane == 0) {
-      const int n = atomicAdd(count, 1);
-      if (n < kListCap) list[n] = u;  // the grid is sized so that n stays below kListCap
-    }
+    __threadfence_block();
+    __syncthreads();
+    n_my = min(*count, kListCap);
+    if (n_my == 0) return;
   }
-  __threadfence_block();
-  __syncthreads();
-  const int n_my = min(*count, kListCap);
-  if (n_my == 0) return;
 
-  // ---- set-up: H_128 in shared memory, two TMEM accumulators, two mbarriers ----
+  // ---- set-up: H_128 in shared memory, the TMEM accumulators, one mbarrier ----
   for (int q = tid; q < 128 * 16; q += kThreads) {
     const int n = q >> 4, c8 = q & 15;
     uint32_t w[4];
@@ -837,118 +1261,106 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    mbar_init(&mbar[0], 1);
-    mbar_init(&mbar[1], 1);
+    mbar_init(&mbar[0], 1);  // rotation B of a unit done
+    mbar_init(&mbar[1], 1);  // rotation A of a unit done
     fence_mbar_init();
   }
-  {
-    const __half* src;
-    int64_t ts;
-    uint8_t* rec;
-    tc::unit_io(p, list[0], src, ts, rec);
-    load_tile(sbase + kZOff, src, ts, p.d0);
-    cp_async_commit();
-    if (n_my > 1) {
-      tc::unit_io(p, list[1], src, ts, rec);
-      load_tile(sbase + kZOff + kOpBytes, src, ts, p.d0);
-    }
+  if (p.append) {  // tile mode requested the first tile at the start
+    load_tile(sbase + kZOff, srcs[0], tstride, p.d0);
     cp_async_commit();
   }
-  const float isd = 0.08838834764831845f;
-  bool ok = true;
-  // issue the rotation of list[i] (its tile is in Z buffer i % 2) into TMEM buffer i % 2
-  auto issue_mma = [&](int i, uint32_t tmem_base) {
-    if (tid == 0) {
-      const bool is_v = (list[i] & 1) != 0;
-      const uint32_t z = sbase + kZOff + (i & 1) * kOpBytes, hm = sbase + kHOff;
-      const uint32_t a = is_v ? hm : z, b = is_v ? z : hm;
-      const uint32_t d = tmem_base + (i & 1) * 128;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t da = smem_desc(a + kk * 2 * kLbo), db = smem_desc(b + kk * 2 * kLbo);
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-            "l"(da), "l"(db), "r"(kIdesc), "r"((uint32_t)kk));
-      }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_u32(&mbar[i & 1]))
-                   : "memory");
-    }
-  };
+  if (n_my > 1) load_tile(sbase + kZOff + kOpBytes, srcs[1], tstride, p.d0);
+  cp_async_commit();
   cp_async_wait<1>();
   fence_proxy_async_smem();  // H and tile 0 written by the generic proxy, read by the MMA
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  issue_mma(0, tmem_base);
-
-  int issued = 1;  // MMAs issued so far (for draining after a timeout)
+  // One rotation of the tile in Z buffer zb into TMEM columns `cols`: B = H.Z^T (lanes =
+  // channels) or A = Z.H (lanes = tokens); completes on mbar[0] (B) or mbar[1] (A).
+  auto issue_rotation = [&](int zb, uint32_t cols, bool orient_b) {
+    if (tid == 0) {
+      const uint32_t z = sbase + kZOff + zb * kOpBytes, hm = sbase + kHOff;
+      const uint32_t a = orient_b ? hm : z, bb = orient_b ? z : hm;
+      const uint32_t d = tmem_base + cols;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t da = smem_desc(a + kk * 2 * kLbo), db = smem_desc(bb + kk * 2 * kLbo);
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+            "l"(da), "l"(db), "r"(kIdesc), "r"((uint32_t)kk));
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(&mbar[orient_b ? 0 : 1]))
+                   : "memory");
+    }
+  };
+  // Unit i's rotations sit in TMEM columns (bufB, bufA).  The next unit's B is issued into the
+  // buffer unit i's group pass has finished with, its A into the buffer of unit i's codes pass
+  // once that pass is done: the next unit's rotations overlap this unit's codes and its own
+  // first channel step.
+  uint32_t bufB = 128, bufA = 0;
+  issue_rotation(0, bufB, true);
+  issue_rotation(0, bufA, false);
+  int issued = 1;  // rotation pairs issued (for draining after a timeout)
+  bool ok = true;
   for (int i = 0; i < n_my; ++i) {
     // one decision for the whole CTA, so that no thread leaves while others wait at a barrier
-    ok = __syncthreads_and(mbar_wait(&mbar[i & 1], (i >> 1) & 1) ? 1 : 0) != 0;
-    if (!ok && tid == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+    ok = __syncthreads_and(mbar_wait(&mbar[0], i & 1) ? 1 : 0) != 0;
+    if (!ok) break;
     tc_fence_after();
-    float x[4][16];
-    {
-      const uint32_t col = tmem_base + (i & 1) * 128 + 64 * (warp >> 2);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld_16x256b_x8(col + ((uint32_t)(32 * (warp & 3) + 16 * half) << 16), r);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float2 a = mul2(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])),
-                                make_float2(isd, isd));
-          const float2 c = mul2(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])),
-                                make_float2(isd, isd));
-          x[2 * half][2 * u] = a.x;
-          x[2 * half][2 * u + 1] = a.y;
-          x[2 * half + 1][2 * u] = c.x;
-          x[2 * half + 1][2 * u + 1] = c.y;
-        }
-      }
+    bool a_ready = false;
+    auto wait_a = [&]() -> bool {
+      if (a_ready) return true;
+      a_ready = true;
+      const bool ok_a = __syncthreads_and(mbar_wait(&mbar[1], i & 1) ? 1 : 0) != 0;
+      tc_fence_after();
+      if (!ok_a) return false;
+      // both rotations of unit i are done, its Z buffer is free: fetch list[i + 2] into it
+      if (i + 2 < n_my) load_tile(sbase + kZOff + (i & 1) * kOpBytes, srcs[i + 2], tstride, p.d0);
+      cp_async_commit();
+      return true;
+    };
+    uint32_t next_b = bufB;
+    auto group_done = [&](uint32_t freed) {
+      next_b = freed;
+      if (i + 1 < n_my) issue_rotation((i + 1) & 1, freed, true);
+    };
+    uint8_t* rec = recs[i];
+    const bool is_v = (list[i] & 1) != 0;
+    const int used = tc::quantize_unit_tc<KB, VB>(
+        is_v, tmem_base, bufB, bufA, rec, p, fT, fC, xbuf, qpair,
+        [&]() -> bool {
+          if (!wait_a()) return false;
+          cp_async_wait<1>();          // the tile of list[i + 1] has landed (list[i + 2] may not)
+          fence_proxy_async_smem();    // visible to the tensor core after the pass' barrier
+          return true;
+        },
+        group_done);
+    if (used < 0) {
+      ok = false;
+      break;
     }
-    // Z buffer i % 2 is free (its MMA completed): fetch list[i + 2] into it
-    if (i + 2 < n_my) {
-      const __half* src;
-      int64_t ts;
-      uint8_t* rec;
-      tc::unit_io(p, list[i + 2], src, ts, rec);
-      load_tile(sbase + kZOff + (i & 1) * kOpBytes, src, ts, p.d0);
-    }
-    cp_async_commit();
-    // rotate list[i + 1] (loaded one iteration ago) into the other TMEM buffer
+    if (p.iters_out != nullptr && !p.append && tid == 0) p.iters_out[list[i]] = used;
+    const uint32_t codes_buf = is_v ? bufB : bufA;  // free once every thread is past the codes
     if (i + 1 < n_my) {
-      cp_async_wait<1>();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
-      if (ok) {
-        issue_mma(i + 1, tmem_base);
-        ++issued;
-      }
+      issue_rotation((i + 1) & 1, codes_buf, false);
+      ++issued;
     }
-    if (!ok) break;
-    {
-      const __half* src;
-      int64_t ts;
-      uint8_t* rec;
-      tc::unit_io(p, list[i], src, ts, rec);
-      const int used = (list[i] & 1) != 0
-                           ? quantize_rotated<128, true, KB, VB>(x, rec, p.iters, p.eps, p.tol_lo, p.tol_hi, scratch)
-                           : quantize_rotated<128, false, KB, VB>(x, rec, p.iters, p.eps, p.tol_lo, p.tol_hi, scratch);
-      if (p.iters_out != nullptr && !p.append && tid == 0) p.iters_out[list[i]] = used;
-    }
-    __syncthreads();  // the scratch of this unit is dead before the next one starts
+    bufB = next_b;
+    bufA = codes_buf;
   }
+  if (!ok && tid == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
   // ---- tear-down: no MMA may still write TMEM when it is released ----
   cp_async_wait<0>();
-  if (!ok && tid == 0) {  // the last batch issued into each buffer (earlier ones precede it)
-    for (int j = max(0, issued - 2); j < issued; ++j) mbar_wait(&mbar[j & 1], (j >> 1) & 1);
+  if (!ok && tid == 0) {  // the last rotations issued (bounded waits)
+    mbar_wait(&mbar[0], (issued - 1) & 1);
+    mbar_wait(&mbar[1], (issued - 1) & 1);
   }
   tc_fence_before();
   __syncthreads();

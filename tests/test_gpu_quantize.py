@@ -133,3 +133,23 @@ def test_dequantize_parity(kv, d0):
             src = k[128 * i:128 * i + 128, h].double().cpu().numpy()
             rel = np.linalg.norm(kc[i, h] - src) / np.linalg.norm(src)
             assert rel < 0.2
+
+
+@pytest.mark.parametrize("d0", [128, 256])
+def test_quantize_page_id_outside_pool(kv, d0):
+    # a tile whose page id lies outside the pool is flagged and writes nothing; the other tiles
+    # are quantised as usual and the pool keeps no stray bytes
+    k, v = synth.outlier_kv(128 * 3, 2, d0, seed=61, device="cuda")
+    desc = kv.desc_from_preset(d0, 2)
+    pool = kv.alloc_pool(desc, 3)
+    pool.fill_(0xA5)
+    ids = torch.tensor([2, 7, 0], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv.quantize_tiles(desc, k, v, ids, pool, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & kv.DEV_BAD_PAGE_ID
+    assert bool((pool[1] == 0xA5).all()), "page 1 (no tile) was written"
+    ref = kv.alloc_pool(desc, 3)
+    kv.quantize_tiles(desc, k, v, torch.tensor([2, 1, 0], dtype=torch.int32, device="cuda"), ref)
+    torch.cuda.synchronize()
+    assert torch.equal(pool[0], ref[0]) and torch.equal(pool[2], ref[2])
