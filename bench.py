@@ -33,7 +33,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "K4V2 g128 decode-attn KV tokens/s & HBM GB/s; quantize tokens/s (1 GB300)"
-QUANT_OPS_PER_ELEMENT = 37  # fp32 ops per quantised element (derivation at the quantize timing)
+QUANT_OPS_PER_ELEMENT = 38  # fp32 ops per quantised element (derivation at the quantize timing)
 SM_MAX_MHZ = 2070.0
 ADAPTIVE_TOL = 0.05  # early-stop tolerance of the normalisation (log-factor change per iteration)
 DEC_EVENT_SAMPLES = 40  # live samples of the decode call's duration, spread over the timed steps
@@ -601,8 +601,7 @@ def _time_long_stream(torch, kv, synth, d0, peak, steps=512, batch=4, hq=32, hkv
         lens[0].copy_(starts.to(torch.int32))
         pk.copy_(pk0)
         pv.copy_(pv0)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(0, steps, every)]
+        ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(0, steps, every)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         torch.cuda._sleep(200000)  # the host enqueues the first steps while the GPU waits
@@ -611,18 +610,24 @@ def _time_long_stream(torch, kv, synth, d0, peak, steps=512, batch=4, hq=32, hkv
             c = i % 2
             kv.append_token(desc, kn[i % 4], vn[i % 4], pk, pv, lens[c], table, pool,
                             seq_lens_out=lens[1 - c], status=status, stream=stream)
-            if i % every == 0:
-                ev[i // every][0].record(stream)
-            kv.decode_attention(desc, qs[i % 4], pool, table, lens[1 - c], out, ws, partial_k=pk,
-                                partial_v=pv, softmax_scale=scale, status=status, stream=stream)
-            if i % every == 0:
-                ev[i // every][1].record(stream)
+            dargs = (desc, qs[i % 4], pool, table, lens[1 - c], out, ws)
+            dkw = dict(partial_k=pk, partial_v=pv, softmax_scale=scale, status=status, stream=stream)
+            if i % every == 0:  # decode_kernel and combine_kernel as two calls, events around
+                e = ev[i // every]
+                e[0].record(stream)
+                kv.decode_attention(*dargs, phase="partials", **dkw)
+                e[1].record(stream)
+                kv.decode_attention(*dargs, phase="combine", **dkw)
+                e[2].record(stream)
+            else:
+                kv.decode_attention(*dargs, **dkw)
         t1.record(stream)
         torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError("device status %d in the long-context stream" % int(status.item()))
     total_ms = t0.elapsed_time(t1)
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    call_ms = [a.elapsed_time(c) for a, _, c in ev]
     d_pad = desc.head_dim_padded
     new_tok = 2 * batch * hkv * d0 * 2            # k_new + v_new
     dec_bytes, step_bytes, seals = [], 0, 0
@@ -650,7 +655,9 @@ def _time_long_stream(torch, kv, synth, d0, peak, steps=512, batch=4, hq=32, hkv
         "algorithmic_bytes_per_step": step_bytes / steps,
         "hbm_gbs": step_gbs, "frac": step_gbs / peak,
         "decode_us": statistics.mean(dec_ms) * 1e3, "decode_hbm_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
-        "decode_duration_source": "CUDA events around the decode call on every %dth step" % every,
+        "decode_call_us": statistics.mean(call_ms) * 1e3,
+        "decode_duration_source": "CUDA events around decode_kernel (decode_us) and around the whole "
+                                  "decode call with the merge (decode_call_us) on every %dth step" % every,
         "kv_tokens_per_s": sum(int((starts + i + 1).sum()) for i in range(steps)) / (total_ms * 1e-3),
     }
 
@@ -711,14 +718,18 @@ def _run_kvarn(args, torch, world, rank):
         c = state["cur"]
         kv.append_token(S["desc"], kn, vn, S["pk"], S["pv"], S["lens"][c], S["table"], S["pool"],
                         seq_lens_out=S["lens"][1 - c], status=S["status"], stream=stream)
-        if ev is not None:
+        args = (S["desc"], q, S["pool"], S["table"], S["lens"][1 - c], S["out"] if out is None else out,
+                S["ws"])
+        kw = dict(partial_k=S["pk"], partial_v=S["pv"], softmax_scale=1 / math.sqrt(D0),
+                  status=S["status"], stream=stream)
+        if ev is None:
+            kv.decode_attention(*args, **kw)
+        else:  # the same two kernels as two calls, an event between them
             ev[0].record(stream)
-        kv.decode_attention(S["desc"], q, S["pool"], S["table"], S["lens"][1 - c],
-                            S["out"] if out is None else out, S["ws"],
-                            partial_k=S["pk"], partial_v=S["pv"], softmax_scale=1 / math.sqrt(D0),
-                            status=S["status"], stream=stream)
-        if ev is not None:
+            kv.decode_attention(*args, phase="partials", **kw)
             ev[1].record(stream)
+            kv.decode_attention(*args, phase="combine", **kw)
+            ev[2].record(stream)
         state["cur"] = 1 - c
         state["step"] += 1
 
@@ -733,7 +744,7 @@ def _run_kvarn(args, torch, world, rank):
     # decode ends their programmatic-launch overlap, so the other steps run without it.
     every = max(DEC_EVENT_EVERY_MIN, args.steps // DEC_EVENT_SAMPLES)
     sampled = [i for i in range(args.steps) if i % every == 0]
-    dec_ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
+    dec_ev = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for i in sampled}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(_device_id(torch))
     clocks.start()
@@ -748,7 +759,8 @@ def _run_kvarn(args, torch, world, rank):
     w1 = clocks.mark()
     clk = clocks.stop(window=(w0, w1))
     elapsed_ms = t0.elapsed_time(t1)
-    dec_ms = [a.elapsed_time(b) for a, b in dec_ev.values()]
+    dec_ms = [a.elapsed_time(b) for a, b, _ in dec_ev.values()]      # decode_kernel
+    call_ms = [a.elapsed_time(c) for a, _, c in dec_ev.values()]     # decode_kernel + combine_kernel
     status = int(S["status"].item())
     if status != 0:
         raise RuntimeError("device status %d during the timed steps" % status)
@@ -758,6 +770,7 @@ def _run_kvarn(args, torch, world, rank):
     dec_bytes = [_decode_bytes((lens_before + i + 1).tolist(), S["rec_bytes"]) for i in sampled]
     peak, peak_kind = _peaks()
     avg_dec = statistics.mean(dec_ms)
+    avg_call = statistics.mean(call_ms)
     achieved = statistics.mean(dec_bytes) / (avg_dec * 1e-3) / 1e9
 
     # ---- end to end through the public API: pinned host q/k/v in, fp16 out back each step.
@@ -827,11 +840,12 @@ def _run_kvarn(args, torch, world, rank):
             ms, nb = _time_quantize(torch, kv, synth, dev, stream, preset=name, reps=10)
             q_presets[name] = {"us": ms * 1e3, "tokens_per_s": Q_TOKENS / (ms * 1e-3),
                                "hbm_gbs": nb / (ms * 1e-3) / 1e9}
-    # Quantisation is bound by fp32 arithmetic, not by HBM.  Per element it needs 37 fp32 ops:
-    # 4 in each of the 8 std steps (product with the other axis' factor, its share of the sum,
-    # minus the mean, square-accumulate) and 5 to quantise (two factor products, minus the zero
-    # point, times 1/scale, plus the rounding constant).  Peak: one fp32 op per lane per clock,
-    # 128 lanes per SM.
+    # Quantisation is bound by fp32 arithmetic, not by HBM.  Per element it needs 38 fp32 ops:
+    # 4 in each of the 8 std steps (product with the other axis' factor, its share of the
+    # pairwise sum, minus the half-line mean, square-accumulate), 3 for the group extremes
+    # (product, min, max) and 3 to quantise (product with the row factor, fused product with the
+    # column factor minus the zero point, fused product with 1/s plus the rounding constant).
+    # Peak: one fp32 op per lane per clock, 128 lanes per SM.
     q_elems = 2 * Q_TOKENS * Q_HEADS * D0
     q_ops = QUANT_OPS_PER_ELEMENT * q_elems / (q_med * 1e-3) / 1e9
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -868,8 +882,12 @@ def _run_kvarn(args, torch, world, rank):
         "config": _workload_config(lens_before, args.steps),
         "decode_hbm_gbs": achieved,
         "decode_us": avg_dec * 1e3,
+        "decode_call": {"us": avg_call * 1e3,
+                        "hbm_gbs": statistics.mean(dec_bytes) / (avg_call * 1e-3) / 1e9,
+                        "note": "kvarn_decode_attention as a whole: decode_kernel + combine_kernel "
+                                "(the merge of the splits and the inverse rotation)"},
         "roofline": {
-            "kernel": "kvarn_decode_attention (decode_kernel + combine_kernel)",
+            "kernel": "decode_kernel (kvarn_decode_partials)",
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -879,8 +897,10 @@ def _run_kvarn(args, torch, world, rank):
                               "algorithmic bytes (profiles/decode_kernel_batch24_d128.md); null "
                               "when decode.cu changed since that capture",
             "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
-            "duration_source": "CUDA events on the launching stream around the decode call on every "
-                               "%dth timed step (%d of %d)" % (every, len(dec_ms), args.steps),
+            "duration_source": "CUDA events on the launching stream around decode_kernel (the "
+                               "decode call as kvarn_decode_partials + kvarn_decode_combine, an "
+                               "event between them) on every %dth timed step (%d of %d)"
+                               % (every, len(dec_ms), args.steps),
         },
         "quantize": {
             "workload": "one layer, 8 KV heads x 16384 tokens x head_dim 128 (K and V), L2 flushed",

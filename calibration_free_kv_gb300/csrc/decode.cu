@@ -985,12 +985,15 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
-  grid_launch_dependents();  // the next kernel (say, the next step's append) may start arriving
-  if (gw >= p.batch * p.chunk * p.num_q_heads) return;
+  const bool live = gw < p.batch * p.chunk * p.num_q_heads;
   const int b = gw / (p.chunk * p.num_q_heads);
   const int cap = p.max_pages * kTile + (kTile - 1);
-  int len = p.seq_lens[b];
+  // The lengths come from before decode_kernel, which waited for their writer before it let
+  // this kernel start: they can be read ahead of the wait for the split partials.
+  int len = live ? p.seq_lens[b] : 0;
+  grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
+  grid_launch_dependents();  // the next kernel (say, the next step's append) may start arriving
+  if (!live) return;
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_sealed = len / kTile;
   const int n_splits = (n_sealed + p.pages_per_split - 1) / p.pages_per_split + (len % kTile > 0 ? 1 : 0) +
@@ -1073,7 +1076,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
 }
 
 template <int D, int NT, int KB, int VB>
-static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+static int launch_decode_t(const DecodeParams& p, int phases, cudaStream_t stream) {
   using S = DecodeShape<D, NT, KB, VB>;
   static PerDeviceOnce smem_once;  // the attribute is set once per device
   const void* fn = reinterpret_cast<const void*>(decode_kernel<D, NT, KB, VB>);
@@ -1093,7 +1096,9 @@ static int launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess) return KVARN_ERR_CUDA;
+  if ((phases & kDecodeSplits) != 0 && cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess)
+    return KVARN_ERR_CUDA;
+  if ((phases & kDecodeMerge) == 0) return KVARN_OK;
   const int warps = p.batch * p.chunk * p.num_q_heads;
   cfg.gridDim = dim3((warps + 3) / 4);
   cfg.blockDim = dim3(128);
@@ -1270,23 +1275,23 @@ int decode_split_pages(int d, int nt, int kb, int vb, int64_t units, int max_pag
 }
 
 template <int KB, int VB>
-static int launch_decode_bits(int d, int nt, const DecodeParams& p, cudaStream_t stream) {
+static int launch_decode_bits(int d, int nt, const DecodeParams& p, int phases, cudaStream_t stream) {
   if (nt == 1) {
-    if (d == 64) return launch_decode_t<64, 1, KB, VB>(p, stream);
-    if (d == 128) return launch_decode_t<128, 1, KB, VB>(p, stream);
-    if (d == 256) return launch_decode_t<256, 1, KB, VB>(p, stream);
+    if (d == 64) return launch_decode_t<64, 1, KB, VB>(p, phases, stream);
+    if (d == 128) return launch_decode_t<128, 1, KB, VB>(p, phases, stream);
+    if (d == 256) return launch_decode_t<256, 1, KB, VB>(p, phases, stream);
   } else if (nt == 2) {
-    if (d == 64) return launch_decode_t<64, 2, KB, VB>(p, stream);
-    if (d == 128) return launch_decode_t<128, 2, KB, VB>(p, stream);
+    if (d == 64) return launch_decode_t<64, 2, KB, VB>(p, phases, stream);
+    if (d == 128) return launch_decode_t<128, 2, KB, VB>(p, phases, stream);
   }
   return KVARN_ERR_UNSUPPORTED;
 }
 
-int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream) {
-  if (kb == 4 && vb == 2) return launch_decode_bits<4, 2>(d, nt, p, stream);
-  if (kb == 4 && vb == 4) return launch_decode_bits<4, 4>(d, nt, p, stream);
-  if (kb == 2 && vb == 2) return launch_decode_bits<2, 2>(d, nt, p, stream);
-  if (kb == 8 && vb == 4) return launch_decode_bits<8, 4>(d, nt, p, stream);
+int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream, int phases) {
+  if (kb == 4 && vb == 2) return launch_decode_bits<4, 2>(d, nt, p, phases, stream);
+  if (kb == 4 && vb == 4) return launch_decode_bits<4, 4>(d, nt, p, phases, stream);
+  if (kb == 2 && vb == 2) return launch_decode_bits<2, 2>(d, nt, p, phases, stream);
+  if (kb == 8 && vb == 4) return launch_decode_bits<8, 4>(d, nt, p, phases, stream);
   return KVARN_ERR_UNSUPPORTED;
 }
 

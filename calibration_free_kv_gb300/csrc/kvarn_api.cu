@@ -223,12 +223,11 @@ int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const 
 
 extern "C" {
 
-int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
-                           const void* page_pool, int64_t num_pool_pages,
-                           const int32_t* block_table, int max_pages, const int32_t* seq_lens,
-                           const void* partial_k, const void* partial_v, float softmax_scale,
-                           void* out, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, void* stream) {
+static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                         const void* page_pool, int64_t num_pool_pages, const int32_t* block_table,
+                         int max_pages, const int32_t* seq_lens, const void* partial_k,
+                         const void* partial_v, float softmax_scale, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t* dev_status, void* stream, int phases) {
   const int st = decode_args_check(desc, batch, num_q_heads, q, page_pool, num_pool_pages,
                                    block_table, max_pages, seq_lens, partial_k, partial_v,
                                    softmax_scale, out);
@@ -264,7 +263,40 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
   p.vgroups = 1;
   p.status = dev_status;
   return launch_decode_any(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p,
-                           static_cast<cudaStream_t>(stream));
+                           static_cast<cudaStream_t>(stream), phases);
+}
+
+int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                           const void* page_pool, int64_t num_pool_pages,
+                           const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                           const void* partial_k, const void* partial_v, float softmax_scale,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, void* stream) {
+  return decode_phases(desc, batch, num_q_heads, q, page_pool, num_pool_pages, block_table,
+                       max_pages, seq_lens, partial_k, partial_v, softmax_scale, out, workspace,
+                       workspace_bytes, dev_status, stream, kDecodeSplits | kDecodeMerge);
+}
+
+int kvarn_decode_partials(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                          const void* page_pool, int64_t num_pool_pages,
+                          const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                          const void* partial_k, const void* partial_v, float softmax_scale,
+                          void* out, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream) {
+  return decode_phases(desc, batch, num_q_heads, q, page_pool, num_pool_pages, block_table,
+                       max_pages, seq_lens, partial_k, partial_v, softmax_scale, out, workspace,
+                       workspace_bytes, dev_status, stream, kDecodeSplits);
+}
+
+int kvarn_decode_combine(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                         const void* page_pool, int64_t num_pool_pages,
+                         const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                         const void* partial_k, const void* partial_v, float softmax_scale,
+                         void* out, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, void* stream) {
+  return decode_phases(desc, batch, num_q_heads, q, page_pool, num_pool_pages, block_table,
+                       max_pages, seq_lens, partial_k, partial_v, softmax_scale, out, workspace,
+                       workspace_bytes, dev_status, stream, kDecodeMerge);
 }
 
 size_t kvarn_prefill_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,

@@ -91,7 +91,10 @@ int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const 
                       const void* partial_v, float softmax_scale, const void* out);
 
 int launch_quantize_any(int d, int kb, int vb, const QuantizeParams& p, int units, cudaStream_t stream);
-int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream);
+// Kernels of a decode launch: the split partials (decode_kernel), the merge (combine_kernel).
+constexpr int kDecodeSplits = 1, kDecodeMerge = 2;
+int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream,
+                      int phases = kDecodeSplits | kDecodeMerge);
 // Sealed pages per decode CTA for `units` (sequence, kv head, vector group) rows of a block
 // table `max_pages` wide: 32, or for tables over 256 pages the size in [32, 128] that fills
 // the GPU's CTA slots best.  Never below 32, the size the workspace is laid out for.

@@ -44,6 +44,8 @@ EXPORTED_SYMBOLS = (
     "kvarn_fp16_decode_attention",
     "kvarn_selftest_wait_timeout",
     "kvarn_quantization_error",
+    "kvarn_decode_partials",
+    "kvarn_decode_combine",
 )
 
 # Size of the library's fixed decode scratch (KVARN_DECODE_NOALLOC_SCRATCH_BYTES in kvarn.h).
@@ -100,6 +102,10 @@ def _load():
                                               P, P, ctypes.c_size_t, P, P]),
         "kvarn_selftest_wait_timeout": (i32, [P, P]),
         "kvarn_quantization_error": (i32, [D, P, P, i64, i64, i32, P, P, i64, P, P, P]),
+        "kvarn_decode_partials": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P, ctypes.c_float,
+                                        P, P, ctypes.c_size_t, P, P]),
+        "kvarn_decode_combine": (i32, [D, i32, i32, P, P, i64, P, i32, P, P, P, ctypes.c_float,
+                                       P, P, ctypes.c_size_t, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -219,17 +225,22 @@ def alloc_workspace(desc: KvarnDesc, batch: int, num_q_heads: int, max_pages: in
 
 
 def decode_attention(desc: KvarnDesc, q, pool, block_table, seq_lens, out, workspace,
-                     partial_k=None, partial_v=None, softmax_scale=None, status=None, stream=None):
-    """q, out: fp16 [batch, Hq, d0]; seq_lens: int32 [batch] total lengths."""
+                     partial_k=None, partial_v=None, softmax_scale=None, status=None, stream=None,
+                     phase: str = "all"):
+    """q, out: fp16 [batch, Hq, d0]; seq_lens: int32 [batch] total lengths.  phase "all"
+    (kvarn_decode_attention), or "partials" then "combine" with the same arguments
+    (kvarn_decode_partials / kvarn_decode_combine)."""
+    fn = {"all": "kvarn_decode_attention", "partials": "kvarn_decode_partials",
+          "combine": "kvarn_decode_combine"}[phase]
     batch, hq, d0 = q.shape
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d0)
-    _check(_lib.kvarn_decode_attention(ctypes.byref(desc), batch, hq, _ptr(q), _ptr(pool),
-                                       pool.shape[0], _ptr(block_table), block_table.shape[1],
-                                       _ptr(seq_lens), _ptr(partial_k), _ptr(partial_v),
-                                       float(softmax_scale), _ptr(out), _ptr(workspace),
-                                       workspace.numel() * workspace.element_size(),
-                                       _ptr(status), _stream(stream)), "kvarn_decode_attention")
+    _check(getattr(_lib, fn)(ctypes.byref(desc), batch, hq, _ptr(q), _ptr(pool),
+                             pool.shape[0], _ptr(block_table), block_table.shape[1],
+                             _ptr(seq_lens), _ptr(partial_k), _ptr(partial_v),
+                             float(softmax_scale), _ptr(out), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(),
+                             _ptr(status), _stream(stream)), fn)
 
 
 def prefill_workspace_bytes(desc: KvarnDesc, batch: int, num_q_heads: int, chunk_len: int,

@@ -179,6 +179,27 @@ int kvarn_decode_attention(const kvarn_desc* desc, int batch, int num_q_heads, c
                            void* out, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, void* stream);
 
+/* kvarn_decode_attention in two launches, for callers that schedule the merge themselves (or
+ * time the two kernels apart): kvarn_decode_partials runs the page splits and leaves their
+ * partials (m, l, unnormalised output, rotated basis) in the workspace; kvarn_decode_combine,
+ * called with the same arguments after it on the same stream (the workspace untouched in
+ * between), merges them and writes `out`.  The pair gives the same bytes as
+ * kvarn_decode_attention; arguments, checks and errors are those of kvarn_decode_attention
+ * (each call checks them all; only decode_combine writes `out`, only decode_partials reads
+ * the page pool and the partial tiles). */
+int kvarn_decode_partials(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                          const void* page_pool, int64_t num_pool_pages,
+                          const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                          const void* partial_k, const void* partial_v, float softmax_scale,
+                          void* out, void* workspace, size_t workspace_bytes,
+                          int32_t* dev_status, void* stream);
+int kvarn_decode_combine(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
+                         const void* page_pool, int64_t num_pool_pages,
+                         const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                         const void* partial_k, const void* partial_v, float softmax_scale,
+                         void* out, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, void* stream);
+
 /* Size of the fixed device buffer used by kvarn_decode_attention_noalloc (16 MiB). */
 #define KVARN_DECODE_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

@@ -310,3 +310,29 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(kv):
     assert 0.5 < waited < 30.0
     err = _run_oracle_cache_case(kv, 2, 1, 4, 128, [300, 129], seed=21)
     print("wait gave up after %.2f s; decode afterwards: max scaled err %.2e" % (waited, err))
+
+
+@pytest.mark.parametrize("group", [4, 8])
+def test_two_phase_decode_matches_one_call(kv, group):
+    # kvarn_decode_partials then kvarn_decode_combine give the bytes of kvarn_decode_attention
+    hkv, d0 = 2, 128
+    lens = [0, 5, 128, 700, 4096 + 77]
+    seqs, table, n_pool, q = _build_case(len(lens), hkv, group, d0, lens, seed=77)
+    desc = kv.desc_from_preset(d0, hkv)
+    pool = kv.alloc_pool(desc, n_pool)
+    for b, (k, v) in enumerate(seqs):
+        n = k.shape[0] // 128
+        if n:
+            kv.quantize_tiles(desc, k[:128 * n].cuda(), v[:128 * n].cuda(),
+                              torch.from_numpy(table[b, :n].copy()).cuda(), pool)
+    pk, pv = (t.cuda() for t in _partials(seqs, hkv, d0))
+    qd, tb = q.cuda(), torch.from_numpy(table).cuda()
+    ln = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = kv.alloc_workspace(desc, len(lens), q.shape[1], table.shape[1])
+    one = torch.empty_like(qd)
+    kv.decode_attention(desc, qd, pool, tb, ln, one, ws, partial_k=pk, partial_v=pv)
+    two = torch.full_like(qd, float("nan"))
+    for phase in ("partials", "combine"):
+        kv.decode_attention(desc, qd, pool, tb, ln, two, ws, partial_k=pk, partial_v=pv, phase=phase)
+    torch.cuda.synchronize()
+    assert torch.equal(one, two)
