@@ -57,7 +57,8 @@ def _peaks():
 # DRAM traffic / algorithmic bytes of one decode_kernel launch, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum at batch 24), valid only for the decode.cu source
 # it was taken on: the traffic is reported as null once that file changes.
-DECODE_TRAFFIC = {"decode_cu_sha256": "", "dram_over_algorithmic": None}
+DECODE_TRAFFIC = {"decode_cu_sha256": "ce8ff59a6431249a75bb74c189b3805a8e9aa849594206a4448d1523e6efda8e",
+                  "dram_over_algorithmic": 1.0179}
 
 
 def _decode_traffic_ratio():
@@ -893,9 +894,9 @@ def _run_kvarn(args, torch, world, rank):
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "traffic": (None if _decode_traffic_ratio() is None
                         else _decode_traffic_ratio() * statistics.mean(dec_bytes)),
-            "traffic_source": "ncu dram__bytes_read+write of decode_kernel at batch 24, scaled by "
-                              "algorithmic bytes (profiles/decode_kernel_batch24_d128.md); null "
-                              "when decode.cu changed since that capture",
+            "traffic_source": "ncu dram__bytes_read+write of one decode_kernel launch at batch 24 "
+                              "(DECODE_TRAFFIC), scaled by algorithmic bytes; null when decode.cu "
+                              "changed since that capture",
             "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
             "duration_source": "CUDA events on the launching stream around decode_kernel (the "
                                "decode call as kvarn_decode_partials + kvarn_decode_combine, an "

@@ -1030,6 +1030,41 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
     warp_fwht<D>(v, lane);
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] *= inv;
+  } else if (n_splits > 0 && n_splits <= 32) {
+    // up to 32 splits: (m, l) one split per lane in one load, then the partial outputs eight
+    // splits at a time with all eight loads issued before their use
+    const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
+    const bool mine = lane < n_splits;
+    const float2 ml = mine ? *reinterpret_cast<const float2*>(base + lane * (D + 4)) : make_float2(-INFINITY, 0.0f);
+    float M = ml.x;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
+    const float w = mine ? exp2f(ml.x - M) : 0.0f;
+    float lsum = w * ml.y;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, msk);
+    for (int s0 = 0; s0 < n_splits; s0 += 8) {
+      float o[8][E];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < n_splits) {
+          load_f32<E>(base + (s0 + j) * (D + 4) + 4 + lane * E, o[j]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) o[j][e] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (s0 + j) & 31);  // 0 past the last split
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = fmaf(wj, o[j][e], v[e]);
+      }
+    }
+    const float inv = inv_sqrt_d<D>() / lsum;
+    warp_fwht<D>(v, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] *= inv;
   } else if (n_splits > 0) {
     const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
     // split statistics, one split per lane, 32 per pass
