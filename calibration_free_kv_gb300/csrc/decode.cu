@@ -51,7 +51,7 @@ struct DecodeShape {
   static constexpr int kRecBytes = kWarps * kRec;    // one K slot + one V slot per warp
   static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + kWarps * 2 * 8;
   static_assert(kSmemBytes <= kMaxSmem, "page slots fit in shared memory");
-  static_assert(kRecBytes >= kWarps * kNH * (D + 2) * 4, "the merge scratch fits the page slots");
+  static_assert(kRecBytes >= (kWarps * kNH * (D + 3) + 2 * kNH) * 4, "the merge scratch fits the page slots");
   // two CTAs per SM where their shared memory fits (registers then capped at 128 a thread)
   static constexpr int kMinBlocks = 2 * (kSmemBytes + 1024) <= 233472 ? 2 : 1;
 };
@@ -800,26 +800,39 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;
+    float* scS = oS + kDecWarps * NH * D;  // per (warp, head slot): exp2(m_w - M)
+    float* MS = scS + kDecWarps * NH;       // per head slot: max over the warps, merged l
+    float* LS = MS + NH;
     Path::store(st, warp, lane, mS, lS, oS);
+    __syncthreads();
+    // the warps' rescale factors of each head slot, once
+    if (threadIdx.x < NH) {
+      const int hl = threadIdx.x;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mS[w * NH + hl]);
+      float l = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float sc = exp2f(mS[w * NH + hl] - M);
+        scS[w * NH + hl] = sc;
+        l = fmaf(sc, lS[w * NH + hl], l);
+      }
+      MS[hl] = M;
+      LS[hl] = l;
+    }
     __syncthreads();
     for (int idx = threadIdx.x; idx < NH * D; idx += blockDim.x) {
       const int hl = idx / D, j = idx - hl * D;
       if (!valid(hl)) continue;
-      float M = -INFINITY;
+      float o = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, mS[w * NH + hl]);
-      float o = 0.0f, l = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float sc = exp2f(mS[w * NH + hl] - M);
-        o = fmaf(sc, oS[(w * NH + hl) * D + j], o);
-        l = fmaf(sc, lS[w * NH + hl], l);
-      }
+      for (int w = 0; w < kDecWarps; ++w) o = fmaf(scS[w * NH + hl], oS[(w * NH + hl) * D + j], o);
       float* dst = part_row(hl);
       dst[4 + j] = o;
       if (j == 0) {
-        dst[0] = M;
-        dst[1] = l;
+        dst[0] = MS[hl];
+        dst[1] = LS[hl];
       }
     }
     return;
