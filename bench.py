@@ -321,7 +321,7 @@ def _time_error_telemetry(torch, kv, synth, dev, stream, reps=10):
 
 
 def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, seed, reps=5,
-                        preset="kvarn_k4v2_g128"):
+                        preset="kvarn_k4v2_g128", kernel=None):
     """Decode over `layers` independent packed caches (one pool per layer, one shared permuted
     block table, every sequence at seq_len), launched back to back on one stream: median ms
     per pass over all layers, and the algorithmic bytes of one pass."""
@@ -353,20 +353,30 @@ def _time_decode_layers(torch, kv, synth, batch, seq_len, hq, hkv, d0, layers, s
             kv.decode_attention(desc, qs[layer], pools[layer], table, lens, outs[layer], ws,
                                 softmax_scale=scale, status=status, stream=stream)
 
-    for _ in range(3):
-        one_pass()
-    ms = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        # keep the GPU busy (~100 us) while the host enqueues the pass, so that the events
-        # time the kernels and not the host's launch latency of the first one
-        torch.cuda._sleep(200000)
-        a.record(stream)
-        one_pass()
-        b.record(stream)
-        torch.cuda.synchronize()
-        ms.append(a.elapsed_time(b))
+    # kernel "tc": the library's tcgen05 decode of GQA 8 (selected by KVARN_DECODE_KERNEL)
+    saved = os.environ.get("KVARN_DECODE_KERNEL")
+    if kernel is not None:
+        os.environ["KVARN_DECODE_KERNEL"] = kernel
+    try:
+        for _ in range(3):
+            one_pass()
+        ms = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            # keep the GPU busy (~100 us) while the host enqueues the pass, so that the events
+            # time the kernels and not the host's launch latency of the first one
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            one_pass()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+    finally:
+        if saved is None:
+            os.environ.pop("KVARN_DECODE_KERNEL", None)
+        else:
+            os.environ["KVARN_DECODE_KERNEL"] = saved
     if int(status.item()) != 0:
         raise RuntimeError("device status %d in the layered decode" % int(status.item()))
     nbytes = layers * (batch * pages * hkv * desc.page_record_bytes + 2 * batch * hq * d0 * 2)
@@ -668,6 +678,8 @@ def _decode_configs(torch, kv, synth, peak, args):
     res = {}
     for key, group, cfg in (
             ("decode_32b_step", "32b", dict(batch=32, seq_len=16384, hq=64, hkv=8, d0=128, layers=64, seed=4)),
+            ("decode_32b_8_layers_tcgen05", "32b", dict(batch=32, seq_len=16384, hq=64, hkv=8, d0=128, layers=8,
+                                                        seed=4, kernel="tc")),
             ("decode_long_d256", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=256, layers=1, seed=5)),
             ("decode_long_d96", "long", dict(batch=4, seq_len=131072, hq=32, hkv=8, d0=96, layers=1, seed=5)),
             ("preset_kvarn_k4v2_g128", "presets", dict(batch=64, seq_len=8704, hq=32, hkv=8, d0=128, layers=1,
@@ -687,9 +699,10 @@ def _decode_configs(torch, kv, synth, peak, args):
         ms, nbytes = _time_decode_layers(torch, kv, synth, **cfg)
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[key] = {
-            "workload": "%d layer(s) x batch %d at %d tokens, %d q heads / %d kv heads, head_dim %d, %s"
+            "workload": "%d layer(s) x batch %d at %d tokens, %d q heads / %d kv heads, head_dim %d, %s%s"
                         % (cfg["layers"], cfg["batch"], cfg["seq_len"], cfg["hq"], cfg["hkv"], cfg["d0"],
-                           cfg.get("preset", "kvarn_k4v2_g128")),
+                           cfg.get("preset", "kvarn_k4v2_g128"),
+                           ", tcgen05 kernel" if cfg.get("kernel") == "tc" else ""),
             "ms_per_step": ms, "algorithmic_bytes": nbytes, "hbm_gbs": gbs, "frac": gbs / peak,
             "ideal_ms_at_peak": nbytes / (peak * 1e9) * 1e3,
             "kv_tokens_per_s": cfg["batch"] * cfg["seq_len"] / (ms * 1e-3),

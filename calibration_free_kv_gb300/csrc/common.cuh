@@ -176,4 +176,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// Bounded wait for warps that share their scheduler with busy ones: between polls the thread
+// sleeps (32 ns doubling to 256 ns), so a waiting warp takes few issue slots.  Gives up after
+// ~2 s of wall time and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t ns = 32;
+  for (uint32_t it = 1; it < (1u << 26); ++it) {
+    __nanosleep(ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (ns < 256) ns <<= 1;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > 2000000000ull) return false;
+  }
+  return false;
+}
+
 }  // namespace kvarn

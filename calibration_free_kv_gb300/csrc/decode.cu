@@ -649,6 +649,12 @@ struct PagePath<D, 2, KB, VB> {
   }
 };
 
+// Warp-collective: the splits the tcgen05 kernel's partition gives row (b, h) (a cold path of
+// the partial-tile launch, kept out of line).
+__device__ __noinline__ int tc_row_segments(const DecodeParams& p, int b, int h, int lane) {
+  return row_segments(p, page_partition(p, lane), b, h, lane);
+}
+
 template <int D, int NT, int KB, int VB>
 __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, DecodeShape<D, NT, KB, VB>::kMinBlocks)
     decode_kernel(DecodeParams p) {
@@ -666,7 +672,8 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   uint2* qhl = reinterpret_cast<uint2*>(smem_d + S::kRecBytes + S::kQBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kQhBytes);
 
-  const int split = blockIdx.x, b = blockIdx.z;
+  int split = blockIdx.x;
+  const int b = blockIdx.z;
   const int h = blockIdx.y / p.vgroups, vg = blockIdx.y - h * p.vgroups;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // head slot hl of this CTA is query vector vh = vg * NH + hl of kv head h: chunk token
@@ -685,7 +692,13 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     len = len < 0 ? 0 : cap;
   }
   const int n_sealed = len / kTile, n_part = len % kTile;
-  const int n_ss = (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
+  int n_ss = (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
+  if constexpr (D == 128 && NT == 2 && KB == 4 && VB == 2) {
+    if (p.tc_ctas > 0) {  // the tcgen05 kernel took the sealed pages: the partial tile's split only
+      n_ss = tc_row_segments(p, b, h, lane);
+      split = n_ss;
+    }
+  }
   const bool partial_split = (split == n_ss) && n_part > 0;
   if (split >= n_ss && !partial_split) return;
   if (partial_split && (p.partial_k == nullptr || p.partial_v == nullptr)) {
@@ -1009,8 +1022,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   if (!live) return;
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_sealed = len / kTile;
-  const int n_splits = (n_sealed + p.pages_per_split - 1) / p.pages_per_split + (len % kTile > 0 ? 1 : 0) +
-                       (p.chunk_k != nullptr ? 1 : 0);
+  const int n_cache = p.tc_ctas > 0 ? tc_row_segments(p, b, (gw % p.num_q_heads) / p.group, lane)
+                                    : (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
+  const int n_splits = n_cache + (len % kTile > 0 ? 1 : 0) + (p.chunk_k != nullptr ? 1 : 0);
   float v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) v[e] = 0.0f;
@@ -1147,12 +1161,47 @@ static int launch_decode_t(const DecodeParams& p, int phases, cudaStream_t strea
   if ((phases & kDecodeSplits) != 0 && cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess)
     return KVARN_ERR_CUDA;
   if ((phases & kDecodeMerge) == 0) return KVARN_OK;
+  return launch_decode_combine(D, p, stream);
+}
+
+template <int D>
+static int launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
   const int warps = p.batch * p.chunk * p.num_q_heads;
   cfg.gridDim = dim3((warps + 3) / 4);
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  if (cudaLaunchKernelEx(&cfg, combine_kernel<D>, p) != cudaSuccess) return KVARN_ERR_CUDA;
-  return KVARN_OK;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
+int launch_decode_combine(int d, const DecodeParams& p, cudaStream_t stream) {
+  if (d == 64) return launch_combine_t<64>(p, stream);
+  if (d == 128) return launch_combine_t<128>(p, stream);
+  if (d == 256) return launch_combine_t<256>(p, stream);
+  return KVARN_ERR_UNSUPPORTED;
+}
+
+int launch_decode_partial_tiles(const DecodeParams& p, cudaStream_t stream) {
+  using S = DecodeShape<128, 2, 4, 2>;
+  static PerDeviceOnce smem_once;
+  const void* fn = reinterpret_cast<const void*>(decode_kernel<128, 2, 4, 2>);
+  if (const int st = set_smem_limit(smem_once, fn, S::kSmemBytes); st != KVARN_OK) return st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, p.num_kv_heads * p.vgroups, p.batch);
+  cfg.blockDim = dim3(S::kWarps * 32);
+  cfg.dynamicSmemBytes = S::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<128, 2, 4, 2>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
 // Causal attention of each chunk query to the chunk's own raw fp16 tokens (prefill): one
@@ -1336,6 +1385,10 @@ static int launch_decode_bits(int d, int nt, const DecodeParams& p, int phases, 
 }
 
 int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream, int phases) {
+  if (p.tc_ctas > 0) {
+    if (!decode_tc_serves(d, nt, kb, vb, p)) return KVARN_ERR_INVALID_ARG;
+    return launch_decode_tc(p, phases, stream);
+  }
   if (kb == 4 && vb == 2) return launch_decode_bits<4, 2>(d, nt, p, phases, stream);
   if (kb == 4 && vb == 4) return launch_decode_bits<4, 4>(d, nt, p, phases, stream);
   if (kb == 2 && vb == 2) return launch_decode_bits<2, 2>(d, nt, p, phases, stream);

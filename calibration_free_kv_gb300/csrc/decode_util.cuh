@@ -2,6 +2,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "params.cuh"
 
 namespace kvarn {
 
@@ -128,6 +129,62 @@ __device__ __forceinline__ void load_f32(const float* src, float (&f)[E]) {
 template <int D>
 __device__ __forceinline__ float inv_sqrt_d() {
   return D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
+}
+
+// ---- balanced page partition of the tcgen05 decode ---------------------------------------
+// The sealed pages of all (sequence b, kv head h) rows, in (b, h, page) order, are cut into
+// `ctas` contiguous ranges of floor or ceil(total / ctas) pages, one per CTA, with ctas no
+// larger than total / 32: every range holds at least 32 pages.  A row's pages then fall in
+// row_segments <= ceil(n / 32) + 1 ranges (n its sealed pages), and the segment that starts at
+// global page x writes split owner_cta(x) - owner_cta(first page of the row).  Every kernel of
+// the launch derives the same partition from seq_lens.
+constexpr int kMinRangePages = 32;
+
+__device__ __forceinline__ int sealed_pages(const DecodeParams& p, int b) {
+  const int cap = p.max_pages * kTile + (kTile - 1);
+  int len = p.seq_lens[b];
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  return len / kTile;
+}
+
+// Warp-collective: sealed pages of sequences 0..lim-1 (every lane gets the sum).
+__device__ __forceinline__ int64_t sealed_prefix(const DecodeParams& p, int lim, int lane) {
+  long long s = 0;
+  for (int b = lane; b < lim; b += 32) s += sealed_pages(p, b);
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+  return s;
+}
+
+struct PagePartition {
+  int64_t total;  // sealed pages of all rows
+  int64_t ctas;   // ranges (CTAs with work); 0 when there are no sealed pages
+};
+
+__device__ __forceinline__ PagePartition page_partition(const DecodeParams& p, int lane) {
+  PagePartition pp;
+  pp.total = sealed_prefix(p, p.batch, lane) * p.num_kv_heads;
+  int64_t c = pp.total / kMinRangePages;
+  c = c < 1 ? 1 : (c > p.tc_ctas ? p.tc_ctas : c);
+  pp.ctas = pp.total > 0 ? c : 0;
+  return pp;
+}
+
+// First global page of range c, and the range that holds global page x.
+__device__ __forceinline__ int64_t range_start(const PagePartition& pp, int64_t c) {
+  return c * pp.total / pp.ctas;
+}
+__device__ __forceinline__ int64_t owner_cta(const PagePartition& pp, int64_t x) {
+  return ((x + 1) * pp.ctas + pp.total - 1) / pp.total - 1;
+}
+
+// Warp-collective: the number of splits the sealed pages of row (b, h) fill.
+__device__ __forceinline__ int row_segments(const DecodeParams& p, const PagePartition& pp, int b, int h,
+                                            int lane) {
+  const int n = sealed_pages(p, b);
+  const int64_t a = sealed_prefix(p, b, lane) * p.num_kv_heads + (int64_t)h * n;
+  if (n == 0) return 0;
+  return (int)(owner_cta(pp, a + n - 1) - owner_cta(pp, a) + 1);
 }
 
 }  // namespace kvarn

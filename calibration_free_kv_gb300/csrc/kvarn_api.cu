@@ -1,10 +1,10 @@
 // C ABI of the KVarN kernels: argument validation, launch configuration, status codes.
 // Nothing here allocates, synchronises or keeps state between calls.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
-
 #include "params.cuh"
 
 using namespace kvarn;
@@ -187,7 +187,7 @@ size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q
                                     int max_pages) {
   if (check_desc(desc) != KVARN_OK || batch < 0 || num_q_heads < 1 || max_pages < 1) return 0;
   const int pps = decode_pages_per_split(desc, max_pages);
-  const int64_t max_splits = (max_pages + pps - 1) / pps + 1;
+  const int64_t max_splits = (max_pages + pps - 1) / pps + 2;  // + the partial tile + one
   return (size_t)batch * num_q_heads * max_splits * (desc->head_dim_padded + 4) * sizeof(float);
 }
 
@@ -223,6 +223,14 @@ int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const 
 
 extern "C" {
 
+// KVARN_DECODE_KERNEL=tc in the environment runs GQA-8 decode (head_dim 128, K4V2) on the
+// tcgen05 kernel instead of the mma.sync kernel, which is faster on this shape; read on every
+// call.
+static bool decode_tc_requested() {
+  const char* v = std::getenv("KVARN_DECODE_KERNEL");
+  return v != nullptr && std::strcmp(v, "tc") == 0;
+}
+
 static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
                          const void* page_pool, int64_t num_pool_pages, const int32_t* block_table,
                          int max_pages, const int32_t* seq_lens, const void* partial_k,
@@ -256,12 +264,16 @@ static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, con
   p.num_q_heads = num_q_heads;
   p.group = group;
   p.d0 = desc->head_dim;
-  p.max_splits = (max_pages + pps - 1) / pps + 1;  // workspace stride at the smallest size
+  p.max_splits = (max_pages + pps - 1) / pps + 2;  // workspace stride at the smallest size
   p.pages_per_split = decode_split_pages(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits,
                                          (int64_t)batch * desc->num_kv_heads, max_pages);
   p.chunk = 1;
   p.vgroups = 1;
   p.status = dev_status;
+  if (decode_tc_requested() && decode_tc_serves(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p)) {
+    p.tc_ctas = decode_tc_ctas();
+    if (p.tc_ctas < 1) return KVARN_ERR_CUDA;
+  }
   return launch_decode_any(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p,
                            static_cast<cudaStream_t>(stream), phases);
 }

@@ -62,6 +62,10 @@ struct DecodeParams {
   const __half* chunk_k;
   const __half* chunk_v;
   int32_t* status;
+  // tcgen05 decode (decode_tc.cu): 0, or the CTAs its balanced page partition is cut for.  When
+  // set, the sealed pages' partials of row (b, kv head) fill splits [0, row_segments) and
+  // decode_kernel, launched over (1, Hkv, batch), writes only the partial tile's split after them.
+  int tc_ctas;
 };
 
 struct DequantParams {
@@ -100,6 +104,14 @@ int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cuda
 // the GPU's CTA slots best.  Never below 32, the size the workspace is laid out for.
 int decode_split_pages(int d, int nt, int kb, int vb, int64_t units, int max_pages);
 int launch_chunk_any(int d, const DecodeParams& p, cudaStream_t stream);
+// The tcgen05 decode of GQA groups of 8 at head_dim 128, K4V2 (decode_tc.cu): whether it
+// serves this launch, its CTA count, and the launch of the phases requested.
+bool decode_tc_serves(int d, int nt, int kb, int vb, const DecodeParams& p);
+int decode_tc_ctas();
+int launch_decode_tc(const DecodeParams& p, int phases, cudaStream_t stream);
+// decode_kernel<128, 2, 4, 2> over (1, Hkv, batch) for the partial tiles of a tcgen05 launch
+int launch_decode_partial_tiles(const DecodeParams& p, cudaStream_t stream);
+int launch_decode_combine(int d, const DecodeParams& p, cudaStream_t stream);
 int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pages, cudaStream_t stream);
 
 }  // namespace kvarn

@@ -155,9 +155,14 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
                        void* stream);
 
 /* Workspace bytes kvarn_decode_attention needs for this batch shape (host only): fp32 split
- * partials laid out for 32-page splits, the smallest split size; a launch over a block table
- * wider than 256 pages may take larger splits (chosen from the GPU's SM count) and fills fewer
- * of them.  Needs no GPU. */
+ * partials, ceil(max_pages / 32) + 2 per query row.  The mma.sync kernels fill one per split
+ * of 32 or more pages (a block table wider than 256 pages may take larger splits, chosen from
+ * the GPU's SM count) plus the raw partial tile's; the tcgen05 kernel of GQA groups of 8 (head_dim
+ * 128, K4V2) cuts all sealed pages of the batch into ranges of equal size, one per SM and each
+ * at least 32 pages, so that a row's pages fall in at most ceil(n / 32) + 1 ranges.  Needs no
+ * GPU.  Setting KVARN_DECODE_KERNEL=tc in the environment runs GQA-8 decode at head_dim 128, K4V2
+ * on the tcgen05 kernel (read on every call); by default it runs on the mma.sync kernel, which
+ * is faster on that shape. */
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
                                     int max_pages);
 
