@@ -49,7 +49,8 @@ struct DecodeShape {
   // warps per CTA: 8, or 4 where 8 page slots would not fit in shared memory
   static constexpr int kWarps = 8 * kRec + kQBytes + kQhBytes + 8 * 16 <= kMaxSmem ? 8 : 4;
   static constexpr int kRecBytes = kWarps * kRec;    // one K slot + one V slot per warp
-  static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + kWarps * 2 * 8;
+  // page slots, q, and the barriers: two per warp plus one for the raw partial tile
+  static constexpr int kSmemBytes = kRecBytes + kQBytes + kQhBytes + (kWarps * 2 + 1) * 8;
   static_assert(kSmemBytes <= kMaxSmem, "page slots fit in shared memory");
   static_assert(kRecBytes >= (kWarps * kNH * (D + 3) + 2 * kNH) * 4, "the merge scratch fits the page slots");
   // two CTAs per SM where their shared memory fits (registers then capped at 128 a thread)
@@ -671,10 +672,17 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   float* qsm = reinterpret_cast<float*>(smem_d + S::kRecBytes);
   uint2* qhl = reinterpret_cast<uint2*>(smem_d + S::kRecBytes + S::kQBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_d + S::kRecBytes + S::kQBytes + S::kQhBytes);
+  uint64_t* pbar = bars + 2 * kDecWarps;  // the raw partial tile's copies
+  uint32_t pph = 0;                        // its phase
+  if (threadIdx.x == 0) {
+    mbar_init(pbar, 1);
+    fence_mbar_init();
+  }
 
   int split = blockIdx.x;
-  const int b = blockIdx.z;
-  const int h = blockIdx.y / p.vgroups, vg = blockIdx.y - h * p.vgroups;
+  int b = blockIdx.z;  // the row (b, h) changes per segment in the persistent mode
+  int h = blockIdx.y / p.vgroups;
+  const int vg = blockIdx.y - h * p.vgroups;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // head slot hl of this CTA is query vector vh = vg * NH + hl of kv head h: chunk token
   // vh / group, query head h * group + vh % group (decode: chunk 1, vh = group member)
@@ -686,31 +694,10 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   };
   grid_dependency_wait();  // lengths, partial tiles and pages come from the previous kernel
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
-  int len = p.seq_lens[b];
-  if (len < 0 || len > cap) {
-    if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
-    len = len < 0 ? 0 : cap;
-  }
-  const int n_sealed = len / kTile, n_part = len % kTile;
-  int n_ss = (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
-  if constexpr (D == 128 && NT == 2 && KB == 4 && VB == 2) {
-    if (p.tc_ctas > 0) {  // the tcgen05 kernel took the sealed pages: the partial tile's split only
-      n_ss = tc_row_segments(p, b, h, lane);
-      split = n_ss;
-    }
-  }
-  const bool partial_split = (split == n_ss) && n_part > 0;
-  if (split >= n_ss && !partial_split) return;
-  if (partial_split && (p.partial_k == nullptr || p.partial_v == nullptr)) {
-    if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
-    return;
-  }
-
-  auto part_row = [&](int hl) { return p.part + (vrow(hl) * p.max_splits + split) * (D + 4); };
-
-  if (!partial_split) {
-    const int first = split * p.pages_per_split;
-    const int n = min(n_sealed, first + p.pages_per_split) - first;  // pages of this CTA
+  auto part_row = [&](int hl, int slot) { return p.part + (vrow(hl) * p.max_splits + slot) * (D + 4); };
+  // Sealed pages first..first+n-1 of row (b, h) -> partial row `slot`.  pc counts the pages this
+  // warp has taken in earlier calls (the phases of its two barriers); `init` sets them up.
+  auto sealed_run = [&](int first, int n, int slot, int& pc, bool init) {
     const int cnt = n > warp ? (n - warp + kDecWarps - 1) / kDecWarps : 0;  // pages of this warp
     uint8_t* kslot = recs + warp * REC;
     uint8_t* vslot = kslot + KH;
@@ -727,11 +714,14 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     };
     // start this warp's page stream before anything else
     if (lane == 0) {
-      mbar_init(kbar, 1);
-      mbar_init(vbar, 1);
-      fence_mbar_init();
+      if (init) {
+        mbar_init(kbar, 1);
+        mbar_init(vbar, 1);
+        fence_mbar_init();
+      }
       if (cnt > 0) {
         const uint8_t* src = page_src(0);
+        fence_proxy_async_smem();  // the slots held the previous merge's scratch
         mbar_expect_tx(kbar, KH);
         bulk_copy_g2s(kslot, src, KH, kbar);
         mbar_expect_tx(vbar, VH);
@@ -772,12 +762,13 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     // never waits on the block-table load
     const uint8_t* nxt = cnt > 1 ? page_src(1) : nullptr;
     for (int j = 0; j < cnt; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(kbar, j & 1))) {
+      const uint32_t par = (uint32_t)((pc + j) & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(kbar, par))) {
         // a copy never arrived: report, drain this warp's copies still in flight, stop
         if (lane == 0) {
           flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
-          mbar_wait(kbar, j & 1);
-          mbar_wait(vbar, j & 1);
+          mbar_wait(kbar, par);
+          mbar_wait(vbar, par);
         }
         break;
       }
@@ -790,11 +781,11 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
         mbar_expect_tx(kbar, KH);
         bulk_copy_g2s(kslot, nxt, KH, kbar);
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(vbar, j & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(vbar, par))) {
         if (lane == 0) {
           flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
-          mbar_wait(vbar, j & 1);
-          if (more) mbar_wait(kbar, (j + 1) & 1);
+          mbar_wait(vbar, par);
+          if (more) mbar_wait(kbar, par ^ 1u);
         }
         break;
       }
@@ -841,168 +832,235 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       float o = 0.0f;
 #pragma unroll
       for (int w = 0; w < kDecWarps; ++w) o = fmaf(scS[w * NH + hl], oS[(w * NH + hl) * D + j], o);
-      float* dst = part_row(hl);
+      float* dst = part_row(hl, slot);
       dst[4 + j] = o;
       if (j == 0) {
         dst[0] = MS[hl];
         dst[1] = LS[hl];
       }
     }
-    return;
-  }
+    pc += cnt;
+    __syncthreads();  // the merge scratch overlays the page slots the next run fills
+  };
 
   // ---- partial tile: raw fp16 tokens in the original basis ---------------------------------
-  // The n_part rows of K and of V are contiguous for one (sequence, kv head): two bulk copies
-  // bring them into the page-slot area, then logits, softmax and PV run from shared memory.
-  // Layout there: K rows [0, 256 D), V rows [256 D, 512 D) (row stride d0), probabilities
-  // [t][NH] after them, then the head maxima and sums; the PV warp sums later overlay K.
-  constexpr int E = D / 32;   // channels per lane, lane-contiguous
-  constexpr int R = 32 / NH;  // tokens per logit round: 32 (token, head slot) pairs
-  static_assert(S::kRecBytes >= 512 * D + 4 * NH * (kTile + 2), "partial tile fits the page slots");
-  static_assert(kDecWarps * NH * D * 4 <= 256 * D, "PV warp sums fit over the K rows");
-  const __half* Ks = reinterpret_cast<const __half*>(recs);
-  const __half* Vs = reinterpret_cast<const __half*>(recs + 256 * D);
-  float* pS = reinterpret_cast<float*>(recs + 512 * D);
-  float* mS = pS + kTile * NH;
-  float* lS = mS + NH;
-  // q in the original basis: the fp32 q~ area, or after the softmax scratch where there is none
-  constexpr int kPartQ = (512 * D + 4 * NH * (kTile + 2) + 15) & ~15;
-  static_assert(S::kQBytes > 0 || S::kRecBytes >= kPartQ + NH * QLD * 4, "partial q fits");
-  float* qp = S::kQBytes > 0 ? qsm : reinterpret_cast<float*>(recs + kPartQ);
-  const int c0 = lane * E;
-  const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
-  if (threadIdx.x == 0) {
-    const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
-    const uint32_t bytes = (uint32_t)(n_part * p.d0 * 2);  // a multiple of 16
-    mbar_init(bars, 1);
-    fence_mbar_init();
-    mbar_expect_tx(bars, 2 * bytes);
-    bulk_copy_g2s(recs, p.partial_k + base, bytes, bars);
-    bulk_copy_g2s(recs + 256 * D, p.partial_v + base, bytes, bars);
-  }
-  for (int hl = warp; hl < NH; hl += kDecWarps) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int j = c0 + e;
-      qp[hl * QLD + j] =
-          (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) * p.qscale : 0.0f;
-    }
-  }
-  __syncthreads();  // q staged, the barrier initialised
-  if (!__syncthreads_and(mbar_wait(bars, 0) ? 1 : 0)) {
+  // Row (b, h)'s n_part raw tokens -> partial row `split`; false if its copies never arrived.
+  auto partial_run = [&](int n_part, int split) -> bool {
+    // The n_part rows of K and of V are contiguous for one (sequence, kv head): two bulk copies
+    // bring them into the page-slot area, then logits, softmax and PV run from shared memory.
+    // Layout there: K rows [0, 256 D), V rows [256 D, 512 D) (row stride d0), probabilities
+    // [t][NH] after them, then the head maxima and sums; the PV warp sums later overlay K.
+    constexpr int E = D / 32;   // channels per lane, lane-contiguous
+    constexpr int R = 32 / NH;  // tokens per logit round: 32 (token, head slot) pairs
+    static_assert(S::kRecBytes >= 512 * D + 4 * NH * (kTile + 2), "partial tile fits the page slots");
+    static_assert(kDecWarps * NH * D * 4 <= 256 * D, "PV warp sums fit over the K rows");
+    const __half* Ks = reinterpret_cast<const __half*>(recs);
+    const __half* Vs = reinterpret_cast<const __half*>(recs + 256 * D);
+    float* pS = reinterpret_cast<float*>(recs + 512 * D);
+    float* mS = pS + kTile * NH;
+    float* lS = mS + NH;
+    // q in the original basis: the fp32 q~ area, or after the softmax scratch where there is none
+    constexpr int kPartQ = (512 * D + 4 * NH * (kTile + 2) + 15) & ~15;
+    static_assert(S::kQBytes > 0 || S::kRecBytes >= kPartQ + NH * QLD * 4, "partial q fits");
+    float* qp = S::kQBytes > 0 ? qsm : reinterpret_cast<float*>(recs + kPartQ);
+    const int c0 = lane * E;
+    const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
     if (threadIdx.x == 0) {
-      flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
-      mbar_wait(bars, 0);  // the copies may still land: wait (bounded) before leaving
+      const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
+      const uint32_t bytes = (uint32_t)(n_part * p.d0 * 2);  // a multiple of 16
+      mbar_expect_tx(pbar, 2 * bytes);
+      bulk_copy_g2s(recs, p.partial_k + base, bytes, pbar);
+      bulk_copy_g2s(recs + 256 * D, p.partial_v + base, bytes, pbar);
     }
-    return;
-  }
-  // logits: each lane sums its E channels for the 32 pairs of a round, then a halving
-  // butterfly leaves pair i = r * NH + hl complete in lane i
-  for (int tb = warp; tb * R < n_part; tb += kDecWarps) {
-    float v[32];
-    float qv[NH][E];
-#pragma unroll
-    for (int hl = 0; hl < NH; ++hl) load_f32<E>(qp + hl * QLD + c0, qv[hl]);
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int t = tb * R + r;
-      float kf[E];
-      if (t < n_part && in) {
-        load_f16<E>(Ks + t * p.d0 + c0, kf);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) kf[e] = 0.0f;
-      }
-#pragma unroll
-      for (int hl = 0; hl < NH; ++hl) {
-        float acc = 0.0f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc = fmaf(qv[hl][e], kf[e], acc);
-        v[r * NH + hl] = acc;
+    for (int hl = warp; hl < NH; hl += kDecWarps) {
+  #pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int j = c0 + e;
+        qp[hl * QLD + j] =
+            (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) * p.qscale : 0.0f;
       }
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < o; ++i) {
-        const float send = up ? v[i] : v[i + o];
-        const float keep = up ? v[i + o] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    __syncthreads();  // q staged
+    if (!__syncthreads_and(mbar_wait(pbar, pph) ? 1 : 0)) {
+      if (threadIdx.x == 0) {
+        flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+        mbar_wait(pbar, pph);  // the copies may still land: wait (bounded) before leaving
       }
+      return false;
     }
-    const int t = tb * R + lane / NH;
-    if (t < n_part) pS[t * NH + lane % NH] = v[0];
-  }
-  __syncthreads();
-  // softmax over the partial tokens, one warp per head slot
-  for (int hl = warp; hl < NH; hl += kDecWarps) {
-    if (!valid(hl)) break;
-    float mx = -INFINITY;
-    for (int t = lane; t < n_part; t += 32) mx = fmaxf(mx, pS[t * NH + hl]);
-#pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
-    float sum = 0.0f;
-    for (int t = lane; t < n_part; t += 32) {
-      const float pv = exp2f(pS[t * NH + hl] - mx);
-      pS[t * NH + hl] = pv;
-      sum += pv;
-    }
-#pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, msk);
-    if (lane == 0) {
-      mS[hl] = mx;
-      lS[hl] = sum;
-    }
-  }
-  __syncthreads();
-  // PV: warp w takes tokens w, w + kDecWarps, ...; the warp sums meet in shared memory
-  {
-    float acc[NH][E];
-#pragma unroll
-    for (int hl = 0; hl < NH; ++hl)
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[hl][e] = 0.0f;
-    if (in) {
-      for (int t = warp; t < n_part; t += kDecWarps) {
-        float vf[E];
-        load_f16<E>(Vs + t * p.d0 + c0, vf);
-#pragma unroll
+    // logits: each lane sums its E channels for the 32 pairs of a round, then a halving
+    // butterfly leaves pair i = r * NH + hl complete in lane i
+    for (int tb = warp; tb * R < n_part; tb += kDecWarps) {
+      float v[32];
+      float qv[NH][E];
+  #pragma unroll
+      for (int hl = 0; hl < NH; ++hl) load_f32<E>(qp + hl * QLD + c0, qv[hl]);
+  #pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int t = tb * R + r;
+        float kf[E];
+        if (t < n_part && in) {
+          load_f16<E>(Ks + t * p.d0 + c0, kf);
+        } else {
+  #pragma unroll
+          for (int e = 0; e < E; ++e) kf[e] = 0.0f;
+        }
+  #pragma unroll
         for (int hl = 0; hl < NH; ++hl) {
-          const float pw = pS[t * NH + hl];
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc[hl][e] = fmaf(pw, vf[e], acc[hl][e]);
+          float acc = 0.0f;
+  #pragma unroll
+          for (int e = 0; e < E; ++e) acc = fmaf(qv[hl][e], kf[e], acc);
+          v[r * NH + hl] = acc;
         }
       }
+  #pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+  #pragma unroll
+        for (int i = 0; i < o; ++i) {
+          const float send = up ? v[i] : v[i + o];
+          const float keep = up ? v[i + o] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      const int t = tb * R + lane / NH;
+      if (t < n_part) pS[t * NH + lane % NH] = v[0];
     }
-    float* oS = reinterpret_cast<float*>(recs);  // K rows are no longer read
-#pragma unroll
-    for (int hl = 0; hl < NH; ++hl)
-#pragma unroll
-      for (int e = 0; e < E; ++e) oS[(warp * NH + hl) * D + c0 + e] = acc[hl][e];
-  }
-  __syncthreads();
-  // sum the warps, rotate o into the basis of the sealed splits, store
-  for (int hl = warp; hl < NH; hl += kDecWarps) {
-    if (!valid(hl)) break;
-    const float* oS = reinterpret_cast<const float*>(recs);
-    float v[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w)
-#pragma unroll
-      for (int e = 0; e < E; ++e) v[e] += oS[(w * NH + hl) * D + c0 + e];
-    warp_fwht<D>(v, lane);
-    float* dst = part_row(hl);
-#pragma unroll
-    for (int e = 0; e < E; ++e) dst[4 + c0 + e] = v[e] * inv_sqrt_d<D>();
-    if (lane == 0) {
-      dst[0] = mS[hl];
-      dst[1] = lS[hl];
+    __syncthreads();
+    // softmax over the partial tokens, one warp per head slot
+    for (int hl = warp; hl < NH; hl += kDecWarps) {
+      if (!valid(hl)) break;
+      float mx = -INFINITY;
+      for (int t = lane; t < n_part; t += 32) mx = fmaxf(mx, pS[t * NH + hl]);
+  #pragma unroll
+      for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+      float sum = 0.0f;
+      for (int t = lane; t < n_part; t += 32) {
+        const float pv = exp2f(pS[t * NH + hl] - mx);
+        pS[t * NH + hl] = pv;
+        sum += pv;
+      }
+  #pragma unroll
+      for (int msk = 16; msk > 0; msk >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, msk);
+      if (lane == 0) {
+        mS[hl] = mx;
+        lS[hl] = sum;
+      }
     }
+    __syncthreads();
+    // PV: warp w takes tokens w, w + kDecWarps, ...; the warp sums meet in shared memory
+    {
+      float acc[NH][E];
+  #pragma unroll
+      for (int hl = 0; hl < NH; ++hl)
+  #pragma unroll
+        for (int e = 0; e < E; ++e) acc[hl][e] = 0.0f;
+      if (in) {
+        for (int t = warp; t < n_part; t += kDecWarps) {
+          float vf[E];
+          load_f16<E>(Vs + t * p.d0 + c0, vf);
+  #pragma unroll
+          for (int hl = 0; hl < NH; ++hl) {
+            const float pw = pS[t * NH + hl];
+  #pragma unroll
+            for (int e = 0; e < E; ++e) acc[hl][e] = fmaf(pw, vf[e], acc[hl][e]);
+          }
+        }
+      }
+      float* oS = reinterpret_cast<float*>(recs);  // K rows are no longer read
+  #pragma unroll
+      for (int hl = 0; hl < NH; ++hl)
+  #pragma unroll
+        for (int e = 0; e < E; ++e) oS[(warp * NH + hl) * D + c0 + e] = acc[hl][e];
+    }
+    __syncthreads();
+    // sum the warps, rotate o into the basis of the sealed splits, store
+    for (int hl = warp; hl < NH; hl += kDecWarps) {
+      if (!valid(hl)) break;
+      const float* oS = reinterpret_cast<const float*>(recs);
+      float v[E];
+  #pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = 0.0f;
+  #pragma unroll
+      for (int w = 0; w < kDecWarps; ++w)
+  #pragma unroll
+        for (int e = 0; e < E; ++e) v[e] += oS[(w * NH + hl) * D + c0 + e];
+      warp_fwht<D>(v, lane);
+      float* dst = part_row(hl, split);
+  #pragma unroll
+      for (int e = 0; e < E; ++e) dst[4 + c0 + e] = v[e] * inv_sqrt_d<D>();
+      if (lane == 0) {
+        dst[0] = mS[hl];
+        dst[1] = lS[hl];
+      }
+    }
+    pph ^= 1u;
+    __syncthreads();  // the page slots are reused next
+    return true;
+  };
+  if (p.part_mode == 1) {
+    // persistent: this CTA's range of the balanced partition, segment by segment
+    __shared__ Walk walk0;
+    if (warp == 0) {
+      const Walk w = range_walk(p, blockIdx.x, lane);
+      if (lane == 0) walk0 = w;
+    }
+    if (blockIdx.x == 0) {  // the length checks of the one-CTA-per-split form, once
+      for (int bb = threadIdx.x; bb < p.batch; bb += blockDim.x) {
+        const int lb = p.seq_lens[bb];
+        if (lb < 0 || lb > cap) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
+        else if (lb % kTile != 0 && p.partial_k == nullptr) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
+      }
+    }
+    __syncthreads();
+    int pc = 0;
+    bool init = true;
+    for (Walk w = walk0; w.left > 0; w.next(p)) {
+      b = w.b;
+      h = w.h;
+      sealed_run(w.j, w.count(), w.slot, pc, init);
+      init = false;
+    }
+    // raw partial tiles: row k = b * Hkv + h goes to CTA k mod gridDim.x, its split after the
+    // row's sealed segments
+    for (int k = blockIdx.x; k < p.batch * p.num_kv_heads; k += gridDim.x) {
+      b = k / p.num_kv_heads;
+      h = k - b * p.num_kv_heads;
+      int lb = p.seq_lens[b];
+      lb = lb < 0 ? 0 : (lb > cap ? cap : lb);
+      const int np = lb % kTile;
+      if (np == 0 || p.partial_k == nullptr || p.partial_v == nullptr) continue;
+      if (!partial_run(np, tc_row_segments(p, b, h, lane))) break;
+    }
+    grid_launch_dependents();
+    return;
   }
+  int len = p.seq_lens[b];
+  if (len < 0 || len > cap) {
+    if (threadIdx.x == 0 && split == 0 && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
+    len = len < 0 ? 0 : cap;
+  }
+  const int n_sealed = len / kTile, n_part = len % kTile;
+  int n_ss = (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
+  if (p.part_mode == 2) {  // the persistent kernel took the sealed pages: the partial tile's split
+    n_ss = tc_row_segments(p, b, h, lane);
+    split = n_ss;
+  }
+  const bool partial_split = (split == n_ss) && n_part > 0;
+  if (split >= n_ss && !partial_split) return;
+  if (partial_split && (p.partial_k == nullptr || p.partial_v == nullptr)) {
+    if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
+    return;
+  }
+  if (!partial_split) {
+    int pc = 0;
+    const int first = split * p.pages_per_split;
+    sealed_run(first, min(n_sealed, first + p.pages_per_split) - first, split, pc, true);
+    return;
+  }
+  partial_run(n_part, split);
 }
+
 
 // One warp per (sequence, chunk token, query head): merge the splits, normalise, undo the
 // rotation.
@@ -1022,7 +1080,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   if (!live) return;
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_sealed = len / kTile;
-  const int n_cache = p.tc_ctas > 0 ? tc_row_segments(p, b, (gw % p.num_q_heads) / p.group, lane)
+  const int n_cache = p.part_ctas > 0 ? tc_row_segments(p, b, (gw % p.num_q_heads) / p.group, lane)
                                     : (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
   const int n_splits = n_cache + (len % kTile > 0 ? 1 : 0) + (p.chunk_k != nullptr ? 1 : 0);
   float v[E];
@@ -1149,17 +1207,24 @@ static int launch_decode_t(const DecodeParams& p, int phases, cudaStream_t strea
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  // the sealed splits at this split size plus the partial tile's (the workspace stride
-  // max_splits is laid out for the smallest size and may be larger)
-  const int splits = min(p.max_splits, (p.max_pages + p.pages_per_split - 1) / p.pages_per_split + 1);
-  cfg.gridDim = dim3(splits, p.num_kv_heads * p.vgroups, p.batch);
   cfg.blockDim = dim3(S::kWarps * 32);
   cfg.dynamicSmemBytes = S::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if ((phases & kDecodeSplits) != 0 && cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess)
-    return KVARN_ERR_CUDA;
+  if ((phases & kDecodeSplits) != 0) {
+    if (p.part_mode == 1) {
+      // persistent CTAs over the sealed pages and the raw partial tiles
+      cfg.gridDim = dim3(p.part_ctas);
+      if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess) return KVARN_ERR_CUDA;
+    } else {
+      // the sealed splits at this split size plus the partial tile's (the workspace stride
+      // max_splits is laid out for the smallest size and may be larger)
+      const int splits = min(p.max_splits, (p.max_pages + p.pages_per_split - 1) / p.pages_per_split + 1);
+      cfg.gridDim = dim3(splits, p.num_kv_heads * p.vgroups, p.batch);
+      if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess) return KVARN_ERR_CUDA;
+    }
+  }
   if ((phases & kDecodeMerge) == 0) return KVARN_OK;
   return launch_decode_combine(D, p, stream);
 }
@@ -1201,7 +1266,39 @@ int launch_decode_partial_tiles(const DecodeParams& p, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<128, 2, 4, 2>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  DecodeParams pt = p;
+  pt.part_mode = 2;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<128, 2, 4, 2>, pt) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
+template <int D, int NT, int KB, int VB>
+static int persistent_ctas_t() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 0;
+  return sms * DecodeShape<D, NT, KB, VB>::kMinBlocks;
+}
+
+template <int KB, int VB>
+static int persistent_ctas_bits(int d, int nt) {
+  if (nt == 1) {
+    if (d == 64) return persistent_ctas_t<64, 1, KB, VB>();
+    if (d == 128) return persistent_ctas_t<128, 1, KB, VB>();
+    if (d == 256) return persistent_ctas_t<256, 1, KB, VB>();
+  } else if (nt == 2) {
+    if (d == 64) return persistent_ctas_t<64, 2, KB, VB>();
+    if (d == 128) return persistent_ctas_t<128, 2, KB, VB>();
+  }
+  return 0;
+}
+
+int decode_persistent_ctas(int d, int nt, int kb, int vb) {
+  if (kb == 4 && vb == 2) return persistent_ctas_bits<4, 2>(d, nt);
+  if (kb == 4 && vb == 4) return persistent_ctas_bits<4, 4>(d, nt);
+  if (kb == 2 && vb == 2) return persistent_ctas_bits<2, 2>(d, nt);
+  if (kb == 8 && vb == 4) return persistent_ctas_bits<8, 4>(d, nt);
+  return 0;
 }
 
 // Causal attention of each chunk query to the chunk's own raw fp16 tokens (prefill): one
@@ -1385,8 +1482,8 @@ static int launch_decode_bits(int d, int nt, const DecodeParams& p, int phases, 
 }
 
 int launch_decode_any(int d, int nt, int kb, int vb, const DecodeParams& p, cudaStream_t stream, int phases) {
-  if (p.tc_ctas > 0) {
-    if (!decode_tc_serves(d, nt, kb, vb, p)) return KVARN_ERR_INVALID_ARG;
+  if (p.part_mode == 3) {
+    if (!decode_tc_serves(d, nt, kb, vb, p) || p.part_ctas < 1) return KVARN_ERR_INVALID_ARG;
     return launch_decode_tc(p, phases, stream);
   }
   if (kb == 4 && vb == 2) return launch_decode_bits<4, 2>(d, nt, p, phases, stream);

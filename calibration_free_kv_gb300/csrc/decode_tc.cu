@@ -170,46 +170,13 @@ __device__ __forceinline__ void ld_sum2(uint32_t taddr, float (&sum)[16]) {
   for (int n = 0; n < 16; ++n) sum[n] = __uint_as_float(r[n]) + __uint_as_float(r[16 + n]);
 }
 
-// Segment walk over this CTA's range: a maximal run of pages of one row.
-struct Walk {
-  int b, h, j, n;    // row (sequence b, kv head h), first page j of the segment, sealed pages n
-  int slot;          // split the segment's partial goes to
-  int64_t left;      // pages of the range from this segment on
-  __device__ int count() const { return (int)min((int64_t)(n - j), left); }
-  // next segment: the next row with sealed pages (slot 0, page 0)
-  __device__ void next(const DecodeParams& p) {
-    left -= count();
-    if (left <= 0) return;
-    j = 0;
-    slot = 0;
-    for (;;) {
-      if (++h == p.num_kv_heads) {
-        h = 0;
-        ++b;
-      }
-      if (b >= p.batch) {  // unreachable while the lengths match the partition
-        left = 0;
-        return;
-      }
-      n = sealed_pages(p, b);
-      if (n > 0) return;
-      h = p.num_kv_heads - 1;  // skip the whole sequence
-    }
-  }
-};
-
-struct WorkStart {
-  long long x0, x1;
-  int b, h, j, slot;
-};
-
 }  // namespace dtc
 
 using namespace dtc;
 
 __global__ void __launch_bounds__(dtc::kThreads, 1) decode_tc_kernel(DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t sm[];
-  __shared__ WorkStart ws;
+  __shared__ Walk ws;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t* rec_full = reinterpret_cast<uint64_t*>(sm + kBarOff);
@@ -224,46 +191,8 @@ __global__ void __launch_bounds__(dtc::kThreads, 1) decode_tc_kernel(DecodeParam
 
   grid_dependency_wait();  // lengths and pages may come from the previous kernel
   if (warp == kLoadWarp) {
-    const PagePartition pp = page_partition(p, lane);
-    const int64_t c = blockIdx.x;
-    long long x0 = 0, x1 = 0;
-    int b = 0, h = 0, j = 0, slot = 0;
-    if (c < pp.ctas) {
-      x0 = range_start(pp, c);
-      x1 = range_start(pp, c + 1);
-      // the row holding global page x0: scan the sequences 32 at a time
-      long long cum = 0;
-      for (int b0 = 0; b0 < p.batch; b0 += 32) {
-        const int bb = b0 + lane;
-        const int n = bb < p.batch ? sealed_pages(p, bb) : 0;
-        long long incl = (long long)n * p.num_kv_heads;
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-          const long long o = __shfl_up_sync(0xffffffffu, incl, m);
-          if (lane >= m) incl += o;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, cum + incl > x0);
-        if (hit != 0u) {
-          const int l = __ffs(hit) - 1;
-          const int nb = __shfl_sync(0xffffffffu, n, l);
-          const long long excl = cum + __shfl_sync(0xffffffffu, incl, l) - (long long)nb * p.num_kv_heads;
-          b = b0 + l;
-          h = (int)((x0 - excl) / nb);
-          j = (int)((x0 - excl) - (long long)h * nb);
-          slot = (int)(c - owner_cta(pp, x0 - j));
-          break;
-        }
-        cum += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-    if (lane == 0) {
-      ws.x0 = x0;
-      ws.x1 = x1;
-      ws.b = b;
-      ws.h = h;
-      ws.j = j;
-      ws.slot = slot;
-    }
+    const Walk w = range_walk(p, blockIdx.x, lane);
+    if (lane == 0) ws = w;
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSlots; ++i) {
@@ -282,7 +211,7 @@ __global__ void __launch_bounds__(dtc::kThreads, 1) decode_tc_kernel(DecodeParam
     fence_mbar_init();
   }
   __syncthreads();
-  const int64_t total = ws.x1 - ws.x0;
+  const int64_t total = ws.left;
   if (total <= 0) {
     grid_launch_dependents();
     return;
@@ -301,13 +230,7 @@ __global__ void __launch_bounds__(dtc::kThreads, 1) decode_tc_kernel(DecodeParam
     *abort_v = 1;
     flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
   };
-  Walk w0;
-  w0.b = ws.b;
-  w0.h = ws.h;
-  w0.j = ws.j;
-  w0.n = sealed_pages(p, ws.b);
-  w0.slot = ws.slot;
-  w0.left = total;
+  const Walk w0 = ws;
   uint8_t* recs = sm;
   auto stage_tmem = [&](int s) { return tmem + kColStage * (uint32_t)s; };
   auto b_qk = [&](int s) { return sm + kBOff + 2 * s * kBTile; };
@@ -774,7 +697,7 @@ int decode_tc_ctas() {
 }
 
 int launch_decode_tc(const DecodeParams& p, int phases, cudaStream_t stream) {
-  if (p.tc_ctas < 1) return KVARN_ERR_INVALID_ARG;
+  if (p.part_ctas < 1) return KVARN_ERR_INVALID_ARG;
   if ((phases & kDecodeSplits) != 0) {
     static PerDeviceOnce smem_once;
     const void* fn = reinterpret_cast<const void*>(decode_tc_kernel);
@@ -783,7 +706,7 @@ int launch_decode_tc(const DecodeParams& p, int phases, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.tc_ctas);
+    cfg.gridDim = dim3(p.part_ctas);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

@@ -131,7 +131,7 @@ __device__ __forceinline__ float inv_sqrt_d() {
   return D == 64 ? 0.125f : (D == 128 ? 0.08838834764831845f : 0.0625f);
 }
 
-// ---- balanced page partition of the tcgen05 decode ---------------------------------------
+// ---- balanced page partition of the persistent decode kernels -----------------------------
 // The sealed pages of all (sequence b, kv head h) rows, in (b, h, page) order, are cut into
 // `ctas` contiguous ranges of floor or ceil(total / ctas) pages, one per CTA, with ctas no
 // larger than total / 32: every range holds at least 32 pages.  A row's pages then fall in
@@ -165,7 +165,7 @@ __device__ __forceinline__ PagePartition page_partition(const DecodeParams& p, i
   PagePartition pp;
   pp.total = sealed_prefix(p, p.batch, lane) * p.num_kv_heads;
   int64_t c = pp.total / kMinRangePages;
-  c = c < 1 ? 1 : (c > p.tc_ctas ? p.tc_ctas : c);
+  c = c < 1 ? 1 : (c > p.part_ctas ? p.part_ctas : c);
   pp.ctas = pp.total > 0 ? c : 0;
   return pp;
 }
@@ -185,6 +185,71 @@ __device__ __forceinline__ int row_segments(const DecodeParams& p, const PagePar
   const int64_t a = sealed_prefix(p, b, lane) * p.num_kv_heads + (int64_t)h * n;
   if (n == 0) return 0;
   return (int)(owner_cta(pp, a + n - 1) - owner_cta(pp, a) + 1);
+}
+
+// Segment walk over a CTA's range: a maximal run of pages of one row.
+struct Walk {
+  int b, h, j, n;    // row (sequence b, kv head h), first page j of the segment, sealed pages n
+  int slot;          // split the segment's partial goes to
+  int64_t left;      // pages of the range from this segment on
+  __device__ int count() const { return (int)min((int64_t)(n - j), left); }
+  // next segment: the next row with sealed pages (slot 0, page 0)
+  __device__ void next(const DecodeParams& p) {
+    left -= count();
+    if (left <= 0) return;
+    j = 0;
+    slot = 0;
+    for (;;) {
+      if (++h == p.num_kv_heads) {
+        h = 0;
+        ++b;
+      }
+      if (b >= p.batch) {  // unreachable while the lengths match the partition
+        left = 0;
+        return;
+      }
+      n = sealed_pages(p, b);
+      if (n > 0) return;
+      h = p.num_kv_heads - 1;  // skip the whole sequence
+    }
+  }
+};
+
+// Warp-collective: the walk of CTA c's range (left = 0 when the CTA has no pages).
+__device__ __forceinline__ Walk range_walk(const DecodeParams& p, int64_t c, int lane) {
+  const PagePartition pp = page_partition(p, lane);
+  Walk w;
+  w.b = w.h = w.j = w.n = w.slot = 0;
+  w.left = 0;
+  if (c >= pp.ctas) return w;
+  const int64_t x0 = range_start(pp, c);
+  // the row holding global page x0: scan the sequences 32 at a time
+  long long cum = 0;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int bb = b0 + lane;
+    const int n = bb < p.batch ? sealed_pages(p, bb) : 0;
+    long long incl = (long long)n * p.num_kv_heads;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const long long o = __shfl_up_sync(0xffffffffu, incl, m);
+      if (lane >= m) incl += o;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, cum + incl > x0);
+    if (hit != 0u) {
+      const int l = __ffs(hit) - 1;
+      const int nb = __shfl_sync(0xffffffffu, n, l);
+      const long long excl = cum + __shfl_sync(0xffffffffu, incl, l) - (long long)nb * p.num_kv_heads;
+      w.b = b0 + l;
+      w.n = nb;
+      w.h = (int)((x0 - excl) / nb);
+      w.j = (int)((x0 - excl) - (long long)w.h * nb);
+      w.slot = (int)(c - owner_cta(pp, x0 - w.j));
+      w.left = range_start(pp, c + 1) - x0;
+      return w;
+    }
+    cum += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return w;
 }
 
 }  // namespace kvarn

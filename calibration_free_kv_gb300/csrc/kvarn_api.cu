@@ -223,13 +223,18 @@ int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const 
 
 extern "C" {
 
-// KVARN_DECODE_KERNEL=tc in the environment runs GQA-8 decode (head_dim 128, K4V2) on the
-// tcgen05 kernel instead of the mma.sync kernel, which is faster on this shape; read on every
-// call.
-static bool decode_tc_requested() {
+// KVARN_DECODE_KERNEL in the environment (read on every call) picks the decode kernels for
+// comparing them: "tc" runs GQA-8 decode (head_dim 128, K4V2) on the tcgen05 kernel, "split" the
+// mma.sync kernel with one CTA per split of 32 or more pages, "persistent" the mma.sync kernel as
+// persistent CTAs over a balanced partition of the sealed pages.  By default GQA 8 runs
+// persistent (its rows are long; no tail of short splits) and smaller groups split (on mixed
+// lengths the hardware's CTA scheduling balances the splits, and the raw partial tiles run as
+// CTAs of their own beside them).
+static bool decode_kernel_env(const char* name) {
   const char* v = std::getenv("KVARN_DECODE_KERNEL");
-  return v != nullptr && std::strcmp(v, "tc") == 0;
+  return v != nullptr && std::strcmp(v, name) == 0;
 }
+static bool decode_tc_requested() { return decode_kernel_env("tc"); }
 
 static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
                          const void* page_pool, int64_t num_pool_pages, const int32_t* block_table,
@@ -271,9 +276,13 @@ static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, con
   p.vgroups = 1;
   p.status = dev_status;
   if (decode_tc_requested() && decode_tc_serves(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p)) {
-    p.tc_ctas = decode_tc_ctas();
-    if (p.tc_ctas < 1) return KVARN_ERR_CUDA;
+    p.part_mode = 3;
+    p.part_ctas = decode_tc_ctas();
+  } else if (decode_kernel_env("persistent") || (nt == 2 && !decode_kernel_env("split"))) {
+    p.part_mode = 1;
+    p.part_ctas = decode_persistent_ctas(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits);
   }
+  if (p.part_mode != 0 && p.part_ctas < 1) return KVARN_ERR_CUDA;
   return launch_decode_any(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p,
                            static_cast<cudaStream_t>(stream), phases);
 }

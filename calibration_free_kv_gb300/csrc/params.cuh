@@ -62,10 +62,14 @@ struct DecodeParams {
   const __half* chunk_k;
   const __half* chunk_v;
   int32_t* status;
-  // tcgen05 decode (decode_tc.cu): 0, or the CTAs its balanced page partition is cut for.  When
-  // set, the sealed pages' partials of row (b, kv head) fill splits [0, row_segments) and
-  // decode_kernel, launched over (1, Hkv, batch), writes only the partial tile's split after them.
-  int tc_ctas;
+  // Persistent decode (decode_kernel with part_mode 1, or decode_tc.cu): 0, or the CTAs the
+  // balanced page partition of the sealed pages is cut for (decode_util.cuh).  When set, the
+  // sealed pages' partials of row (b, kv head) fill splits [0, row_segments) and decode_kernel
+  // with part_mode 2, launched over (1, Hkv, batch), writes the partial tile's split after them.
+  int part_ctas;
+  int part_mode;  // 0: one CTA per split (grid splits x Hkv*vgroups x batch); 1: persistent
+                  // CTAs over the partition's sealed pages; 2: partial tiles only; 3: the
+                  // tcgen05 kernel over the sealed pages
 };
 
 struct DequantParams {
@@ -111,6 +115,8 @@ int decode_tc_ctas();
 int launch_decode_tc(const DecodeParams& p, int phases, cudaStream_t stream);
 // decode_kernel<128, 2, 4, 2> over (1, Hkv, batch) for the partial tiles of a tcgen05 launch
 int launch_decode_partial_tiles(const DecodeParams& p, cudaStream_t stream);
+// CTAs of the persistent mma.sync decode for this shape (SMs x CTAs per SM), 0 on error.
+int decode_persistent_ctas(int d, int nt, int kb, int vb);
 int launch_decode_combine(int d, const DecodeParams& p, cudaStream_t stream);
 int launch_dequant_any(int d, int kb, int vb, const DequantParams& p, int num_pages, cudaStream_t stream);
 

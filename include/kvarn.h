@@ -160,9 +160,10 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
  * the GPU's SM count) plus the raw partial tile's; the tcgen05 kernel of GQA groups of 8 (head_dim
  * 128, K4V2) cuts all sealed pages of the batch into ranges of equal size, one per SM and each
  * at least 32 pages, so that a row's pages fall in at most ceil(n / 32) + 1 ranges.  Needs no
- * GPU.  Setting KVARN_DECODE_KERNEL=tc in the environment runs GQA-8 decode at head_dim 128, K4V2
- * on the tcgen05 kernel (read on every call); by default it runs on the mma.sync kernel, which
- * is faster on that shape. */
+ * GPU.  KVARN_DECODE_KERNEL in the environment (read on every call) picks the decode kernels:
+ * "split" (one CTA per split of 32 or more pages), "persistent" (CTAs over equal ranges of all
+ * sealed pages, at least 32 each), "tc" (GQA 8, head_dim 128, K4V2: the tcgen05 kernel, over the
+ * same ranges); by default GQA 8 runs persistent and smaller groups split. */
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
                                     int max_pages);
 

@@ -147,19 +147,17 @@ def test_decode_parity_ragged(kv, d0, group):
     print("d0=%d G=%d max scaled err %.2e" % (d0, group, err))
 
 
-@pytest.mark.parametrize("kernel", ["tc", "mma"])
-def test_decode_g8_partition(kv, kernel, monkeypatch):
-    # KVARN_DECODE_KERNEL=tc runs GQA 8 at head_dim 128 on the tcgen05 kernel, which cuts the
-    # batch's sealed pages into equal ranges of at least 32 pages: here 316 pages over 9 ranges,
-    # so rows split across CTAs (up to three segments), some rows have no sealed page, and raw
-    # partial tiles follow.  The default (mma.sync kernel) runs the same case.
-    if kernel == "tc":
-        monkeypatch.setenv("KVARN_DECODE_KERNEL", "tc")
-    else:
-        monkeypatch.delenv("KVARN_DECODE_KERNEL", raising=False)
+@pytest.mark.parametrize("group,kernel", [(8, "tc"), (8, "persistent"), (8, "split"), (4, "persistent"),
+                                          (4, "split"), (2, "persistent")])
+def test_decode_partition(kv, group, kernel, monkeypatch):
+    # The persistent kernels (mma.sync "persistent", tcgen05 "tc") cut the batch's sealed pages
+    # into equal ranges of at least 32 pages: here 316 pages over 9 ranges, so rows split across
+    # CTAs (up to three segments), some rows have no sealed page, and raw partial tiles follow;
+    # "split" runs one CTA per split.  KVARN_DECODE_KERNEL selects the kernel.
+    monkeypatch.setenv("KVARN_DECODE_KERNEL", kernel)
     seq_lens = [0, 5 * 128, 129, 40 * 128 + 17, 128, 64 * 128, 3, 33 * 128, 1000, 7 * 128 + 127]
-    err = _run_oracle_cache_case(kv, len(seq_lens), 2, 8, 128, seq_lens, seed=808)
-    print("G=8 partition (%s) max scaled err %.2e" % (kernel, err))
+    err = _run_oracle_cache_case(kv, len(seq_lens), 2, group, 128, seq_lens, seed=808)
+    print("G=%d partition (%s) max scaled err %.2e" % (group, kernel, err))
 
 
 def test_decode_gpu_quantised_cache(kv):
@@ -270,16 +268,16 @@ def test_decode_full_size_sampled(kv):
         print("full size b=%d (L=%d) h=%d: max scaled err %.2e" % (b, L, h, err))
 
 
-@pytest.mark.parametrize("kernel", ["mma", "tc"])
+@pytest.mark.parametrize("kernel", ["default", "tc", "split"])
 def test_decode_32b_layer_sampled(kv, kernel, monkeypatch):
     # one layer of the 32B-class decode step: batch 32 at 16384 tokens, 64 query heads over
     # 8 KV heads (GQA 8), head_dim 128, permuted block table, GPU-quantised cache; three
     # sampled (sequence, kv head) caches are replaced by oracle records and compared; on the
-    # mma.sync kernel (default) and on the tcgen05 kernel (KVARN_DECODE_KERNEL=tc)
-    if kernel == "tc":
-        monkeypatch.setenv("KVARN_DECODE_KERNEL", "tc")
-    else:
+    # default kernel (persistent mma.sync), the tcgen05 kernel and the one-CTA-per-split form
+    if kernel == "default":
         monkeypatch.delenv("KVARN_DECODE_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("KVARN_DECODE_KERNEL", kernel)
     hkv, group, d0, batch, L = 8, 8, 128, 32, 16384
     pages = L // 128
     g = torch.Generator().manual_seed(4)
@@ -333,13 +331,11 @@ def test_bounded_wait_times_out_and_the_context_stays_usable(kv):
     print("wait gave up after %.2f s; decode afterwards: max scaled err %.2e" % (waited, err))
 
 
-@pytest.mark.parametrize("group,kernel", [(4, "mma"), (8, "mma"), (8, "tc")])
+@pytest.mark.parametrize("group,kernel", [(4, "split"), (4, "persistent"), (8, "persistent"), (8, "split"),
+                                          (8, "tc")])
 def test_two_phase_decode_matches_one_call(kv, group, kernel, monkeypatch):
     # kvarn_decode_partials then kvarn_decode_combine give the bytes of kvarn_decode_attention
-    if kernel == "tc":
-        monkeypatch.setenv("KVARN_DECODE_KERNEL", "tc")
-    else:
-        monkeypatch.delenv("KVARN_DECODE_KERNEL", raising=False)
+    monkeypatch.setenv("KVARN_DECODE_KERNEL", kernel)
     hkv, d0 = 2, 128
     lens = [0, 5, 128, 700, 4096 + 77]
     seqs, table, n_pool, q = _build_case(len(lens), hkv, group, d0, lens, seed=77)
