@@ -252,10 +252,19 @@ def _workload_config(lens_before, steps):
 
 
 def _decode_bytes(lens, rec_bytes):
-    """Algorithmic bytes of one decode launch: packed pages + partial fp16 tokens + q + out."""
+    """Algorithmic bytes of one decode call: packed pages + raw fp16 tokens of the open tiles + q +
+    out."""
     sealed = sum(int(L) // 128 for L in lens)
     part = sum(int(L) % 128 for L in lens)
     return (sealed * HKV * rec_bytes + part * HKV * D0 * 2 * 2 + 2 * BATCH * HQ * D0 * 2)
+
+
+def _decode_kernel_bytes(lens, rec_bytes):
+    """Algorithmic bytes of decode_kernel alone (kvarn_decode_partials): the packed pages and q.
+    The raw tokens of the open tiles and the output belong to the merge kernel, which attends to
+    the open tiles itself."""
+    sealed = sum(int(L) // 128 for L in lens)
+    return sealed * HKV * rec_bytes + BATCH * HQ * D0 * 2
 
 
 def _time_quantize(torch, kv, synth, dev, stream, preset="kvarn_k4v2_g128", reps=20, tol=None, d0=D0):
@@ -646,13 +655,13 @@ def _time_long_stream(torch, kv, synth, d0, peak, steps=512, batch=4, hq=32, hkv
         L = starts + i + 1                          # lengths the step's decode attends to
         sealed = int((L // 128).sum())
         part = int((L % 128).sum())
-        db = sealed * hkv * rec + part * hkv * d0 * 2 * 2 + 2 * batch * hq * d0 * 2
+        db = sealed * hkv * rec + part * hkv * d0 * 2 * 2 + 2 * batch * hq * d0 * 2  # the call
         n_seal = int(((starts + i) % 128 == 127).sum())   # tiles that fill in this step's append
         seals += n_seal
         ab = 2 * new_tok + n_seal * hkv * (2 * 128 * d0 * 2 + rec)  # read + write the token; seal
         step_bytes += db + ab
         if i % every == 0:
-            dec_bytes.append(db)
+            dec_bytes.append(sealed * hkv * rec + batch * hq * d0 * 2)  # decode_kernel: pages + q
     dec_gbs = statistics.mean(dec_bytes) / (statistics.mean(dec_ms) * 1e-3) / 1e9
     step_gbs = step_bytes / (total_ms * 1e-3) / 1e9
     del pool, ws
@@ -781,7 +790,8 @@ def _run_kvarn(args, torch, world, rank):
 
     # attended tokens per step: lengths after each step's append
     tokens = sum(int(lens_before.sum()) + BATCH * (i + 1) for i in range(args.steps))
-    dec_bytes = [_decode_bytes((lens_before + i + 1).tolist(), S["rec_bytes"]) for i in sampled]
+    dec_bytes = [_decode_kernel_bytes((lens_before + i + 1).tolist(), S["rec_bytes"]) for i in sampled]
+    call_bytes = [_decode_bytes((lens_before + i + 1).tolist(), S["rec_bytes"]) for i in sampled]
     peak, peak_kind = _peaks()
     avg_dec = statistics.mean(dec_ms)
     avg_call = statistics.mean(call_ms)
@@ -897,9 +907,12 @@ def _run_kvarn(args, torch, world, rank):
         "decode_hbm_gbs": achieved,
         "decode_us": avg_dec * 1e3,
         "decode_call": {"us": avg_call * 1e3,
-                        "hbm_gbs": statistics.mean(dec_bytes) / (avg_call * 1e-3) / 1e9,
+                        "algorithmic_bytes": statistics.mean(call_bytes),
+                        "hbm_gbs": statistics.mean(call_bytes) / (avg_call * 1e-3) / 1e9,
+                        "frac": statistics.mean(call_bytes) / (avg_call * 1e-3) / 1e9 / peak,
                         "note": "kvarn_decode_attention as a whole: decode_kernel + combine_kernel "
-                                "(the merge of the splits and the inverse rotation)"},
+                                "(the raw open tiles, the merge of the splits and the inverse "
+                                "rotation)"},
         "roofline": {
             "kernel": "decode_kernel (kvarn_decode_partials)",
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

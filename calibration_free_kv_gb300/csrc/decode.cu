@@ -1009,7 +1009,8 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       for (int bb = threadIdx.x; bb < p.batch; bb += blockDim.x) {
         const int lb = p.seq_lens[bb];
         if (lb < 0 || lb > cap) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
-        else if (lb % kTile != 0 && p.partial_k == nullptr) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
+        else if (lb % kTile != 0 && p.partial_k == nullptr && p.partial_in_merge == 0)
+          flag_error(p.status, KVARN_DEV_NO_PARTIAL);
       }
     }
     __syncthreads();
@@ -1021,9 +1022,9 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       sealed_run(w.j, w.count(), w.slot, pc, init);
       init = false;
     }
-    // raw partial tiles: row k = b * Hkv + h goes to CTA k mod gridDim.x, its split after the
-    // row's sealed segments
-    for (int k = blockIdx.x; k < p.batch * p.num_kv_heads; k += gridDim.x) {
+    // raw partial tiles (unless the merge takes them): row k = b * Hkv + h goes to CTA k mod
+    // gridDim.x, its split after the row's sealed segments
+    for (int k = blockIdx.x; p.partial_in_merge == 0 && k < p.batch * p.num_kv_heads; k += gridDim.x) {
       b = k / p.num_kv_heads;
       h = k - b * p.num_kv_heads;
       int lb = p.seq_lens[b];
@@ -1046,7 +1047,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     n_ss = tc_row_segments(p, b, h, lane);
     split = n_ss;
   }
-  const bool partial_split = (split == n_ss) && n_part > 0;
+  const bool partial_split = (split == n_ss) && n_part > 0 && p.partial_in_merge == 0;
   if (split >= n_ss && !partial_split) return;
   if (partial_split && (p.partial_k == nullptr || p.partial_v == nullptr)) {
     if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
@@ -1062,33 +1063,189 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
 }
 
 
-// One warp per (sequence, chunk token, query head): merge the splits, normalise, undo the
-// rotation.
+// Attention of one query (E = D/32 channels per lane, original basis, times tau log2(e)) to
+// n_tok raw fp16 tokens whose rows start at k_row / v_row (this lane's channels; row stride
+// rstride): online softmax in the log2 domain, unnormalised output o in the original basis.
+// 32 tokens at a time: each lane sums its channels for 32 tokens, a halving shuffle butterfly
+// leaves token t0 + i's logit complete in lane i.
 template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+__device__ __forceinline__ void raw_attend(const float (&q)[D / 32], const __half* k_row, const __half* v_row,
+                                           int64_t rstride, int n_tok, bool in, int lane, float& m, float& l,
+                                           float (&o)[D / 32]) {
+  constexpr int E = D / 32;
+  for (int t0 = 0; t0 < n_tok; t0 += 32) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float kf[E];
+      if (t0 + i < n_tok && in) {
+        load_f16<E>(k_row + (t0 + i) * rstride, kf);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) kf[e] = 0.0f;
+      }
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc = fmaf(q[e], kf[e], acc);
+      v[i] = acc;
+    }
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {
+      const bool up = (lane & w) != 0;
+#pragma unroll
+      for (int i = 0; i < w; ++i) {
+        const float send = up ? v[i] : v[i + w];
+        const float keep = up ? v[i + w] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+      }
+    }
+    const bool live = t0 + lane < n_tok;
+    float mx = live ? v[0] : -INFINITY;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
+    const float mnew = fmaxf(m, mx);
+    const float a = exp2f(m - mnew);
+    const float pv = live ? exp2f(v[0] - mnew) : 0.0f;
+    float ps = pv;
+#pragma unroll
+    for (int msk = 16; msk > 0; msk >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, msk);
+    m = mnew;
+    l = fmaf(l, a, ps);
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[e] *= a;
+    // PV eight tokens at a time, their eight row loads issued before the first use
+    const int cnt = min(32, n_tok - t0);
+    for (int i0 = 0; i0 < cnt; i0 += 8) {
+      float vf[8][E];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (in && i0 + i < cnt) {
+          load_f16<E>(v_row + (t0 + i0 + i) * rstride, vf[i]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) vf[i][e] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float pw = __shfl_sync(0xffffffffu, pv, (i0 + i) & 31);  // 0 past the last token
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = fmaf(pw, vf[i][e], o[e]);
+      }
+    }
+  }
+}
+
+// One warp per (sequence, chunk token, query head): merge the splits, normalise, undo the
+// rotation.  When p.partial_in_merge is set (decode), the warp also attends to the sequence's raw
+// partial tile itself, before waiting for the splits (the tile does not depend on them): its
+// output is in the original basis and joins after the inverse rotation [vatt §四個步驟: R is
+// orthonormal and symmetric, so R (sum_s w_s o~_s) + w_p o_p is the merged output].
+// RAW (decode with p.partial_in_merge): one CTA per (sequence, kv head), four warps per query
+// head of the group; the CTA brings the row's raw partial tile into shared memory with two bulk
+// copies, warp (head w, quarter t) attends to tokens 32t..32t+31 there, the quarters meet in
+// shared memory and the head's first warp goes on to the merge.  Otherwise four warps per CTA
+// over (sequence, chunk token, query head), and any partial tile is a split of its own.
+constexpr int kRawQuarters = 4;  // 32-token quarters of a raw partial tile
+template <int D, bool RAW>
+__global__ void __launch_bounds__(RAW ? 1024 : 128) combine_kernel(DecodeParams p) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int wi = threadIdx.x >> 5;
+  const int wq = RAW ? wi / p.group : 0;  // RAW: the warp's token quarter
+  const int gw = RAW ? (blockIdx.x / p.num_kv_heads) * p.num_q_heads + (blockIdx.x % p.num_kv_heads) * p.group +
+                           wi % p.group
+                     : blockIdx.x * (blockDim.x / 32) + wi;
   const bool live = gw < p.batch * p.chunk * p.num_q_heads;
   const int b = gw / (p.chunk * p.num_q_heads);
+  const int hq = gw % p.num_q_heads, h = hq / p.group;
   const int cap = p.max_pages * kTile + (kTile - 1);
-  // The lengths come from before decode_kernel, which waited for their writer before it let
-  // this kernel start: they can be read ahead of the wait for the split partials.
+  // The lengths and the raw partial tiles come from before decode_kernel, which waited for their
+  // writer before it let this kernel start: they can be read ahead of the wait for the splits.
   int len = live ? p.seq_lens[b] : 0;
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int n_part = len % kTile;
+  float mp = -INFINITY, lp = 0.0f, op[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) op[e] = 0.0f;
+  bool has_part = false;
+  if constexpr (RAW) {
+    // every warp of the CTA shares (b, h) and so n_part
+    extern __shared__ __align__(128) uint8_t raw_s[];  // K rows [0, 128 d0), V rows after them,
+                                                       // then the quarters' (m, l, o) per head
+    __shared__ __align__(8) uint64_t raw_bar;
+    has_part = n_part > 0 && p.partial_k != nullptr && p.partial_v != nullptr;
+    if (n_part > 0 && !has_part && threadIdx.x == 0) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
+    if (has_part) {
+      if (threadIdx.x == 0) {
+        const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
+        const uint32_t bytes = (uint32_t)(n_part * p.d0 * 2);  // a multiple of 16
+        mbar_init(&raw_bar, 1);
+        fence_mbar_init();
+        mbar_expect_tx(&raw_bar, 2 * bytes);
+        bulk_copy_g2s(raw_s, p.partial_k + base, bytes, &raw_bar);
+        bulk_copy_g2s(raw_s + kTile * p.d0 * 2, p.partial_v + base, bytes, &raw_bar);
+      }
+      const int c0 = lane * E;
+      const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
+      float q[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) q[e] = in ? __half2float(p.q[(int64_t)gw * p.d0 + c0 + e]) * p.qscale : 0.0f;
+      __syncthreads();  // the barrier is initialised
+      const bool landed = mbar_wait(&raw_bar, 0);
+      const int t0 = 32 * wq, nt = min(32, n_part - t0);
+      if (landed && nt > 0) {
+        const __half* ks = reinterpret_cast<const __half*>(raw_s) + (int64_t)t0 * p.d0 + c0;
+        raw_attend<D>(q, ks, ks + kTile * p.d0, p.d0, nt, in, lane, mp, lp, op);
+      }
+      // the head's quarters meet: (m, l) then o, per (quarter, head slot)
+      float* qm = reinterpret_cast<float*>(raw_s + 2 * kTile * D * 2);
+      float* ql = qm + kRawQuarters * p.group;
+      float* qo = ql + kRawQuarters * p.group;
+      const int slot = wq * p.group + wi % p.group;
+      if (lane == 0) {
+        qm[slot] = mp;
+        ql[slot] = lp;
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) qo[slot * D + lane * E + e] = op[e];
+      if (!__syncthreads_and(landed ? 1 : 0)) {
+        if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
+        has_part = false;
+      } else if (wq == 0) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kRawQuarters; ++k) M = fmaxf(M, qm[k * p.group + slot]);
+        lp = 0.0f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) op[e] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kRawQuarters; ++k) {
+          const float mk = qm[k * p.group + slot];
+          const float w = mk > -INFINITY ? exp2f(mk - M) : 0.0f;  // quarters past n_part are empty
+          lp = fmaf(w, ql[k * p.group + slot], lp);
+#pragma unroll
+          for (int e = 0; e < E; ++e) op[e] = fmaf(w, qo[(k * p.group + slot) * D + lane * E + e], op[e]);
+        }
+        mp = M;
+      }
+    }
+    if (wq != 0) return;  // the head's first warp merges
+  }
   grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
   grid_launch_dependents();  // the next kernel (say, the next step's append) may start arriving
   if (!live) return;
-  len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_sealed = len / kTile;
-  const int n_cache = p.part_ctas > 0 ? tc_row_segments(p, b, (gw % p.num_q_heads) / p.group, lane)
+  const int n_cache = p.part_ctas > 0 ? tc_row_segments(p, b, h, lane)
                                     : (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
-  const int n_splits = n_cache + (len % kTile > 0 ? 1 : 0) + (p.chunk_k != nullptr ? 1 : 0);
+  const int n_splits = n_cache + (n_part > 0 && p.partial_in_merge == 0 ? 1 : 0) + (p.chunk_k != nullptr ? 1 : 0);
+  const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
   float v[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) v[e] = 0.0f;
+  float M = mp, lsum = 0.0f;  // over the splits and the raw tile
   if (n_splits > 0 && n_splits <= 4) {
     // up to four splits (the common case): every load issued before the first use
-    const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
     float2 ml[4];
     float o[4][E];
 #pragma unroll
@@ -1102,8 +1259,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
         for (int e = 0; e < E; ++e) o[s][e] = 0.0f;
       }
     }
-    const float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
-    float lsum = 0.0f;
+    M = fmaxf(M, fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x)));
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const float w = s < n_splits ? exp2f(ml[s].x - M) : 0.0f;
@@ -1111,21 +1267,17 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
 #pragma unroll
       for (int e = 0; e < E; ++e) v[e] = fmaf(w, o[s][e], v[e]);
     }
-    const float inv = inv_sqrt_d<D>() / lsum;
-    warp_fwht<D>(v, lane);
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] *= inv;
   } else if (n_splits > 0 && n_splits <= 32) {
     // up to 32 splits: (m, l) one split per lane in one load, then the partial outputs eight
     // splits at a time with all eight loads issued before their use
-    const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
     const bool mine = lane < n_splits;
     const float2 ml = mine ? *reinterpret_cast<const float2*>(base + lane * (D + 4)) : make_float2(-INFINITY, 0.0f);
-    float M = ml.x;
+    float Ms = ml.x;
 #pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
+    for (int msk = 16; msk > 0; msk >>= 1) Ms = fmaxf(Ms, __shfl_xor_sync(0xffffffffu, Ms, msk));
+    M = fmaxf(M, Ms);
     const float w = mine ? exp2f(ml.x - M) : 0.0f;
-    float lsum = w * ml.y;
+    lsum = w * ml.y;
 #pragma unroll
     for (int msk = 16; msk > 0; msk >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, msk);
     for (int s0 = 0; s0 < n_splits; s0 += 8) {
@@ -1146,14 +1298,8 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
         for (int e = 0; e < E; ++e) v[e] = fmaf(wj, o[j][e], v[e]);
       }
     }
-    const float inv = inv_sqrt_d<D>() / lsum;
-    warp_fwht<D>(v, lane);
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] *= inv;
   } else if (n_splits > 0) {
-    const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
     // split statistics, one split per lane, 32 per pass
-    float M = -INFINITY;
     for (int s0 = 0; s0 < n_splits; s0 += 32) {
       const int s = s0 + lane;
       float m = s < n_splits ? base[s * (D + 4)] : -INFINITY;
@@ -1161,7 +1307,6 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
       for (int msk = 16; msk > 0; msk >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, msk));
       M = fmaxf(M, m);
     }
-    float lsum = 0.0f;
     for (int s0 = 0; s0 < n_splits; s0 += 32) {
       const int s = s0 + lane;
       const float w = s < n_splits ? exp2f(base[s * (D + 4)] - M) : 0.0f;
@@ -1182,11 +1327,14 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
         }
       }
     }
-    const float inv = inv_sqrt_d<D>() / lsum;
-    warp_fwht<D>(v, lane);
-#pragma unroll
-    for (int e = 0; e < E; ++e) v[e] *= inv;
   }
+  // the raw tile joins after the inverse rotation of the splits' sum
+  const float wp = has_part ? exp2f(mp - M) : 0.0f;
+  lsum = fmaf(wp, lp, lsum);
+  if (n_splits > 0) warp_fwht<D>(v, lane);
+  const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = fmaf(v[e], inv_sqrt_d<D>(), wp * op[e]) * inv;
   __half* dst = p.out + (int64_t)gw * p.d0;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -1220,7 +1368,8 @@ static int launch_decode_t(const DecodeParams& p, int phases, cudaStream_t strea
     } else {
       // the sealed splits at this split size plus the partial tile's (the workspace stride
       // max_splits is laid out for the smallest size and may be larger)
-      const int splits = min(p.max_splits, (p.max_pages + p.pages_per_split - 1) / p.pages_per_split + 1);
+      const int splits = min(p.max_splits, (p.max_pages + p.pages_per_split - 1) / p.pages_per_split +
+                                               (p.partial_in_merge != 0 ? 0 : 1));
       cfg.gridDim = dim3(splits, p.num_kv_heads * p.vgroups, p.batch);
       if (cudaLaunchKernelEx(&cfg, decode_kernel<D, NT, KB, VB>, p) != cudaSuccess) return KVARN_ERR_CUDA;
     }
@@ -1235,13 +1384,25 @@ static int launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  const int warps = p.batch * p.chunk * p.num_q_heads;
-  cfg.gridDim = dim3((warps + 3) / 4);
-  cfg.blockDim = dim3(128);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<D>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  if (p.partial_in_merge != 0 && p.chunk == 1) {
+    // one CTA per (sequence, kv head), the raw partial tile in shared memory
+    // raw K and V rows, then (m, l, o) of each quarter of each head slot (up to 8)
+    constexpr int kRawSmem = 2 * kTile * D * 2 + kRawQuarters * 8 * (D + 2) * 4;
+    static PerDeviceOnce smem_once;
+    const void* fn = reinterpret_cast<const void*>(combine_kernel<D, true>);
+    if (const int st = set_smem_limit(smem_once, fn, kRawSmem); st != KVARN_OK) return st;
+    cfg.gridDim = dim3(p.batch * p.num_kv_heads);
+    cfg.blockDim = dim3(32 * p.group * kRawQuarters);
+    cfg.dynamicSmemBytes = kRawSmem;
+    return cudaLaunchKernelEx(&cfg, combine_kernel<D, true>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  }
+  const int warps = p.batch * p.chunk * p.num_q_heads;
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
 int launch_decode_combine(int d, const DecodeParams& p, cudaStream_t stream) {
@@ -1329,60 +1490,7 @@ __global__ void __launch_bounds__(128) chunk_kernel(DecodeParams p) {
   const int64_t rstride = (int64_t)p.num_kv_heads * p.d0;
   const __half* kbase = p.chunk_k + ((int64_t)b * p.chunk * p.num_kv_heads + h) * p.d0 + c0;
   const __half* vbase = p.chunk_v + ((int64_t)b * p.chunk * p.num_kv_heads + h) * p.d0 + c0;
-  for (int t0 = 0; t0 < n_tok; t0 += 32) {
-    // logits of tokens t0 + i: each lane sums its channels for 32 tokens, a halving shuffle
-    // butterfly leaves token t0 + i complete in lane i
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float kf[E];
-      if (t0 + i < n_tok && in) {
-        load_f16<E>(kbase + (t0 + i) * rstride, kf);
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) kf[e] = 0.0f;
-      }
-      float acc = 0.0f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc = fmaf(q[e], kf[e], acc);
-      v[i] = acc;
-    }
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-      const bool up = (lane & w) != 0;
-#pragma unroll
-      for (int i = 0; i < w; ++i) {
-        const float send = up ? v[i] : v[i + w];
-        const float keep = up ? v[i + w] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-      }
-    }
-    const bool live = t0 + lane < n_tok;
-    float mx = live ? v[0] : -INFINITY;
-#pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, msk));
-    const float mnew = fmaxf(m, mx);
-    const float a = exp2f(m - mnew);
-    const float pv = live ? exp2f(v[0] - mnew) : 0.0f;
-    float ps = pv;
-#pragma unroll
-    for (int msk = 16; msk > 0; msk >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, msk);
-    m = mnew;
-    l = fmaf(l, a, ps);
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[e] *= a;
-    const int cnt = min(32, n_tok - t0);
-#pragma unroll 8
-    for (int i = 0; i < cnt; ++i) {
-      const float pw = __shfl_sync(0xffffffffu, pv, i);
-      if (in) {
-        float vf[E];
-        load_f16<E>(vbase + (t0 + i) * rstride, vf);
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = fmaf(pw, vf[e], o[e]);
-      }
-    }
-  }
+  raw_attend<D>(q, kbase, vbase, rstride, n_tok, in, lane, m, l, o);
   warp_fwht<D>(o, lane);
   const int cap = p.max_pages * kTile + (kTile - 1);
   int len = p.seq_lens[b];

@@ -713,7 +713,7 @@ int launch_decode_tc(const DecodeParams& p, int phases, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, decode_tc_kernel, p) != cudaSuccess) return KVARN_ERR_CUDA;
-    if (p.partial_k != nullptr) {
+    if (p.partial_k != nullptr && p.partial_in_merge == 0) {
       if (const int st = launch_decode_partial_tiles(p, stream); st != KVARN_OK) return st;
     }
   }

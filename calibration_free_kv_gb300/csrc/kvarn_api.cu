@@ -223,17 +223,18 @@ int decode_args_check(const kvarn_desc* desc, int batch, int num_q_heads, const 
 
 extern "C" {
 
-// KVARN_DECODE_KERNEL in the environment (read on every call) picks the decode kernels for
-// comparing them: "tc" runs GQA-8 decode (head_dim 128, K4V2) on the tcgen05 kernel, "split" the
-// mma.sync kernel with one CTA per split of 32 or more pages, "persistent" the mma.sync kernel as
-// persistent CTAs over a balanced partition of the sealed pages.  By default GQA 8 runs
-// persistent (its rows are long; no tail of short splits) and smaller groups split (on mixed
-// lengths the hardware's CTA scheduling balances the splits, and the raw partial tiles run as
-// CTAs of their own beside them).
-static bool decode_kernel_env(const char* name) {
-  const char* v = std::getenv("KVARN_DECODE_KERNEL");
-  return v != nullptr && std::strcmp(v, name) == 0;
+// The decode kernels, chosen for comparing them through the environment (read on every call):
+// KVARN_DECODE_KERNEL "split" runs the mma.sync kernel with one CTA per split of 32 or more
+// pages, "tc" GQA-8 decode (head_dim 128, K4V2) on the tcgen05 kernel; by default the mma.sync
+// kernel runs as persistent CTAs over a balanced partition of the sealed pages (no tail of short
+// splits, one pipeline per CTA).  KVARN_DECODE_OPEN_TILES "split" attends to the raw partial
+// tiles in the decode kernels, as splits of their own; by default the merge kernel attends to
+// them (from shared memory, one CTA per sequence and kv head).
+static bool decode_env(const char* var, const char* value) {
+  const char* v = std::getenv(var);
+  return v != nullptr && std::strcmp(v, value) == 0;
 }
+static bool decode_kernel_env(const char* name) { return decode_env("KVARN_DECODE_KERNEL", name); }
 static bool decode_tc_requested() { return decode_kernel_env("tc"); }
 
 static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, const void* q,
@@ -275,10 +276,11 @@ static int decode_phases(const kvarn_desc* desc, int batch, int num_q_heads, con
   p.chunk = 1;
   p.vgroups = 1;
   p.status = dev_status;
+  p.partial_in_merge = decode_env("KVARN_DECODE_OPEN_TILES", "split") ? 0 : 1;
   if (decode_tc_requested() && decode_tc_serves(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits, p)) {
     p.part_mode = 3;
     p.part_ctas = decode_tc_ctas();
-  } else if (decode_kernel_env("persistent") || (nt == 2 && !decode_kernel_env("split"))) {
+  } else if (!decode_kernel_env("split")) {
     p.part_mode = 1;
     p.part_ctas = decode_persistent_ctas(desc->head_dim_padded, nt, desc->k_bits, desc->v_bits);
   }

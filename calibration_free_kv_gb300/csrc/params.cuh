@@ -67,6 +67,9 @@ struct DecodeParams {
   // sealed pages' partials of row (b, kv head) fill splits [0, row_segments) and decode_kernel
   // with part_mode 2, launched over (1, Hkv, batch), writes the partial tile's split after them.
   int part_ctas;
+  // 1: the merge kernel attends to the raw partial tiles itself (decode); decode_kernel and the
+  // tcgen05 kernel then leave them alone and no split holds them
+  int partial_in_merge;
   int part_mode;  // 0: one CTA per split (grid splits x Hkv*vgroups x batch); 1: persistent
                   // CTAs over the partition's sealed pages; 2: partial tiles only; 3: the
                   // tcgen05 kernel over the sealed pages

@@ -160,10 +160,11 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
  * the GPU's SM count) plus the raw partial tile's; the tcgen05 kernel of GQA groups of 8 (head_dim
  * 128, K4V2) cuts all sealed pages of the batch into ranges of equal size, one per SM and each
  * at least 32 pages, so that a row's pages fall in at most ceil(n / 32) + 1 ranges.  Needs no
- * GPU.  KVARN_DECODE_KERNEL in the environment (read on every call) picks the decode kernels:
- * "split" (one CTA per split of 32 or more pages), "persistent" (CTAs over equal ranges of all
- * sealed pages, at least 32 each), "tc" (GQA 8, head_dim 128, K4V2: the tcgen05 kernel, over the
- * same ranges); by default GQA 8 runs persistent and smaller groups split. */
+ * GPU.  Two environment variables (read on every call) pick the decode kernels for comparing
+ * them: KVARN_DECODE_KERNEL "split" (one CTA per split of 32 or more pages) or "tc" (GQA 8,
+ * head_dim 128, K4V2: the tcgen05 kernel); by default persistent CTAs take equal ranges of all
+ * sealed pages, at least 32 each.  KVARN_DECODE_OPEN_TILES "split" attends to the raw partial
+ * tiles in the decode kernels as splits of their own; by default the merge kernel does. */
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
                                     int max_pages);
 

@@ -147,17 +147,22 @@ def test_decode_parity_ragged(kv, d0, group):
     print("d0=%d G=%d max scaled err %.2e" % (d0, group, err))
 
 
-@pytest.mark.parametrize("group,kernel", [(8, "tc"), (8, "persistent"), (8, "split"), (4, "persistent"),
-                                          (4, "split"), (2, "persistent")])
-def test_decode_partition(kv, group, kernel, monkeypatch):
+@pytest.mark.parametrize("group,kernel,tiles", [(8, "tc", "merge"), (8, "persistent", "merge"),
+                                                (8, "split", "merge"), (4, "persistent", "merge"),
+                                                (4, "split", "merge"), (2, "persistent", "merge"),
+                                                (4, "persistent", "split"), (4, "split", "split"),
+                                                (8, "tc", "split"), (1, "persistent", "merge")])
+def test_decode_partition(kv, group, kernel, tiles, monkeypatch):
     # The persistent kernels (mma.sync "persistent", tcgen05 "tc") cut the batch's sealed pages
     # into equal ranges of at least 32 pages: here 316 pages over 9 ranges, so rows split across
     # CTAs (up to three segments), some rows have no sealed page, and raw partial tiles follow;
-    # "split" runs one CTA per split.  KVARN_DECODE_KERNEL selects the kernel.
+    # "split" runs one CTA per split.  The raw partial tiles are attended by the merge kernel
+    # ("merge") or by the decode kernels as splits of their own ("split").
     monkeypatch.setenv("KVARN_DECODE_KERNEL", kernel)
+    monkeypatch.setenv("KVARN_DECODE_OPEN_TILES", tiles)
     seq_lens = [0, 5 * 128, 129, 40 * 128 + 17, 128, 64 * 128, 3, 33 * 128, 1000, 7 * 128 + 127]
     err = _run_oracle_cache_case(kv, len(seq_lens), 2, group, 128, seq_lens, seed=808)
-    print("G=%d partition (%s) max scaled err %.2e" % (group, kernel, err))
+    print("G=%d partition (%s, open tiles: %s) max scaled err %.2e" % (group, kernel, tiles, err))
 
 
 def test_decode_gpu_quantised_cache(kv):
