@@ -57,8 +57,8 @@ def _peaks():
 # DRAM traffic / algorithmic bytes of one decode_kernel launch, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum at batch 24), valid only for the decode.cu source
 # it was taken on: the traffic is reported as null once that file changes.
-DECODE_TRAFFIC = {"decode_cu_sha256": "ce8ff59a6431249a75bb74c189b3805a8e9aa849594206a4448d1523e6efda8e",
-                  "dram_over_algorithmic": 1.0179}
+DECODE_TRAFFIC = {"decode_cu_sha256": "8daec1178c4ccfc21146f1292f67a8297af9aaeed28a75c2940d9e5385b1bae9",
+                  "dram_over_algorithmic": 1.0208}
 
 
 def _decode_traffic_ratio():
