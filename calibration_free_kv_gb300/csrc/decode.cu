@@ -1141,28 +1141,29 @@ __device__ __forceinline__ void raw_attend(const float (&q)[D / 32], const __hal
 // partial tile itself, before waiting for the splits (the tile does not depend on them): its
 // output is in the original basis and joins after the inverse rotation [vatt §四個步驟: R is
 // orthonormal and symmetric, so R (sum_s w_s o~_s) + w_p o_p is the merged output].
-// RAW (decode with p.partial_in_merge): one CTA per (sequence, kv head), four warps per query
-// head of the group; the CTA brings the row's raw partial tile into shared memory with two bulk
-// copies, warp (head w, quarter t) attends to tokens 32t..32t+31 there, the quarters meet in
-// shared memory and the head's first warp goes on to the merge.  Otherwise four warps per CTA
-// over (sequence, chunk token, query head), and any partial tile is a split of its own.
-constexpr int kRawQuarters = 4;  // 32-token quarters of a raw partial tile
-template <int D, bool RAW>
-__global__ void __launch_bounds__(RAW ? 1024 : 128) combine_kernel(DecodeParams p) {
+// RAW (decode with p.partial_in_merge): one CTA of 8 warps per (sequence, kv head); the row's raw
+// partial tile is staged in shared memory as one fp16 page (K rows 0..127, V rows 128..255,
+// 16-byte chunks XOR-swizzled by row, rows past the tile zero-filled) and attended on the tensor
+// cores: warp w takes tokens 16w..16w+15, QK as mma.sync m16n8k16 with A = K rows by ldmatrix and
+// B = the fp16 queries (heads 4nt + j in column pairs (j, 0)), PV with A = V^T by ldmatrix.trans
+// and B = the probabilities in fp16 hi + lo; the warps meet in shared memory, and warp w < G then
+// merges query head w's splits.  Otherwise four warps per CTA over (sequence, chunk token, query
+// head), and any partial tile is a split of its own.
+template <int D, bool RAW, int NT = 1>
+__global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p) {
   constexpr int E = D / 32;
+  constexpr int NH = 4 * NT;  // RAW: head slots (the group padded to 4 or 8)
   const int lane = threadIdx.x & 31;
   const int wi = threadIdx.x >> 5;
-  const int wq = RAW ? wi / p.group : 0;  // RAW: the warp's token quarter
-  const int gw = RAW ? (blockIdx.x / p.num_kv_heads) * p.num_q_heads + (blockIdx.x % p.num_kv_heads) * p.group +
-                           wi % p.group
+  const int gw = RAW ? (blockIdx.x / p.num_kv_heads) * p.num_q_heads + (blockIdx.x % p.num_kv_heads) * p.group + wi
                      : blockIdx.x * (blockDim.x / 32) + wi;
-  const bool live = gw < p.batch * p.chunk * p.num_q_heads;
-  const int b = gw / (p.chunk * p.num_q_heads);
-  const int hq = gw % p.num_q_heads, h = hq / p.group;
+  const bool live = RAW ? wi < p.group : gw < p.batch * p.chunk * p.num_q_heads;
+  const int b = RAW ? blockIdx.x / p.num_kv_heads : gw / (p.chunk * p.num_q_heads);
+  const int h = RAW ? blockIdx.x % p.num_kv_heads : (gw % p.num_q_heads) / p.group;
   const int cap = p.max_pages * kTile + (kTile - 1);
   // The lengths and the raw partial tiles come from before decode_kernel, which waited for their
   // writer before it let this kernel start: they can be read ahead of the wait for the splits.
-  int len = live ? p.seq_lens[b] : 0;
+  int len = (RAW || live) ? p.seq_lens[b] : 0;
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_part = len % kTile;
   float mp = -INFINITY, lp = 0.0f, op[E];
@@ -1170,67 +1171,138 @@ __global__ void __launch_bounds__(RAW ? 1024 : 128) combine_kernel(DecodeParams 
   for (int e = 0; e < E; ++e) op[e] = 0.0f;
   bool has_part = false;
   if constexpr (RAW) {
-    // every warp of the CTA shares (b, h) and so n_part
-    extern __shared__ __align__(128) uint8_t raw_s[];  // K rows [0, 128 d0), V rows after them,
-                                                       // then the quarters' (m, l, o) per head
-    __shared__ __align__(8) uint64_t raw_bar;
+    extern __shared__ __align__(128) uint8_t raw_s[];  // the page [256][2 D], then q [NH][D]
     has_part = n_part > 0 && p.partial_k != nullptr && p.partial_v != nullptr;
     if (n_part > 0 && !has_part && threadIdx.x == 0) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
     if (has_part) {
-      if (threadIdx.x == 0) {
+      const int g = lane >> 2, tq = lane & 3;
+      const uint32_t sbase = smem_u32(raw_s);
+      __half* qs = reinterpret_cast<__half*>(raw_s + 256 * 2 * D);
+      {
         const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
-        const uint32_t bytes = (uint32_t)(n_part * p.d0 * 2);  // a multiple of 16
-        mbar_init(&raw_bar, 1);
-        fence_mbar_init();
-        mbar_expect_tx(&raw_bar, 2 * bytes);
-        bulk_copy_g2s(raw_s, p.partial_k + base, bytes, &raw_bar);
-        bulk_copy_g2s(raw_s + kTile * p.d0 * 2, p.partial_v + base, bytes, &raw_bar);
+        const int dch = p.d0 / 8;  // 16-byte chunks of a raw row (d0 % 8 == 0)
+        for (int qi = threadIdx.x; qi < 256 * (D / 8); qi += blockDim.x) {
+          const int r = qi / (D / 8), c = qi - r * (D / 8);
+          const int t = r & (kTile - 1);
+          const bool in = t < n_part && c < dch;
+          const __half* src = (r < kTile ? p.partial_k : p.partial_v) + base + (int64_t)t * p.d0 + 8 * c;
+          cp_async_16(sbase + swz_row<D>(r, c), in ? src : p.partial_k, in ? 16u : 0u);
+        }
+        cp_async_commit_all();
       }
-      const int c0 = lane * E;
-      const bool in = c0 < p.d0;  // d0 % 8 == 0: a lane's channels are all inside or all outside
-      float q[E];
+      for (int i = threadIdx.x; i < NH * D; i += blockDim.x) {
+        const int hl = i / D, c = i - hl * D;
+        qs[i] = (hl < p.group && c < p.d0) ? p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + c]
+                                           : __float2half(0.0f);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      const int t0 = 16 * wi;  // this warp's tokens
+      float m[NT], l[NT], o[D / 16][NT][2];
 #pragma unroll
-      for (int e = 0; e < E; ++e) q[e] = in ? __half2float(p.q[(int64_t)gw * p.d0 + c0 + e]) * p.qscale : 0.0f;
-      __syncthreads();  // the barrier is initialised
-      const bool landed = mbar_wait(&raw_bar, 0);
-      const int t0 = 32 * wq, nt = min(32, n_part - t0);
-      if (landed && nt > 0) {
-        const __half* ks = reinterpret_cast<const __half*>(raw_s) + (int64_t)t0 * p.d0 + c0;
-        raw_attend<D>(q, ks, ks + kTile * p.d0, p.d0, nt, in, lane, mp, lp, op);
-      }
-      // the head's quarters meet: (m, l) then o, per (quarter, head slot)
-      float* qm = reinterpret_cast<float*>(raw_s + 2 * kTile * D * 2);
-      float* ql = qm + kRawQuarters * p.group;
-      float* qo = ql + kRawQuarters * p.group;
-      const int slot = wq * p.group + wi % p.group;
-      if (lane == 0) {
-        qm[slot] = mp;
-        ql[slot] = lp;
-      }
+      for (int nt = 0; nt < NT; ++nt) {
+        m[nt] = -INFINITY;
+        l[nt] = 0.0f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) qo[slot * D + lane * E + e] = op[e];
-      if (!__syncthreads_and(landed ? 1 : 0)) {
-        if (threadIdx.x == 0) flag_error(p.status, KVARN_DEV_WAIT_TIMEOUT);
-        has_part = false;
-      } else if (wq == 0) {
+        for (int mc = 0; mc < D / 16; ++mc) o[mc][nt][0] = o[mc][nt][1] = 0.0f;
+      }
+      if (t0 < n_part) {
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.0f;
+        {
+          const int row = t0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            uint32_t a[4];
+            ldsm_x4(sbase + swz_row<D>(row, 2 * kk + (lane >> 4)), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              // B: column 2j = head 4nt + j, column 2j + 1 = 0
+              const __half* qr = qs + (4 * nt + (g >> 1)) * D + 16 * kk + 2 * tq;
+              const bool zero = (g & 1) != 0;
+              const uint32_t b0 = zero ? 0u : *reinterpret_cast<const uint32_t*>(qr);
+              const uint32_t b1 = zero ? 0u : *reinterpret_cast<const uint32_t*>(qr + 8);
+              mma16816(acc[nt], a, b0, b1);
+            }
+          }
+        }
+        const bool v0 = t0 + g < n_part, v1 = t0 + g + 8 < n_part;
+        float pr[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float s0 = v0 ? (acc[nt][0] + acc[nt][1]) * p.qscale : -INFINITY;
+          const float s1 = v1 ? (acc[nt][2] + acc[nt][3]) * p.qscale : -INFINITY;
+          float mx = fmaxf(s0, s1);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          m[nt] = mx;  // finite: token t0 (g = 0) is in the tile
+          pr[nt][0] = exp2f(s0 - mx);
+          pr[nt][1] = exp2f(s1 - mx);
+          l[nt] = pr[nt][0] + pr[nt][1];
+        }
+        uint32_t bw[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const __half2 hi = __floats2half2_rn(pr[nt][0], pr[nt][1]);
+          const float2 hf = __half22float2(hi);
+          const __half2 lo = __floats2half2_rn(pr[nt][0] - hf.x, pr[nt][1] - hf.y);
+          bw[nt][0] = movmatrix_trans(h2u(__lows2half2(hi, lo)));   // (hi, lo) of token row g
+          bw[nt][1] = movmatrix_trans(h2u(__highs2half2(hi, lo)));  // (hi, lo) of token row g + 8
+        }
+        const int row = kTile + t0 + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+        for (int mc = 0; mc < D / 16; ++mc) {
+          uint32_t a[4];
+          ldsm_x4_trans(sbase + swz_row<D>(row, 2 * mc + ((lane >> 3) & 1)), a);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            float pacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma16816(pacc, a, bw[nt][0], bw[nt][1]);
+            o[mc][nt][0] = pacc[0] + pacc[1];
+            o[mc][nt][1] = pacc[2] + pacc[3];
+          }
+        }
+      }
+      // the warps meet: (m, l, o) per (warp, head slot) over the page buffer
+      __syncthreads();
+      float* mS = reinterpret_cast<float*>(raw_s);
+      float* lS = mS + 8 * NH;
+      float* oS = lS + 8 * NH;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float lt = l[nt];
+        lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+        lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+        const int hl = 4 * nt + tq;
+        if (g == 0) {
+          mS[wi * NH + hl] = m[nt];
+          lS[wi * NH + hl] = lt;
+        }
+#pragma unroll
+        for (int mc = 0; mc < D / 16; ++mc) {
+          oS[(wi * NH + hl) * D + 16 * mc + g] = o[mc][nt][0];
+          oS[(wi * NH + hl) * D + 16 * mc + g + 8] = o[mc][nt][1];
+        }
+      }
+      __syncthreads();
+      if (live) {  // warp wi merges head slot wi's eight parts; its lanes hold channels lane*E..
         float M = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < kRawQuarters; ++k) M = fmaxf(M, qm[k * p.group + slot]);
-        lp = 0.0f;
+        for (int w = 0; w < 8; ++w) M = fmaxf(M, mS[w * NH + wi]);
 #pragma unroll
-        for (int e = 0; e < E; ++e) op[e] = 0.0f;
+        for (int w = 0; w < 8; ++w) {
+          const float mw = mS[w * NH + wi];
+          const float sc = mw == -INFINITY ? 0.0f : exp2f(mw - M);  // warps that saw no token
+          lp = fmaf(sc, lS[w * NH + wi], lp);
 #pragma unroll
-        for (int k = 0; k < kRawQuarters; ++k) {
-          const float mk = qm[k * p.group + slot];
-          const float w = mk > -INFINITY ? exp2f(mk - M) : 0.0f;  // quarters past n_part are empty
-          lp = fmaf(w, ql[k * p.group + slot], lp);
-#pragma unroll
-          for (int e = 0; e < E; ++e) op[e] = fmaf(w, qo[(k * p.group + slot) * D + lane * E + e], op[e]);
+          for (int e = 0; e < E; ++e) op[e] = fmaf(sc, oS[(w * NH + wi) * D + lane * E + e], op[e]);
         }
         mp = M;
       }
     }
-    if (wq != 0) return;  // the head's first warp merges
   }
   grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
   grid_launch_dependents();  // the next kernel (say, the next step's append) may start arriving
@@ -1388,21 +1460,32 @@ static int launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.partial_in_merge != 0 && p.chunk == 1) {
-    // one CTA per (sequence, kv head), the raw partial tile in shared memory
-    // raw K and V rows, then (m, l, o) of each quarter of each head slot (up to 8)
-    constexpr int kRawSmem = 2 * kTile * D * 2 + kRawQuarters * 8 * (D + 2) * 4;
-    static PerDeviceOnce smem_once;
-    const void* fn = reinterpret_cast<const void*>(combine_kernel<D, true>);
-    if (const int st = set_smem_limit(smem_once, fn, kRawSmem); st != KVARN_OK) return st;
+    // one CTA of 8 warps per (sequence, kv head), the raw partial tile in shared memory as one
+    // fp16 page, then the fp16 queries of 4 or 8 head slots
     cfg.gridDim = dim3(p.batch * p.num_kv_heads);
-    cfg.blockDim = dim3(32 * p.group * kRawQuarters);
-    cfg.dynamicSmemBytes = kRawSmem;
-    return cudaLaunchKernelEx(&cfg, combine_kernel<D, true>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+    cfg.blockDim = dim3(256);
+    if (p.group <= 4) {
+      constexpr int kSmem = 256 * 2 * D + 4 * D * 2;
+      static PerDeviceOnce smem_once;
+      const void* fn = reinterpret_cast<const void*>(combine_kernel<D, true, 1>);
+      if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
+      cfg.dynamicSmemBytes = kSmem;
+      return cudaLaunchKernelEx(&cfg, combine_kernel<D, true, 1>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+    }
+    if constexpr (D <= 128) {
+      constexpr int kSmem = 256 * 2 * D + 8 * D * 2;
+      static PerDeviceOnce smem_once;
+      const void* fn = reinterpret_cast<const void*>(combine_kernel<D, true, 2>);
+      if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
+      cfg.dynamicSmemBytes = kSmem;
+      return cudaLaunchKernelEx(&cfg, combine_kernel<D, true, 2>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+    }
+    return KVARN_ERR_UNSUPPORTED;
   }
   const int warps = p.batch * p.chunk * p.num_q_heads;
   cfg.gridDim = dim3((warps + 3) / 4);
   cfg.blockDim = dim3(128);
-  return cudaLaunchKernelEx(&cfg, combine_kernel<D, false>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<D, false, 1>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
 }
 
 int launch_decode_combine(int d, const DecodeParams& p, cudaStream_t stream) {

@@ -65,6 +65,31 @@ __device__ __forceinline__ void unpack_v(uint32_t x, uint32_t (&a0)[4], uint32_t
   a1[3] = y & 0x00C000C0u;
 }
 
+// ---- fp16 rows in shared memory for ldmatrix -----------------------------------------------
+// Byte offset of 16-byte chunk c of row r in a buffer of D-channel fp16 rows, chunk c of row r
+// stored at chunk c ^ (r % 8), so that the 8 rows an ldmatrix reads fall in distinct banks.
+template <int D>
+__device__ __forceinline__ uint32_t swz_row(int r, int c) {
+  return (uint32_t)(r * 2 * D + ((c ^ (r & 7)) << 4));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// 16-byte global -> shared copy, zero-filled beyond `bytes` (0 or 16)
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_all() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Walsh-Hadamard transform of D values spread over a warp, lane holding D/32 consecutive.
 template <int D>
 __device__ __forceinline__ void warp_fwht(float (&v)[D / 32], int lane) {
