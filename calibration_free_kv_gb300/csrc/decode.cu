@@ -1142,13 +1142,15 @@ __device__ __forceinline__ void raw_attend(const float (&q)[D / 32], const __hal
 // output is in the original basis and joins after the inverse rotation [vatt §四個步驟: R is
 // orthonormal and symmetric, so R (sum_s w_s o~_s) + w_p o_p is the merged output].
 // RAW (decode with p.partial_in_merge): one CTA of 8 warps per (sequence, kv head); the row's raw
-// partial tile is staged in shared memory as one fp16 page (K rows 0..127, V rows 128..255,
-// 16-byte chunks XOR-swizzled by row, rows past the tile zero-filled) and attended on the tensor
-// cores: warp w takes tokens 16w..16w+15, QK as mma.sync m16n8k16 with A = K rows by ldmatrix and
-// B = the fp16 queries (heads 4nt + j in column pairs (j, 0)), PV with A = V^T by ldmatrix.trans
-// and B = the probabilities in fp16 hi + lo; the warps meet in shared memory, and warp w < G then
-// merges query head w's splits.  Otherwise four warps per CTA over (sequence, chunk token, query
-// head), and any partial tile is a split of its own.
+// partial tile is staged in shared memory as fp16 rows (16-byte chunks XOR-swizzled by row, rows
+// past the tile zero-filled): K tokens 0..127 in rows 0..127 and V tokens 0..63 in rows 128..191,
+// then, once every warp's QK has read them, V tokens 64..127 over rows 0..63 (48 KB, so that four
+// CTAs share an SM and a batch of 64 x 8 rows is one wave).  It is attended on the tensor cores:
+// warp w takes tokens 16w..16w+15, QK as mma.sync m16n8k16 with A = K rows by ldmatrix and B = the
+// fp16 queries (heads 4nt + j in column pairs (j, 0)), PV with A = V^T by ldmatrix.trans and B =
+// the probabilities in fp16 hi + lo; the warps meet in shared memory, and warp w < G then merges
+// query head w's splits.  Otherwise four warps per CTA over (sequence, chunk token, query head),
+// and any partial tile is a split of its own.
 template <int D, bool RAW, int NT = 1>
 __global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p) {
   constexpr int E = D / 32;
@@ -1166,43 +1168,55 @@ __global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p
   int len = (RAW || live) ? p.seq_lens[b] : 0;
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int n_part = len % kTile;
+  // the splits of the row's sealed pages (a warp-collective; lengths and block tables are inputs)
+  auto cache_splits = [&]() -> int {
+    return p.part_ctas > 0 ? tc_row_segments(p, b, h, lane)
+                           : (len / kTile + p.pages_per_split - 1) / p.pages_per_split;
+  };
+  int n_cache = -1;
   float mp = -INFINITY, lp = 0.0f, op[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) op[e] = 0.0f;
   bool has_part = false;
   if constexpr (RAW) {
-    extern __shared__ __align__(128) uint8_t raw_s[];  // the page [256][2 D], then q [NH][D]
+    extern __shared__ __align__(128) uint8_t raw_s[];  // rows [192][2 D], then q [NH][D]
+    constexpr int kRows = kTile + kTile / 2;
     has_part = n_part > 0 && p.partial_k != nullptr && p.partial_v != nullptr;
     if (n_part > 0 && !has_part && threadIdx.x == 0) flag_error(p.status, KVARN_DEV_NO_PARTIAL);
     if (has_part) {
       const int g = lane >> 2, tq = lane & 3;
       const uint32_t sbase = smem_u32(raw_s);
-      __half* qs = reinterpret_cast<__half*>(raw_s + 256 * 2 * D);
-      {
-        const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
-        const int dch = p.d0 / 8;  // 16-byte chunks of a raw row (d0 % 8 == 0)
-        for (int qi = threadIdx.x; qi < 256 * (D / 8); qi += blockDim.x) {
-          const int r = qi / (D / 8), c = qi - r * (D / 8);
-          const int t = r & (kTile - 1);
-          const bool in = t < n_part && c < dch;
-          const __half* src = (r < kTile ? p.partial_k : p.partial_v) + base + (int64_t)t * p.d0 + 8 * c;
-          cp_async_16(sbase + swz_row<D>(r, c), in ? src : p.partial_k, in ? 16u : 0u);
-        }
-        cp_async_commit_all();
+      __half* qs = reinterpret_cast<__half*>(raw_s + kRows * 2 * D);
+      const int64_t base = ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
+      const int dch = p.d0 / 8;  // 16-byte chunks of a raw row (d0 % 8 == 0)
+      // row r of the staging area <- token t of K or V (zero past the tile)
+      auto stage = [&](int r, int c, const __half* src_base, int t) {
+        const bool in = t < n_part && c < dch;
+        cp_async_16(sbase + swz_row<D>(r, c), in ? src_base + base + (int64_t)t * p.d0 + 8 * c : p.partial_k,
+                    in ? 16u : 0u);
+      };
+      for (int qi = threadIdx.x; qi < kRows * (D / 8); qi += blockDim.x) {
+        const int r = qi / (D / 8), c = qi - r * (D / 8);
+        if (r < kTile) stage(r, c, p.partial_k, r);
+        else stage(r, c, p.partial_v, r - kTile);
       }
+      cp_async_commit_all();
       for (int i = threadIdx.x; i < NH * D; i += blockDim.x) {
         const int hl = i / D, c = i - hl * D;
         qs[i] = (hl < p.group && c < p.d0) ? p.q[((int64_t)b * p.num_q_heads + h * p.group + hl) * p.d0 + c]
                                            : __float2half(0.0f);
       }
+      if (live) n_cache = cache_splits();  // while the tile is in flight
       cp_async_wait_all();
       __syncthreads();
       const int t0 = 16 * wi;  // this warp's tokens
       float m[NT], l[NT], o[D / 16][NT][2];
+      uint32_t bw[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         m[nt] = -INFINITY;
         l[nt] = 0.0f;
+        bw[nt][0] = bw[nt][1] = 0u;
 #pragma unroll
         for (int mc = 0; mc < D / 16; ++mc) o[mc][nt][0] = o[mc][nt][1] = 0.0f;
       }
@@ -1228,7 +1242,6 @@ __global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p
           }
         }
         const bool v0 = t0 + g < n_part, v1 = t0 + g + 8 < n_part;
-        float pr[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float s0 = v0 ? (acc[nt][0] + acc[nt][1]) * p.qscale : -INFINITY;
@@ -1238,20 +1251,27 @@ __global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           m[nt] = mx;  // finite: token t0 (g = 0) is in the tile
-          pr[nt][0] = exp2f(s0 - mx);
-          pr[nt][1] = exp2f(s1 - mx);
-          l[nt] = pr[nt][0] + pr[nt][1];
-        }
-        uint32_t bw[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const __half2 hi = __floats2half2_rn(pr[nt][0], pr[nt][1]);
+          const float p0 = exp2f(s0 - mx), p1 = exp2f(s1 - mx);
+          l[nt] = p0 + p1;
+          const __half2 hi = __floats2half2_rn(p0, p1);
           const float2 hf = __half22float2(hi);
-          const __half2 lo = __floats2half2_rn(pr[nt][0] - hf.x, pr[nt][1] - hf.y);
+          const __half2 lo = __floats2half2_rn(p0 - hf.x, p1 - hf.y);
           bw[nt][0] = movmatrix_trans(h2u(__lows2half2(hi, lo)));   // (hi, lo) of token row g
           bw[nt][1] = movmatrix_trans(h2u(__highs2half2(hi, lo)));  // (hi, lo) of token row g + 8
         }
-        const int row = kTile + t0 + (lane & 7) + 8 * (lane >> 4);
+      }
+      // every warp's QK is done: V tokens 64..127 replace K tokens 0..63
+      __syncthreads();
+      const bool second = n_part > kTile / 2;  // the same for the whole CTA
+      if (second) {
+        for (int qi = threadIdx.x; qi < (kTile / 2) * (D / 8); qi += blockDim.x) {
+          const int r = qi / (D / 8), c = qi - r * (D / 8);
+          stage(r, c, p.partial_v, r + kTile / 2);
+        }
+        cp_async_commit_all();
+      }
+      auto pv = [&](int vrow) {  // V rows of this warp's tokens start at vrow
+        const int row = vrow + (lane & 7) + 8 * (lane >> 4);
 #pragma unroll
         for (int mc = 0; mc < D / 16; ++mc) {
           uint32_t a[4];
@@ -1264,8 +1284,12 @@ __global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p
             o[mc][nt][1] = pacc[2] + pacc[3];
           }
         }
-      }
-      // the warps meet: (m, l, o) per (warp, head slot) over the page buffer
+      };
+      if (t0 < kTile / 2 && t0 < n_part) pv(kTile + t0);
+      if (second) cp_async_wait_all();
+      __syncthreads();
+      if (t0 >= kTile / 2 && t0 < n_part) pv(t0 - kTile / 2);
+      // the warps meet: (m, l, o) per (warp, head slot) over the staging rows
       __syncthreads();
       float* mS = reinterpret_cast<float*>(raw_s);
       float* lS = mS + 8 * NH;
@@ -1304,12 +1328,10 @@ __global__ void __launch_bounds__(RAW ? 256 : 128) combine_kernel(DecodeParams p
       }
     }
   }
+  if (live && n_cache < 0) n_cache = cache_splits();
   grid_dependency_wait();  // the split partials of decode_kernel (and of the chunk kernel)
   grid_launch_dependents();  // the next kernel (say, the next step's append) may start arriving
   if (!live) return;
-  const int n_sealed = len / kTile;
-  const int n_cache = p.part_ctas > 0 ? tc_row_segments(p, b, h, lane)
-                                    : (n_sealed + p.pages_per_split - 1) / p.pages_per_split;
   const int n_splits = n_cache + (n_part > 0 && p.partial_in_merge == 0 ? 1 : 0) + (p.chunk_k != nullptr ? 1 : 0);
   const float* base = p.part + (int64_t)gw * p.max_splits * (D + 4);
   float v[E];
@@ -1460,12 +1482,12 @@ static int launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (p.partial_in_merge != 0 && p.chunk == 1) {
-    // one CTA of 8 warps per (sequence, kv head), the raw partial tile in shared memory as one
-    // fp16 page, then the fp16 queries of 4 or 8 head slots
+    // one CTA of 8 warps per (sequence, kv head): 192 fp16 rows of the raw partial tile in shared
+    // memory, then the fp16 queries of 4 or 8 head slots
     cfg.gridDim = dim3(p.batch * p.num_kv_heads);
     cfg.blockDim = dim3(256);
     if (p.group <= 4) {
-      constexpr int kSmem = 256 * 2 * D + 4 * D * 2;
+      constexpr int kSmem = (kTile + kTile / 2) * 2 * D + 4 * D * 2;
       static PerDeviceOnce smem_once;
       const void* fn = reinterpret_cast<const void*>(combine_kernel<D, true, 1>);
       if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
@@ -1473,7 +1495,7 @@ static int launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
       return cudaLaunchKernelEx(&cfg, combine_kernel<D, true, 1>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
     }
     if constexpr (D <= 128) {
-      constexpr int kSmem = 256 * 2 * D + 8 * D * 2;
+      constexpr int kSmem = (kTile + kTile / 2) * 2 * D + 8 * D * 2;
       static PerDeviceOnce smem_once;
       const void* fn = reinterpret_cast<const void*>(combine_kernel<D, true, 2>);
       if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
