@@ -57,8 +57,8 @@ def _peaks():
 # DRAM traffic / algorithmic bytes of one decode_kernel launch, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum at batch 24), valid only for the decode.cu source
 # it was taken on: the traffic is reported as null once that file changes.
-DECODE_TRAFFIC = {"decode_cu_sha256": "8daec1178c4ccfc21146f1292f67a8297af9aaeed28a75c2940d9e5385b1bae9",
-                  "dram_over_algorithmic": 1.0208}
+DECODE_TRAFFIC = {"decode_cu_sha256": "1f1e24d06d0bc3db0a414709abc62f2e05f99840e15bf0d3dc5db7cbb2ac36f7",
+                  "dram_over_algorithmic": 1.0224}
 
 
 def _decode_traffic_ratio():
