@@ -695,9 +695,32 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   grid_dependency_wait();  // lengths, partial tiles and pages come from the previous kernel
   const int cap = p.max_pages * kTile + (kTile - 1);  // sealed pages must fit the block table
   auto part_row = [&](int hl, int slot) { return p.part + (vrow(hl) * p.max_splits + slot) * (D + 4); };
+  // This warp's fp16 query values of row (bb, hh) for the staging of the rotated queries: head
+  // slot warp + i * kDecWarps, channels lane * D / 32 .., zero outside the group and past d0.
+  // Loaded ahead of the run that stages them (the persistent walk fetches the next segment's).
+  constexpr int kQPer = (NH + kDecWarps - 1) / kDecWarps;
+  __half2 qv[kQPer][D / 64];
+  auto q_load = [&](int bb, int hh) {
+#pragma unroll
+    for (int i = 0; i < kQPer; ++i) {
+      const int hl = warp + i * kDecWarps;
+      const int vh = vg * NH + hl;
+      const bool ok = hl < NH && vh < n_vh;
+      const int64_t row = ((int64_t)bb * p.chunk + vh / p.group) * p.num_q_heads + hh * p.group + vh % p.group;
+      const __half* src = p.q + (ok ? row : 0) * p.d0;
+#pragma unroll
+      for (int e2 = 0; e2 < D / 64; ++e2) {
+        const int j = lane * (D / 32) + 2 * e2;
+        const __half lo = (ok && j < p.d0) ? src[j] : __float2half(0.0f);
+        const __half hi = (ok && j + 1 < p.d0) ? src[j + 1] : __float2half(0.0f);
+        qv[i][e2] = __halves2half2(lo, hi);
+      }
+    }
+  };
   // Sealed pages first..first+n-1 of row (b, h) -> partial row `slot`.  pc counts the pages this
-  // warp has taken in earlier calls (the phases of its two barriers); `init` sets them up.
-  auto sealed_run = [&](int first, int n, int slot, int& pc, bool init) {
+  // warp has taken in earlier calls (the phases of its two barriers); `init` sets them up.  The
+  // row's queries are in qv; after they are staged, ahead() runs (it may load the next run's).
+  auto sealed_run = [&](int first, int n, int slot, int& pc, bool init, auto&& ahead) {
     const int cnt = n > warp ? (n - warp + kDecWarps - 1) / kDecWarps : 0;  // pages of this warp
     uint8_t* kslot = recs + warp * REC;
     uint8_t* vslot = kslot + KH;
@@ -732,12 +755,16 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     // (channels 16k + {2t, 2t+1, 2t+8, 2t+9} adjacent), fp16 hi + lo for the B operand
     // (times the QkScale factors of the code width; one {hi pair, lo pair} entry per channel
     // pair)
-    for (int hl = warp; hl < NH; hl += kDecWarps) {
+#pragma unroll
+    for (int i = 0; i < kQPer; ++i) {
+      const int hl = warp + i * kDecWarps;
+      if (hl >= NH) break;
       float v[D / 32];
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) {
-        const int j = lane * (D / 32) + e;
-        v[e] = (valid(hl) && j < p.d0) ? __half2float(p.q[vrow(hl) * p.d0 + j]) : 0.0f;
+      for (int e2 = 0; e2 < D / 64; ++e2) {
+        const float2 f = __half22float2(qv[i][e2]);
+        v[2 * e2] = f.x;
+        v[2 * e2 + 1] = f.y;
       }
       warp_fwht<D>(v, lane);
       const float sc = p.qscale * inv_sqrt_d<D>();
@@ -754,6 +781,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       }
     }
     __syncthreads();  // q in shared memory for every warp
+    ahead();
 
     using Path = PagePath<D, NT, KB, VB>;
     typename Path::State st;
@@ -800,7 +828,7 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
     }
     // ---- merge the warps of this CTA ----
     __syncthreads();  // every warp is done with its slots
-    grid_launch_dependents();
+    if (p.part_mode != 1) grid_launch_dependents();  // (the persistent walk signals once, up front)
     float* mS = reinterpret_cast<float*>(recs);
     float* lS = mS + kDecWarps * NH;
     float* oS = lS + kDecWarps * NH;
@@ -1014,13 +1042,23 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
       }
     }
     __syncthreads();
+    // the dependent merge kernel may be scheduled now: its CTAs take an SM's resources only as
+    // this grid's CTAs leave, and it waits for this grid's completion before reading the splits
+    grid_launch_dependents();
     int pc = 0;
     bool init = true;
-    for (Walk w = walk0; w.left > 0; w.next(p)) {
+    Walk w = walk0;
+    q_load(w.b, w.h);
+    while (w.left > 0) {
       b = w.b;
       h = w.h;
-      sealed_run(w.j, w.count(), w.slot, pc, init);
+      Walk wn = w;  // the next segment, and its queries while this one runs
+      sealed_run(w.j, w.count(), w.slot, pc, init, [&]() {
+        wn.next(p);
+        if (wn.left > 0) q_load(wn.b, wn.h);
+      });
       init = false;
+      w = wn;
     }
     // raw partial tiles (unless the merge takes them): row k = b * Hkv + h goes to CTA k mod
     // gridDim.x, its split after the row's sealed segments
@@ -1056,7 +1094,8 @@ __global__ void __launch_bounds__(DecodeShape<D, NT, KB, VB>::kWarps * 32, Decod
   if (!partial_split) {
     int pc = 0;
     const int first = split * p.pages_per_split;
-    sealed_run(first, min(n_sealed, first + p.pages_per_split) - first, split, pc, true);
+    q_load(b, h);
+    sealed_run(first, min(n_sealed, first + p.pages_per_split) - first, split, pc, true, []() {});
     return;
   }
   partial_run(n_part, split);
