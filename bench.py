@@ -55,22 +55,31 @@ def _peaks():
 
 
 # DRAM traffic / algorithmic bytes of one decode_kernel launch, from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum at batch 24), valid only for the decode.cu source
-# it was taken on: the traffic is reported as null once that file changes.
-DECODE_TRAFFIC = {"decode_cu_sha256": "1f1e24d06d0bc3db0a414709abc62f2e05f99840e15bf0d3dc5db7cbb2ac36f7",
-                  "dram_over_algorithmic": 1.0224}
+# (dram__bytes_read.sum + dram__bytes_write.sum at batch 24), valid only for the sources it was
+# taken on (decode.cu and decode_util.cuh, which holds the page partition): the traffic is
+# reported as null once either changes.
+DECODE_TRAFFIC = {"sources_sha256": None, "dram_over_algorithmic": None}
+DECODE_SOURCES = ("decode.cu", "decode_util.cuh")
+
+
+def _decode_sources_digest():
+    """sha256 over the decode sources named in DECODE_SOURCES, in that order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "calibration_free_kv_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def _decode_traffic_ratio():
-    """DRAM bytes / algorithmic bytes of the decode kernel, or None when decode.cu changed since
-    the capture DECODE_TRAFFIC records."""
-    import hashlib
+    """DRAM bytes / algorithmic bytes of the decode kernel, or None when its sources changed
+    since the capture DECODE_TRAFFIC records."""
     try:
-        with open(os.path.join(ROOT, "calibration_free_kv_gb300", "csrc", "decode.cu"), "rb") as fh:
-            digest = hashlib.sha256(fh.read()).hexdigest()
+        digest = _decode_sources_digest()
     except OSError:
         return None
-    if DECODE_TRAFFIC["dram_over_algorithmic"] is None or digest != DECODE_TRAFFIC["decode_cu_sha256"]:
+    if DECODE_TRAFFIC["dram_over_algorithmic"] is None or digest != DECODE_TRAFFIC["sources_sha256"]:
         return None
     return float(DECODE_TRAFFIC["dram_over_algorithmic"])
 
@@ -922,7 +931,7 @@ def _run_kvarn(args, torch, world, rank):
                         else _decode_traffic_ratio() * statistics.mean(dec_bytes)),
             "traffic_source": "ncu dram__bytes_read+write of one decode_kernel launch at batch 24 "
                               "(DECODE_TRAFFIC), scaled by algorithmic bytes; null when decode.cu "
-                              "changed since that capture",
+                              "or decode_util.cuh changed since that capture",
             "algorithmic_bytes_per_launch": statistics.mean(dec_bytes),
             "duration_source": "CUDA events on the launching stream around decode_kernel (the "
                                "decode call as kvarn_decode_partials + kvarn_decode_combine, an "

@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(dtc::kThreads, 1) decode_tc_kernel(DecodeParam
     fence_mbar_init();
   }
   __syncthreads();
-  const int64_t total = ws.left;
+  int64_t total = 0;  // pages of this CTA's range
+  for (Walk w = ws; w.left > 0; w.next(p)) total += w.count();
   if (total <= 0) {
     grid_launch_dependents();
     return;

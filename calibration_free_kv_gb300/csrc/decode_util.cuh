@@ -157,13 +157,17 @@ __device__ __forceinline__ float inv_sqrt_d() {
 }
 
 // ---- balanced page partition of the persistent decode kernels -----------------------------
-// The sealed pages of all (sequence b, kv head h) rows, in (b, h, page) order, are cut into
-// `ctas` contiguous ranges of floor or ceil(total / ctas) pages, one per CTA, with ctas no
-// larger than total / 32: every range holds at least 32 pages.  A row's pages then fall in
-// row_segments <= ceil(n / 32) + 1 ranges (n its sealed pages), and the segment that starts at
-// global page x writes split owner_cta(x) - owner_cta(first page of the row).  Every kernel of
-// the launch derives the same partition from seq_lens.
+// The sealed pages of all (sequence b, kv head h) rows, in (b, h, page) order, are laid on a
+// line of virtual pages where every row with sealed pages first takes kSegPages units for the
+// fixed work of a segment (its queries, its first page's latency, the CTA merge), then one unit
+// per page.  The line is cut into `ctas` contiguous ranges of floor or ceil(total / ctas) units,
+// one per CTA, with ctas no larger than total / 32: every range holds at least 32 units, so a
+// row's pages (n consecutive units) fall in row_segments <= ceil(n / 32) + 1 ranges, and the
+// segment whose first page sits at unit x writes split owner_cta(x) - owner_cta(the row's first
+// page).  A range may hold only the fixed units of a row (no page): that CTA has no work.  Every
+// kernel of the launch derives the same partition from seq_lens.
 constexpr int kMinRangePages = 32;
+constexpr int kSegPages = 8;  // virtual pages of a segment's fixed work
 
 __device__ __forceinline__ int sealed_pages(const DecodeParams& p, int b) {
   const int cap = p.max_pages * kTile + (kTile - 1);
@@ -172,30 +176,34 @@ __device__ __forceinline__ int sealed_pages(const DecodeParams& p, int b) {
   return len / kTile;
 }
 
-// Warp-collective: sealed pages of sequences 0..lim-1 (every lane gets the sum).
-__device__ __forceinline__ int64_t sealed_prefix(const DecodeParams& p, int lim, int lane) {
+// Virtual length of one row of n sealed pages.
+__device__ __forceinline__ int row_units(int n) { return n > 0 ? n + kSegPages : 0; }
+
+// Warp-collective: virtual length of one kv head's rows of sequences 0..lim-1 (every lane gets
+// the sum).
+__device__ __forceinline__ int64_t units_prefix(const DecodeParams& p, int lim, int lane) {
   long long s = 0;
-  for (int b = lane; b < lim; b += 32) s += sealed_pages(p, b);
+  for (int b = lane; b < lim; b += 32) s += row_units(sealed_pages(p, b));
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
   return s;
 }
 
 struct PagePartition {
-  int64_t total;  // sealed pages of all rows
-  int64_t ctas;   // ranges (CTAs with work); 0 when there are no sealed pages
+  int64_t total;  // virtual pages of all rows
+  int64_t ctas;   // ranges; 0 when there are no sealed pages
 };
 
 __device__ __forceinline__ PagePartition page_partition(const DecodeParams& p, int lane) {
   PagePartition pp;
-  pp.total = sealed_prefix(p, p.batch, lane) * p.num_kv_heads;
+  pp.total = units_prefix(p, p.batch, lane) * p.num_kv_heads;
   int64_t c = pp.total / kMinRangePages;
   c = c < 1 ? 1 : (c > p.part_ctas ? p.part_ctas : c);
   pp.ctas = pp.total > 0 ? c : 0;
   return pp;
 }
 
-// First global page of range c, and the range that holds global page x.
+// First unit of range c, and the range that holds unit x.
 __device__ __forceinline__ int64_t range_start(const PagePartition& pp, int64_t c) {
   return c * pp.total / pp.ctas;
 }
@@ -207,8 +215,9 @@ __device__ __forceinline__ int64_t owner_cta(const PagePartition& pp, int64_t x)
 __device__ __forceinline__ int row_segments(const DecodeParams& p, const PagePartition& pp, int b, int h,
                                             int lane) {
   const int n = sealed_pages(p, b);
-  const int64_t a = sealed_prefix(p, b, lane) * p.num_kv_heads + (int64_t)h * n;
   if (n == 0) return 0;
+  // the unit of the row's first page
+  const int64_t a = units_prefix(p, b, lane) * p.num_kv_heads + (int64_t)h * row_units(n) + kSegPages;
   return (int)(owner_cta(pp, a + n - 1) - owner_cta(pp, a) + 1);
 }
 
@@ -216,9 +225,9 @@ __device__ __forceinline__ int row_segments(const DecodeParams& p, const PagePar
 struct Walk {
   int b, h, j, n;    // row (sequence b, kv head h), first page j of the segment, sealed pages n
   int slot;          // split the segment's partial goes to
-  int64_t left;      // pages of the range from this segment on
+  int64_t left;      // units of the range from page j of this row on (0: no more pages)
   __device__ int count() const { return (int)min((int64_t)(n - j), left); }
-  // next segment: the next row with sealed pages (slot 0, page 0)
+  // next segment: the next row with sealed pages (slot 0, page 0), past its fixed units
   __device__ void next(const DecodeParams& p) {
     left -= count();
     if (left <= 0) return;
@@ -234,7 +243,11 @@ struct Walk {
         return;
       }
       n = sealed_pages(p, b);
-      if (n > 0) return;
+      if (n > 0) {
+        left -= kSegPages;  // the range may end inside the row's fixed units
+        if (left < 0) left = 0;
+        return;
+      }
       h = p.num_kv_heads - 1;  // skip the whole sequence
     }
   }
@@ -247,13 +260,13 @@ __device__ __forceinline__ Walk range_walk(const DecodeParams& p, int64_t c, int
   w.b = w.h = w.j = w.n = w.slot = 0;
   w.left = 0;
   if (c >= pp.ctas) return w;
-  const int64_t x0 = range_start(pp, c);
-  // the row holding global page x0: scan the sequences 32 at a time
+  const int64_t x0 = range_start(pp, c), x1 = range_start(pp, c + 1);
+  // the row holding unit x0: scan the sequences 32 at a time
   long long cum = 0;
   for (int b0 = 0; b0 < p.batch; b0 += 32) {
     const int bb = b0 + lane;
     const int n = bb < p.batch ? sealed_pages(p, bb) : 0;
-    long long incl = (long long)n * p.num_kv_heads;
+    long long incl = (long long)row_units(n) * p.num_kv_heads;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
       const long long o = __shfl_up_sync(0xffffffffu, incl, m);
@@ -261,15 +274,19 @@ __device__ __forceinline__ Walk range_walk(const DecodeParams& p, int64_t c, int
     }
     const unsigned hit = __ballot_sync(0xffffffffu, cum + incl > x0);
     if (hit != 0u) {
-      const int l = __ffs(hit) - 1;
+      const int l = __ffs(hit) - 1;  // a sequence with sealed pages: its units hold x0
       const int nb = __shfl_sync(0xffffffffu, n, l);
-      const long long excl = cum + __shfl_sync(0xffffffffu, incl, l) - (long long)nb * p.num_kv_heads;
+      const int ru = row_units(nb);
+      const long long excl = cum + __shfl_sync(0xffffffffu, incl, l) - (long long)ru * p.num_kv_heads;
       w.b = b0 + l;
       w.n = nb;
-      w.h = (int)((x0 - excl) / nb);
-      w.j = (int)((x0 - excl) - (long long)w.h * nb);
-      w.slot = (int)(c - owner_cta(pp, x0 - w.j));
-      w.left = range_start(pp, c + 1) - x0;
+      w.h = (int)((x0 - excl) / ru);
+      const int off = (int)((x0 - excl) - (long long)w.h * ru);  // unit of the row, fixed ones first
+      const long long first = excl + (long long)w.h * ru + kSegPages;  // unit of the row's page 0
+      w.j = off < kSegPages ? 0 : off - kSegPages;
+      w.slot = (int)(c - owner_cta(pp, first));
+      w.left = x1 - (first + w.j);
+      if (w.left < 0) w.left = 0;  // the range ends inside the row's fixed units
       return w;
     }
     cum += __shfl_sync(0xffffffffu, incl, 31);

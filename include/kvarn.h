@@ -157,13 +157,14 @@ int kvarn_append_token(const kvarn_desc* desc, int batch, const void* k_new, con
 /* Workspace bytes kvarn_decode_attention needs for this batch shape (host only): fp32 split
  * partials, ceil(max_pages / 32) + 2 per query row.  The mma.sync kernels fill one per split
  * of 32 or more pages (a block table wider than 256 pages may take larger splits, chosen from
- * the GPU's SM count) plus the raw partial tile's; the tcgen05 kernel of GQA groups of 8 (head_dim
- * 128, K4V2) cuts all sealed pages of the batch into ranges of equal size, one per SM and each
- * at least 32 pages, so that a row's pages fall in at most ceil(n / 32) + 1 ranges.  Needs no
- * GPU.  Two environment variables (read on every call) pick the decode kernels for comparing
- * them: KVARN_DECODE_KERNEL "split" (one CTA per split of 32 or more pages) or "tc" (GQA 8,
- * head_dim 128, K4V2: the tcgen05 kernel); by default persistent CTAs take equal ranges of all
- * sealed pages, at least 32 each.  KVARN_DECODE_OPEN_TILES "split" attends to the raw partial
+ * the GPU's SM count) plus the raw partial tile's; the persistent kernels (the default, and the
+ * tcgen05 kernel of GQA groups of 8 at head_dim 128, K4V2) lay the sealed pages of the batch on a
+ * line where each row with pages first takes 8 units for a segment's fixed work, then one unit per
+ * page, and cut it into ranges of equal length, each at least 32 units, so that a row's pages fall
+ * in at most ceil(n / 32) + 1 ranges.  Needs no GPU.  Two environment variables (read on every
+ * call) pick the decode kernels for comparing them: KVARN_DECODE_KERNEL "split" (one CTA per split
+ * of 32 or more pages) or "tc" (GQA 8, head_dim 128, K4V2: the tcgen05 kernel); by default
+ * persistent CTAs take those ranges.  KVARN_DECODE_OPEN_TILES "split" attends to the raw partial
  * tiles in the decode kernels as splits of their own; by default the merge kernel does. */
 size_t kvarn_decode_workspace_bytes(const kvarn_desc* desc, int batch, int num_q_heads,
                                     int max_pages);
