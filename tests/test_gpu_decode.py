@@ -153,16 +153,29 @@ def test_decode_parity_ragged(kv, d0, group):
                                                 (4, "persistent", "split"), (4, "split", "split"),
                                                 (8, "tc", "split"), (1, "persistent", "merge")])
 def test_decode_partition(kv, group, kernel, tiles, monkeypatch):
-    # The persistent kernels (mma.sync "persistent", tcgen05 "tc") cut the batch's sealed pages
-    # into equal ranges of at least 32 pages: here 316 pages over 9 ranges, so rows split across
-    # CTAs (up to three segments), some rows have no sealed page, and raw partial tiles follow;
-    # "split" runs one CTA per split.  The raw partial tiles are attended by the merge kernel
-    # ("merge") or by the decode kernels as splits of their own ("split").
+    # The persistent kernels (mma.sync "persistent", tcgen05 "tc") cut a line of virtual pages
+    # (each row with sealed pages: 8 units for a segment's fixed work, then one per page) into
+    # equal ranges of at least 32 units: here 316 pages of 16 rows, 444 units over 13 ranges, so
+    # rows split across CTAs (up to three segments), some rows have no sealed page, and raw
+    # partial tiles follow; "split" runs one CTA per split.  The raw partial tiles are attended
+    # by the merge kernel ("merge") or by the decode kernels as splits of their own ("split").
     monkeypatch.setenv("KVARN_DECODE_KERNEL", kernel)
     monkeypatch.setenv("KVARN_DECODE_OPEN_TILES", tiles)
     seq_lens = [0, 5 * 128, 129, 40 * 128 + 17, 128, 64 * 128, 3, 33 * 128, 1000, 7 * 128 + 127]
     err = _run_oracle_cache_case(kv, len(seq_lens), 2, group, 128, seq_lens, seed=808)
     print("G=%d partition (%s, open tiles: %s) max scaled err %.2e" % (group, kernel, tiles, err))
+
+
+@pytest.mark.parametrize("group,kernel", [(4, "persistent"), (8, "persistent"), (8, "tc"), (1, "persistent")])
+def test_decode_partition_short_rows(kv, group, kernel, monkeypatch):
+    # 48 sequences of 0-3 sealed pages plus raw tails, 2 kv heads: 72 rows with pages, 720
+    # virtual units over 22 ranges, so most ranges hold several rows, 14 of the 21 range ends
+    # fall inside a row's fixed units (the next CTA starts at that row's first page) and rows of
+    # two or three pages split across two CTAs
+    monkeypatch.setenv("KVARN_DECODE_KERNEL", kernel)
+    seq_lens = [128 * ((i * 7) % 4) + (i * 37) % 128 for i in range(48)]
+    err = _run_oracle_cache_case(kv, len(seq_lens), 2, group, 128, seq_lens, seed=909)
+    print("G=%d short rows (%s) max scaled err %.2e" % (group, kernel, err))
 
 
 def test_decode_gpu_quantised_cache(kv):
