@@ -1649,6 +1649,250 @@ __global__ void __launch_bounds__(128) chunk_kernel(DecodeParams p) {
   }
 }
 
+// The same causal attention on the tensor cores (head_dim 64 and 128): one CTA of 8 warps per
+// (128 query rows, kv head, sequence), query row r = c * G + j for chunk token c and group head
+// j, warp w taking rows 16w..16w+15.  The chunk's K and V rows stream through shared memory 64
+// tokens at a time (cp.async into swizzled fp16 rows, two stages).  QK is mma.sync m16n8k16
+// with A = the fp16 queries (exact products, the scale applied to the fp32 sums) and B = K rows
+// by ldmatrix; the softmax is online in the log2 domain with the tokens past a row's own masked;
+// PV takes A = the probabilities as fp16 hi + lo, read from the QK accumulators' layout, and B =
+// V rows by ldmatrix.trans.  The unnormalised output is rotated in registers (its channels are
+// 8n + 2tq + e for n-tile n, quad lane tq and pair element e: butterflies within the lane, across
+// the quad and across n-tiles) and written as the split after the cache's [vatt §四個步驟].
+template <int D>
+__global__ void __launch_bounds__(256, 1) chunk_tc_kernel(DecodeParams p) {
+  constexpr int NB = 64;      // tokens per stage
+  constexpr int NN = D / 8;   // channel n-tiles
+  constexpr int KK = D / 16;  // channel k-steps
+  constexpr uint32_t kStage = 2 * NB * 2 * D;  // K rows then V rows, fp16
+  extern __shared__ __align__(128) uint8_t cs[];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int G = p.group, C = p.chunk;
+  const int rows = C * G;
+  const int rbase = blockIdx.x * 128;
+  const int r0 = rbase + 16 * wi;  // this warp's first query row
+  const bool warp_live = r0 < rows;
+  const int c_last_w = (min(r0 + 15, rows - 1)) / G;      // the warp's last chunk token
+  const int c_last = (min(rbase + 127, rows - 1)) / G;    // the CTA's
+  const int ra = r0 + g, rb = r0 + g + 8;                 // the lane's two rows
+  const int ca = ra < rows ? ra / G : -1, cb = rb < rows ? rb / G : -1;  // -1: padding row
+  grid_dependency_wait();
+  const uint32_t sbase = smem_u32(cs);
+  const int64_t rstride = (int64_t)p.num_kv_heads * p.d0;
+  const __half* kg = p.chunk_k + ((int64_t)b * C * p.num_kv_heads + h) * p.d0;
+  const __half* vg = p.chunk_v + ((int64_t)b * C * p.num_kv_heads + h) * p.d0;
+  const int dch = p.d0 / 8;  // 16-byte chunks of a row (d0 % 8 == 0)
+  const int nblk = c_last / NB + 1;
+  auto stage = [&](int blk) {
+    const uint32_t base = sbase + (uint32_t)(blk & 1) * kStage;
+    for (int qi = threadIdx.x; qi < 2 * NB * (D / 8); qi += blockDim.x) {
+      const int r = qi / (D / 8), c = qi - r * (D / 8);
+      const int t = blk * NB + (r < NB ? r : r - NB);
+      const bool in = t < C && c < dch;
+      const __half* src = (r < NB ? kg : vg) + (int64_t)t * rstride + 8 * c;
+      cp_async_16(base + swz_row<D>(r, c), in ? src : kg, in ? 16u : 0u);
+    }
+    cp_async_commit_all();
+  };
+  stage(0);
+  // the warp's queries as A fragments: rows g (ra) and g + 8 (rb), channels 16kk + 2tq.. and +8
+  uint32_t aq[KK][4];
+  {
+    auto qrow = [&](int r) {
+      const int c = r / G, j = r - c * G;
+      return p.q + (((int64_t)b * C + c) * p.num_q_heads + h * G + j) * p.d0;
+    };
+    const __half* qa = qrow(ca >= 0 ? ra : 0);
+    const __half* qb = qrow(cb >= 0 ? rb : 0);
+    auto pair = [&](const __half* row, bool ok, int ch) -> uint32_t {
+      return (ok && ch < p.d0) ? h2u(__halves2half2(row[ch], row[ch + 1])) : 0u;
+    };
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk) {
+      const int ch = 16 * kk + 2 * tq;
+      aq[kk][0] = pair(qa, ca >= 0, ch);
+      aq[kk][1] = pair(qb, cb >= 0, ch);
+      aq[kk][2] = pair(qa, ca >= 0, ch + 8);
+      aq[kk][3] = pair(qb, cb >= 0, ch + 8);
+    }
+  }
+  float ma = -INFINITY, mb = -INFINITY, la = 0.0f, lb = 0.0f;  // l: this lane's share
+  float o[NN][4];
+#pragma unroll
+  for (int n = 0; n < NN; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+  for (int blk = 0; blk < nblk; ++blk) {
+    if (blk + 1 < nblk) {
+      stage(blk + 1);  // its buffer was released by the barrier closing blk - 1
+      cp_async_wait_prev();
+    } else {
+      cp_async_wait_all();
+    }
+    __syncthreads();
+    const int t0 = blk * NB;
+    if (warp_live && t0 <= c_last_w) {
+      const uint32_t base = sbase + (uint32_t)(blk & 1) * kStage;
+      float s[NB / 8][4];
+#pragma unroll
+      for (int nt = 0; nt < NB / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.0f;
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk) {
+#pragma unroll
+        for (int np = 0; np < NB / 16; ++np) {  // token n-tiles 2np, 2np + 1
+          uint32_t bk[4];
+          ldsm_x4(base + swz_row<D>(16 * np + (lane & 7) + 8 * (lane >> 4), 2 * kk + ((lane >> 3) & 1)), bk);
+          mma16816(s[2 * np], aq[kk], bk[0], bk[1]);
+          mma16816(s[2 * np + 1], aq[kk], bk[2], bk[3]);
+        }
+      }
+      // logits of rows ra (s[.][0..1]) and rb (s[.][2..3]), tokens t0 + 8nt + 2tq + e
+      float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < NB / 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = t0 + 8 * nt + 2 * tq + e;
+          s[nt][e] = t <= ca ? s[nt][e] * p.qscale : -INFINITY;
+          s[nt][2 + e] = t <= cb ? s[nt][2 + e] * p.qscale : -INFINITY;
+          mxa = fmaxf(mxa, s[nt][e]);
+          mxb = fmaxf(mxb, s[nt][2 + e]);
+        }
+      }
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
+      mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
+      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
+      mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
+      const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
+      // a row with no token yet keeps m = -inf, l = 0 and o = 0
+      const float sa = na == -INFINITY ? 0.0f : na, sb = nb == -INFINITY ? 0.0f : nb;
+      const float aa = ma == -INFINITY ? 0.0f : exp2f(ma - na);
+      const float ab = mb == -INFINITY ? 0.0f : exp2f(mb - nb);
+      ma = na;
+      mb = nb;
+      float pa = 0.0f, pb = 0.0f;
+#pragma unroll
+      for (int nt = 0; nt < NB / 8; ++nt) {
+        s[nt][0] = exp2f(s[nt][0] - sa);
+        s[nt][1] = exp2f(s[nt][1] - sa);
+        s[nt][2] = exp2f(s[nt][2] - sb);
+        s[nt][3] = exp2f(s[nt][3] - sb);
+        pa += s[nt][0] + s[nt][1];
+        pb += s[nt][2] + s[nt][3];
+      }
+      la = fmaf(la, aa, pa);
+      lb = fmaf(lb, ab, pb);
+#pragma unroll
+      for (int n = 0; n < NN; ++n) {
+        o[n][0] *= aa;
+        o[n][1] *= aa;
+        o[n][2] *= ab;
+        o[n][3] *= ab;
+      }
+#pragma unroll
+      for (int ks = 0; ks < NB / 16; ++ks) {
+        if (t0 + 16 * ks > c_last_w) break;  // every row masked from here on (warp-uniform)
+        // A = p of tokens t0 + 16ks..: n-tiles 2ks (k 0..7) and 2ks + 1 (k 8..15), hi + lo
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x = s[2 * ks + (i >> 1)][2 * (i & 1)], y = s[2 * ks + (i >> 1)][2 * (i & 1) + 1];
+          const __half2 hi = __floats2half2_rn(x, y);
+          const float2 hf = __half22float2(hi);
+          ah[i] = h2u(hi);
+          al[i] = h2u(__floats2half2_rn(x - hf.x, y - hf.y));
+        }
+#pragma unroll
+        for (int np = 0; np < NN / 2; ++np) {  // channel n-tiles 2np, 2np + 1
+          uint32_t bv[4];
+          ldsm_x4_trans(base + swz_row<D>(NB + 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1), 2 * np + (lane >> 4)), bv);
+          mma16816(o[2 * np], ah, bv[0], bv[1]);
+          mma16816(o[2 * np], al, bv[0], bv[1]);
+          mma16816(o[2 * np + 1], ah, bv[2], bv[3]);
+          mma16816(o[2 * np + 1], al, bv[2], bv[3]);
+        }
+      }
+    }
+    __syncthreads();  // the stage buffer is refilled two blocks on
+  }
+  if (!warp_live) return;
+  la += __shfl_xor_sync(0xffffffffu, la, 1);
+  la += __shfl_xor_sync(0xffffffffu, la, 2);
+  lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+  lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+  // rotation: channel bit 0 within the lane, bits 1-2 across the quad, bits 3.. across n-tiles
+#pragma unroll
+  for (int n = 0; n < NN; ++n) {
+#pragma unroll
+    for (int r = 0; r < 4; r += 2) {
+      const float x = o[n][r], y = o[n][r + 1];
+      o[n][r] = x + y;
+      o[n][r + 1] = x - y;
+    }
+  }
+#pragma unroll
+  for (int msk = 1; msk <= 2; msk <<= 1) {
+    const bool upper = (tq & msk) != 0;
+#pragma unroll
+    for (int n = 0; n < NN; ++n)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float v = o[n][r], w = __shfl_xor_sync(0xffffffffu, v, msk);
+        o[n][r] = upper ? w - v : v + w;
+      }
+  }
+#pragma unroll
+  for (int st = 1; st < NN; st <<= 1)
+#pragma unroll
+    for (int n = 0; n < NN; ++n)
+      if ((n & st) == 0)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float x = o[n][r], y = o[n + st][r];
+          o[n][r] = x + y;
+          o[n + st][r] = x - y;
+        }
+  const int cap = p.max_pages * kTile + (kTile - 1);
+  int len = p.seq_lens[b];
+  len = len < 0 ? 0 : (len > cap ? cap : len);
+  const int split = (len / kTile + p.pages_per_split - 1) / p.pages_per_split + (len % kTile > 0 ? 1 : 0);
+  auto store = [&](int r, int c, int hf, float m, float l) {  // hf: o[.][2 hf..2 hf + 1]
+    const int j = r - c * G;
+    const int64_t gw = ((int64_t)b * C + c) * p.num_q_heads + h * G + j;
+    float* dst = p.part + (gw * p.max_splits + split) * (D + 4);
+#pragma unroll
+    for (int n = 0; n < NN; ++n)
+      *reinterpret_cast<float2*>(dst + 4 + 8 * n + 2 * tq) =
+          make_float2(o[n][2 * hf] * inv_sqrt_d<D>(), o[n][2 * hf + 1] * inv_sqrt_d<D>());
+    if (tq == 0) {
+      dst[0] = m;
+      dst[1] = l;
+    }
+  };
+  if (ca >= 0) store(ra, ca, 0, ma, la);
+  if (cb >= 0) store(rb, cb, 1, mb, lb);
+}
+
+template <int D>
+static int launch_chunk_tc_t(const DecodeParams& p, cudaStream_t stream) {
+  constexpr int kSmem = 2 * 2 * 64 * 2 * D;
+  static PerDeviceOnce smem_once;
+  const void* fn = reinterpret_cast<const void*>(chunk_tc_kernel<D>);
+  if (const int st = set_smem_limit(smem_once, fn, kSmem); st != KVARN_OK) return st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  const int64_t rows = (int64_t)p.chunk * p.group;
+  cfg.gridDim = dim3((unsigned)((rows + 127) / 128), p.num_kv_heads, p.batch);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, chunk_tc_kernel<D>, p) == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA;
+}
+
 template <int D>
 static int launch_chunk_t(const DecodeParams& p, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
@@ -1665,8 +1909,8 @@ static int launch_chunk_t(const DecodeParams& p, cudaStream_t stream) {
 }
 
 int launch_chunk_any(int d, const DecodeParams& p, cudaStream_t stream) {
-  if (d == 64) return launch_chunk_t<64>(p, stream);
-  if (d == 128) return launch_chunk_t<128>(p, stream);
+  if (d == 64) return launch_chunk_tc_t<64>(p, stream);
+  if (d == 128) return launch_chunk_tc_t<128>(p, stream);
   if (d == 256) return launch_chunk_t<256>(p, stream);
   return KVARN_ERR_UNSUPPORTED;
 }

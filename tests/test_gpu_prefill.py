@@ -106,6 +106,16 @@ def test_prefill_long_chunk(kv):
     print("prefill chunk 33 over 16424 cached tokens: max scaled error %.2e" % err)
 
 
+@pytest.mark.parametrize("chunk,group,d0,cache_lens", [(150, 4, 128, [0, 300]), (130, 8, 96, [200]),
+                                                       (70, 1, 64, [129])])
+def test_prefill_multi_block_chunk(kv, chunk, group, d0, cache_lens):
+    # chunks longer than one 64-token stage of the causal part and query rows over several CTAs
+    # of 128 rows (600, 1040 and 70 rows), so the online softmax runs over 2-3 stages and rows
+    # past the chunk's end pad the last CTA
+    err = _prefill_case(kv, cache_lens, chunk, 1, group, d0, seed=chunk + group)
+    print("prefill chunk=%d G=%d d0=%d: max scaled error %.2e" % (chunk, group, d0, err))
+
+
 def test_prefill_chunk64(kv):
     # the bench's prefill shape at a smaller batch: 64-token chunks, GQA 4 (256 query vectors
     # per kv head, four CTAs of 64), 8195 and 2000 cached tokens
