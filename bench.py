@@ -608,9 +608,9 @@ def _time_long_stream(torch, kv, synth, d0, peak, steps=512, batch=4, hq=32, hkv
     n_pool = batch * width
     g = torch.Generator().manual_seed(seed)
     table = torch.randperm(n_pool, generator=g).view(batch, width).to(torch.int32)
+    pool = kv.alloc_pool(desc, n_pool, device=dev)  # before the temporaries, as in the layered runs
     k, v = synth.outlier_kv(int(sealed0.sum()) * 128, hkv, d0, seed=seed, device=dev)
     ids = torch.cat([table[b, :int(sealed0[b])] for b in range(batch)]).to(dev)
-    pool = kv.alloc_pool(desc, n_pool, device=dev)
     kv.quantize_tiles(desc, k, v, ids, pool)
     del k, v
     kp, vp = synth.outlier_kv(batch * 128, hkv, d0, seed=seed + 1, device=dev)
