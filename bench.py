@@ -769,12 +769,6 @@ def _run_kvarn(args, torch, world, rank):
         state["cur"] = 1 - c
         state["step"] += 1
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    lens_before = S["lens"][state["cur"]].to(torch.int64).cpu()
     # The decode call's own duration is sampled live on at most DEC_EVENT_SAMPLES evenly spaced
     # timed steps, at most one in DEC_EVENT_EVERY_MIN: an event recorded between append and
     # decode ends their programmatic-launch overlap, so the other steps run without it.
@@ -782,10 +776,19 @@ def _run_kvarn(args, torch, world, rank):
     sampled = [i for i in range(args.steps) if i % every == 0]
     dec_ev = {i: tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for i in sampled}
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the clock sampler starts before the warm-up: its start-up wait (0.3 s for nvidia-smi's
+    # first samples) left the GPU idle between the warm-up and the timed steps, and a short
+    # timed window then began cold (20 steps: decode_kernel 101 us against 93 us at the same
+    # lengths in a 200-step window)
     clocks = ClockSampler(_device_id(torch))
     clocks.start()
     time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    lens_before = S["lens"][state["cur"]].to(torch.int64).cpu()
     w0 = clocks.mark()
     t0.record(stream)
     for i in range(args.steps):
