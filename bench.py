@@ -742,7 +742,7 @@ def _run_kvarn(args, torch, world, rank):
     from calibration_free_kv_gb300 import synth
 
     dev = torch.device("cuda")
-    S = _setup_decode(torch, kv, synth, args.warmup + 2 * args.steps + 4)
+    S = _setup_decode(torch, kv, synth, 2 * args.warmup + 2 * args.steps + 4)
     stream = torch.cuda.current_stream()
     state = {"cur": 0, "step": 0}
 
@@ -827,11 +827,15 @@ def _run_kvarn(args, torch, world, rank):
               b[nq + nk:].view(S["vn"][0].shape)) for b in d_in]
     copy = torch.cuda.Stream()
     e_steps = args.steps
-    lens_e = S["lens"][state["cur"]].to(torch.int64).cpu()
     up = [torch.cuda.Event() for _ in range(e_steps)]        # inputs of step i on the device
     done = [torch.cuda.Event() for _ in range(e_steps)]      # step i computed
     down = [torch.cuda.Event() for _ in range(e_steps)]      # output of step i on the host
+    # the same W warm-up steps as before the timed steps, after the host-side set-up above, so
+    # that the end-to-end steps do not begin on an idle GPU
+    for _ in range(args.warmup):
+        step()
     torch.cuda.synchronize()
+    lens_e = S["lens"][state["cur"]].to(torch.int64).cpu()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     copy.wait_stream(stream)
