@@ -1209,15 +1209,18 @@ __global__ void __launch_bounds__(tc::kThreads, 2) quantize_tc_kernel(QuantizePa
     for (int u = blockIdx.x + gridDim.x * warp; u < units; u += gridDim.x * kWarps) {
       const int h = (u >> 1) % p.num_kv_heads, b = (u >> 1) / p.num_kv_heads;
       const bool is_v = (u & 1) != 0;
+      // the new token's 16-byte chunk of this lane (d0 <= 128 here) is read before the length,
+      // so that the two loads are in flight together
+      const __half* nw = (is_v ? p.v_new : p.k_new) + ((int64_t)b * p.num_kv_heads + h) * p.d0;
+      const int c = lane * 8;
+      const uint4 tok = c < p.d0 ? *reinterpret_cast<const uint4*>(nw + c) : make_uint4(0u, 0u, 0u, 0u);
       const int len = p.seq_lens[b];
       if (len < 0 || len >= p.max_pages * kTile) {
         if (lane == 0 && !is_v && h == 0) flag_error(p.status, KVARN_DEV_SEQ_TOO_LONG);
         continue;
       }
       __half* part = (is_v ? p.partial_v : p.partial_k) + ((int64_t)b * p.num_kv_heads + h) * kTile * p.d0;
-      const __half* nw = (is_v ? p.v_new : p.k_new) + ((int64_t)b * p.num_kv_heads + h) * p.d0;
-      for (int c = lane * 8; c < p.d0; c += 32 * 8)
-        *reinterpret_cast<uint4*>(part + (len % kTile) * p.d0 + c) = *reinterpret_cast<const uint4*>(nw + c);
+      if (c < p.d0) *reinterpret_cast<uint4*>(part + (len % kTile) * p.d0 + c) = tok;
       if (lane == 0 && !is_v && h == 0 && p.seq_lens_out != nullptr) p.seq_lens_out[b] = len + 1;
       if (len % kTile != kTile - 1) continue;
       const __half* src;
