@@ -6,11 +6,13 @@
 // [vatt §四個步驟: the rotation is orthonormal so attention scores are unchanged;
 //  hotdry §非对称量化与尺度折叠: the folded scales are multiplied back at read time]
 //
-// decode_kernel: grid (split, kv head x query block, sequence).  A CTA owns up to
-// `pages_per_split` sealed pages of one (sequence, kv head), or the raw fp16 partial tile, for
-// up to 4 * NT query vectors of that kv head (decode: its G query heads; prefill: blocks of
-// the chunk's C * G query vectors).  Its warps (8, or 4 where 8 page slots do not fit) take
-// whole pages round-robin.  Every warp owns two shared-memory slots, one for the K half of a page
+// decode_kernel: by default (decode) persistent CTAs, two per SM, each walking one range of
+// the segment-weighted page partition (decode_util.cuh) as segments of one (sequence, kv head)
+// row; otherwise (prefill, and the split form kept for comparison) grid (split, kv head x
+// query block, sequence), a CTA owning up to `pages_per_split` sealed pages of one (sequence,
+// kv head), or the raw fp16 partial tile.  Either way a CTA serves up to 4 * NT query vectors
+// of that kv head (decode: its G query heads; prefill: blocks of the chunk's C * G query
+// vectors).  Its warps (8, or 4 where 8 page slots do not fit) take whole pages round-robin.  Every warp owns two shared-memory slots, one for the K half of a page
 // record and one for the V half, each filled by a 1-D bulk copy completed on its own
 // mbarrier: the K half of the next page streams in while the warp works on the current
 // page's V half, and the V half of the next page while it works on the next K half.
@@ -24,9 +26,11 @@
 // Codes enter the MMAs as exact fp16 subnormals: masking a code into the low mantissa bits
 // of a zero exponent gives code * 2^-24 (code * 2^-22 .. 2^-18 for higher bit positions), so
 // unpacking costs one AND per two codes; the powers of two are folded into B and into the
-// fp32 results.  The CTA merges its warps and writes (m, l, unnormalised o~) for its split;
-// combine_kernel merges the splits, divides by l, undoes the rotation and stores fp16.
-// chunk_kernel adds the causal part of a prefill chunk as one more split.
+// fp32 results.  The CTA merges its warps and writes (m, l, unnormalised o~) for its split (G = 8
+// and prefill use NT = 2 with the heads on the MMA's M axis instead, qk_page_t / pv_page_t).
+// combine_kernel attends to the raw open tiles (decode), merges the splits, divides by l,
+// undoes the rotation and stores fp16.  chunk_tc_kernel (chunk_kernel at head_dim 256) adds
+// the causal part of a prefill chunk as one more split.
 #include "common.cuh"
 #include "decode_util.cuh"
 #include "params.cuh"
