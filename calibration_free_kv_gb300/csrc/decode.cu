@@ -1710,8 +1710,12 @@ __global__ void __launch_bounds__(256, 1) chunk_tc_kernel(DecodeParams p) {
     };
     const __half* qa = qrow(ca >= 0 ? ra : 0);
     const __half* qb = qrow(cb >= 0 ? rb : 0);
+    // rows start at even element offsets (d0 is a multiple of 8), so with q 4-byte aligned a
+    // channel pair is one 32-bit load
+    const bool q4 = (reinterpret_cast<uintptr_t>(p.q) & 3u) == 0u;
     auto pair = [&](const __half* row, bool ok, int ch) -> uint32_t {
-      return (ok && ch < p.d0) ? h2u(__halves2half2(row[ch], row[ch + 1])) : 0u;
+      if (!(ok && ch < p.d0)) return 0u;
+      return q4 ? *reinterpret_cast<const uint32_t*>(row + ch) : h2u(__halves2half2(row[ch], row[ch + 1]));
     };
 #pragma unroll
     for (int kk = 0; kk < KK; ++kk) {
